@@ -1,0 +1,570 @@
+"""Benchmark of the INSTANT low-rank linear backward on one GB300 (or N replicas).
+
+A step is one training step of a BERT-base-block-shaped linear layer
+(B=32, L=512, Cx=Cy=768, Rx=Ry=8, bf16 with fp32 accumulation) through every
+row of the hot path: activation compression (x_hat = P x), the one-read
+gradient projection, g_w, g_hat_x and the rank-R expansion, captured as one
+CUDA graph per rotating buffer set; every N_t steps (default 100, counted from
+the first timed step) the calibration phase runs eagerly: the autocorrelation
+statistics of the step's batch plus one resident calibration batch (64 samples)
+and the two eigen-solves that rewrite [P; Q].
+
+Output: one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "low-rank linear-backward layers/s and achieved HBM GB/s (% of roofline) on 1 GB300"
+UNIT = "layers/s"
+CONFIG = 2
+NSETS = 8
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--nt", type=int, default=100, help="recalibration period N_t")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-iters", type=int, default=400)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(elapsed_s: float, units_per_rank: float, world: int, device=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    slowest = max_over_ranks(elapsed_s, device)
+    return units_per_rank * world / slowest, slowest
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def layer_bytes(B, L, Cx, Cy, Rx, Ry):
+    """Compulsory HBM bytes of one step (bf16 tensors, fp32 g_w)."""
+    return {
+        "compress_act": B * L * Cx * 2 + Rx * L * 2 + B * Rx * Cx * 2,
+        "project_grad": B * L * Cy * 2 + (Rx + Ry) * L * 2 + B * (Rx + Ry) * Cy * 2,
+        "grad_w": B * Rx * (Cy + Cx) * 2 + Cy * Cx * 4,
+        "grad_x_core": B * Ry * Cy * 2 + Cy * Cx * 2 + B * Ry * Cx * 4,
+        "expand": B * Ry * Cx * 4 + Ry * L * 2 + B * L * Cx * 2,
+    }
+
+
+def layer_flops(B, L, Cx, Cy, Rx, Ry):
+    return {
+        "compress_act": 2 * B * Rx * L * Cx,
+        "project_grad": 2 * B * (Rx + Ry) * L * Cy,
+        "grad_w": 2 * B * Rx * Cy * Cx,
+        "grad_x_core": 2 * B * Ry * Cy * Cx,
+        "expand": 2 * B * Ry * L * Cx,
+    }
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+KERNEL_SOURCES = {
+    "compress_act": "project.cu", "project_grad": "project.cu", "grad_w": "gemm.cu",
+    "grad_x_core": "gemm.cu", "expand": "expand.cu",
+}
+
+
+def source_hash(kernel: str) -> str:
+    d = os.path.join(ROOT, "rank_compressed_backprop_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES[kernel], "tc.cuh", "kernels.h"):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
+    sources are unchanged since; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel:
+            if parts[2] != source_hash(kernel):
+                return None
+            return float(parts[1])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/instant_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader",
+                 "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1].split()[0]))
+                smax = float(f[2].split()[0])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def make_workload():
+    import workloads as W
+
+    wl = W.workload(CONFIG)
+    li = W.LayerInputs(wl)
+    B = wl.B
+    return wl, li, {"x": li.x(), "g": li.g_y(), "w": li.w(),
+                    "xc": li.calib_x(1, B), "gc": li.calib_g(1, B)}
+
+
+def to_dev(a, dev):
+    import numpy as np
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+    dist_init("nccl" if world > 1 else "gloo")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from rank_compressed_backprop_gb300.build import build
+
+    build()
+    from rank_compressed_backprop_gb300 import InstantLinear, api
+
+    wl, li, data = make_workload()
+    B, L, Rx, Ry = wl.B, wl.L, wl.Rx, wl.Ry
+    Cx, Cy = li.Cx, li.Cy
+    bf = torch.bfloat16
+    w = to_dev(data["w"], dev)
+    lay = InstantLinear(w, B=B, L=L, Rx=Rx, Ry=Ry, n_t=args.nt, eps=wl.eps, p=wl.p)
+    x0, g0 = to_dev(data["x"], dev), to_dev(data["g"], dev)
+    xc, gc = to_dev(data["xc"], dev), to_dev(data["gc"], dev)
+    sets = []
+    for _ in range(NSETS):
+        sets.append({
+            "x": x0.clone(), "g": g0.clone(),
+            "xhat": torch.empty(B, Rx, Cx, dtype=bf, device=dev),
+            "gw": torch.empty(Cy, Cx, dtype=torch.float32, device=dev),
+            "gx": torch.empty(B, L, Cx, dtype=bf, device=dev),
+        })
+    set_bytes = sum(t.numel() * t.element_size() for t in sets[0].values())
+
+    def calibrate(s):
+        lay.accumulate(s["x"], s["g"])
+        lay.accumulate(xc, gc)
+        return lay.recalibrate()
+
+    def step_eager(s):
+        lay.compress(s["x"], out=s["xhat"])
+        lay.backward(s["g"], xhat=s["xhat"], gw=s["gw"], gx=s["gx"])
+
+    # first calibration, then one eager step per set (sets kernel attributes)
+    cal0 = calibrate(sets[0])
+    for s in sets:
+        step_eager(s)
+    torch.cuda.synchronize()
+    launches_per_step = None
+    c0 = api.launch_count()
+    step_eager(sets[0])
+    launches_per_step = api.launch_count() - c0
+
+    # one CUDA graph per buffer set
+    graphs = []
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cs):
+        for s in sets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                step_eager(s)
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(cs)
+    torch.cuda.synchronize()
+
+    # ---- warm-up ----
+    for i in range(args.warmup):
+        graphs[i % NSETS].replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region ----
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_cal = 0
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        lc0 = api.launch_count()
+        start.record(stream)
+        for i in range(args.steps):
+            if i % args.nt == 0:
+                calibrate(sets[i % NSETS])
+                n_cal += 1
+            graphs[i % NSETS].replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+        lc1 = api.launch_count()
+        barrier()
+    elapsed = start.elapsed_time(end) / 1e3
+    graph_launches = launches_per_step * args.steps
+    gpu_launches = (lc1 - lc0) + graph_launches  # eager calibration launches + graph kernels
+    value, slowest = aggregate(elapsed, float(args.steps), world, dev)
+    ms_per_step = slowest * 1e3 / args.steps
+
+    # ---- per-kernel durations (eager launches on the current stream) ----
+    ws = lay.ws_gx
+    kern = {
+        "compress_act": lambda s: api.compress_act(s["x"], lay.P, s["xhat"]),
+        "project_grad": lambda s: api.project_grad(s["g"], lay.PQ, lay.Sx, lay.Sq, Rx, Ry),
+        "grad_w": lambda s: api.grad_w(lay.Sx, s["xhat"], s["gw"], B),
+        "grad_x_core": lambda s: api.grad_x_core(lay.Sq, w, ws, B),
+        "expand": lambda s: api.expand(lay.Q, s["gx"], ws, Cy),
+    }
+    kus = {}
+    for name, fn in kern.items():
+        for i in range(10):
+            fn(sets[i % NSETS])
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.kernel_iters):
+            fn(sets[i % NSETS])
+        b.record(stream)
+        torch.cuda.synchronize()
+        kus[name] = a.elapsed_time(b) * 1e3 / args.kernel_iters
+    # graph-only backward (no calibration) for context
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for i in range(2000):
+        graphs[i % NSETS].replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    step_only_us = a.elapsed_time(b) * 1e3 / 2000
+    # calibration phase alone
+    t0 = time.perf_counter()
+    for i in range(5):
+        calibrate(sets[i % NSETS])
+    torch.cuda.synchronize()
+    cal_ms = (time.perf_counter() - t0) * 1e3 / 5
+
+    peaks = measured_peaks()
+    nbytes = layer_bytes(B, L, Cx, Cy, Rx, Ry)
+    nflops = layer_flops(B, L, Cx, Cy, Rx, Ry)
+    dom = max(kus, key=kus.get)
+    achieved = nbytes[dom] / (kus[dom] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": peaks["source"] + " (burst copy)",
+                "bytes_per_launch": nbytes[dom], "traffic": ncu_traffic(dom)}
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = run_e2e(args, lay, data, dev, xc, gc)
+
+    # ---- CPU baseline (the oracle as it stands) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, data, args.nt)
+
+    clocks = clk.summary()
+    step_bytes = sum(nbytes.values())
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded planted-spectrum activations and gradients)",
+        "config": {
+            "workload": "BERT-base-block linear, B=32 L=512 Cx=Cy=768 Rx=Ry=8, sigma_i ~ i^-1.5",
+            "B": B, "L": L, "Cx": Cx, "Cy": Cy, "Rx": Rx, "Ry": Ry,
+            "step": "compress_act + project_grad + grad_w + grad_x (CUDA graph); "
+                    "calibration (2x accumulate over 64 samples + 2 solves) every N_t steps",
+            "calibration_every": args.nt, "calibrations_timed": n_cal,
+            "l2": f"{NSETS} rotating buffer sets of {set_bytes / 1e6:.0f} MB "
+                  f"({NSETS * set_bytes / 1e6:.0f} MB > 129 MB L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(gpu_launches),
+        "clocks": clocks,
+        "detail": {
+            "kernel_us": {k: round(v, 3) for k, v in kus.items()},
+            "kernel_gbs": {k: round(nbytes[k] / (kus[k] * 1e-6) / 1e9, 1) for k in kus},
+            "kernel_tflops": {k: round(nflops[k] / (kus[k] * 1e-6) / 1e12, 2) for k in kus},
+            "step_graph_us": round(step_only_us, 3),
+            "step_graph_layers_per_s": round(1e6 / step_only_us, 1),
+            "step_algorithmic_bytes": step_bytes,
+            "step_graph_hbm_gbs": round(step_bytes / (step_only_us * 1e-6) / 1e9, 1),
+            "calibration_ms": round(cal_ms, 3),
+            "launches_per_step": launches_per_step,
+            "calibration_k": [cal0[0].k, cal0[1].k],
+            "flops_vanilla_per_layer": 4 * B * L * Cx * Cy,
+            "flops_low_rank_per_layer": 2 * B * (Rx + Ry) * (Cx * Cy + L * Cx + L * Cy),
+            "activation_memory_ratio": L / Rx,
+        },
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, lay, data, dev, xc, gc):
+    """Same metric through the public API, inputs from pinned host memory and
+    results read back every step."""
+    import numpy as np
+    import torch
+
+    x_h = torch.from_numpy(np.ascontiguousarray(data["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    g_h = torch.from_numpy(np.ascontiguousarray(data["g"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    x_d, g_d = torch.empty_like(x_h, device=dev), torch.empty_like(g_h, device=dev)
+    gw_h = torch.empty(lay.gw.shape, dtype=torch.float32).pin_memory()
+    gx_h = torch.empty(lay.gx.shape, dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream()
+    steps = args.e2e_steps
+
+    def one(i):
+        x_d.copy_(x_h, non_blocking=True)
+        g_d.copy_(g_h, non_blocking=True)
+        if i % args.nt == 0:
+            lay.accumulate(x_d, g_d)
+            lay.accumulate(xc, gc)
+            lay.recalibrate()
+        lay.compress(x_d)
+        gw, gx = lay.backward(g_d)
+        gw_h.copy_(gw, non_blocking=True)
+        gx_h.copy_(gx, non_blocking=True)
+
+    for i in range(3):
+        one(i + 1)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for i in range(steps):
+        one(i)
+    b.record(stream)
+    torch.cuda.synchronize()
+    el = a.elapsed_time(b) / 1e3
+    _, world, _ = dist_env()
+    val, _ = aggregate(el, float(steps), world, dev)
+    return {"value": round(val, 2), "unit": UNIT,
+            "h2d_bytes_per_step": x_h.numel() * 2 + g_h.numel() * 2,
+            "d2h_bytes_per_step": gw_h.numel() * 4 + gx_h.numel() * 2,
+            "steps": steps, "api": "InstantLinear.compress/backward (eager) + torch copies"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def oracle_sample_step(O, data, Pb, Qb, bs):
+    O.low_rank_backward(data["x"][:bs], data["g"][:bs], data["w"], Pb, Qb)
+
+
+def oracle_calibration(O, data, wl, frac_samples):
+    import numpy as np
+
+    CX = O.accumulate_autocorrelation(data["x"][:frac_samples])
+    CX = O.accumulate_autocorrelation(data["xc"][:frac_samples], CX)
+    CG = O.accumulate_autocorrelation(data["g"][:frac_samples])
+    CG = O.accumulate_autocorrelation(data["gc"][:frac_samples], CG)
+    n = 2 * frac_samples
+    cx = O.calibrate(CX, n, eps=wl.eps, p=wl.p, r_override=wl.Rx)
+    cg = O.calibrate(CG, n, eps=wl.eps, p=wl.p, r_override=wl.Ry)
+    return cx, cg, np
+
+
+def cpu_baseline(wl, data, nt, budget_s: float = 15.0):
+    """Oracle step time on a bounded sample: bs of B samples per step and the
+    calibration on the same fraction of its 64 samples, amortised over N_t."""
+    import oracle as O
+    import workloads as W
+
+    bs = max(1, wl.B // 8)
+    t0 = time.perf_counter()
+    cx, cg, _ = oracle_calibration(O, data, wl, bs)
+    t_cal = time.perf_counter() - t0
+    Pb = W.f32_to_bf16_bits(cx["rows"])
+    Qb = W.f32_to_bf16_bits(cg["rows"])
+    n, t1 = 0, time.perf_counter()
+    while True:
+        oracle_sample_step(O, data, Pb, Qb, bs)
+        n += 1
+        if time.perf_counter() - t1 > budget_s or n >= 200:
+            break
+    t_step = (time.perf_counter() - t1) / n
+    frac = bs / wl.B
+    per_layer = (t_step + t_cal / nt) / frac
+    return {"value": round(1.0 / per_layer, 4), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle: {n} steps on {bs} of {wl.B} samples "
+                      f"({t_step:.3f} s each) + one calibration on {2 * bs} of 64 samples "
+                      f"({t_cal:.2f} s) amortised over N_t={nt}; scaled to whole layers"}
+
+
+def run_reference(args):
+    """The oracle arm: same metric, config and unit, on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    import workloads as W
+
+    wl, _, data = make_workload()
+    bs = max(1, wl.B // 8)
+    cx, cg, _ = oracle_calibration(O, data, wl, bs)
+    Pb, Qb = W.f32_to_bf16_bits(cx["rows"]), W.f32_to_bf16_bits(cg["rows"])
+    steps = min(args.steps, 60)
+    for _ in range(min(args.warmup, 3)):
+        oracle_sample_step(O, data, Pb, Qb, bs)
+    t0 = time.perf_counter()
+    n_cal = 0
+    for i in range(steps):
+        if i % args.nt == 0:
+            cx, cg, _ = oracle_calibration(O, data, wl, bs)
+            Pb, Qb = W.f32_to_bf16_bits(cx["rows"]), W.f32_to_bf16_bits(cg["rows"])
+            n_cal += 1
+        oracle_sample_step(O, data, Pb, Qb, bs)
+    el = time.perf_counter() - t0
+    frac = bs / wl.B
+    value = steps * frac / el
+    sample = (f"{steps} oracle steps on {bs} of {wl.B} samples each, {n_cal} calibration(s) on "
+              f"{2 * bs} of 64 samples; layers counted as fractions")
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+           "n_gpus": world, "steps": steps, "warmup": min(args.warmup, 3),
+           "ms_per_step": round(el * 1e3 / steps, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": "BERT-base-block linear, B=32 L=512 Cx=Cy=768 Rx=Ry=8",
+                      "calibration_every": args.nt},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": _cores(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

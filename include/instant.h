@@ -1,0 +1,197 @@
+/*
+ * instant.h -- C ABI of the GB300 (sm_103a) low-rank linear-backward library.
+ *
+ * The library computes the per-step path and the calibration of INSTANT
+ * low-rank backpropagation for one linear layer y = x w^T, as described on the
+ * page "INSTANT: Compressing Gradients and Activations for Resource-Efficient
+ * Training" (ICLR 2026 paper notes): sections 整体框架 (overall framework) and
+ * 关键设计 1-3 (key designs 1-3).
+ *
+ * Notation (one sample b of a batch of B):
+ *   x_b   [L, Cx]  layer input          g_y,b [L, Cy]  output gradient
+ *   w     [Cy, Cx] weight                P [Rx, L], Q [Ry, L] projectors
+ *   PQ    [Rx+Ry, L]  = [P; Q] stacked row-wise (P rows first)
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor argument is a DEVICE pointer to caller-owned memory,
+ *     row-major and contiguous, unless the argument says "host".  The library
+ *     never allocates or frees device memory; scratch comes from `ws`.
+ *   - Device pointers must be 16-byte aligned, and for INSTANT_BF16 the
+ *     innermost extent of every 2-D/3-D operand read by TMA (L for PQ/P/Q is
+ *     exempt) must be a multiple of 8 elements; otherwise INSTANT_ERR_ALIGN.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream except instant_calib_solve and
+ *     instant_device_status, which synchronise it.
+ *   - Argument, shape and dtype errors are reported before anything is
+ *     launched; nothing is written in that case.  A launch error returns
+ *     INSTANT_ERR_CUDA.  Kernels never trap: a device-side wait that runs out
+ *     of time sets a sticky device status that instant_device_status reads.
+ *   - dtype INSTANT_BF16: bf16 inputs and outputs, fp32 accumulation
+ *     (tcgen05 tensor cores).  INSTANT_F32: fp32 everywhere, plain FFMA (no
+ *     TF32), intended for small problems.
+ */
+#ifndef INSTANT_H_
+#define INSTANT_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  INSTANT_OK = 0,
+  INSTANT_ERR_ARG = 1,           /* null pointer or bad scalar argument          */
+  INSTANT_ERR_SHAPE = 2,         /* unsupported or inconsistent extent           */
+  INSTANT_ERR_DTYPE = 3,         /* unknown dtype                                */
+  INSTANT_ERR_ALIGN = 4,         /* pointer or row pitch not 16-byte aligned     */
+  INSTANT_ERR_WORKSPACE = 5,     /* workspace missing or too small               */
+  INSTANT_ERR_CUDA = 6,          /* CUDA runtime / launch error                  */
+  INSTANT_ERR_NOT_CONVERGED = 7, /* eigensolver hit its iteration cap            */
+  INSTANT_ERR_NONFINITE = 8,     /* autocorrelation has no finite positive energy*/
+  INSTANT_ERR_DEVICE = 9         /* a device-side wait ran out of time           */
+} instant_status;
+
+typedef enum { INSTANT_F32 = 0, INSTANT_BF16 = 1 } instant_dtype;
+
+/* Calibration parameters (关键设计 2). */
+typedef struct {
+  double eps;       /* energy threshold epsilon (the page fixes 0.95)            */
+  int p;            /* oversampling p: R = min(k + p, L)                         */
+  int r_override;   /* > 0: output exactly this many rows (k is still reported)  */
+  int scale_on;     /* 1: rows scaled by (sum_{i<=R} sigma_i^2)^(-1/2); 0: off   */
+  int max_iter;     /* subspace-iteration cap; 0 selects 300                     */
+  double tol;       /* Ritz residual tolerance relative to sigma_1; 0 selects 2e-5 */
+} instant_calib_params;
+
+/*
+ * Activation compression x_hat_b = P x_b (整体框架: the forward stores
+ * x_hat = P x instead of x).
+ *   x     [B, L, Cx]  dtype dt (read)
+ *   P     [Rx, L]     dtype dt (read)
+ *   xhat  [B, Rx, Cx] dtype dt (written)
+ * Limits: 1 <= Rx <= 64.
+ */
+instant_status instant_compress_act(const void* x, const void* P, void* xhat,
+                                    int B, int L, int Cx, int Rx,
+                                    instant_dtype dt, void* stream);
+
+/*
+ * Gradient projection with one read of g_y (关键设计 3):
+ *   Sx_b = P g_y,b  (so g_hat_y1,b = Sx_b^T)    Sq_b = Q g_y,b  (g_hat_y2,b)
+ *   gy  [B, L, Cy]      dtype dt (read)
+ *   PQ  [Rx+Ry, L]      dtype dt (read), P rows then Q rows
+ *   Sx  [B*Rx, Cy]      dtype dt (written), row b*Rx + r
+ *   Sq  [B*Ry, Cy]      dtype dt (written), row b*Ry + r
+ * Limits: 1 <= Rx, Ry and Rx + Ry <= 128.
+ */
+instant_status instant_project_grad(const void* gy, const void* PQ, void* Sx, void* Sq,
+                                    int B, int L, int Cy, int Rx, int Ry,
+                                    instant_dtype dt, void* stream);
+
+/*
+ * Weight gradient g_w = sum_b Sx_b^T x_hat_b = Sx^T x_hat (关键设计 3:
+ * g_w ~ g_hat_y1 x_hat), contraction over K = B*Rx.
+ *   Sx    [B*Rx, Cy]  dtype dt (read)
+ *   xhat  [B*Rx, Cx]  dtype dt (read; the [B, Rx, Cx] output of compress_act)
+ *   gw    [Cy, Cx]    fp32 (written, or accumulated into when accumulate != 0)
+ */
+instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int accumulate,
+                              int B, int Rx, int Cx, int Cy,
+                              instant_dtype dt, void* stream);
+
+/*
+ * Input gradient g_tilde_x,b = Q^T (Sq_b w) (关键设计 3: g_hat_x = g_hat_y2 w,
+ * g_tilde_x = Q^T g_hat_x).
+ *   Sq  [B*Ry, Cy]  dtype dt (read)
+ *   w   [Cy, Cx]    dtype dt (read)
+ *   Q   [Ry, L]     dtype dt (read)
+ *   gx  [B, L, Cx]  dtype dt (written)
+ *   ws  device scratch of at least instant_grad_x_workspace_bytes(...) bytes
+ *       (may be NULL when that size is 0).  Contents are overwritten.
+ * Limits: 1 <= Ry <= 64.
+ */
+instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx,
+                              void* ws, size_t ws_bytes,
+                              int B, int L, int Cx, int Cy, int Ry,
+                              instant_dtype dt, void* stream);
+
+size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt);
+
+/*
+ * The two halves of instant_grad_x, for callers that schedule or time them
+ * separately.  instant_grad_x_core computes g_hat_x = Sq w (关键设计 3,
+ * g_hat_x = g_hat_y2 w) into `ws` as fp32 split-K partial planes whose number
+ * depends only on (B, Cx, Cy, Ry, dt); instant_expand sums those planes and
+ * writes g_tilde_x,b = Q^T g_hat_x,b.  Call them with the same sizes and the
+ * same workspace (of instant_grad_x_workspace_bytes bytes), in that order on
+ * one stream; the layout of `ws` between the two calls is private.
+ */
+instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes,
+                                   int B, int Cx, int Cy, int Ry,
+                                   instant_dtype dt, void* stream);
+instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws_bytes,
+                              int B, int L, int Cx, int Cy, int Ry,
+                              instant_dtype dt, void* stream);
+
+/*
+ * Autocorrelation statistic (关键设计 1: C = E[t t^T], only statistics are
+ * accumulated during calibration, not the batch):
+ *   C += sum_b t_b t_b^T
+ *   t  [B, L, Cdim]  dtype dt (read)
+ *   C  [L, L]        fp32, accumulated in place (caller zeroes it and keeps
+ *                    the sample count; E[t t^T] = C / count)
+ * Limits: L <= 8192.
+ */
+instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, int Cdim,
+                                        instant_dtype dt, void* stream);
+
+/*
+ * Projector from an accumulated statistic (关键设计 1 and 2):
+ *   C/n = U Sigma U^T (symmetric PSD, so the SVD is the eigendecomposition);
+ *   E = ||C/n||_F^2 (fp64, from C directly);
+ *   k = smallest index with sum_{i<=k} sigma_i^2 >= eps * E  (fp64);
+ *   R = r_override if > 0, else min(k + p, L);
+ *   s = (sum_{i<=R} sigma_i^2)^(-1/2) if scale_on, else 1;
+ *   rows_out[i, :] = s * u_i^T for i < R, each u_i signed so that its
+ *   largest-magnitude entry is positive.
+ * Arguments
+ *   C          [L, L] fp32 device (read): the accumulated sum
+ *   n_samples  number of samples summed into C (> 0)
+ *   rows_out   [r_cap, L] device, dtype dt: rows 0..R-1 written, rows R..r_cap-1 zeroed
+ *   k_out, r_out, scale_out, energy_out: HOST pointers (energy_out may be NULL)
+ *   eig_out    HOST, r_cap doubles (may be NULL): sigma_1..sigma_{r_cap}, 0 past
+ *              the solved block
+ *   ws         device scratch of instant_calib_workspace_bytes(L, r_cap) bytes
+ * Method: L <= 128 -> one-CTA cyclic Jacobi on the full matrix; larger L ->
+ * block subspace iteration with Rayleigh-Ritz (block <= 128 columns).
+ * Returns INSTANT_ERR_NOT_CONVERGED when the cap is hit or when k + p does not
+ * fit the block, INSTANT_ERR_NONFINITE when E is not finite and positive.
+ * Synchronises `stream`.
+ */
+instant_status instant_calib_solve(const float* C, long long n_samples, int L,
+                                   const instant_calib_params* prm,
+                                   void* rows_out, int r_cap, instant_dtype dt,
+                                   int* k_out, int* r_out, float* scale_out,
+                                   double* energy_out, double* eig_out,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+size_t instant_calib_workspace_bytes(int L, int r_cap);
+
+/* Reads (and clears when clear != 0) the sticky device status word after
+ * synchronising `stream`; INSTANT_OK when no device-side wait ran out. */
+instant_status instant_device_status(int clear, void* stream);
+
+const char* instant_status_string(instant_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int instant_version(void);
+
+/* Number of kernels the library has launched in this process (host-side
+ * counter, incremented at every launch; monotonic). */
+unsigned long long instant_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* INSTANT_H_ */

@@ -1,0 +1,218 @@
+"""Python binding of the C ABI, one function per entry point of include/instant.h.
+
+Each function takes torch CUDA tensors, checks their shapes against each other,
+and passes raw device pointers, extents and the current CUDA stream to the
+library.  No arithmetic of the method happens here.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from ._lib import INSTANT_BF16, INSTANT_F32, CalibParams, check, lib
+
+__all__ = [
+    "compress_act",
+    "project_grad",
+    "grad_w",
+    "grad_x",
+    "grad_x_workspace_bytes",
+    "grad_x_core",
+    "expand",
+    "launch_count",
+    "calib_accumulate",
+    "calib_solve",
+    "calib_workspace_bytes",
+    "device_status",
+    "CalibResult",
+    "dtype_code",
+]
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return INSTANT_BF16
+    if t == torch.float32:
+        return INSTANT_F32
+    raise TypeError(f"unsupported dtype {t}: use torch.bfloat16 or torch.float32")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _same_dtype(dt, *pairs):
+    for name, t in pairs:
+        if t.dtype != dt:
+            raise TypeError(f"{name} has dtype {t.dtype}, expected {dt}")
+
+
+def compress_act(x: torch.Tensor, P: torch.Tensor, xhat: torch.Tensor, stream=None) -> torch.Tensor:
+    """``xhat[b] = P @ x[b]``: x ``[B, L, Cx]``, P ``[Rx, L]``, xhat ``[B, Rx, Cx]``."""
+    B, L, Cx = x.shape
+    Rx = P.shape[0]
+    if P.shape != (Rx, L) or xhat.shape != (B, Rx, Cx):
+        raise ValueError("compress_act: inconsistent shapes")
+    _same_dtype(x.dtype, ("P", P), ("xhat", xhat))
+    check(lib().instant_compress_act(_dev(x, "x"), _dev(P, "P"), _dev(xhat, "xhat"), B, L, Cx, Rx,
+                                     dtype_code(x.dtype), _stream(stream)), "instant_compress_act")
+    return xhat
+
+
+def project_grad(g_y: torch.Tensor, PQ: torch.Tensor, Sx: torch.Tensor, Sq: torch.Tensor,
+                 Rx: int, Ry: int, stream=None):
+    """``Sx[b] = P g_y[b]``, ``Sq[b] = Q g_y[b]`` with ``PQ = [P; Q]``.
+
+    g_y ``[B, L, Cy]``, PQ ``[Rx+Ry, L]``, Sx ``[B*Rx, Cy]``, Sq ``[B*Ry, Cy]``."""
+    B, L, Cy = g_y.shape
+    if PQ.shape != (Rx + Ry, L) or Sx.shape != (B * Rx, Cy) or Sq.shape != (B * Ry, Cy):
+        raise ValueError("project_grad: inconsistent shapes")
+    _same_dtype(g_y.dtype, ("PQ", PQ), ("Sx", Sx), ("Sq", Sq))
+    check(lib().instant_project_grad(_dev(g_y, "g_y"), _dev(PQ, "PQ"), _dev(Sx, "Sx"), _dev(Sq, "Sq"),
+                                     B, L, Cy, Rx, Ry, dtype_code(g_y.dtype), _stream(stream)),
+          "instant_project_grad")
+    return Sx, Sq
+
+
+def grad_w(Sx: torch.Tensor, xhat: torch.Tensor, gw: torch.Tensor, B: int, accumulate: bool = False,
+           stream=None) -> torch.Tensor:
+    """``gw (+)= Sx^T xhat``: Sx ``[B*Rx, Cy]``, xhat ``[B*Rx, Cx]`` (or ``[B, Rx, Cx]``),
+    gw ``[Cy, Cx]`` fp32."""
+    K, Cy = Sx.shape
+    xh = xhat.reshape(K, -1) if xhat.dim() == 3 else xhat
+    Cx = xh.shape[1]
+    if K % B != 0 or xh.shape[0] != K or gw.shape != (Cy, Cx) or gw.dtype != torch.float32:
+        raise ValueError("grad_w: inconsistent shapes")
+    _same_dtype(Sx.dtype, ("xhat", xhat))
+    check(lib().instant_grad_w(_dev(Sx, "Sx"), _dev(xhat, "xhat"), _dev(gw, "gw"), int(bool(accumulate)),
+                               B, K // B, Cx, Cy, dtype_code(Sx.dtype), _stream(stream)),
+          "instant_grad_w")
+    return gw
+
+
+def grad_x_workspace_bytes(B: int, L: int, Cx: int, Cy: int, Ry: int, dtype: torch.dtype) -> int:
+    return int(lib().instant_grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dtype_code(dtype)))
+
+
+def grad_x(Sq: torch.Tensor, w: torch.Tensor, Q: torch.Tensor, gx: torch.Tensor,
+           ws: torch.Tensor, stream=None) -> torch.Tensor:
+    """``gx[b] = Q^T (Sq[b] w)``: Sq ``[B*Ry, Cy]``, w ``[Cy, Cx]``, Q ``[Ry, L]``,
+    gx ``[B, L, Cx]``; ws is scratch of ``grad_x_workspace_bytes`` bytes."""
+    B, L, Cx = gx.shape
+    Ry = Q.shape[0]
+    Cy = w.shape[0]
+    if Q.shape != (Ry, L) or w.shape != (Cy, Cx) or Sq.shape != (B * Ry, Cy):
+        raise ValueError("grad_x: inconsistent shapes")
+    _same_dtype(Sq.dtype, ("w", w), ("Q", Q), ("gx", gx))
+    check(lib().instant_grad_x(_dev(Sq, "Sq"), _dev(w, "w"), _dev(Q, "Q"), _dev(gx, "gx"),
+                               _dev(ws, "ws"), ws.numel() * ws.element_size(), B, L, Cx, Cy, Ry,
+                               dtype_code(Sq.dtype), _stream(stream)), "instant_grad_x")
+    return gx
+
+
+def grad_x_core(Sq: torch.Tensor, w: torch.Tensor, ws: torch.Tensor, B: int, stream=None):
+    """First half of :func:`grad_x`: ``g_hat_x = Sq w`` into the workspace."""
+    Cy, Cx = w.shape
+    Ry = Sq.shape[0] // B
+    if Sq.shape != (B * Ry, Cy):
+        raise ValueError("grad_x_core: inconsistent shapes")
+    _same_dtype(Sq.dtype, ("w", w))
+    check(lib().instant_grad_x_core(_dev(Sq, "Sq"), _dev(w, "w"), _dev(ws, "ws"),
+                                    ws.numel() * ws.element_size(), B, Cx, Cy, Ry,
+                                    dtype_code(Sq.dtype), _stream(stream)), "instant_grad_x_core")
+    return ws
+
+
+def expand(Q: torch.Tensor, gx: torch.Tensor, ws: torch.Tensor, Cy: int, stream=None):
+    """Second half of :func:`grad_x`: ``gx[b] = Q^T g_hat_x[b]`` from the workspace."""
+    B, L, Cx = gx.shape
+    Ry = Q.shape[0]
+    if Q.shape != (Ry, L):
+        raise ValueError("expand: inconsistent shapes")
+    _same_dtype(Q.dtype, ("gx", gx))
+    check(lib().instant_expand(_dev(Q, "Q"), _dev(gx, "gx"), _dev(ws, "ws"),
+                               ws.numel() * ws.element_size(), B, L, Cx, Cy, Ry,
+                               dtype_code(Q.dtype), _stream(stream)), "instant_expand")
+    return gx
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().instant_launch_count())
+
+
+def calib_accumulate(t: torch.Tensor, C: torch.Tensor, stream=None) -> torch.Tensor:
+    """``C += sum_b t[b] t[b]^T``: t ``[B, L, C]``, C ``[L, L]`` fp32."""
+    B, L, Cd = t.shape
+    if C.shape != (L, L) or C.dtype != torch.float32:
+        raise ValueError("calib_accumulate: C must be [L, L] float32")
+    check(lib().instant_calib_accumulate(_dev(t, "t"), _dev(C, "C"), B, L, Cd, dtype_code(t.dtype),
+                                         _stream(stream)), "instant_calib_accumulate")
+    return C
+
+
+def calib_workspace_bytes(L: int, r_cap: int) -> int:
+    return int(lib().instant_calib_workspace_bytes(L, r_cap))
+
+
+@dataclasses.dataclass
+class CalibResult:
+    k: int
+    R: int
+    scale: float
+    energy: float
+    eigenvalues: list
+
+
+def calib_solve(C: torch.Tensor, n_samples: int, rows_out: torch.Tensor, *, eps: float = 0.95,
+                p: int = 0, r_override: int = 0, scale_on: bool = True, max_iter: int = 0,
+                tol: float = 0.0, ws: torch.Tensor | None = None, stream=None,
+                raise_on_error: bool = True):
+    """Projector rows from an accumulated statistic; synchronises the stream.
+
+    Returns a :class:`CalibResult` (and the raw status when ``raise_on_error``
+    is False)."""
+    L = C.shape[0]
+    r_cap = rows_out.shape[0]
+    if C.shape != (L, L) or C.dtype != torch.float32 or rows_out.shape[1] != L:
+        raise ValueError("calib_solve: inconsistent shapes")
+    if ws is None:
+        ws = torch.empty(calib_workspace_bytes(L, r_cap), dtype=torch.uint8, device=C.device)
+    prm = CalibParams(eps, p, r_override, int(bool(scale_on)), max_iter, tol)
+    k = ctypes.c_int(0)
+    R = ctypes.c_int(0)
+    s = ctypes.c_float(0)
+    E = ctypes.c_double(0)
+    eig = (ctypes.c_double * r_cap)()
+    st = lib().instant_calib_solve(_dev(C, "C"), int(n_samples), L, ctypes.byref(prm),
+                                   _dev(rows_out, "rows_out"), r_cap, dtype_code(rows_out.dtype),
+                                   ctypes.byref(k), ctypes.byref(R), ctypes.byref(s),
+                                   ctypes.byref(E), eig, _dev(ws, "ws"),
+                                   ws.numel() * ws.element_size(), _stream(stream))
+    res = CalibResult(k.value, R.value, s.value, E.value, list(eig))
+    if raise_on_error:
+        check(st, "instant_calib_solve")
+        return res
+    return res, st
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """Sticky device-side status (0 when no bounded wait ran out)."""
+    return int(lib().instant_device_status(int(clear), _stream(stream)))

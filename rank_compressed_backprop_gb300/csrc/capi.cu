@@ -1,0 +1,469 @@
+// capi.cu -- the extern "C" boundary declared in include/instant.h: argument
+// validation, tensor-map encoding, launch planning and the host loop of the
+// calibration solve.  No device memory is allocated here.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+
+#include "instant.h"
+#include "kernels.h"
+
+using namespace instant;
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void instant::count_launches(unsigned int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kTargetCtas = 2 * 152;  // two waves' worth of work on 152 SMs
+
+// ---------------------------------------------------------------------------
+// tensor maps (driver entry point fetched through the runtime; no -lcuda)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 tiled map with the 128-byte swizzle; dims/strides innermost first
+bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn f = encoder();
+  if (!f) return false;
+  cuuint64_t d[5], s[5];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i < rank - 1) s[i] = strides_bytes[i];
+  }
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+instant_status from_cuda(cudaError_t e) { return e == cudaSuccess ? INSTANT_OK : INSTANT_ERR_CUDA; }
+
+bool dtype_ok(instant_dtype dt) { return dt == INSTANT_F32 || dt == INSTANT_BF16; }
+
+bool fault_injected(const char* what) {
+  const char* v = std::getenv("INSTANT_FAULT");
+  return v && std::strcmp(v, what) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// projection (shared by compress_act and project_grad)
+// ---------------------------------------------------------------------------
+instant_status project(const void* t, const void* pq, void* out0, void* out1, int B, int L, int C,
+                       int Rx, int Ry, instant_dtype dt, cudaStream_t st) {
+  ProjectArgs a;
+  a.B = B;
+  a.L = L;
+  a.C = C;
+  a.Rx = Rx;
+  a.Ry = Ry;
+  a.NT = round_up(Rx + Ry, 16);
+  a.nk = cdiv(L, 64);
+  a.pq = pq;
+  a.out0 = out0;
+  a.out1 = out1;
+  if (dt == INSTANT_F32) {
+    a.pq_tma = 0;
+    return from_cuda(launch_project_f32(a, static_cast<const float*>(t), st));
+  }
+  a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
+  if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
+  CUtensorMap mt, mpq;
+  std::memset(&mpq, 0, sizeof(mpq));
+  const uint64_t dt3[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t st3[2] = {static_cast<uint64_t>(C) * 2, static_cast<uint64_t>(L) * C * 2};
+  const uint32_t bx3[3] = {64, 64, 1};
+  if (!make_map(&mt, t, 3, dt3, st3, bx3)) return INSTANT_ERR_CUDA;
+  if (a.pq_tma) {
+    const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Rx + Ry)};
+    const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
+    const uint32_t b2[2] = {64, static_cast<uint32_t>(a.NT)};
+    if (!make_map(&mpq, pq, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+  }
+  return from_cuda(launch_project_bf16(mt, mpq, a, st));
+}
+
+// ---------------------------------------------------------------------------
+// g_hat_x plan: N tile and split-K factor of Sq w
+// ---------------------------------------------------------------------------
+struct GxPlan {
+  int BN, splits, cps, nk;
+};
+
+GxPlan plan_grad_x(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
+  GxPlan p;
+  p.nk = cdiv(Cy, 64);
+  if (dt == INSTANT_F32) {
+    p.BN = 128;
+    p.splits = 1;
+    p.cps = p.nk;
+    return p;
+  }
+  const int M = B * Ry;
+  p.BN = Cx >= 1024 ? 256 : 128;
+  const int tiles = cdiv(M, 128) * cdiv(Cx, p.BN);
+  int s = cdiv(kTargetCtas / 2, tiles);
+  if (s > 8) s = 8;
+  if (s > p.nk) s = p.nk;
+  if (s < 1) s = 1;
+  p.cps = cdiv(p.nk, s);
+  p.splits = cdiv(p.nk, p.cps);
+  return p;
+}
+
+size_t grad_x_ws(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
+  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
+  return static_cast<size_t>(p.splits) * B * Ry * Cx * sizeof(float);
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* instant_status_string(instant_status s) {
+  switch (s) {
+    case INSTANT_OK: return "ok";
+    case INSTANT_ERR_ARG: return "invalid argument";
+    case INSTANT_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case INSTANT_ERR_DTYPE: return "unsupported dtype";
+    case INSTANT_ERR_ALIGN: return "misaligned pointer or row pitch";
+    case INSTANT_ERR_WORKSPACE: return "workspace missing or too small";
+    case INSTANT_ERR_CUDA: return "CUDA error";
+    case INSTANT_ERR_NOT_CONVERGED: return "eigensolver did not converge";
+    case INSTANT_ERR_NONFINITE: return "autocorrelation energy not finite and positive";
+    case INSTANT_ERR_DEVICE: return "a device-side wait ran out of time";
+  }
+  return "unknown status";
+}
+
+int instant_version(void) { return 100; }
+
+unsigned long long instant_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+instant_status instant_compress_act(const void* x, const void* P, void* xhat, int B, int L, int Cx,
+                                    int Rx, instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!x || !P || !xhat) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Rx < 1 || Rx > 64) return INSTANT_ERR_SHAPE;
+  if (dt == INSTANT_BF16 && (!aligned16(x) || !aligned16(xhat) || Cx % 8 != 0))
+    return INSTANT_ERR_ALIGN;
+  return project(x, P, xhat, nullptr, B, L, Cx, Rx, 0, dt, static_cast<cudaStream_t>(stream));
+}
+
+instant_status instant_project_grad(const void* gy, const void* PQ, void* Sx, void* Sq, int B,
+                                    int L, int Cy, int Rx, int Ry, instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!gy || !PQ || !Sx || !Sq) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cy < 1 || Rx < 1 || Ry < 1 || Rx + Ry > 128) return INSTANT_ERR_SHAPE;
+  if (dt == INSTANT_BF16 && (!aligned16(gy) || !aligned16(Sx) || !aligned16(Sq) || Cy % 8 != 0))
+    return INSTANT_ERR_ALIGN;
+  return project(gy, PQ, Sx, Sq, B, L, Cy, Rx, Ry, dt, static_cast<cudaStream_t>(stream));
+}
+
+instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int accumulate, int B,
+                              int Rx, int Cx, int Cy, instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!Sx || !xhat || !gw) return INSTANT_ERR_ARG;
+  if (B < 1 || Rx < 1 || Cx < 1 || Cy < 1) return INSTANT_ERR_SHAPE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmArgs g;
+  g.M = Cy;
+  g.N = Cx;
+  g.K = B * Rx;
+  g.a_mn_major = 1;
+  g.b_mn_major = 1;
+  g.nk = cdiv(g.K, 64);
+  g.splits = 1;
+  g.chunks_per_split = g.nk;
+  g.accumulate = accumulate ? 1 : 0;
+  g.out = gw;
+  if (dt == INSTANT_F32) {
+    g.BN = 128;
+    return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sx),
+                                     static_cast<const float*>(xhat), st));
+  }
+  if (!aligned16(Sx) || !aligned16(xhat) || !aligned16(gw) || Cx % 8 != 0 || Cy % 8 != 0)
+    return INSTANT_ERR_ALIGN;
+  const int tm = cdiv(Cy, 128);
+  g.BN = 64;
+  for (int bn : {256, 128}) {
+    if (tm * cdiv(Cx, bn) >= 148) {
+      g.BN = bn;
+      break;
+    }
+  }
+  CUtensorMap ma, mb;
+  const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.K)};
+  const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
+  const uint32_t ba[2] = {64, 64};
+  const uint64_t db[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(g.K)};
+  const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bb[2] = {64, 64};
+  if (!make_map(&ma, Sx, 2, da, sa, ba) || !make_map(&mb, xhat, 2, db, sb, bb))
+    return INSTANT_ERR_CUDA;
+  return from_cuda(launch_gemm_bf16(ma, mb, g, st));
+}
+
+size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt) {
+  (void)L;
+  if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || !dtype_ok(dt)) return 0;
+  return grad_x_ws(B, Cx, Cy, Ry, dt);
+}
+
+instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes, int B,
+                                   int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!Sq || !w) return INSTANT_ERR_ARG;
+  if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
+  GemmArgs g;
+  g.M = B * Ry;
+  g.N = Cx;
+  g.K = Cy;
+  g.a_mn_major = 0;
+  g.b_mn_major = 1;
+  g.BN = p.BN;
+  g.nk = p.nk;
+  g.splits = p.splits;
+  g.chunks_per_split = p.cps;
+  g.accumulate = 0;
+  g.out = static_cast<float*>(ws);
+  if (dt == INSTANT_F32)
+    return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sq), static_cast<const float*>(w), st));
+  if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
+    return INSTANT_ERR_ALIGN;
+  CUtensorMap ma, mb;
+  const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.M)};
+  const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
+  const uint32_t ba[2] = {64, 128};
+  const uint64_t db[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
+  const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bb[2] = {64, 64};
+  if (!make_map(&ma, Sq, 2, da, sa, ba) || !make_map(&mb, w, 2, db, sb, bb)) return INSTANT_ERR_CUDA;
+  return from_cuda(launch_gemm_bf16(ma, mb, g, st));
+}
+
+instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws_bytes, int B, int L,
+                              int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!Q || !gx) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
+  ExpandArgs e;
+  e.B = B;
+  e.L = L;
+  e.Cx = Cx;
+  e.Ry = Ry;
+  e.KR = round_up(Ry, 16);
+  e.BN = Cx > 128 ? 256 : 128;
+  e.splits = p.splits;
+  e.gxh = static_cast<const float*>(ws);
+  e.Q = Q;
+  e.out = gx;
+  if (dt == INSTANT_F32) return from_cuda(launch_expand_f32(e, st));
+  if (!aligned16(gx) || !aligned16(ws) || Cx % 8 != 0) return INSTANT_ERR_ALIGN;
+  return from_cuda(launch_expand_bf16(e, st));
+}
+
+instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
+                              size_t ws_bytes, int B, int L, int Cx, int Cy, int Ry,
+                              instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!Sq || !w || !Q || !gx) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
+  if (dt == INSTANT_BF16 && (!aligned16(Sq) || !aligned16(w) || !aligned16(gx) || !aligned16(ws) ||
+                             Cx % 8 != 0 || Cy % 8 != 0))
+    return INSTANT_ERR_ALIGN;
+  const instant_status s = instant_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, stream);
+  if (s != INSTANT_OK) return s;
+  return instant_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
+}
+
+instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, int Cdim,
+                                        instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!t || !C) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || L > 8192 || Cdim < 1) return INSTANT_ERR_SHAPE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SyrkArgs s;
+  s.B = B;
+  s.L = L;
+  s.C = Cdim;
+  s.nblk = cdiv(L, 128);
+  s.ntiles = s.nblk * (s.nblk + 1) / 2;
+  s.nkc = cdiv(Cdim, 64);
+  s.Cout = C;
+  if (dt == INSTANT_F32) {
+    s.splits = 1;
+    s.b_per_split = B;
+    return from_cuda(launch_syrk_f32(s, static_cast<const float*>(t), st));
+  }
+  if (!aligned16(t) || !aligned16(C) || Cdim % 8 != 0) return INSTANT_ERR_ALIGN;
+  int splits = cdiv(kTargetCtas, s.ntiles);
+  if (splits > B) splits = B;
+  if (splits < 1) splits = 1;
+  s.b_per_split = cdiv(B, splits);
+  s.splits = cdiv(B, s.b_per_split);
+  CUtensorMap mt;
+  const uint64_t d3[3] = {static_cast<uint64_t>(Cdim), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t s3[2] = {static_cast<uint64_t>(Cdim) * 2, static_cast<uint64_t>(L) * Cdim * 2};
+  const uint32_t b3[3] = {64, 128, 1};
+  if (!make_map(&mt, t, 3, d3, s3, b3)) return INSTANT_ERR_CUDA;
+  return from_cuda(launch_syrk_bf16(mt, s, st));
+}
+
+size_t instant_calib_workspace_bytes(int L, int r_cap) {
+  (void)r_cap;
+  if (L < 1) return 0;
+  return solver_workspace_bytes(L);
+}
+
+instant_status instant_calib_solve(const float* C, long long n_samples, int L,
+                                   const instant_calib_params* prm, void* rows_out, int r_cap,
+                                   instant_dtype dt, int* k_out, int* r_out, float* scale_out,
+                                   double* energy_out, double* eig_out, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!C || !prm || !rows_out || !k_out || !r_out || !scale_out) return INSTANT_ERR_ARG;
+  if (n_samples < 1 || !(prm->eps > 0.0 && prm->eps <= 1.0) || prm->p < 0 || prm->r_override < 0)
+    return INSTANT_ERR_ARG;
+  if (L < 1 || L > 8192 || r_cap < 1 || r_cap > 128 || r_cap > L) return INSTANT_ERR_SHAPE;
+  if (prm->r_override > r_cap) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < solver_workspace_bytes(L)) return INSTANT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return INSTANT_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool noconv = fault_injected("solve_noconv");
+  const int max_iter = noconv ? 1 : (prm->max_iter > 0 ? prm->max_iter : 300);
+  const int max_sweeps = noconv ? 0 : 60;
+  const double tol = prm->tol > 0.0 ? prm->tol : 2e-5;
+  const double inv_n = 1.0 / static_cast<double>(n_samples);
+  const double inv_n2 = inv_n * inv_n;
+  const int out_bf16 = dt == INSTANT_BF16 ? 1 : 0;
+
+  SolverWs w = solver_carve(ws, L);
+  if (launch_solver_energy(C, L, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  SolverResult res;
+  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  const double E = res.energy_sum * inv_n2;
+  if (res.nonfinite || !std::isfinite(E) || !(E > 0.0)) return INSTANT_ERR_NONFINITE;
+
+  instant_status status = INSTANT_OK;
+  int m = L;
+  if (L <= 128) {
+    if (launch_jacobi_full(C, L, inv_n, max_sweeps, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  } else {
+    const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
+    m = round_up(std::max(2 * r_guess, r_guess + 16), 32);
+    if (m < 32) m = 32;
+    if (m > 128) m = 128;
+    bool converged = false;
+    for (;;) {
+      if (launch_subspace_init(L, m, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+      bool grow = false;
+      for (int it = 0; it < max_iter; ++it) {
+        if (launch_subspace_iteration(C, L, m, inv_n, max_sweeps, w, st) != cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if ((it + 1) % 4 != 0 && it != max_iter - 1) continue;
+        if (launch_subspace_check(L, m, prm->eps, prm->p, prm->r_override, tol, inv_n2, w, st) !=
+            cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if (res.converged) {
+          converged = true;
+          break;
+        }
+        if (res.block_short && it >= 15 && m < 128) {
+          grow = true;
+          break;
+        }
+      }
+      if (grow) {
+        m = std::min(128, 2 * m);
+        continue;
+      }
+      break;
+    }
+    if (!converged) status = INSTANT_ERR_NOT_CONVERGED;
+  }
+  if (launch_solver_finalize(L, m, prm->eps, prm->p, prm->r_override, prm->scale_on ? 1 : 0,
+                             rows_out, r_cap, out_bf16, inv_n2, w, st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  if (res.jacobi_failed) status = INSTANT_ERR_NOT_CONVERGED;
+  if (L > 128 && res.R > r_cap) status = INSTANT_ERR_SHAPE;
+  *k_out = res.k;
+  *r_out = res.R < r_cap ? res.R : r_cap;
+  *scale_out = res.scale;
+  if (energy_out) *energy_out = E;
+  if (eig_out)
+    for (int i = 0; i < r_cap; ++i) eig_out[i] = i < m ? res.theta[i] : 0.0;
+  if (L <= 128 && res.R > r_cap && status == INSTANT_OK) status = INSTANT_ERR_SHAPE;
+  return status;
+}
+
+instant_status instant_device_status(int clear, void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  unsigned int total = 0, v = 0;
+  if (read_fault_project(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_gemm(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_expand(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_syrk(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_eig(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  return total ? INSTANT_ERR_DEVICE : INSTANT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,687 @@
+// eig.cu -- calibration solve of INSTANT (page "INSTANT: Compressing Gradients
+// and Activations for Resource-Efficient Training", 关键设计 1 and 2):
+//   C/n = U Sigma U^T (symmetric PSD: the SVD is the eigendecomposition),
+//   E = ||C/n||_F^2, k = min{k : sum_{i<=k} sigma_i^2 >= eps E}, R = k + p,
+//   rows = (sum_{i<=R} sigma_i^2)^(-1/2) U_R^T.
+//
+// Only the top R eigenpairs are needed.  L <= 128: one CTA runs a cyclic
+// (round-robin parallel) Jacobi method on the whole matrix in shared memory.
+// Larger L: block subspace iteration with a Rayleigh-Ritz step every
+// iteration.  Each iteration is five launches:
+//   orth   (1 CTA)  T = D W_G Lambda_G^(-1/2) from the Gram matrix of Z
+//   apply  (grid)   V = Z T                         (orthonormal basis)
+//   cv     (grid)   Y = C V / n,  H += V^T Y
+//   rr     (1 CTA)  H = W Theta W^T  (Jacobi, sorted descending)
+//   ritz   (grid)   U = V W, Z = Y W = C U / n, G += Z^T Z, res_j += |Z_j - theta_j U_j|^2
+// Because U holds Ritz vectors, the columns of Z are nearly orthogonal with
+// norms ~theta_j; normalising them with D before the Gram eigensolve keeps the
+// fp32 orthonormalisation well conditioned.  The energy E is a fp64 sum over
+// C itself (the iteration never sees the spectrum's tail), and the k rule runs
+// in fp64.  Every loop is bounded; a Jacobi solve that hits its sweep cap
+// records that in the result block instead of spinning.
+#include <math.h>
+
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace instant {
+
+namespace {
+
+constexpr int kMaxBlock = 128;
+constexpr int kJacThreads = 512;
+constexpr int kRows = 32;  // rows of the tall matrices per CTA in grid kernels
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// block-wide sum (blockDim.x a multiple of 32, <= 1024); every thread gets it
+__device__ float block_sum_f(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_f(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int i = 0; i < nw; ++i) t += red[i];
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// reset + energy
+// ---------------------------------------------------------------------------
+__global__ void k_solver_reset(SolverResult* r) {
+  double* d = reinterpret_cast<double*>(r);
+  for (int i = threadIdx.x; i < static_cast<int>(sizeof(SolverResult) / sizeof(double)); i += blockDim.x)
+    d[i] = 0.0;
+}
+
+__global__ void k_solver_energy(const float* __restrict__ C, size_t count, SolverResult* r) {
+  double acc = 0.0;
+  int bad = 0;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < count;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float v = C[i];
+    if (!isfinite(v)) bad = 1;
+    acc += static_cast<double>(v) * static_cast<double>(v);
+  }
+  acc = warp_sum_d(acc);
+  __shared__ double red[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = acc;
+  if (bad) r->nonfinite = 1;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += red[i];
+    atomicAdd(&r->energy_sum, t);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// cyclic Jacobi on a symmetric n x n matrix in shared memory (n <= 128).
+// A[i*ld + j]; V accumulates the rotations (starts as the identity).
+// Round-robin ordering: in each of the N-1 rounds (N = n rounded up to even)
+// the N/2 disjoint pairs are rotated together.  Rotation angle as in the
+// classical symmetric 2x2 Schur decomposition (Golub & Van Loan, Matrix
+// Computations, sec. 8.5): tau = (a_qq - a_pp) / (2 a_pq),
+// t = sign(tau) / (|tau| + sqrt(1 + tau^2)), c = 1/sqrt(1 + t^2), s = t c.
+// Returns true when the off-diagonal mass fell below tol * ||A||_F.
+// ---------------------------------------------------------------------------
+__device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int max_sweeps,
+                             float* cs, int* pairs, float* red) {
+  const int N = n + (n & 1);
+  const int half = N / 2;
+  for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
+    const int i = idx / n, j = idx - (idx / n) * n;
+    V[i * ld + j] = (i == j) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  bool converged = false;
+  for (int sweep = 0; sweep <= max_sweeps; ++sweep) {
+    float off = 0.f, tot = 0.f;
+    for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
+      const int i = idx / n, j = idx - (idx / n) * n;
+      const float a = A[i * ld + j];
+      tot += a * a;
+      if (i != j) off += a * a;
+    }
+    off = block_sum_f(off, red);
+    tot = block_sum_f(tot, red);
+    if (off <= tol * tol * tot || tot == 0.f) {
+      converged = true;
+      break;
+    }
+    if (sweep == max_sweeps) break;
+    for (int r = 0; r < N - 1; ++r) {
+      if (threadIdx.x < half) {
+        const int k = threadIdx.x;
+        int p, q;
+        if (k == 0) {
+          p = r;
+          q = N - 1;
+        } else {
+          p = (r + k) % (N - 1);
+          q = (r - k + N - 1) % (N - 1);
+        }
+        if (p > q) {
+          const int t = p;
+          p = q;
+          q = t;
+        }
+        float c = 1.f, s = 0.f;
+        if (q < n) {
+          const float apq = A[p * ld + q];
+          if (fabsf(apq) > 1e-30f) {
+            const float app = A[p * ld + p], aqq = A[q * ld + q];
+            const float tau = (aqq - app) / (2.f * apq);
+            float t;
+            if (fabsf(tau) > 1e18f) {
+              t = 0.5f / tau;
+            } else {
+              t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+            }
+            c = 1.f / sqrtf(1.f + t * t);
+            s = t * c;
+          }
+        }
+        pairs[2 * k] = p;
+        pairs[2 * k + 1] = q;
+        cs[2 * k] = c;
+        cs[2 * k + 1] = s;
+      }
+      __syncthreads();
+      // rows: A <- J^T A
+      for (int idx = threadIdx.x; idx < half * n; idx += blockDim.x) {
+        const int k = idx / n, j = idx - (idx / n) * n;
+        const int p = pairs[2 * k], q = pairs[2 * k + 1];
+        if (q >= n) continue;
+        const float c = cs[2 * k], s = cs[2 * k + 1];
+        if (s == 0.f) continue;
+        const float ap = A[p * ld + j], aq = A[q * ld + j];
+        A[p * ld + j] = c * ap - s * aq;
+        A[q * ld + j] = s * ap + c * aq;
+      }
+      __syncthreads();
+      // columns: A <- A J, V <- V J
+      for (int idx = threadIdx.x; idx < half * n; idx += blockDim.x) {
+        const int k = idx / n, i = idx - (idx / n) * n;
+        const int p = pairs[2 * k], q = pairs[2 * k + 1];
+        if (q >= n) continue;
+        const float c = cs[2 * k], s = cs[2 * k + 1];
+        if (s == 0.f) continue;
+        const float ap = A[i * ld + p], aq = A[i * ld + q];
+        A[i * ld + p] = c * ap - s * aq;
+        A[i * ld + q] = s * ap + c * aq;
+        const float vp = V[i * ld + p], vq = V[i * ld + q];
+        V[i * ld + p] = c * vp - s * vq;
+        V[i * ld + q] = s * vp + c * vq;
+      }
+      __syncthreads();
+    }
+  }
+  __syncthreads();
+  return converged;
+}
+
+// rank of diagonal entry i in descending order (ties: lower index first)
+__device__ __forceinline__ int desc_rank(const float* A, int ld, int n, int i) {
+  const float v = A[i * ld + i];
+  int r = 0;
+  for (int j = 0; j < n; ++j) {
+    const float u = A[j * ld + j];
+    r += (u > v) || (u == v && j < i);
+  }
+  return r;
+}
+
+struct JacSmem {
+  float* A;
+  float* V;
+  float* cs;
+  int* pairs;
+  float* red;
+  int* rank;
+};
+
+__device__ JacSmem jac_carve(uint8_t* smem, int n) {
+  JacSmem s;
+  const int ld = n + 1;
+  s.A = reinterpret_cast<float*>(smem);
+  s.V = s.A + n * ld;
+  s.cs = s.V + n * ld;
+  s.pairs = reinterpret_cast<int*>(s.cs + kMaxBlock + 2);
+  s.red = reinterpret_cast<float*>(s.pairs + kMaxBlock + 2);
+  s.rank = reinterpret_cast<int*>(s.red + 32);
+  return s;
+}
+
+size_t jac_smem_bytes(int n) {
+  const int ld = n + 1;
+  return sizeof(float) * (2 * n * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
+}
+
+// ---------------------------------------------------------------------------
+// full Jacobi (L <= 128): theta (desc) -> res->theta, vectors -> U[:, rank]
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kJacThreads) k_jacobi_full(const float* __restrict__ C, int L,
+                                                             float inv_n, int max_sweeps,
+                                                             SolverWs w) {
+  extern __shared__ uint8_t smem[];
+  JacSmem s = jac_carve(smem, L);
+  const int ld = L + 1;
+  for (int idx = threadIdx.x; idx < L * L; idx += blockDim.x) {
+    const int i = idx / L, j = idx - (idx / L) * L;
+    s.A[i * ld + j] = 0.5f * (C[i * L + j] + C[j * L + i]) * inv_n;
+  }
+  __syncthreads();
+  const bool ok = block_jacobi(s.A, s.V, L, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  for (int i = threadIdx.x; i < L; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, L, i);
+  __syncthreads();
+  for (int i = threadIdx.x; i < L; i += blockDim.x)
+    w.res->theta[s.rank[i]] = static_cast<double>(s.A[i * ld + i]);
+  for (int idx = threadIdx.x; idx < L * L; idx += blockDim.x) {
+    const int row = idx / L, col = idx - (idx / L) * L;
+    w.U[row * L + s.rank[col]] = s.V[row * ld + col];
+  }
+  if (threadIdx.x == 0) {
+    if (!ok) w.res->jacobi_failed = 1;
+    w.res->converged = ok ? 1 : 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// subspace iteration kernels
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float hash_uniform(uint32_t i, uint32_t j) {
+  // integer hash -> [-1, 1): deterministic starting block
+  uint32_t h = i * 0x9E3779B1u ^ (j + 0x7F4A7C15u) * 0x85EBCA77u;
+  h ^= h >> 15;
+  h *= 0x2C1B3C6Du;
+  h ^= h >> 12;
+  h *= 0x297A2D39u;
+  h ^= h >> 15;
+  return static_cast<float>(h) * (2.0f / 4294967296.0f) - 1.0f;
+}
+
+__global__ void k_sub_init(int L, int m, SolverWs w) {
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < L * m; idx += gridDim.x * blockDim.x) {
+    const int i = idx / m, j = idx - (idx / m) * m;
+    w.Z[idx] = hash_uniform(i, j);
+  }
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < m * m; idx += gridDim.x * blockDim.x) {
+    w.G[idx] = 0.f;
+    w.H[idx] = 0.f;
+  }
+}
+
+// G += Z[rows]^T Z[rows]
+__global__ void k_sub_gram(int L, int m, SolverWs w) {
+  extern __shared__ float zs[];  // [kRows][m]
+  const int i0 = blockIdx.x * kRows;
+  const int nr = min(kRows, L - i0);
+  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
+    const int r = idx / m;
+    zs[idx] = r < nr ? w.Z[(i0 + r) * m + (idx - r * m)] : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int a = idx / m, b = idx - (idx / m) * m;
+    if (b < a) continue;
+    float acc = 0.f;
+    for (int r = 0; r < nr; ++r) acc = fmaf(zs[r * m + a], zs[r * m + b], acc);
+    atomicAdd(&w.G[a * m + b], acc);
+    if (a != b) atomicAdd(&w.G[b * m + a], acc);
+  }
+}
+
+// 1 CTA: T = D W_G Lambda^(-1/2) with D = diag(G)^(-1/2); zeroes G
+__global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps, SolverWs w) {
+  extern __shared__ uint8_t smem[];
+  JacSmem s = jac_carve(smem, m);
+  const int ld = m + 1;
+  __shared__ float dsc[kMaxBlock];
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    const float g = w.G[i * m + i];
+    dsc[i] = g > 0.f ? 1.f / sqrtf(g) : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int i = idx / m, j = idx - (idx / m) * m;
+    s.A[i * ld + j] = 0.5f * (w.G[i * m + j] + w.G[j * m + i]) * dsc[i] * dsc[j];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.G[idx] = 0.f;
+  const bool ok = block_jacobi(s.A, s.V, m, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  float lmax = 0.f;
+  for (int j = 0; j < m; ++j) lmax = fmaxf(lmax, s.A[j * ld + j]);
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int a = idx / m, j = idx - (idx / m) * m;
+    const float lam = s.A[j * ld + j];
+    const float f = lam > 1e-10f * lmax ? 1.f / sqrtf(lam) : 0.f;
+    w.T[a * m + j] = dsc[a] * s.V[a * ld + j] * f;
+  }
+  if (threadIdx.x == 0 && !ok) w.res->jacobi_failed = 1;
+}
+
+// out[rows] = in[rows] * M   (M m x m), rows of kRows per CTA
+__global__ void k_sub_apply(const float* __restrict__ in, const float* __restrict__ M, float* out,
+                            int L, int m) {
+  extern __shared__ float sm[];
+  float* Ms = sm;            // [m][m]
+  float* rs = sm + m * m;    // [kRows][m]
+  const int i0 = blockIdx.x * kRows;
+  const int nr = min(kRows, L - i0);
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) Ms[idx] = M[idx];
+  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
+    const int r = idx / m;
+    rs[idx] = r < nr ? in[(i0 + r) * m + (idx - r * m)] : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < nr * m; idx += blockDim.x) {
+    const int r = idx / m, j = idx - (idx / m) * m;
+    float acc = 0.f;
+    for (int k = 0; k < m; ++k) acc = fmaf(rs[r * m + k], Ms[k * m + j], acc);
+    out[(i0 + r) * m + j] = acc;
+  }
+}
+
+// Y[rows] = C[rows, :] V / n ;  H += V[rows]^T Y[rows]
+__global__ void k_sub_cv(const float* __restrict__ C, int L, int m, float inv_n, SolverWs w) {
+  extern __shared__ float sm[];
+  float* cs = sm;                       // [kRows][33]
+  float* vs = cs + kRows * 33;          // [32][m]
+  float* ys = vs + 32 * m;              // [kRows][m]
+  float* vr = ys + kRows * m;           // [kRows][m]  V rows of this block
+  const int i0 = blockIdx.x * kRows;
+  const int nr = min(kRows, L - i0);
+  const int per = (kRows * m + blockDim.x - 1) / blockDim.x;  // outputs per thread (<= 16)
+  float acc[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += 32) {
+    const int nj = min(32, L - j0);
+    for (int idx = threadIdx.x; idx < kRows * 32; idx += blockDim.x) {
+      const int r = idx >> 5, c = idx & 31;
+      cs[r * 33 + c] = (r < nr && c < nj) ? C[static_cast<size_t>(i0 + r) * L + j0 + c] : 0.f;
+    }
+    for (int idx = threadIdx.x; idx < 32 * m; idx += blockDim.x) {
+      const int r = idx / m;
+      vs[idx] = r < nj ? w.V[(j0 + r) * m + (idx - r * m)] : 0.f;
+    }
+    __syncthreads();
+    for (int q = 0; q < per; ++q) {
+      const int o = threadIdx.x + q * blockDim.x;
+      if (o >= kRows * m) break;
+      const int r = o / m, col = o - (o / m) * m;
+      float a = acc[q];
+#pragma unroll 8
+      for (int c = 0; c < 32; ++c) a = fmaf(cs[r * 33 + c], vs[c * m + col], a);
+      acc[q] = a;
+    }
+    __syncthreads();
+  }
+  for (int q = 0; q < per; ++q) {
+    const int o = threadIdx.x + q * blockDim.x;
+    if (o >= kRows * m) break;
+    const int r = o / m, col = o - (o / m) * m;
+    const float y = acc[q] * inv_n;
+    ys[o] = r < nr ? y : 0.f;
+    if (r < nr) w.Y[(i0 + r) * m + col] = y;
+  }
+  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
+    const int r = idx / m;
+    vr[idx] = r < nr ? w.V[(i0 + r) * m + (idx - r * m)] : 0.f;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int a = idx / m, b = idx - (idx / m) * m;
+    float h = 0.f;
+    for (int r = 0; r < nr; ++r) h = fmaf(vr[r * m + a], ys[r * m + b], h);
+    atomicAdd(&w.H[a * m + b], h);
+  }
+}
+
+// 1 CTA: Rayleigh-Ritz on H -> W (columns sorted by descending theta), theta;
+// zeroes H and the residual accumulators
+__global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, SolverWs w) {
+  extern __shared__ uint8_t smem[];
+  JacSmem s = jac_carve(smem, m);
+  const int ld = m + 1;
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int i = idx / m, j = idx - (idx / m) * m;
+    s.A[i * ld + j] = 0.5f * (w.H[i * m + j] + w.H[j * m + i]);
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.H[idx] = 0.f;
+  const bool ok = block_jacobi(s.A, s.V, m, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  for (int i = threadIdx.x; i < m; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, m, i);
+  __syncthreads();
+  for (int i = threadIdx.x; i < m; i += blockDim.x) {
+    w.res->theta[s.rank[i]] = static_cast<double>(s.A[i * ld + i]);
+    w.res->res2[i] = 0.f;
+  }
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int row = idx / m, col = idx - (idx / m) * m;
+    w.W[row * m + s.rank[col]] = s.V[row * ld + col];
+  }
+  if (threadIdx.x == 0 && !ok) w.res->jacobi_failed = 1;
+}
+
+// U = V W, Z = Y W; G += Z^T Z; res2_j += |Z_j - theta_j U_j|^2 over this block's rows
+__global__ void k_sub_ritz(int L, int m, SolverWs w) {
+  extern __shared__ float sm[];
+  float* Ws = sm;                 // [m][m]
+  float* vs = Ws + m * m;         // [kRows][m]
+  float* ys = vs + kRows * m;     // [kRows][m]
+  float* us = ys + kRows * m;     // [kRows][m]
+  float* zs = us + kRows * m;     // [kRows][m]
+  __shared__ float th[kMaxBlock];
+  const int i0 = blockIdx.x * kRows;
+  const int nr = min(kRows, L - i0);
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) Ws[idx] = w.W[idx];
+  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
+    const int r = idx / m, c = idx - (idx / m) * m;
+    vs[idx] = r < nr ? w.V[(i0 + r) * m + c] : 0.f;
+    ys[idx] = r < nr ? w.Y[(i0 + r) * m + c] : 0.f;
+  }
+  for (int j = threadIdx.x; j < m; j += blockDim.x) th[j] = static_cast<float>(w.res->theta[j]);
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
+    const int r = idx / m, j = idx - (idx / m) * m;
+    float u = 0.f, z = 0.f;
+    for (int k = 0; k < m; ++k) {
+      const float wk = Ws[k * m + j];
+      u = fmaf(vs[r * m + k], wk, u);
+      z = fmaf(ys[r * m + k], wk, z);
+    }
+    us[idx] = u;
+    zs[idx] = z;
+    if (r < nr) {
+      w.U[(i0 + r) * m + j] = u;
+      w.Z[(i0 + r) * m + j] = z;
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < m; j += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < nr; ++r) {
+      const float d = zs[r * m + j] - th[j] * us[r * m + j];
+      acc = fmaf(d, d, acc);
+    }
+    atomicAdd(&w.res->res2[j], acc);
+  }
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int a = idx / m, b = idx - (idx / m) * m;
+    if (b < a) continue;
+    float acc = 0.f;
+    for (int r = 0; r < nr; ++r) acc = fmaf(zs[r * m + a], zs[r * m + b], acc);
+    atomicAdd(&w.G[a * m + b], acc);
+    if (a != b) atomicAdd(&w.G[b * m + a], acc);
+  }
+}
+
+// k rule in fp64: smallest k with sum_{i<=k} theta_i^2 >= eps * E; m + 1 if none
+__device__ int k_rule(const double* theta, int m, double target) {
+  double cum = 0.0;
+  for (int i = 0; i < m; ++i) {
+    cum += theta[i] * theta[i];
+    if (cum >= target) return i + 1;
+  }
+  return m + 1;
+}
+
+__global__ void k_sub_check(int L, int m, double eps, int p, int r_override, double tol,
+                            double inv_n2, SolverWs w) {
+  if (threadIdx.x != 0) return;
+  SolverResult* r = w.res;
+  const double E = r->energy_sum * inv_n2;
+  const int k = k_rule(r->theta, m, eps * E);
+  int R = r_override > 0 ? r_override : k + p;
+  if (R > L) R = L;
+  r->k = k;
+  r->R = R;
+  const bool fits = k <= m && R <= m - 1;
+  r->block_short = fits ? 0 : 1;
+  int conv = fits ? 1 : 0;
+  const double th1 = r->theta[0];
+  const double lim = tol * tol * th1 * th1;
+  for (int i = 0; i < R && i < m && conv; ++i)
+    if (!(static_cast<double>(r->res2[i]) <= lim)) conv = 0;
+  r->converged = conv;
+}
+
+__global__ void k_finalize(int L, int m, double eps, int p, int r_override, int scale_on,
+                           void* rows_out, int r_cap, int out_bf16, double inv_n2, SolverWs w) {
+  __shared__ int sR;
+  __shared__ float ss;
+  SolverResult* r = w.res;
+  if (threadIdx.x == 0) {
+    const double E = r->energy_sum * inv_n2;
+    int k = k_rule(r->theta, m, eps * E);
+    if (k > L) k = L;
+    int R = r_override > 0 ? r_override : k + p;
+    if (R > L) R = L;
+    if (R > m) R = m;
+    double cum = 0.0;
+    for (int i = 0; i < R; ++i) cum += r->theta[i] * r->theta[i];
+    const double s = scale_on ? 1.0 / sqrt(cum) : 1.0;
+    r->k = k;
+    r->R = R;
+    r->scale = static_cast<float>(s);
+    sR = R;
+    ss = static_cast<float>(s);
+  }
+  __syncthreads();
+  const int R = sR;
+  const float s = ss;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int i = warp; i < r_cap; i += nw) {
+    float sign = 1.f;
+    if (i < R) {
+      // argmax |u_j| with the lowest index on ties
+      float best = -1.f;
+      int bidx = 0x7fffffff;
+      for (int j = lane; j < L; j += 32) {
+        const float a = fabsf(w.U[j * m + i]);
+        if (a > best || (a == best && j < bidx)) {
+          best = a;
+          bidx = j;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (ob > best || (ob == best && oi < bidx)) {
+          best = ob;
+          bidx = oi;
+        }
+      }
+      sign = w.U[bidx * m + i] < 0.f ? -1.f : 1.f;
+    }
+    for (int j = lane; j < L; j += 32) {
+      const float v = i < R ? s * sign * w.U[j * m + i] : 0.f;
+      if (out_bf16)
+        static_cast<uint16_t*>(rows_out)[static_cast<size_t>(i) * L + j] = bf16_bits(v);
+      else
+        static_cast<float*>(rows_out)[static_cast<size_t>(i) * L + j] = v;
+    }
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+
+size_t solver_workspace_bytes(int L) {
+  const size_t tall = align256(sizeof(float) * static_cast<size_t>(L) * kMaxBlock);
+  const size_t ufull = align256(sizeof(float) * static_cast<size_t>(L) * (L > kMaxBlock ? kMaxBlock : L));
+  const size_t sq = align256(sizeof(float) * kMaxBlock * kMaxBlock);
+  return align256(sizeof(SolverResult)) + 3 * tall + (ufull > tall ? ufull : tall) + 4 * sq;
+}
+
+SolverWs solver_carve(void* ws, int L) {
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  const size_t tall = align256(sizeof(float) * static_cast<size_t>(L) * kMaxBlock);
+  const size_t ufull = align256(sizeof(float) * static_cast<size_t>(L) * (L > kMaxBlock ? kMaxBlock : L));
+  const size_t sq = align256(sizeof(float) * kMaxBlock * kMaxBlock);
+  SolverWs w;
+  w.res = reinterpret_cast<SolverResult*>(p);
+  p += align256(sizeof(SolverResult));
+  w.V = reinterpret_cast<float*>(p); p += tall;
+  w.Y = reinterpret_cast<float*>(p); p += tall;
+  w.Z = reinterpret_cast<float*>(p); p += tall;
+  w.U = reinterpret_cast<float*>(p); p += (ufull > tall ? ufull : tall);
+  w.H = reinterpret_cast<float*>(p); p += sq;
+  w.G = reinterpret_cast<float*>(p); p += sq;
+  w.W = reinterpret_cast<float*>(p); p += sq;
+  w.T = reinterpret_cast<float*>(p);
+  return w;
+}
+
+cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t st) {
+  k_solver_reset<<<1, 256, 0, st>>>(w.res);
+  const size_t count = static_cast<size_t>(L) * L;
+  int blocks = static_cast<int>((count + 255) / 256);
+  if (blocks > 1024) blocks = 1024;
+  k_solver_energy<<<blocks, 256, 0, st>>>(C, count, w.res);
+  count_launches(2);
+  return cudaGetLastError();
+}
+
+static cudaError_t set_smem(const void* f, size_t bytes) {
+  // 200 KB up front for every solver kernel: one attribute call per kernel
+  (void)bytes;
+  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_sweeps, SolverWs w,
+                               cudaStream_t st) {
+  const size_t bytes = jac_smem_bytes(L);
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(k_jacobi_full), bytes);
+  if (e != cudaSuccess) return e;
+  k_jacobi_full<<<1, kJacThreads, bytes, st>>>(C, L, static_cast<float>(inv_n), max_sweeps, w);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st) {
+  k_sub_init<<<64, 256, 0, st>>>(L, m, w);
+  const size_t gb = sizeof(float) * kRows * m;
+  k_sub_gram<<<(L + kRows - 1) / kRows, 256, gb, st>>>(L, m, w);
+  count_launches(2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n, int max_sweeps,
+                                      SolverWs w, cudaStream_t st) {
+  const int nb = (L + kRows - 1) / kRows;
+  const size_t jb = jac_smem_bytes(m);
+  const size_t ab = sizeof(float) * (m * m + kRows * m);
+  const size_t cb = sizeof(float) * (kRows * 33 + 32 * m + 2 * kRows * m);
+  const size_t rb = sizeof(float) * (m * m + 4 * kRows * m);
+  cudaError_t e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_orth), jb)) != cudaSuccess) return e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_rr), jb)) != cudaSuccess) return e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_apply), ab)) != cudaSuccess) return e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_cv), cb)) != cudaSuccess) return e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_ritz), rb)) != cudaSuccess) return e;
+  k_sub_orth<<<1, kJacThreads, jb, st>>>(m, max_sweeps, w);
+  k_sub_apply<<<nb, 256, ab, st>>>(w.Z, w.T, w.V, L, m);
+  k_sub_cv<<<nb, 256, cb, st>>>(C, L, m, static_cast<float>(inv_n), w);
+  k_sub_rr<<<1, kJacThreads, jb, st>>>(m, max_sweeps, w);
+  k_sub_ritz<<<nb, 256, rb, st>>>(L, m, w);
+  count_launches(5);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_subspace_check(int L, int m, double eps, int p, int r_override, double tol,
+                                  double inv_n2, SolverWs w, cudaStream_t st) {
+  k_sub_check<<<1, 32, 0, st>>>(L, m, eps, p, r_override, tol, inv_n2, w);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_override, int scale_on,
+                                   void* rows_out, int r_cap, int out_bf16, double inv_n2,
+                                   SolverWs w, cudaStream_t st) {
+  k_finalize<<<1, 256, 0, st>>>(L, m, eps, p, r_override, scale_on, rows_out, r_cap, out_bf16,
+                                inv_n2, w);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+INSTANT_FAULT_READER(read_fault_eig)
+
+}  // namespace instant

@@ -1,0 +1,143 @@
+// kernels.h -- launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace instant {
+
+// ---------------------------------------------------------------------------
+// projection along the token axis: out_r[b, c] = sum_l PQ[r, l] t[b, l, c]
+// (compress_act with Ry = 0; project_grad with both planes)
+// ---------------------------------------------------------------------------
+struct ProjectArgs {
+  int B, L, C;       // t is [B, L, C]
+  int Rx, Ry;        // rows 0..Rx-1 -> out0, rows Rx..Rx+Ry-1 -> out1
+  int NT;            // MMA N: Rx + Ry rounded up to a multiple of 16
+  int nk;            // ceil(L / 64)
+  int pq_tma;        // 1: PQ tiles arrive by TMA; 0: threads fill all of PQ up front
+  const void* pq;    // [Rx+Ry, L]
+  void* out0;        // [B*Rx, C]
+  void* out1;        // [B*Ry, C] or null
+};
+
+constexpr int kProjectStages = 4;
+size_t project_bf16_smem_bytes(const ProjectArgs& a);
+cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq,
+                                const ProjectArgs& a, cudaStream_t st);
+cudaError_t launch_project_f32(const ProjectArgs& a, const float* t, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// dense GEMM D[M, N] = sum_k A[m, k] B[k, n] with fp32 output
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  int M, N, K;
+  int a_mn_major;    // 1: A stored [K, M]; 0: A stored [M, K]
+  int b_mn_major;    // 1: B stored [K, N]; 0: B stored [N, K]
+  int BN;            // N tile (64, 128 or 256)
+  int nk;            // ceil(K / 64)
+  int splits;        // split-K factor (grid z); partial planes out + s*M*N
+  int chunks_per_split;
+  int accumulate;    // out += D (only with splits == 1)
+  float* out;        // [splits][M][N]
+};
+
+constexpr int kGemmStages = 4;
+size_t gemm_bf16_smem_bytes(const GemmArgs& g);
+cudaError_t launch_gemm_bf16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                             const GemmArgs& g, cudaStream_t st);
+cudaError_t launch_gemm_f32(const GemmArgs& g, const float* A, const float* Bm, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// rank-R expansion: out[b, l, c] = sum_r Q[r, l] * (sum_s gxh[s][b*Ry + r, c])
+// ---------------------------------------------------------------------------
+struct ExpandArgs {
+  int B, L, Cx, Ry;
+  int KR;            // Ry rounded up to a multiple of 16
+  int BN;            // column tile (128 or 256)
+  int splits;        // number of fp32 partial planes in gxh
+  const float* gxh;  // [splits][B*Ry][Cx]
+  const void* Q;     // [Ry, L]
+  void* out;         // [B, L, Cx]
+};
+
+size_t expand_bf16_smem_bytes(const ExpandArgs& e);
+cudaError_t launch_expand_bf16(const ExpandArgs& e, cudaStream_t st);
+cudaError_t launch_expand_f32(const ExpandArgs& e, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// autocorrelation accumulation: Cout[i, j] += sum_b sum_c t[b,i,c] t[b,j,c]
+// ---------------------------------------------------------------------------
+struct SyrkArgs {
+  int B, L, C;
+  int nblk;          // ceil(L / 128)
+  int ntiles;        // nblk * (nblk + 1) / 2 upper-triangle tiles
+  int splits;        // sample splits (grid y)
+  int b_per_split;
+  int nkc;           // ceil(C / 64)
+  float* Cout;       // [L, L]
+};
+
+constexpr int kSyrkStages = 4;
+size_t syrk_bf16_smem_bytes();
+cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st);
+cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// symmetric eigensolver for calibration
+// ---------------------------------------------------------------------------
+struct SolverResult {      // lives at the start of the solver workspace
+  double energy_sum;       // sum_ij C_sum[i,j]^2 (fp64)
+  int nonfinite;           // any non-finite entry in C_sum
+  int converged;           // set by the check step
+  int k, R;
+  float scale;
+  int jacobi_failed;       // a Jacobi solve hit its sweep cap
+  int block_short;         // k + p does not fit the block
+  int pad_;
+  double theta[128];       // Ritz values (descending)
+  float res2[128];         // squared residual norms of the Ritz vectors
+};
+
+struct SolverWs {
+  SolverResult* res;
+  float* V;      // [L, m] orthonormal basis
+  float* Y;      // [L, m] C V
+  float* Z;      // [L, m]
+  float* U;      // [L, m] Ritz vectors  (full path: [L, L] eigenvectors)
+  float* H;      // [m, m]
+  float* G;      // [m, m]
+  float* W;      // [m, m]
+  float* T;      // [m, m]
+};
+
+size_t solver_workspace_bytes(int L);
+SolverWs solver_carve(void* ws, int L);
+
+cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t st);
+// full Jacobi of C/n (L <= 128): eigenvalues -> res->theta, vectors -> U columns
+cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_sweeps, SolverWs w,
+                               cudaStream_t st);
+// subspace iteration building blocks
+cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st);
+cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n, int max_sweeps,
+                                      SolverWs w, cudaStream_t st);
+cudaError_t launch_subspace_check(int L, int m, double eps, int p, int r_override,
+                                  double tol, double inv_n2, SolverWs w, cudaStream_t st);
+// k, R, s and the projector rows from theta and U (sign-canonical)
+cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_override,
+                                   int scale_on, void* rows_out, int r_cap, int out_bf16,
+                                   double inv_n2, SolverWs w, cudaStream_t st);
+
+// host-side count of kernel launches issued by the library
+void count_launches(unsigned int n);
+
+// sticky device status words, one per translation unit
+cudaError_t read_fault_project(unsigned int* out, int clear);
+cudaError_t read_fault_gemm(unsigned int* out, int clear);
+cudaError_t read_fault_expand(unsigned int* out, int clear);
+cudaError_t read_fault_syrk(unsigned int* out, int clear);
+cudaError_t read_fault_eig(unsigned int* out, int clear);
+
+}  // namespace instant

@@ -1,0 +1,119 @@
+"""Per-layer driver of INSTANT low-rank backpropagation for ``y = x w^T``.
+
+Holds the state the method keeps for one linear layer -- the stacked projector
+``[P; Q]``, the calibration statistics and the step counter -- plus the
+preallocated device buffers, and sequences the library calls of one training
+step (page "INSTANT: Compressing Gradients and Activations for
+Resource-Efficient Training", 整体框架: P and Q are recalibrated every N_t
+steps; the forward stores x_hat = P x; the backward uses low-rank products).
+Every arithmetic step runs in the CUDA library; torch only owns memory.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import api
+
+
+class InstantLinear:
+    def __init__(self, w: torch.Tensor, B: int, L: int, Rx: int, Ry: int, *, n_t: int = 100,
+                 eps: float = 0.95, p: int = 2, scale_on: bool = True):
+        if w.dim() != 2 or not w.is_cuda:
+            raise ValueError("w must be a [Cy, Cx] CUDA tensor")
+        self.w = w
+        self.dtype = w.dtype
+        self.Cy, self.Cx = w.shape
+        self.B, self.L, self.Rx, self.Ry = B, L, Rx, Ry
+        self.n_t, self.eps, self.p, self.scale_on = n_t, eps, p, scale_on
+        dev = w.device
+        f32 = torch.float32
+        self.PQ = torch.zeros(Rx + Ry, L, dtype=self.dtype, device=dev)
+        self.C_X = torch.zeros(L, L, dtype=f32, device=dev)
+        self.C_G = torch.zeros(L, L, dtype=f32, device=dev)
+        self.n_x = 0
+        self.n_g = 0
+        self.t = 0
+        self.xhat = torch.empty(B, Rx, self.Cx, dtype=self.dtype, device=dev)
+        self.Sx = torch.empty(B * Rx, self.Cy, dtype=self.dtype, device=dev)
+        self.Sq = torch.empty(B * Ry, self.Cy, dtype=self.dtype, device=dev)
+        self.gw = torch.empty(self.Cy, self.Cx, dtype=f32, device=dev)
+        self.gx = torch.empty(B, L, self.Cx, dtype=self.dtype, device=dev)
+        nbytes = api.grad_x_workspace_bytes(B, L, self.Cx, self.Cy, Ry, self.dtype)
+        self.ws_gx = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        self.ws_cal = torch.empty(api.calib_workspace_bytes(L, max(Rx, Ry)), dtype=torch.uint8,
+                                  device=dev)
+        self.last_calibration = None
+
+    # views of the stacked projector
+    @property
+    def P(self) -> torch.Tensor:
+        return self.PQ[: self.Rx]
+
+    @property
+    def Q(self) -> torch.Tensor:
+        return self.PQ[self.Rx:]
+
+    # ---- the per-step path -------------------------------------------------
+    def compress(self, x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+        """Forward-side activation compression ``x_hat = P x``."""
+        return api.compress_act(x, self.P, self.xhat if out is None else out)
+
+    def backward(self, g_y: torch.Tensor, xhat: torch.Tensor | None = None,
+                 gw: torch.Tensor | None = None, gx: torch.Tensor | None = None,
+                 accumulate: bool = False):
+        """Low-rank backward: returns ``(g_w, g_tilde_x)``."""
+        xhat = self.xhat if xhat is None else xhat
+        gw = self.gw if gw is None else gw
+        gx = self.gx if gx is None else gx
+        B = g_y.shape[0]
+        api.project_grad(g_y, self.PQ, self.Sx, self.Sq, self.Rx, self.Ry)
+        api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
+        api.grad_x(self.Sq, self.w, self.Q, gx, self.ws_gx)
+        return gw, gx
+
+    # ---- calibration --------------------------------------------------------
+    def accumulate(self, x: torch.Tensor | None = None, g_y: torch.Tensor | None = None) -> None:
+        """Adds the autocorrelation statistics of a batch (no batch is stored)."""
+        if x is not None:
+            api.calib_accumulate(x, self.C_X)
+            self.n_x += x.shape[0]
+        if g_y is not None:
+            api.calib_accumulate(g_y, self.C_G)
+            self.n_g += g_y.shape[0]
+
+    def recalibrate(self, r_override: bool = True):
+        """Solves both statistics into ``P`` and ``Q`` and clears them.
+
+        With ``r_override`` the ranks stay at the buffer sizes ``Rx``/``Ry``;
+        ``k`` and ``k + p`` are still reported."""
+        if self.n_x == 0 or self.n_g == 0:
+            raise RuntimeError("recalibrate: no statistics accumulated")
+        rx = api.calib_solve(self.C_X, self.n_x, self.P, eps=self.eps, p=self.p,
+                             r_override=self.Rx if r_override else 0, scale_on=self.scale_on,
+                             ws=self.ws_cal)
+        rg = api.calib_solve(self.C_G, self.n_g, self.Q, eps=self.eps, p=self.p,
+                             r_override=self.Ry if r_override else 0, scale_on=self.scale_on,
+                             ws=self.ws_cal)
+        self.C_X.zero_()
+        self.C_G.zero_()
+        self.n_x = self.n_g = 0
+        self.last_calibration = (rx, rg)
+        return rx, rg
+
+    def step(self, x: torch.Tensor, g_y: torch.Tensor, calib=()):
+        """One training step of the layer on the recalibration schedule.
+
+        Every ``n_t`` steps the statistics of this batch (and of the extra
+        calibration batches ``calib``, pairs ``(x_c, g_c)``) are accumulated
+        and solved; then the activation is compressed and the low-rank
+        backward runs."""
+        if self.t % self.n_t == 0:
+            self.accumulate(x, g_y)
+            for xc, gc in calib:
+                self.accumulate(xc, gc)
+            self.recalibrate()
+        self.compress(x)
+        out = self.backward(g_y)
+        self.t += 1
+        return out

@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every entry point of
+include/instant.h; host-side validation answers without touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "instant.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rank_compressed_backprop_gb300.build import build
+
+    build()
+    from rank_compressed_backprop_gb300._lib import lib
+
+    return lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(instant_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_six_calls():
+    names = declared_functions()
+    for n in ["instant_compress_act", "instant_project_grad", "instant_grad_w",
+              "instant_grad_x", "instant_calib_accumulate", "instant_calib_solve"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_version_and_status_strings(L):
+    assert L.instant_version() == 100
+    for s in range(10):
+        assert L.instant_status_string(s)
+    assert L.instant_status_string(0) == b"ok"
+
+
+def test_validation_without_gpu(L):
+    fake = ctypes.c_void_p(0x1000)   # never dereferenced: validation returns first
+    null = ctypes.c_void_p(0)
+    # bad dtype
+    assert L.instant_compress_act(fake, fake, fake, 1, 8, 8, 4, 7, null) == 3
+    # null pointer
+    assert L.instant_compress_act(null, fake, fake, 1, 8, 8, 4, 1, null) == 1
+    # bad shape: rank out of range
+    assert L.instant_compress_act(fake, fake, fake, 1, 8, 8, 65, 1, null) == 2
+    assert L.instant_project_grad(fake, fake, fake, fake, 1, 8, 8, 100, 100, 1, null) == 2
+    # misaligned bf16 pointer / row pitch not a multiple of 8 elements
+    odd = ctypes.c_void_p(0x1002)
+    assert L.instant_project_grad(odd, fake, fake, fake, 1, 8, 64, 4, 4, 1, null) == 4
+    assert L.instant_project_grad(fake, fake, fake, fake, 1, 8, 60, 4, 4, 1, null) == 4
+    assert L.instant_grad_w(fake, fake, fake, 0, 2, 4, 60, 64, 1, null) == 4
+    # workspace too small
+    need = L.instant_grad_x_workspace_bytes(4, 64, 256, 256, 8, 1)
+    assert need > 0
+    assert L.instant_grad_x(fake, fake, fake, fake, fake, need - 1, 4, 64, 256, 256, 8, 1, null) == 5
+    assert L.instant_calib_accumulate(fake, fake, 1, 9000, 8, 1, null) == 2
+
+
+def test_calib_solve_validation_without_gpu(L):
+    from rank_compressed_backprop_gb300._lib import CalibParams
+
+    fake = ctypes.c_void_p(0x1000)
+    null = ctypes.c_void_p(0)
+    k, R = ctypes.c_int(), ctypes.c_int()
+    s = ctypes.c_float()
+    prm = CalibParams(0.95, 2, 0, 1, 0, 0.0)
+    need = L.instant_calib_workspace_bytes(512, 16)
+    assert need > 0
+    args = lambda n, Lr, rcap, ws_bytes, p=prm: L.instant_calib_solve(  # noqa: E731
+        fake, n, Lr, ctypes.byref(p), fake, rcap, 1, ctypes.byref(k), ctypes.byref(R),
+        ctypes.byref(s), None, None, fake, ws_bytes, null)
+    assert args(0, 512, 16, need) == 1           # no samples
+    assert args(8, 512, 200, need) == 2          # r_cap beyond the block limit
+    assert args(8, 512, 16, need - 1) == 5       # workspace too small
+    bad = CalibParams(1.5, 2, 0, 1, 0, 0.0)
+    assert args(8, 512, 16, need, bad) == 1      # eps out of (0, 1]
+    over = CalibParams(0.95, 2, 32, 1, 0, 0.0)
+    assert args(8, 512, 16, need, over) == 2     # imposed rank beyond r_cap
+
+
+def test_workspace_sizes_follow_the_plan(L):
+    # fp32 never splits K; bf16 split-K planes grow the workspace
+    f32 = L.instant_grad_x_workspace_bytes(1, 64, 64, 64, 4, 0)
+    assert f32 == 1 * 4 * 64 * 4
+    b2 = L.instant_grad_x_workspace_bytes(32, 512, 768, 768, 8, 1)
+    assert b2 % (32 * 8 * 768 * 4) == 0 and b2 >= 32 * 8 * 768 * 4
+
+
+def test_python_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    from rank_compressed_backprop_gb300 import api
+
+    x = torch.zeros(1, 8, 8, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        api.compress_act(x, torch.zeros(4, 8, dtype=torch.bfloat16),
+                         torch.zeros(1, 4, 8, dtype=torch.bfloat16))

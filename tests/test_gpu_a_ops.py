@@ -1,0 +1,134 @@
+"""Per-entry-point parity of the CUDA library against the fp64 oracle.
+
+Shapes span several tiles and a ragged tail in every tiled dimension.  The
+fp32 cases (plain FFMA kernels) run first, then the bf16 tcgen05 kernels.
+"""
+
+import numpy as np
+import pytest
+
+import oracle as O
+from gpu_util import orthonormal_rows, rel, rng, stored, to_dev, to_np, tol, torch_or_skip
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f32", "bf16"]
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return torch_or_skip()
+
+
+def _api():
+    from rank_compressed_backprop_gb300 import api
+
+    return api
+
+
+def _tdt(torch, dtype):
+    return torch.float32 if dtype == "f32" else torch.bfloat16
+
+
+# --------------------------------------------------------------------------
+# compress_act / project_grad
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("B,L,C,Rx", [(1, 64, 64, 4), (3, 200, 392, 8), (2, 49, 448, 8),
+                                      (2, 130, 264, 16), (1, 512, 136, 5)])
+def test_compress_act(torch, dtype, B, L, C, Rx):
+    g = rng(100 + L + C)
+    x = stored(g.standard_normal((B, L, C)), dtype)
+    P = stored(orthonormal_rows(g, Rx, L), dtype)
+    xh = torch.empty(B, Rx, C, dtype=_tdt(torch, dtype), device="cuda")
+    _api().compress_act(to_dev(x), to_dev(P), xh)
+    torch.cuda.synchronize()
+    ref = O.compress_act(x, P)
+    assert rel(to_np(xh), ref) <= tol(dtype)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("B,L,C,Rx,Ry", [(1, 64, 64, 4, 4), (3, 200, 392, 5, 7),
+                                         (2, 49, 448, 8, 8), (2, 300, 256, 16, 16),
+                                         (1, 2048, 264, 16, 16), (2, 96, 128, 24, 40)])
+def test_project_grad(torch, dtype, B, L, C, Rx, Ry):
+    g = rng(200 + L + C + Rx)
+    gy = stored(g.standard_normal((B, L, C)), dtype)
+    PQ = stored(orthonormal_rows(g, Rx + Ry, L), dtype)
+    dt = _tdt(torch, dtype)
+    Sx = torch.empty(B * Rx, C, dtype=dt, device="cuda")
+    Sq = torch.empty(B * Ry, C, dtype=dt, device="cuda")
+    _api().project_grad(to_dev(gy), to_dev(PQ), Sx, Sq, Rx, Ry)
+    torch.cuda.synchronize()
+    rx, rq = O.project_grad(gy, PQ[:Rx], PQ[Rx:])
+    assert rel(to_np(Sx).reshape(B, Rx, C), rx) <= tol(dtype)
+    assert rel(to_np(Sq).reshape(B, Ry, C), rq) <= tol(dtype)
+
+
+# --------------------------------------------------------------------------
+# grad_w
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("B,Rx,Cx,Cy", [(1, 4, 64, 64), (5, 8, 200, 328), (32, 8, 768, 768),
+                                        (3, 16, 520, 136), (1, 3, 72, 48)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_grad_w(torch, dtype, B, Rx, Cx, Cy, accumulate):
+    g = rng(300 + B + Cx + Cy)
+    Sx = stored(g.standard_normal((B * Rx, Cy)), dtype)
+    xh = stored(g.standard_normal((B, Rx, Cx)), dtype)
+    gw0 = g.standard_normal((Cy, Cx)).astype(np.float32)
+    gw = to_dev(gw0) if accumulate else torch.empty(Cy, Cx, dtype=torch.float32, device="cuda")
+    _api().grad_w(to_dev(Sx), to_dev(xh), gw, B, accumulate=accumulate)
+    torch.cuda.synchronize()
+    ref = O.grad_w(O.decode(Sx).reshape(B, Rx, Cy), O.decode(xh))
+    if accumulate:
+        ref = ref + gw0.astype(np.float64)
+    assert rel(to_np(gw), ref) <= (1e-5 if dtype == "f32" else 2e-3)
+
+
+# --------------------------------------------------------------------------
+# grad_x (g_hat_x = Sq w, then the rank-R expansion)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("B,L,Cx,Cy,Ry", [(1, 64, 64, 64, 4), (3, 150, 272, 520, 8),
+                                          (2, 49, 448, 1792, 8), (2, 300, 1024, 256, 16),
+                                          (1, 200, 136, 72, 32), (4, 130, 2056, 64, 16)])
+def test_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
+    api = _api()
+    g = rng(400 + L + Cx + Cy)
+    Sq = stored(g.standard_normal((B * Ry, Cy)), dtype)
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), dtype)
+    Q = stored(orthonormal_rows(g, Ry, L), dtype)
+    dt = _tdt(torch, dtype)
+    gx = torch.empty(B, L, Cx, dtype=dt, device="cuda")
+    ws = torch.empty(max(api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt), 16), dtype=torch.uint8,
+                     device="cuda")
+    api.grad_x(to_dev(Sq), to_dev(w), to_dev(Q), gx, ws)
+    torch.cuda.synchronize()
+    ref = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
+    assert rel(to_np(gx), ref) <= tol(dtype)
+
+
+# --------------------------------------------------------------------------
+# calib_accumulate
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("B,L,C", [(2, 64, 64), (3, 300, 200), (4, 49, 448), (2, 256, 1032),
+                                   (1, 520, 72)])
+def test_calib_accumulate(torch, dtype, B, L, C):
+    g = rng(500 + L + C)
+    t1 = stored(g.standard_normal((B, L, C)), dtype)
+    t2 = stored(g.standard_normal((B + 1, L, C)), dtype)
+    Cd = torch.zeros(L, L, dtype=torch.float32, device="cuda")
+    api = _api()
+    api.calib_accumulate(to_dev(t1), Cd)
+    api.calib_accumulate(to_dev(t2), Cd)
+    torch.cuda.synchronize()
+    ref = O.accumulate_autocorrelation(t2, O.accumulate_autocorrelation(t1))
+    got = to_np(Cd)
+    assert rel(got, ref) <= (1e-5 if dtype == "f32" else 1e-4)
+    assert np.array_equal(got, got.T) or rel(got, got.T) < 1e-6
+
+
+def test_device_status_clean(torch):
+    assert _api().device_status() == 0

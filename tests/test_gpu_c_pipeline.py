@@ -1,0 +1,95 @@
+"""Workload-level parity: calibration from seeded batches and the full
+compress + low-rank backward at the configured sizes.
+
+The oracle calibrates from the same stored bits in fp64; k and R must match
+exactly.  For the backward both sides consume the oracle's projector rounded
+to the stored dtype, so the comparison isolates the per-step path."""
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from gpu_util import rel, stored, to_dev, to_np, tol, torch_or_skip
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return torch_or_skip()
+
+
+def _run_layer(torch, wl, layer, calib_batches):
+    from rank_compressed_backprop_gb300 import api
+
+    li = W.LayerInputs(wl, layer)
+    dt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+    L, B, Rx, Ry = wl.L, wl.B, wl.Rx, wl.Ry
+    Cx, Cy = li.Cx, li.Cy
+    x, gy, w = li.x(), li.g_y(), li.w()
+    # ---- calibration (a6 + a7) on the GPU vs the oracle ----
+    CX = torch.zeros(L, L, dtype=torch.float32, device="cuda")
+    CG = torch.zeros(L, L, dtype=torch.float32, device="cuda")
+    CXr = np.zeros((L, L))
+    CGr = np.zeros((L, L))
+    n = 0
+    for xc, gc in calib_batches(li):
+        api.calib_accumulate(to_dev(xc), CX)
+        api.calib_accumulate(to_dev(gc), CG)
+        CXr = O.accumulate_autocorrelation(xc, CXr)
+        CGr = O.accumulate_autocorrelation(gc, CGr)
+        n += xc.shape[0]
+    assert rel(to_np(CX), CXr) <= 1e-4
+    assert rel(to_np(CG), CGr) <= 1e-4
+    out = {}
+    for name, Cd, Cr, R in (("P", CX, CXr, Rx), ("Q", CG, CGr, Ry)):
+        rows = torch.empty(R, L, dtype=dt, device="cuda")
+        res = api.calib_solve(Cd, n, rows, eps=wl.eps, p=wl.p, r_override=R, scale_on=True)
+        ref = O.calibrate(Cr, n, eps=wl.eps, p=wl.p, r_override=R, scale_on=True)
+        auto = O.calibrate(Cr, n, eps=wl.eps, p=wl.p, scale_on=True)
+        assert res.k == ref["k"] == auto["k"], name
+        assert res.R == R
+        out[name] = (res, ref)
+    # ---- per-step path with the oracle's projector ----
+    Pr = stored(out["P"][1]["rows"], wl.dtype)
+    Qr = stored(out["Q"][1]["rows"], wl.dtype)
+    PQ = np.concatenate([Pr, Qr], axis=0)
+    ref = O.low_rank_backward(x, gy, w, Pr, Qr)
+    xd, gd, wd, PQd = to_dev(x), to_dev(gy), to_dev(w), to_dev(PQ)
+    xhat = torch.empty(B, Rx, Cx, dtype=dt, device="cuda")
+    Sx = torch.empty(B * Rx, Cy, dtype=dt, device="cuda")
+    Sq = torch.empty(B * Ry, Cy, dtype=dt, device="cuda")
+    gw = torch.empty(Cy, Cx, dtype=torch.float32, device="cuda")
+    gx = torch.empty(B, L, Cx, dtype=dt, device="cuda")
+    ws = torch.empty(max(api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt), 16), dtype=torch.uint8,
+                     device="cuda")
+    api.compress_act(xd, PQd[:Rx], xhat)
+    api.project_grad(gd, PQd, Sx, Sq, Rx, Ry)
+    api.grad_w(Sx, xhat, gw, B)
+    api.grad_x(Sq, wd, PQd[Rx:], gx, ws)
+    torch.cuda.synchronize()
+    errs = {"x_hat": rel(to_np(xhat), ref["x_hat"]), "g_w": rel(to_np(gw), ref["g_w"]),
+            "g_x": rel(to_np(gx), ref["g_x"])}
+    for k, v in errs.items():
+        assert v <= tol(wl.dtype), (k, errs)
+    assert api.device_status() == 0
+    return out, errs
+
+
+def test_config1_fp32_single_linear(torch):
+    wl = W.workload(1)
+    out, errs = _run_layer(torch, wl, 0, lambda li: [(li.calib_x(0, 8), li.calib_g(0, 8))])
+    # planted 2^-i spectrum: k = 2 and k + p = 4 = the configured rank
+    assert out["P"][0].k == 2 and out["Q"][0].k == 2
+
+
+def test_config2_bert_block(torch):
+    wl = W.workload(2)
+    _run_layer(torch, wl, 0, lambda li: [(li.calib_x(j, 32), li.calib_g(j, 32)) for j in range(2)])
+
+
+def test_config4_vit_mlp_pair(torch):
+    wl = W.workload(4)
+    for layer in (0, 1):
+        _run_layer(torch, wl, layer, lambda li: [(li.x(), li.g_y())])
