@@ -44,6 +44,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-iters", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--mode", choices=["bench", "kernels"], default="bench",
+                    help="kernels: launch every kernel of the path a few times and exit "
+                         "(the case ncu captures)")
     return ap.parse_args()
 
 
@@ -274,6 +277,14 @@ def run_ours(args):
     for s in sets:
         step_eager(s)
     torch.cuda.synchronize()
+    if args.mode == "kernels":
+        for i in range(3):
+            step_eager(sets[i % NSETS])
+        calibrate(sets[0])
+        torch.cuda.synchronize()
+        if api.device_status() != 0:
+            raise RuntimeError("device status set")
+        return
     launches_per_step = None
     c0 = api.launch_count()
     step_eager(sets[0])
@@ -331,17 +342,28 @@ def run_ours(args):
         "expand": lambda s: api.expand(lay.Q, s["gx"], ws, Cy),
     }
     kus = {}
+    per_graph = 5 * NSETS
     for name, fn in kern.items():
-        for i in range(10):
-            fn(sets[i % NSETS])
+        # a graph of back-to-back launches of this one kernel over the rotating
+        # sets: device time per launch without host launch overhead
+        for i in range(NSETS):
+            fn(sets[i])
+        kg = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(kg, stream=cs):
+                for i in range(per_graph):
+                    fn(sets[i % NSETS])
+        torch.cuda.current_stream().wait_stream(cs)
+        kg.replay()
         torch.cuda.synchronize()
+        reps = max(1, args.kernel_iters // per_graph)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for i in range(args.kernel_iters):
-            fn(sets[i % NSETS])
+        for _ in range(reps):
+            kg.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        kus[name] = a.elapsed_time(b) * 1e3 / args.kernel_iters
+        kus[name] = a.elapsed_time(b) * 1e3 / (reps * per_graph)
     # graph-only backward (no calibration) for context
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)

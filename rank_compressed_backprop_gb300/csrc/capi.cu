@@ -96,12 +96,20 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   a.pq = pq;
   a.out0 = out0;
   a.out1 = out1;
+  a.splits = 1;
   if (dt == INSTANT_F32) {
     a.pq_tma = 0;
     return from_cuda(launch_project_f32(a, static_cast<const float*>(t), st));
   }
   a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
+  // split the token axis over a 2-CTA cluster when that balances the SMs better
+  a.splits = 1;
+  if (a.NT <= 64 && a.nk >= 4) {
+    const int units = cdiv(C, 128) * B;
+    auto eff = [](int u) { return static_cast<double>(u) / (152.0 * cdiv(u, 152)); };
+    if (eff(2 * units) > eff(units) + 0.05) a.splits = 2;
+  }
   CUtensorMap mt, mpq;
   std::memset(&mpq, 0, sizeof(mpq));
   const uint64_t dt3[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
@@ -118,36 +126,38 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
 }
 
 // ---------------------------------------------------------------------------
-// g_hat_x plan: N tile and split-K factor of Sq w
+// GEMM plan: N tile and split-K cluster size for an M x N x K product
 // ---------------------------------------------------------------------------
-struct GxPlan {
+struct GemmPlan {
   int BN, splits, cps, nk;
 };
 
-GxPlan plan_grad_x(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
-  GxPlan p;
-  p.nk = cdiv(Cy, 64);
-  if (dt == INSTANT_F32) {
-    p.BN = 128;
-    p.splits = 1;
-    p.cps = p.nk;
-    return p;
+GemmPlan plan_gemm(int M, int N, int K) {
+  GemmPlan p;
+  p.nk = cdiv(K, 64);
+  const int tm = cdiv(M, 128);
+  p.BN = 64;
+  for (int bn : {256, 128}) {
+    if (tm * cdiv(N, bn) >= 152) {
+      p.BN = bn;
+      break;
+    }
   }
-  const int M = B * Ry;
-  p.BN = Cx >= 1024 ? 256 : 128;
-  const int tiles = cdiv(M, 128) * cdiv(Cx, p.BN);
-  int s = cdiv(kTargetCtas / 2, tiles);
-  if (s > 8) s = 8;
-  if (s > p.nk) s = p.nk;
-  if (s < 1) s = 1;
-  p.cps = cdiv(p.nk, s);
-  p.splits = cdiv(p.nk, p.cps);
+  const int tiles = tm * cdiv(N, p.BN);
+  p.splits = 1;
+  for (int s : {8, 4, 2}) {
+    if (s <= p.nk && tiles * s <= kTargetCtas) {
+      p.splits = s;
+      break;
+    }
+  }
+  p.cps = cdiv(p.nk, p.splits);
   return p;
 }
 
 size_t grad_x_ws(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
-  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
-  return static_cast<size_t>(p.splits) * B * Ry * Cx * sizeof(float);
+  (void)Cy;
+  return static_cast<size_t>(B) * Ry * Cx * (dt == INSTANT_F32 ? sizeof(float) : 2);
 }
 
 }  // namespace
@@ -209,26 +219,24 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   g.K = B * Rx;
   g.a_mn_major = 1;
   g.b_mn_major = 1;
-  g.nk = cdiv(g.K, 64);
-  g.splits = 1;
-  g.chunks_per_split = g.nk;
   g.accumulate = accumulate ? 1 : 0;
+  g.out_bf16 = 0;
   g.out = gw;
   if (dt == INSTANT_F32) {
     g.BN = 128;
+    g.nk = cdiv(g.K, 64);
+    g.splits = 1;
+    g.chunks_per_split = g.nk;
     return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sx),
                                      static_cast<const float*>(xhat), st));
   }
   if (!aligned16(Sx) || !aligned16(xhat) || !aligned16(gw) || Cx % 8 != 0 || Cy % 8 != 0)
     return INSTANT_ERR_ALIGN;
-  const int tm = cdiv(Cy, 128);
-  g.BN = 64;
-  for (int bn : {256, 128}) {
-    if (tm * cdiv(Cx, bn) >= 148) {
-      g.BN = bn;
-      break;
-    }
-  }
+  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
+  g.BN = p.BN;
+  g.nk = p.nk;
+  g.splits = p.splits;
+  g.chunks_per_split = p.cps;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.K)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
@@ -254,23 +262,30 @@ instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size
   if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
   if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
   GemmArgs g;
   g.M = B * Ry;
   g.N = Cx;
   g.K = Cy;
   g.a_mn_major = 0;
   g.b_mn_major = 1;
+  g.accumulate = 0;
+  g.out = ws;
+  if (dt == INSTANT_F32) {
+    g.out_bf16 = 0;
+    g.BN = 128;
+    g.nk = cdiv(g.K, 64);
+    g.splits = 1;
+    g.chunks_per_split = g.nk;
+    return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sq), static_cast<const float*>(w), st));
+  }
+  if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
+    return INSTANT_ERR_ALIGN;
+  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
+  g.out_bf16 = 1;
   g.BN = p.BN;
   g.nk = p.nk;
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
-  g.accumulate = 0;
-  g.out = static_cast<float*>(ws);
-  if (dt == INSTANT_F32)
-    return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sq), static_cast<const float*>(w), st));
-  if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
-    return INSTANT_ERR_ALIGN;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.M)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
@@ -289,21 +304,40 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
   if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
   if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const GxPlan p = plan_grad_x(B, Cx, Cy, Ry, dt);
   ExpandArgs e;
   e.B = B;
   e.L = L;
   e.Cx = Cx;
   e.Ry = Ry;
   e.KR = round_up(Ry, 16);
-  e.BN = Cx > 128 ? 256 : 128;
-  e.splits = p.splits;
-  e.gxh = static_cast<const float*>(ws);
+  e.nlt = cdiv(L, 128);
+  e.gxh = ws;
   e.Q = Q;
   e.out = gx;
+  e.q_tma = 0;
+  e.BN = 128;
   if (dt == INSTANT_F32) return from_cuda(launch_expand_f32(e, st));
   if (!aligned16(gx) || !aligned16(ws) || Cx % 8 != 0) return INSTANT_ERR_ALIGN;
-  return from_cuda(launch_expand_bf16(e, st));
+  // column strip width: keep at least ~1.5 strips per SM
+  e.BN = cdiv(Cx, 128) * B >= 228 ? 128 : 64;
+  e.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
+  CUtensorMap mq, mg, mo;
+  std::memset(&mq, 0, sizeof(mq));
+  if (e.q_tma) {
+    const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
+    const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
+    const uint32_t b2[2] = {64, static_cast<uint32_t>(e.KR)};
+    if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+  }
+  const uint64_t dg[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Ry), static_cast<uint64_t>(B)};
+  const uint64_t sg[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(Ry) * Cx * 2};
+  const uint32_t bg[3] = {64, static_cast<uint32_t>(e.KR), 1};
+  const uint64_t dout[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t sout[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(L) * Cx * 2};
+  const uint32_t bout[3] = {64, 128, 1};
+  if (!make_map(&mg, ws, 3, dg, sg, bg) || !make_map(&mo, gx, 3, dout, sout, bout))
+    return INSTANT_ERR_CUDA;
+  return from_cuda(launch_expand_bf16(mq, mg, mo, e, st));
 }
 
 instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,

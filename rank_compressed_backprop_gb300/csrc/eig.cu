@@ -90,24 +90,31 @@ __global__ void k_solver_energy(const float* __restrict__ C, size_t count, Solve
 
 // ---------------------------------------------------------------------------
 // cyclic Jacobi on a symmetric n x n matrix in shared memory (n <= 128).
-// A[i*ld + j]; V accumulates the rotations (starts as the identity).
-// Round-robin ordering: in each of the N-1 rounds (N = n rounded up to even)
-// the N/2 disjoint pairs are rotated together.  Rotation angle as in the
-// classical symmetric 2x2 Schur decomposition (Golub & Van Loan, Matrix
-// Computations, sec. 8.5): tau = (a_qq - a_pp) / (2 a_pq),
-// t = sign(tau) / (|tau| + sqrt(1 + tau^2)), c = 1/sqrt(1 + t^2), s = t c.
-// Returns true when the off-diagonal mass fell below tol * ||A||_F.
+// A[i*ld + j] with ld >= N = n rounded up to even; an odd n is padded with a
+// zero row/column that never rotates.  V accumulates the rotations.
+// Round-robin ordering: in each of the N-1 rounds the N/2 disjoint pairs are
+// rotated together, and because the pairs are disjoint every 2x2 block
+// A[{p,q},{p',q'}] <- J_k^T A J_k' is updated by one thread with no ordering
+// between blocks (one barrier per round).  Rotation angle as in the classical
+// symmetric 2x2 Schur decomposition (Golub & Van Loan, Matrix Computations,
+// sec. 8.5): tau = (a_qq - a_pp) / (2 a_pq), t = sign(tau) /
+// (|tau| + sqrt(1 + tau^2)), c = 1/sqrt(1 + t^2), s = t c.
+// Stops when the off-diagonal mass falls below tol * ||A||_F, or when it
+// stops shrinking (the fp32 rounding floor) below 1e-4 * ||A||_F; returns
+// false when neither happens within max_sweeps.
 // ---------------------------------------------------------------------------
 __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int max_sweeps,
                              float* cs, int* pairs, float* red) {
   const int N = n + (n & 1);
   const int half = N / 2;
-  for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
-    const int i = idx / n, j = idx - (idx / n) * n;
+  for (int idx = threadIdx.x; idx < N * N; idx += blockDim.x) {
+    const int i = idx / N, j = idx - (idx / N) * N;
     V[i * ld + j] = (i == j) ? 1.f : 0.f;
+    if (i >= n || j >= n) A[i * ld + j] = 0.f;
   }
   __syncthreads();
   bool converged = false;
+  float prev = 0.f;
   for (int sweep = 0; sweep <= max_sweeps; ++sweep) {
     float off = 0.f, tot = 0.f;
     for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
@@ -122,6 +129,11 @@ __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int m
       converged = true;
       break;
     }
+    if (sweep >= 3 && off > 0.25f * prev && off <= 1e-8f * tot) {
+      converged = true;  // stagnating at the rounding floor
+      break;
+    }
+    prev = off;
     if (sweep == max_sweeps) break;
     for (int r = 0; r < N - 1; ++r) {
       if (threadIdx.x < half) {
@@ -140,20 +152,18 @@ __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int m
           q = t;
         }
         float c = 1.f, s = 0.f;
-        if (q < n) {
-          const float apq = A[p * ld + q];
-          if (fabsf(apq) > 1e-30f) {
-            const float app = A[p * ld + p], aqq = A[q * ld + q];
-            const float tau = (aqq - app) / (2.f * apq);
-            float t;
-            if (fabsf(tau) > 1e18f) {
-              t = 0.5f / tau;
-            } else {
-              t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
-            }
-            c = 1.f / sqrtf(1.f + t * t);
-            s = t * c;
+        const float apq = A[p * ld + q];
+        if (fabsf(apq) > 1e-30f) {
+          const float app = A[p * ld + p], aqq = A[q * ld + q];
+          const float tau = (aqq - app) / (2.f * apq);
+          float t;
+          if (fabsf(tau) > 1e18f) {
+            t = 0.5f / tau;
+          } else {
+            t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
           }
+          c = 1.f / sqrtf(1.f + t * t);
+          s = t * c;
         }
         pairs[2 * k] = p;
         pairs[2 * k + 1] = q;
@@ -161,28 +171,29 @@ __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int m
         cs[2 * k + 1] = s;
       }
       __syncthreads();
-      // rows: A <- J^T A
-      for (int idx = threadIdx.x; idx < half * n; idx += blockDim.x) {
-        const int k = idx / n, j = idx - (idx / n) * n;
+      // A <- J^T A J, one 2x2 block per work item
+      for (int idx = threadIdx.x; idx < half * half; idx += blockDim.x) {
+        const int k = idx / half, k2 = idx - (idx / half) * half;
         const int p = pairs[2 * k], q = pairs[2 * k + 1];
-        if (q >= n) continue;
-        const float c = cs[2 * k], s = cs[2 * k + 1];
-        if (s == 0.f) continue;
-        const float ap = A[p * ld + j], aq = A[q * ld + j];
-        A[p * ld + j] = c * ap - s * aq;
-        A[q * ld + j] = s * ap + c * aq;
+        const int p2 = pairs[2 * k2], q2 = pairs[2 * k2 + 1];
+        const float c1 = cs[2 * k], s1 = cs[2 * k + 1];
+        const float c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
+        if (s1 == 0.f && s2 == 0.f) continue;
+        const float a = A[p * ld + p2], b = A[p * ld + q2];
+        const float c = A[q * ld + p2], d = A[q * ld + q2];
+        const float y00 = c1 * a - s1 * c, y01 = c1 * b - s1 * d;
+        const float y10 = s1 * a + c1 * c, y11 = s1 * b + c1 * d;
+        A[p * ld + p2] = c2 * y00 - s2 * y01;
+        A[p * ld + q2] = s2 * y00 + c2 * y01;
+        A[q * ld + p2] = c2 * y10 - s2 * y11;
+        A[q * ld + q2] = s2 * y10 + c2 * y11;
       }
-      __syncthreads();
-      // columns: A <- A J, V <- V J
-      for (int idx = threadIdx.x; idx < half * n; idx += blockDim.x) {
-        const int k = idx / n, i = idx - (idx / n) * n;
-        const int p = pairs[2 * k], q = pairs[2 * k + 1];
-        if (q >= n) continue;
+      // V <- V J
+      for (int idx = threadIdx.x; idx < N * half; idx += blockDim.x) {
+        const int k = idx / N, i = idx - (idx / N) * N;
         const float c = cs[2 * k], s = cs[2 * k + 1];
         if (s == 0.f) continue;
-        const float ap = A[i * ld + p], aq = A[i * ld + q];
-        A[i * ld + p] = c * ap - s * aq;
-        A[i * ld + q] = s * ap + c * aq;
+        const int p = pairs[2 * k], q = pairs[2 * k + 1];
         const float vp = V[i * ld + p], vq = V[i * ld + q];
         V[i * ld + p] = c * vp - s * vq;
         V[i * ld + q] = s * vp + c * vq;
@@ -217,8 +228,9 @@ struct JacSmem {
 __device__ JacSmem jac_carve(uint8_t* smem, int n) {
   JacSmem s;
   const int ld = n + 1;
+  const int N = n + (n & 1);
   s.A = reinterpret_cast<float*>(smem);
-  s.V = s.A + n * ld;
+  s.V = s.A + N * ld;
   s.cs = s.V + n * ld;
   s.pairs = reinterpret_cast<int*>(s.cs + kMaxBlock + 2);
   s.red = reinterpret_cast<float*>(s.pairs + kMaxBlock + 2);
@@ -228,7 +240,8 @@ __device__ JacSmem jac_carve(uint8_t* smem, int n) {
 
 size_t jac_smem_bytes(int n) {
   const int ld = n + 1;
-  return sizeof(float) * (2 * n * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
+  const int N = n + (n & 1);
+  return sizeof(float) * (2 * N * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
 }
 
 // ---------------------------------------------------------------------------
@@ -305,16 +318,23 @@ __global__ void k_sub_gram(int L, int m, SolverWs w) {
   }
 }
 
-// 1 CTA: T = D W_G Lambda^(-1/2) with D = diag(G)^(-1/2); zeroes G
+// 1 CTA: T with Z T orthonormal, from the Gram matrix G = Z^T Z; zeroes G.
+// Columns are first normalised (D = diag(G)^(-1/2)); the normalised Gram
+// matrix of near-orthogonal Ritz directions is close to I, so a Cholesky
+// factorisation D G D = L L^T is stable and T = D L^(-T).  When a pivot
+// vanishes (Z rank deficient) the symmetric (Lowdin) form T = D W Lambda^(-1/2)
+// from a Jacobi eigensolve is used instead; it zeroes the null directions.
 __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps, SolverWs w) {
   extern __shared__ uint8_t smem[];
   JacSmem s = jac_carve(smem, m);
   const int ld = m + 1;
   __shared__ float dsc[kMaxBlock];
+  __shared__ int deficient;
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
     const float g = w.G[i * m + i];
     dsc[i] = g > 0.f ? 1.f / sqrtf(g) : 0.f;
   }
+  if (threadIdx.x == 0) deficient = 0;
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
     const int i = idx / m, j = idx - (idx / m) * m;
@@ -322,7 +342,50 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.G[idx] = 0.f;
-  const bool ok = block_jacobi(s.A, s.V, m, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  // ---- Cholesky (lower, in V so that A survives for the fallback) ----
+  float* Lc = s.V;
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+    const int i = idx / m, j = idx - (idx / m) * m;
+    Lc[i * ld + j] = j <= i ? s.A[i * ld + j] : 0.f;
+  }
+  __syncthreads();
+  for (int k = 0; k < m; ++k) {
+    if (threadIdx.x == 0) {
+      const float d = Lc[k * ld + k];
+      if (!(d > 1e-6f)) deficient = 1;
+      Lc[k * ld + k] = d > 1e-6f ? sqrtf(d) : 1.f;
+    }
+    __syncthreads();
+    const float piv = Lc[k * ld + k];
+    for (int i = k + 1 + threadIdx.x; i < m; i += blockDim.x) Lc[i * ld + k] /= piv;
+    __syncthreads();
+    const int rem = m - k - 1;
+    for (int idx = threadIdx.x; idx < rem * rem; idx += blockDim.x) {
+      const int i = k + 1 + idx / rem, j = k + 1 + idx % rem;
+      if (j <= i) Lc[i * ld + j] -= Lc[i * ld + k] * Lc[j * ld + k];
+    }
+    __syncthreads();
+  }
+  if (!deficient) {
+    // T = D L^-T.  s.A is free now: X = L^-1 by forward substitution, one
+    // thread per column j (each thread reads only the entries it wrote)
+    for (int j = threadIdx.x; j < m; j += blockDim.x) {
+      for (int i = 0; i < m; ++i) {
+        float acc = i == j ? 1.f : 0.f;
+        for (int k = j; k < i; ++k) acc -= Lc[i * ld + k] * s.A[k * ld + j];
+        s.A[i * ld + j] = i < j ? 0.f : acc / Lc[i * ld + i];
+      }
+    }
+    __syncthreads();
+    // T[a][c] = D_a * (L^-T)[a][c] = D_a * X[c][a]
+    for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+      const int a = idx / m, c = idx - (idx / m) * m;
+      w.T[a * m + c] = dsc[a] * s.A[c * ld + a];
+    }
+    return;
+  }
+  // ---- fallback: symmetric orthonormalisation (A still holds D G D) ----
+  const bool ok = block_jacobi(s.A, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
   float lmax = 0.f;
   for (int j = 0; j < m; ++j) lmax = fmaxf(lmax, s.A[j * ld + j]);
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
@@ -424,7 +487,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, S
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.H[idx] = 0.f;
-  const bool ok = block_jacobi(s.A, s.V, m, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  const bool ok = block_jacobi(s.A, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
   for (int i = threadIdx.x; i < m; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, m, i);
   __syncthreads();
   for (int i = threadIdx.x; i < m; i += blockDim.x) {

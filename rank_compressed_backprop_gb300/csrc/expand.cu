@@ -5,12 +5,20 @@
 // The step writes the full [B, L, Cx] gradient while reading only Q and the
 // small g_hat_x, so it is bound by HBM writes.  With 2*Ry flops per output
 // element the FFMA pipes cannot keep up with the write stream at Ry >= 8, so
-// the contraction runs on the tensor cores: one CTA computes a 128-token x BN
-// tile as a single K = Ry (padded to 16) tcgen05 MMA.  Both operands are tiny
-// and are built by the threads directly in the K-major 128-byte-swizzle layout
-// (Q^T from Q, g_hat_x by summing the split-K partial planes of the previous
-// GEMM and rounding to bf16).  The epilogue converts the fp32 TMEM tile to bf16
-// and writes 32-byte runs per row.
+// the contraction runs on the tensor cores.
+//
+// One CTA owns one (sample, BN-column) strip of the output and walks its
+// 128-token tiles:
+//   warp 0  TMA producer: the strip's g_hat_x block once (MN-major B operand),
+//           then Q^T tiles (MN-major A operand, read straight from Q [Ry, L])
+//           through a 4-stage ring;
+//   warp 1  MMA issuer: one K = Ry (padded to 16) tcgen05 MMA chain per tile
+//           into one of two TMEM accumulators (double buffered);
+//   warps 2-5  epilogue: TMEM -> bf16 -> 128-byte-swizzled staging tile ->
+//           TMA bulk store, two staging buffers in flight, so the MMA of tile
+//           t+1 and the store of tile t overlap.
+// Full 128-byte lines leave the SM through the TMA engine; rows past L are
+// clipped by the tensor map.
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -19,103 +27,193 @@ namespace instant {
 namespace {
 
 constexpr int BM = 128;
+constexpr int BOX = BM * 128;  // one staging box: 128 rows x 64 bf16
+
+struct Lay {
+  uint32_t stg, b, a, bar, a_stage, b_bytes, total;
+};
+
+__host__ __device__ inline Lay expand_layout(int BN, int KR) {
+  Lay l;
+  l.stg = 0;
+  l.b = 2 * (BN / 64) * BOX;
+  l.b_bytes = (BN / 64) * KR * 128;
+  l.a = l.b + l.b_bytes;
+  l.a_stage = 2 * KR * 128;
+  l.bar = l.a + kExpandStages * l.a_stage;
+  l.total = l.bar + 256;
+  return l;
+}
 
 template <int BN>
-__global__ void __launch_bounds__(128, 1) k_expand_bf16(ExpandArgs e) {
+__global__ void __launch_bounds__(192, 1)
+    k_expand_bf16(const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_g,
+                  const __grid_constant__ CUtensorMap tmap_out, ExpandArgs e) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                       // [128 tokens][128 B]: Q^T, K-major
-  uint8_t* sB = smem + BM * 128;            // [BN cols][128 B]: g_hat_x^T, K-major
-  uint64_t* done = reinterpret_cast<uint64_t*>(sB + BN * 128);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const Lay lay = expand_layout(BN, e.KR);
+  uint8_t* stg = smem + lay.stg;
+  uint8_t* sB = smem + lay.b;
+  uint8_t* sA = smem + lay.a;
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + lay.bar);
+  uint64_t* a_empty = a_full + kExpandStages;
+  uint64_t* b_full = a_empty + kExpandStages;
+  uint64_t* t_full = b_full + 1;
+  uint64_t* t_empty = t_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int l0 = blockIdx.y * BM;
-  const int b = blockIdx.z;
+  const int b = blockIdx.y;
+  const int KR = e.KR;
 
   if (threadIdx.x == 0) {
-    mbar_init(done, 1);
+    for (int s = 0; s < kExpandStages; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    mbar_init(b_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&t_full[i], 1);
+      mbar_init(&t_empty[i], 1);
+    }
     fence_barrier_init();
+    if (e.q_tma) prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_g);
+    prefetch_tmap(&tmap_out);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, 2 * BN);
     tmem_relinquish();
   }
-
-  // A[m, k] = Q[k, l0 + m]  (zero past Ry or past L)
-  const uint16_t* Q = static_cast<const uint16_t*>(e.Q);
-  for (int idx = threadIdx.x; idx < e.KR * BM; idx += blockDim.x) {
-    const int k = idx / BM;
-    const int m = idx - k * BM;
-    const int l = l0 + m;
-    const uint16_t v = (k < e.Ry && l < e.L) ? Q[static_cast<size_t>(k) * e.L + l] : 0;
-    *reinterpret_cast<uint16_t*>(sA + sw128_offset(m, k)) = v;
-  }
-  // B[n, k] = sum_s gxh[s][b*Ry + k, n0 + n]  (zero past Ry or past Cx)
-  const size_t plane = static_cast<size_t>(e.B) * e.Ry * e.Cx;
-  for (int idx = threadIdx.x; idx < e.KR * BN; idx += blockDim.x) {
-    const int k = idx / BN;
-    const int n = idx - k * BN;
-    const int c = n0 + n;
-    float acc = 0.f;
-    if (k < e.Ry && c < e.Cx) {
-      const float* src = e.gxh + (static_cast<size_t>(b) * e.Ry + k) * e.Cx + c;
-      for (int s = 0; s < e.splits; ++s) acc += src[s * plane];
-    }
-    *reinterpret_cast<uint16_t*>(sB + sw128_offset(n, k)) = bf16_bits(acc);
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, BN, 0, 0);
-    const uint32_t a_base = smem_u32(sA);
-    const uint32_t b_base = smem_u32(sB);
-    for (int kk = 0; kk < e.KR / 16; ++kk) {
-      const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-      const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-      umma_bf16(tmem, ad, bd, idesc, kk != 0);
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(b_full, lay.b_bytes);
+      for (int h = 0; h < BN / 64; ++h)
+        tma_load_3d(sB + h * KR * 128, &tmap_g, b_full, n0 + 64 * h, 0, b);
     }
-    umma_commit(done);
-  }
-  __syncwarp();
-  if (!mbar_wait(done, 0)) raise_fault(FAULT_WAIT_DONE);
-  tc_fence_after();
-
-  const int l = l0 + warp * 32 + lane;
-  const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  uint16_t* orow = static_cast<uint16_t*>(e.out) + (static_cast<size_t>(b) * e.L + l) * e.Cx;
+    const uint16_t* Q = static_cast<const uint16_t*>(e.Q);
+    int issued = 0;
+    for (int lt = 0; lt < e.nlt; ++lt) {
+      const int s = lt % kExpandStages;
+      bool ok = true;
+      if (lane == 0 && lt >= kExpandStages &&
+          !mbar_wait(&a_empty[s], ((lt / kExpandStages) - 1) & 1)) {
+        raise_fault(FAULT_WAIT_EMPTY);
+        ok = false;
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      uint8_t* dst = sA + s * lay.a_stage;
+      const int l0 = lt * BM;
+      if (e.q_tma) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&a_full[s], lay.a_stage);
+          tma_load_2d(dst, &tmap_q, &a_full[s], l0, 0);
+          tma_load_2d(dst + KR * 128, &tmap_q, &a_full[s], l0 + 64, 0);
+        }
+      } else {
+        // A[k][l] MN-major: two 64-token atoms, KR rows of 128 B each
+        for (int idx = lane; idx < KR * BM; idx += 32) {
+          const int r = idx / BM;
+          const int ll = idx - r * BM;
+          const int l = l0 + ll;
+          const uint16_t v = (r < e.Ry && l < e.L) ? Q[static_cast<size_t>(r) * e.L + l] : 0;
+          *reinterpret_cast<uint16_t*>(dst + (ll >> 6) * KR * 128 + sw128_offset(r, ll & 63)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[s]);
+      }
+      ++issued;
+    }
+    if (lane == 0) {
+      for (int lt = issued - kExpandStages < 0 ? 0 : issued - kExpandStages; lt < issued; ++lt)
+        if (!mbar_wait(&a_full[lt % kExpandStages], (lt / kExpandStages) & 1))
+          raise_fault(FAULT_WAIT_FULL);
+      if (!mbar_wait(b_full, 0)) raise_fault(FAULT_WAIT_FULL);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, /*a_mn=*/1, /*b_mn=*/1);
+      bool ok = mbar_wait(b_full, 0);
+      if (!ok) raise_fault(FAULT_WAIT_FULL);
+      const uint32_t b_base = smem_u32(sB);
+      for (int lt = 0; ok && lt < e.nlt; ++lt) {
+        const int s = lt % kExpandStages;
+        const int buf = lt & 1;
+        if (lt >= 2 && !mbar_wait(&t_empty[buf], ((lt >> 1) - 1) & 1)) {
+          raise_fault(FAULT_WAIT_EMPTY);
+          break;
+        }
+        if (!mbar_wait(&a_full[s], (lt / kExpandStages) & 1)) {
+          raise_fault(FAULT_WAIT_FULL);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sA + s * lay.a_stage);
+        for (int kk = 0; kk < KR / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(a_base + kk * 2048, KR * 128, 1024);
+          const uint64_t bd = sdesc_sw128(b_base + kk * 2048, KR * 128, 1024);
+          umma_bf16(tmem + buf * BN, ad, bd, idesc, kk != 0);
+        }
+        umma_commit(&a_empty[s]);
+        umma_commit(&t_full[buf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int et = threadIdx.x - 64;       // 0..127
+    const int quarter = warp & 3;          // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;   // token row within the tile
+    for (int lt = 0; lt < e.nlt; ++lt) {
+      const int buf = lt & 1;
+      uint8_t* st = stg + buf * (BN / 64) * BOX;
+      if (et == 0 && lt >= 2) tma_store_wait_read<1>();
+      named_barrier(1, 128);
+      if (!mbar_wait(&t_full[buf], (lt >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
+      tc_fence_after();
+      const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-  for (int j0 = 0; j0 < BN; j0 += 16) {
-    float v[16];
-    tmem_ld16(taddr + j0, v);
-    const int c = n0 + j0;
-    if (l < e.L) {
-      if (c + 16 <= e.Cx) {
+      for (int j0 = 0; j0 < BN; j0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + j0, v);
         uint32_t p[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
                  (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-        dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-        dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (c + q < e.Cx) orow[c + q] = bf16_bits(v[q]);
+        uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
+        const int c8 = (j0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(box + ((c8 ^ (row & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<uint4*>(box + (((c8 + 1) ^ (row & 7)) << 4)) =
+            make_uint4(p[4], p[5], p[6], p[7]);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (et == 0) {
+        mbar_arrive(&t_empty[buf]);
+        for (int h = 0; h < BN / 64; ++h)
+          if (n0 + 64 * h < e.Cx) tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, lt * BM, b);
+        tma_store_commit();
       }
     }
+    if (et == 0) tma_store_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, BN);
+  if (warp == 0) tmem_dealloc(tmem, 2 * BN);
 }
 
 // fp32 path: one thread per output element.
@@ -125,44 +223,42 @@ __global__ void k_expand_f32(ExpandArgs e) {
   const int b = blockIdx.z;
   if (c >= e.Cx) return;
   const float* Q = static_cast<const float*>(e.Q);
-  const size_t plane = static_cast<size_t>(e.B) * e.Ry * e.Cx;
+  const float* g = static_cast<const float*>(e.gxh);
   float acc = 0.f;
-  for (int r = 0; r < e.Ry; ++r) {
-    const float* src = e.gxh + (static_cast<size_t>(b) * e.Ry + r) * e.Cx + c;
-    float g = 0.f;
-    for (int s = 0; s < e.splits; ++s) g += src[s * plane];
-    acc = fmaf(Q[static_cast<size_t>(r) * e.L + l], g, acc);
-  }
+  for (int r = 0; r < e.Ry; ++r)
+    acc = fmaf(Q[static_cast<size_t>(r) * e.L + l], g[(static_cast<size_t>(b) * e.Ry + r) * e.Cx + c],
+               acc);
   static_cast<float*>(e.out)[(static_cast<size_t>(b) * e.L + l) * e.Cx + c] = acc;
 }
 
 template <int BN>
-cudaError_t launch_bn(const ExpandArgs& e, cudaStream_t st) {
+cudaError_t launch_bn(const CUtensorMap& tq, const CUtensorMap& tg, const CUtensorMap& to,
+                      const ExpandArgs& e, cudaStream_t st) {
   const size_t bytes = expand_bf16_smem_bytes(e);
   static size_t configured_ = 0;
   if (bytes > configured_) {
     cudaError_t err = cudaFuncSetAttribute(k_expand_bf16<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(bytes));
     if (err != cudaSuccess) return err;
     configured_ = bytes;
   }
-  dim3 grid((e.Cx + BN - 1) / BN, (e.L + BM - 1) / BM, e.B);
-  k_expand_bf16<BN><<<grid, 128, bytes, st>>>(e);
+  dim3 grid((e.Cx + BN - 1) / BN, e.B);
+  k_expand_bf16<BN><<<grid, 192, bytes, st>>>(tq, tg, to, e);
   count_launches(1);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t expand_bf16_smem_bytes(const ExpandArgs& e) {
-  return BM * 128 + static_cast<size_t>(e.BN) * 128 + 64 + 1024;
-}
+size_t expand_bf16_smem_bytes(const ExpandArgs& e) { return expand_layout(e.BN, e.KR).total + 1024; }
 
-cudaError_t launch_expand_bf16(const ExpandArgs& e, cudaStream_t st) {
+cudaError_t launch_expand_bf16(const CUtensorMap& tmap_q, const CUtensorMap& tmap_g,
+                               const CUtensorMap& tmap_out, const ExpandArgs& e, cudaStream_t st) {
   switch (e.BN) {
-    case 128: return launch_bn<128>(e, st);
-    case 256: return launch_bn<256>(e, st);
+    case 64: return launch_bn<64>(tmap_q, tmap_g, tmap_out, e, st);
+    case 128: return launch_bn<128>(tmap_q, tmap_g, tmap_out, e, st);
+    case 256: return launch_bn<256>(tmap_q, tmap_g, tmap_out, e, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -8,9 +8,12 @@
 // operands stream through a 4-stage TMA/mbarrier ring; either operand may be
 // K-major or MN-major (Sx, x_hat and w are contracted over their row index,
 // so they are MN-major operands read straight from their natural layout).
-// One elected thread issues the MMAs; all four warps run the epilogue, which
-// writes (or accumulates into) fp32 rows with 16-byte stores.  Split-K over
-// grid z writes separate fp32 partial planes that the consumer sums.
+// One elected thread issues the MMAs.  These products are small (a few MB), so
+// the grid is widened by splitting K across the CTAs of a thread-block
+// cluster: every CTA parks its fp32 partial tile in its own shared memory, and
+// after a cluster barrier each CTA sums a 128/S-row slice of the tile over
+// all S partials through distributed shared memory and writes it with
+// coalesced stores (fp32, fp32 accumulate, or bf16).  No global scratch.
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -22,7 +25,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 
-__host__ __device__ inline uint32_t b_bytes(int BN) { return BN * BK * 2; }
+__host__ __device__ inline uint32_t stage_bytes(int BN) { return A_BYTES + BN * BK * 2; }
 
 template <int BN, int A_MN, int B_MN>
 __global__ void __launch_bounds__(128, 1)
@@ -32,8 +35,13 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr uint32_t STAGE = A_BYTES + BN * BK * 2;
+  constexpr int RED_LD = BN + 4;  // fp32 reduction tile row pitch (bank spread)
+  constexpr uint32_t RING = kGemmStages * STAGE;
+  constexpr uint32_t REDB = BM * RED_LD * 4;
+  constexpr uint32_t BAR_OFF = RING > REDB ? RING : REDB;
   uint8_t* sbase = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kGemmStages * STAGE);
+  float* red = reinterpret_cast<float*>(smem);  // reuses the stages after the K loop
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   uint64_t* empty = full + kGemmStages;
   uint64_t* done = empty + kGemmStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
@@ -42,7 +50,7 @@ __global__ void __launch_bounds__(128, 1)
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
   const int m0 = blockIdx.y * BM;
-  const int split = blockIdx.z;
+  const int split = blockIdx.z;  // == rank in the cluster (cluster dims 1 x 1 x splits)
   const int kc_begin = split * g.chunks_per_split;
   int kc_end = kc_begin + g.chunks_per_split;
   if (kc_end > g.nk) kc_end = g.nk;
@@ -125,45 +133,71 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncwarp();
 
-  // ---------------- epilogue: TMEM -> fp32 rows ----------------
+  // ---------------- epilogue 1: TMEM -> fp32 partial tile in shared memory ----------------
   const bool have = nkc > 0;
   if (have && !mbar_wait(done, 0)) raise_fault(FAULT_WAIT_DONE);
   tc_fence_after();
-  const int m = m0 + warp * 32 + lane;
-  const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  float* out = g.out + static_cast<size_t>(split) * g.M * g.N;
+  fence_proxy_async_smem();
+  __syncthreads();  // every stage is consumed: the ring becomes the reduction tile
+  {
+    const int row = warp * 32 + lane;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float* dst = red + row * RED_LD;
 #pragma unroll 1
-  for (int j0 = 0; j0 < BN; j0 += 16) {
-    float v[16];
-    if (have) {
-      tmem_ld16(taddr + j0, v);
-    } else {
+    for (int j0 = 0; j0 < BN; j0 += 16) {
+      float v[16];
+      if (have) {
+        tmem_ld16(taddr + j0, v);
+      } else {
 #pragma unroll
-      for (int q = 0; q < 16; ++q) v[q] = 0.f;
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(dst + j0 + 4 * q) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
-    if (m < g.M) {
-      float* row = out + static_cast<size_t>(m) * g.N;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int n = n0 + j0 + 4 * q;
-        if (n + 3 < g.N) {
-          float4 val = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          float4* dst = reinterpret_cast<float4*>(row + n);
-          if (g.accumulate) {
-            const float4 o = *dst;
-            val.x += o.x; val.y += o.y; val.z += o.z; val.w += o.w;
-          }
-          *dst = val;
+  }
+  tc_fence_before();
+  if (g.splits > 1) cluster_sync(); else __syncthreads();
+
+  // ---------------- epilogue 2: reduce a row slice over the cluster, store ----------------
+  {
+    const int rows = BM / g.splits;
+    const int r0 = split * rows;
+    constexpr int C4 = BN / 4;
+    for (int idx = threadIdx.x; idx < rows * C4; idx += blockDim.x) {
+      const int rr = r0 + idx / C4;
+      const int c = (idx % C4) * 4;
+      const float* src = red + rr * RED_LD + c;
+      float4 acc = *reinterpret_cast<const float4*>(src);
+      for (int q = 0; q < g.splits; ++q) {
+        if (q == split) continue;
+        const float4 o = dsmem_ld_f4(dsmem_addr(src, q));
+        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+      }
+      const int m = m0 + rr;
+      const int n = n0 + c;
+      if (m < g.M && n < g.N) {
+        const size_t off = static_cast<size_t>(m) * g.N + n;
+        if (g.out_bf16) {
+          uint2 p;
+          p.x = static_cast<uint32_t>(bf16_bits(acc.x)) | (static_cast<uint32_t>(bf16_bits(acc.y)) << 16);
+          p.y = static_cast<uint32_t>(bf16_bits(acc.z)) | (static_cast<uint32_t>(bf16_bits(acc.w)) << 16);
+          *reinterpret_cast<uint2*>(static_cast<uint16_t*>(g.out) + off) = p;
         } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (n + e < g.N) row[n + e] = g.accumulate ? row[n + e] + v[4 * q + e] : v[4 * q + e];
+          float4* dstp = reinterpret_cast<float4*>(static_cast<float*>(g.out) + off);
+          if (g.accumulate) {
+            const float4 o = *dstp;
+            acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+          }
+          *dstp = acc;
         }
       }
     }
   }
-  tc_fence_before();
-  __syncthreads();
+  // peers may still read this CTA's tile: leave together
+  if (g.splits > 1) cluster_sync(); else __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, BN);
 }
 
@@ -178,7 +212,7 @@ __global__ void k_gemm_f32(const float* __restrict__ A, const float* __restrict_
     const float bv = g.b_mn_major ? Bm[static_cast<size_t>(k) * g.N + n] : Bm[static_cast<size_t>(n) * g.K + k];
     acc = fmaf(av, bv, acc);
   }
-  float* dst = g.out + static_cast<size_t>(m) * g.N + n;
+  float* dst = static_cast<float*>(g.out) + static_cast<size_t>(m) * g.N + n;
   *dst = g.accumulate ? *dst + acc : acc;
 }
 
@@ -189,15 +223,26 @@ cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
   static size_t configured_ = 0;
   if (bytes > configured_) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16<BN, A_MN, B_MN>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.splits);
-  k_gemm_bf16<BN, A_MN, B_MN><<<grid, 128, bytes, st>>>(ta, tb, g);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.splits);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = g.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = g.splits > 1 ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_bf16<BN, A_MN, B_MN>, ta, tb, g);
   count_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int A_MN, int B_MN>
@@ -214,11 +259,14 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmAr
 }  // namespace
 
 size_t gemm_bf16_smem_bytes(const GemmArgs& g) {
-  return kGemmStages * (A_BYTES + b_bytes(g.BN)) + 256 + 1024;
+  const size_t ring = kGemmStages * static_cast<size_t>(stage_bytes(g.BN));
+  const size_t red = static_cast<size_t>(BM) * (g.BN + 4) * sizeof(float);
+  return (ring > red ? ring : red) + 256 + 1024;
 }
 
 cudaError_t launch_gemm_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                              cudaStream_t st) {
+  if (g.splits != 1 && g.splits != 2 && g.splits != 4 && g.splits != 8) return cudaErrorInvalidValue;
   if (g.a_mn_major && g.b_mn_major) return launch_bn<1, 1>(ta, tb, g, st);
   if (!g.a_mn_major && g.b_mn_major) return launch_bn<0, 1>(ta, tb, g, st);
   if (g.a_mn_major && !g.b_mn_major) return launch_bn<1, 0>(ta, tb, g, st);

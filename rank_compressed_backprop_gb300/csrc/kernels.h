@@ -17,6 +17,7 @@ struct ProjectArgs {
   int NT;            // MMA N: Rx + Ry rounded up to a multiple of 16
   int nk;            // ceil(L / 64)
   int pq_tma;        // 1: PQ tiles arrive by TMA; 0: threads fill all of PQ up front
+  int splits;        // token-axis split = cluster size along grid z (1 or 2)
   const void* pq;    // [Rx+Ry, L]
   void* out0;        // [B*Rx, C]
   void* out1;        // [B*Ry, C] or null
@@ -37,10 +38,12 @@ struct GemmArgs {
   int b_mn_major;    // 1: B stored [K, N]; 0: B stored [N, K]
   int BN;            // N tile (64, 128 or 256)
   int nk;            // ceil(K / 64)
-  int splits;        // split-K factor (grid z); partial planes out + s*M*N
+  int splits;        // split-K factor = cluster size along grid z (1, 2, 4 or 8);
+                     // partial tiles are reduced through distributed shared memory
   int chunks_per_split;
-  int accumulate;    // out += D (only with splits == 1)
-  float* out;        // [splits][M][N]
+  int accumulate;    // fp32 output only: out += D
+  int out_bf16;      // 1: bf16 output (round to nearest even); 0: fp32
+  void* out;         // [M][N]
 };
 
 constexpr int kGemmStages = 4;
@@ -55,15 +58,18 @@ cudaError_t launch_gemm_f32(const GemmArgs& g, const float* A, const float* Bm, 
 struct ExpandArgs {
   int B, L, Cx, Ry;
   int KR;            // Ry rounded up to a multiple of 16
-  int BN;            // column tile (128 or 256)
-  int splits;        // number of fp32 partial planes in gxh
-  const float* gxh;  // [splits][B*Ry][Cx]
+  int BN;            // column tile (64, 128 or 256)
+  int nlt;           // ceil(L / 128) token tiles, looped over inside one CTA
+  int q_tma;         // 1: Q tiles arrive by TMA (L % 8 == 0); 0: threads fill them
+  const void* gxh;   // [B*Ry][Cx], same dtype as out (fp32 path: fp32)
   const void* Q;     // [Ry, L]
   void* out;         // [B, L, Cx]
 };
 
+constexpr int kExpandStages = 4;
 size_t expand_bf16_smem_bytes(const ExpandArgs& e);
-cudaError_t launch_expand_bf16(const ExpandArgs& e, cudaStream_t st);
+cudaError_t launch_expand_bf16(const CUtensorMap& tmap_q, const CUtensorMap& tmap_g,
+                               const CUtensorMap& tmap_out, const ExpandArgs& e, cudaStream_t st);
 cudaError_t launch_expand_f32(const ExpandArgs& e, cudaStream_t st);
 
 // ---------------------------------------------------------------------------

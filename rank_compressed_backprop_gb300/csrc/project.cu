@@ -61,6 +61,11 @@ __global__ void __launch_bounds__(128, 1)
   const int lane = threadIdx.x & 31;
   const int c0 = blockIdx.x * BM;
   const int b = blockIdx.y;
+  const int split = blockIdx.z;  // == rank in the cluster (cluster dims 1 x 1 x splits)
+  const int per = (a.nk + a.splits - 1) / a.splits;
+  const int kc_begin = split * per;
+  const int kc_end = kc_begin + per < a.nk ? kc_begin + per : a.nk;
+  const int nkc = kc_end > kc_begin ? kc_end - kc_begin : 0;
   constexpr uint32_t kTmemCols = NT <= 32 ? 32 : (NT <= 64 ? 64 : 128);
 
   if (threadIdx.x == 0) {
@@ -102,10 +107,11 @@ __global__ void __launch_bounds__(128, 1)
     // ---------------- TMA producer ----------------
     const uint32_t bytes = A_BYTES + (a.pq_tma ? lay.b_stage_bytes : 0);
     int issued = 0;
-    for (int kc = 0; kc < a.nk; ++kc) {
-      const int s = kc % kProjectStages;
-      if (kc >= kProjectStages &&
-          !mbar_wait(&empty[s], ((kc / kProjectStages) - 1) & 1)) {
+    for (int i = 0; i < nkc; ++i) {
+      const int kc = kc_begin + i;
+      const int s = i % kProjectStages;
+      if (i >= kProjectStages &&
+          !mbar_wait(&empty[s], ((i / kProjectStages) - 1) & 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
@@ -117,16 +123,17 @@ __global__ void __launch_bounds__(128, 1)
       ++issued;
     }
     // drain: every copy this thread issued has landed before the CTA moves on
-    for (int kc = issued - kProjectStages < 0 ? 0 : issued - kProjectStages; kc < issued; ++kc)
-      if (!mbar_wait(&full[kc % kProjectStages], (kc / kProjectStages) & 1))
+    for (int i = issued - kProjectStages < 0 ? 0 : issued - kProjectStages; i < issued; ++i)
+      if (!mbar_wait(&full[i % kProjectStages], (i / kProjectStages) & 1))
         raise_fault(FAULT_WAIT_FULL);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = idesc_bf16_f32(128, NT, /*a_mn=*/1, /*b_mn=*/0);
     bool ok = true;
-    for (int kc = 0; kc < a.nk; ++kc) {
-      const int s = kc % kProjectStages;
-      if (!mbar_wait(&full[s], (kc / kProjectStages) & 1)) {
+    for (int i = 0; i < nkc; ++i) {
+      const int kc = kc_begin + i;
+      const int s = i % kProjectStages;
+      if (!mbar_wait(&full[s], (i / kProjectStages) & 1)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;
@@ -141,37 +148,85 @@ __global__ void __launch_bounds__(128, 1)
         // 64-column box is HALF_A bytes away.  B (K-major): +32 B per 16 tokens.
         const uint64_t ad = sdesc_sw128(a_base + kk * 2048, HALF_A, 1024);
         const uint64_t bd = sdesc_sw128(b_base + kk * 32, 16, 1024);
-        umma_bf16(tmem, ad, bd, idesc, (kc | kk) != 0);
+        umma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
       }
       umma_commit(&empty[s]);
     }
-    if (ok) umma_commit(done);
+    if (ok && nkc > 0) umma_commit(done);
   }
   __syncwarp();
 
   // ---------------- epilogue: TMEM -> bf16 planes ----------------
-  if (!mbar_wait(done, 0)) raise_fault(FAULT_WAIT_DONE);
+  const bool have = nkc > 0;
+  if (have && !mbar_wait(done, 0)) raise_fault(FAULT_WAIT_DONE);
   tc_fence_after();
   const int row = warp * 32 + lane;
-  const int c = c0 + row;
   const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
   uint16_t* out0 = static_cast<uint16_t*>(a.out0);
   uint16_t* out1 = static_cast<uint16_t*>(a.out1);
+  if (a.splits == 1) {
+    const int c = c0 + row;
 #pragma unroll
-  for (int j0 = 0; j0 < NT; j0 += 16) {
-    float v[16];
-    tmem_ld16(taddr + j0, v);
-    if (c < a.C) {
+    for (int j0 = 0; j0 < NT; j0 += 16) {
+      float v[16];
+      tmem_ld16(taddr + j0, v);
+      if (c < a.C) {
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int r = j0 + jj;
-        if (r < a.Rx) {
-          out0[(static_cast<size_t>(b) * a.Rx + r) * a.C + c] = bf16_bits(v[jj]);
-        } else if (r < a.Rx + a.Ry) {
-          out1[(static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c] = bf16_bits(v[jj]);
+        for (int jj = 0; jj < 16; ++jj) {
+          const int r = j0 + jj;
+          if (r < a.Rx) {
+            out0[(static_cast<size_t>(b) * a.Rx + r) * a.C + c] = bf16_bits(v[jj]);
+          } else if (r < a.Rx + a.Ry) {
+            out1[(static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c] = bf16_bits(v[jj]);
+          }
         }
       }
     }
+  } else {
+    // split over tokens: park the fp32 partial, then each CTA of the cluster
+    // sums a slice of the columns over all partials (distributed shared memory)
+    constexpr int LDR = NT + 4;
+    float* red = reinterpret_cast<float*>(sA);  // the ring is idle after the MMAs
+    fence_proxy_async_smem();
+    __syncthreads();
+#pragma unroll
+    for (int j0 = 0; j0 < NT; j0 += 16) {
+      float v[16];
+      if (have) {
+        tmem_ld16(taddr + j0, v);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(red + row * LDR + j0 + 4 * q) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+    tc_fence_before();
+    cluster_sync();
+    const int cols = BM / a.splits;
+    const int Rt = a.Rx + a.Ry;
+    for (int idx = threadIdx.x; idx < Rt * cols; idx += blockDim.x) {
+      const int r = idx / cols;
+      const int cl = split * cols + (idx - r * cols);
+      const float* src = red + cl * LDR + r;
+      float acc = *src;
+      for (int q = 0; q < a.splits; ++q) {
+        if (q == split) continue;
+        float o;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(o) : "r"(dsmem_addr(src, q)) : "memory");
+        acc += o;
+      }
+      const int c = c0 + cl;
+      if (c < a.C) {
+        if (r < a.Rx)
+          out0[(static_cast<size_t>(b) * a.Rx + r) * a.C + c] = bf16_bits(acc);
+        else
+          out1[(static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c] = bf16_bits(acc);
+      }
+    }
+    cluster_sync();
   }
   tc_fence_before();
   __syncthreads();
@@ -207,10 +262,21 @@ cudaError_t launch_nt(const CUtensorMap& tt, const CUtensorMap& tpq, const Proje
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  dim3 grid((a.C + BM - 1) / BM, a.B);
-  k_project_bf16<NT><<<grid, 128, bytes, st>>>(tt, tpq, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.C + BM - 1) / BM, a.B, a.splits);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = a.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.splits > 1 ? 1 : 0;
+  cudaError_t err = cudaLaunchKernelEx(&cfg, k_project_bf16<NT>, tt, tpq, a);
   count_launches(1);
-  return cudaGetLastError();
+  return err != cudaSuccess ? err : cudaGetLastError();
 }
 
 }  // namespace

@@ -44,6 +44,7 @@ class InstantLinear:
         self.ws_cal = torch.empty(api.calib_workspace_bytes(L, max(Rx, Ry)), dtype=torch.uint8,
                                   device=dev)
         self.last_calibration = None
+        self._side = torch.cuda.Stream(device=dev)
 
     # views of the stacked projector
     @property
@@ -67,9 +68,15 @@ class InstantLinear:
         gw = self.gw if gw is None else gw
         gx = self.gx if gx is None else gx
         B = g_y.shape[0]
+        main = torch.cuda.current_stream()
         api.project_grad(g_y, self.PQ, self.Sx, self.Sq, self.Rx, self.Ry)
-        api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
+        # g_w and g_tilde_x only share the projection's outputs: run them
+        # concurrently (fork/join; also valid inside CUDA-graph capture)
+        self._side.wait_stream(main)
+        with torch.cuda.stream(self._side):
+            api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
         api.grad_x(self.Sq, self.w, self.Q, gx, self.ws_gx)
+        main.wait_stream(self._side)
         return gw, gx
 
     # ---- calibration --------------------------------------------------------
