@@ -231,7 +231,7 @@ __device__ JacSmem jac_carve(uint8_t* smem, int n) {
   const int N = n + (n & 1);
   s.A = reinterpret_cast<float*>(smem);
   s.V = s.A + N * ld;
-  s.cs = s.V + n * ld;
+  s.cs = s.V + N * ld;
   s.pairs = reinterpret_cast<int*>(s.cs + kMaxBlock + 2);
   s.red = reinterpret_cast<float*>(s.pairs + kMaxBlock + 2);
   s.rank = reinterpret_cast<int*>(s.red + 32);
