@@ -23,6 +23,14 @@ std::atomic<unsigned long long> g_launches{0};
 
 void instant::count_launches(unsigned int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+bool instant::pdl_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("INSTANT_NO_PDL");
+    return !(v && v[0] == '1');
+  }();
+  return on;
+}
+
 namespace {
 
 constexpr int kTargetCtas = 2 * 152;  // two waves' worth of work on 152 SMs

@@ -420,57 +420,79 @@ __global__ void k_sub_apply(const float* __restrict__ in, const float* __restric
 }
 
 // Y[rows] = C[rows, :] V / n ;  H += V[rows]^T Y[rows]
-__global__ void k_sub_cv(const float* __restrict__ C, int L, int m, float inv_n, SolverWs w) {
+// 8 warps x 2 rows per CTA.  Tiles of 64 rows of V are staged in shared
+// memory once per CTA; each warp holds its rows' 64 C entries in registers
+// and broadcasts them with shuffles; lane l owns columns l, l+32, ...
+constexpr int kCvRows = 16;
+constexpr int kCvTile = 64;
+__global__ void __launch_bounds__(256) k_sub_cv(const float* __restrict__ C, int L, int m,
+                                                float inv_n, SolverWs w) {
   extern __shared__ float sm[];
-  float* cs = sm;                       // [kRows][33]
-  float* vs = cs + kRows * 33;          // [32][m]
-  float* ys = vs + 32 * m;              // [kRows][m]
-  float* vr = ys + kRows * m;           // [kRows][m]  V rows of this block
-  const int i0 = blockIdx.x * kRows;
-  const int nr = min(kRows, L - i0);
-  const int per = (kRows * m + blockDim.x - 1) / blockDim.x;  // outputs per thread (<= 16)
-  float acc[16];
+  float* vs = sm;                        // [kCvTile][m]
+  float* ys = vs + kCvTile * m;          // [kCvRows][m]
+  float* vr = ys + kCvRows * m;          // [kCvRows][m]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i0 = blockIdx.x * kCvRows;
+  const int r0 = i0 + 2 * warp;          // this warp's two rows
+  const int mq = (m + 31) / 32;          // columns per lane (<= 4)
+  float acc[2][4];
 #pragma unroll
-  for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-  for (int j0 = 0; j0 < L; j0 += 32) {
-    const int nj = min(32, L - j0);
-    for (int idx = threadIdx.x; idx < kRows * 32; idx += blockDim.x) {
-      const int r = idx >> 5, c = idx & 31;
-      cs[r * 33 + c] = (r < nr && c < nj) ? C[static_cast<size_t>(i0 + r) * L + j0 + c] : 0.f;
-    }
-    for (int idx = threadIdx.x; idx < 32 * m; idx += blockDim.x) {
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+  for (int j0 = 0; j0 < L; j0 += kCvTile) {
+    const int nj = min(kCvTile, L - j0);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kCvTile * m; idx += blockDim.x) {
       const int r = idx / m;
-      vs[idx] = r < nj ? w.V[(j0 + r) * m + (idx - r * m)] : 0.f;
+      vs[idx] = r < nj ? w.V[static_cast<size_t>(j0 + r) * m + (idx - r * m)] : 0.f;
     }
     __syncthreads();
-    for (int q = 0; q < per; ++q) {
-      const int o = threadIdx.x + q * blockDim.x;
-      if (o >= kRows * m) break;
-      const int r = o / m, col = o - (o / m) * m;
-      float a = acc[q];
-#pragma unroll 8
-      for (int c = 0; c < 32; ++c) a = fmaf(cs[r * 33 + c], vs[c * m + col], a);
-      acc[q] = a;
+    float cr[2][2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int j = j0 + h * 32 + lane;
+        cr[r][h] = (r0 + r < L && j < L) ? C[static_cast<size_t>(r0 + r) * L + j] : 0.f;
+      }
+#pragma unroll 4
+    for (int jj = 0; jj < kCvTile; ++jj) {
+      const float c0 = __shfl_sync(0xffffffffu, cr[0][jj >> 5], jj & 31);
+      const float c1 = __shfl_sync(0xffffffffu, cr[1][jj >> 5], jj & 31);
+      const float* vrow = vs + jj * m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = lane + 32 * q;
+        if (q < mq && col < m) {
+          const float v = vrow[col];
+          acc[0][q] = fmaf(c0, v, acc[0][q]);
+          acc[1][q] = fmaf(c1, v, acc[1][q]);
+        }
+      }
     }
-    __syncthreads();
   }
-  for (int q = 0; q < per; ++q) {
-    const int o = threadIdx.x + q * blockDim.x;
-    if (o >= kRows * m) break;
-    const int r = o / m, col = o - (o / m) * m;
-    const float y = acc[q] * inv_n;
-    ys[o] = r < nr ? y : 0.f;
-    if (r < nr) w.Y[(i0 + r) * m + col] = y;
-  }
-  for (int idx = threadIdx.x; idx < kRows * m; idx += blockDim.x) {
-    const int r = idx / m;
-    vr[idx] = r < nr ? w.V[(i0 + r) * m + (idx - r * m)] : 0.f;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int row = r0 + r;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = lane + 32 * q;
+      if (q < mq && col < m) {
+        const float y = acc[r][q] * inv_n;
+        ys[(2 * warp + r) * m + col] = row < L ? y : 0.f;
+        vr[(2 * warp + r) * m + col] = row < L ? w.V[static_cast<size_t>(row) * m + col] : 0.f;
+        if (row < L) w.Y[static_cast<size_t>(row) * m + col] = y;
+      }
+    }
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
     const int a = idx / m, b = idx - (idx / m) * m;
     float h = 0.f;
-    for (int r = 0; r < nr; ++r) h = fmaf(vr[r * m + a], ys[r * m + b], h);
+#pragma unroll 4
+    for (int r = 0; r < kCvRows; ++r) h = fmaf(vr[r * m + a], ys[r * m + b], h);
     atomicAdd(&w.H[a * m + b], h);
   }
 }
@@ -694,7 +716,8 @@ cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_swee
   const size_t bytes = jac_smem_bytes(L);
   cudaError_t e = set_smem(reinterpret_cast<const void*>(k_jacobi_full), bytes);
   if (e != cudaSuccess) return e;
-  k_jacobi_full<<<1, kJacThreads, bytes, st>>>(C, L, static_cast<float>(inv_n), max_sweeps, w);
+  const int jt = L <= 32 ? 128 : (L <= 64 ? 256 : kJacThreads);
+  k_jacobi_full<<<1, jt, bytes, st>>>(C, L, static_cast<float>(inv_n), max_sweeps, w);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -712,7 +735,7 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   const int nb = (L + kRows - 1) / kRows;
   const size_t jb = jac_smem_bytes(m);
   const size_t ab = sizeof(float) * (m * m + kRows * m);
-  const size_t cb = sizeof(float) * (kRows * 33 + 32 * m + 2 * kRows * m);
+  const size_t cb = sizeof(float) * (kCvTile * m + 2 * kCvRows * m);
   const size_t rb = sizeof(float) * (m * m + 4 * kRows * m);
   cudaError_t e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_orth), jb)) != cudaSuccess) return e;
@@ -720,10 +743,11 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_apply), ab)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_cv), cb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_ritz), rb)) != cudaSuccess) return e;
-  k_sub_orth<<<1, kJacThreads, jb, st>>>(m, max_sweeps, w);
+  const int jt = m <= 32 ? 128 : (m <= 64 ? 256 : kJacThreads);
+  k_sub_orth<<<1, jt, jb, st>>>(m, max_sweeps, w);
   k_sub_apply<<<nb, 256, ab, st>>>(w.Z, w.T, w.V, L, m);
-  k_sub_cv<<<nb, 256, cb, st>>>(C, L, m, static_cast<float>(inv_n), w);
-  k_sub_rr<<<1, kJacThreads, jb, st>>>(m, max_sweeps, w);
+  k_sub_cv<<<(L + kCvRows - 1) / kCvRows, 256, cb, st>>>(C, L, m, static_cast<float>(inv_n), w);
+  k_sub_rr<<<1, jt, jb, st>>>(m, max_sweeps, w);
   k_sub_ritz<<<nb, 256, rb, st>>>(L, m, w);
   count_launches(5);
   return cudaGetLastError();

@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     // ---------------- producer ----------------
@@ -243,10 +245,8 @@ cudaError_t launch_bn(const CUtensorMap& tq, const CUtensorMap& tg, const CUtens
     if (err != cudaSuccess) return err;
     configured_ = bytes;
   }
-  dim3 grid((e.Cx + BN - 1) / BN, e.B);
-  k_expand_bf16<BN><<<grid, 192, bytes, st>>>(tq, tg, to, e);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_ex(k_expand_bf16<BN>, dim3((e.Cx + BN - 1) / BN, e.B), dim3(192), bytes, st, 1,
+                   pdl_enabled(), tq, tg, to, e);
 }
 
 }  // namespace

@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -171,11 +173,17 @@ __global__ void __launch_bounds__(128, 1)
       const int c = (idx % C4) * 4;
       const float* src = red + rr * RED_LD + c;
       float4 acc = *reinterpret_cast<const float4*>(src);
-      for (int q = 0; q < g.splits; ++q) {
-        if (q == split) continue;
-        const float4 o = dsmem_ld_f4(dsmem_addr(src, q));
-        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
-      }
+      // issue every peer load before the first add (in-order issue would
+      // otherwise stall on each remote round trip)
+      float4 part[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < g.splits && q != split) part[q] = dsmem_ld_f4(dsmem_addr(src, q));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (q < g.splits && q != split) {
+          acc.x += part[q].x; acc.y += part[q].y; acc.z += part[q].z; acc.w += part[q].w;
+        }
       const int m = m0 + rr;
       const int n = n0 + c;
       if (m < g.M && n < g.N) {
@@ -228,21 +236,8 @@ cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const GemmA
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.splits);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = g.splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = g.splits > 1 ? 1 : 0;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_bf16<BN, A_MN, B_MN>, ta, tb, g);
-  count_launches(1);
-  return e != cudaSuccess ? e : cudaGetLastError();
+  return launch_ex(k_gemm_bf16<BN, A_MN, B_MN>, dim3((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.splits),
+                   dim3(128), bytes, st, g.splits, pdl_enabled(), ta, tb, g);
 }
 
 template <int A_MN, int B_MN>

@@ -139,6 +139,41 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
 // host-side count of kernel launches issued by the library
 void count_launches(unsigned int n);
 
+// programmatic dependent launch on/off (INSTANT_NO_PDL=1 turns it off)
+bool pdl_enabled();
+
+// cudaLaunchKernelEx with an optional 1 x 1 x cluster_z cluster and optional
+// programmatic stream serialization (the kernel must call pdl_wait() before
+// its first global-memory access when pdl is set)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, int cluster_z, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (cluster_z > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = static_cast<unsigned>(cluster_z);
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  count_launches(1);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // sticky device status words, one per translation unit
 cudaError_t read_fault_project(unsigned int* out, int clear);
 cudaError_t read_fault_gemm(unsigned int* out, int clear);

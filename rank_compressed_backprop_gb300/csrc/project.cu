@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(128, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  pdl_launch_dependents();
+  pdl_wait();
   if (!a.pq_tma) {
     // whole projector into shared memory, K-major with the 128-byte swizzle
     const int Rt = a.Rx + a.Ry;
@@ -207,23 +209,31 @@ __global__ void __launch_bounds__(128, 1)
     cluster_sync();
     const int cols = BM / a.splits;
     const int Rt = a.Rx + a.Ry;
-    for (int idx = threadIdx.x; idx < Rt * cols; idx += blockDim.x) {
-      const int r = idx / cols;
-      const int cl = split * cols + (idx - r * cols);
-      const float* src = red + cl * LDR + r;
-      float acc = *src;
-      for (int q = 0; q < a.splits; ++q) {
-        if (q == split) continue;
-        float o;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(o) : "r"(dsmem_addr(src, q)) : "memory");
-        acc += o;
-      }
+    for (int idx = threadIdx.x; idx < (NT / 4) * cols; idx += blockDim.x) {
+      const int q4 = idx / cols;
+      const int cl = split * cols + (idx - q4 * cols);
+      const float* src = red + cl * LDR + q4 * 4;
+      float4 acc = *reinterpret_cast<const float4*>(src);
+      float4 part[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (q < a.splits && q != split) part[q] = dsmem_ld_f4(dsmem_addr(src, q));
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (q < a.splits && q != split) {
+          acc.x += part[q].x; acc.y += part[q].y; acc.z += part[q].z; acc.w += part[q].w;
+        }
+      const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
       const int c = c0 + cl;
       if (c < a.C) {
-        if (r < a.Rx)
-          out0[(static_cast<size_t>(b) * a.Rx + r) * a.C + c] = bf16_bits(acc);
-        else
-          out1[(static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c] = bf16_bits(acc);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = q4 * 4 + e;
+          if (r < a.Rx)
+            out0[(static_cast<size_t>(b) * a.Rx + r) * a.C + c] = bf16_bits(vals[e]);
+          else if (r < Rt)
+            out1[(static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c] = bf16_bits(vals[e]);
+        }
       }
     }
     cluster_sync();
@@ -262,21 +272,8 @@ cudaError_t launch_nt(const CUtensorMap& tt, const CUtensorMap& tpq, const Proje
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.C + BM - 1) / BM, a.B, a.splits);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.dynamicSmemBytes = bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = a.splits;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.splits > 1 ? 1 : 0;
-  cudaError_t err = cudaLaunchKernelEx(&cfg, k_project_bf16<NT>, tt, tpq, a);
-  count_launches(1);
-  return err != cudaSuccess ? err : cudaGetLastError();
+  return launch_ex(k_project_bf16<NT>, dim3((a.C + BM - 1) / BM, a.B, a.splits), dim3(128), bytes,
+                   st, a.splits, pdl_enabled(), tt, tpq, a);
 }
 
 }  // namespace

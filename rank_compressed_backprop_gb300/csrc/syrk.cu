@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0 && lane == 0) {
     const uint32_t bytes = diag ? TILE_BYTES : STAGE;
@@ -182,10 +184,8 @@ cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaS
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  dim3 grid(s.ntiles, s.splits);
-  k_syrk_bf16<<<grid, 128, bytes, st>>>(tmap_t, s);
-  count_launches(1);
-  return cudaGetLastError();
+  return launch_ex(k_syrk_bf16, dim3(s.ntiles, s.splits), dim3(128), bytes, st, 1, pdl_enabled(),
+                   tmap_t, s);
 }
 
 cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st) {

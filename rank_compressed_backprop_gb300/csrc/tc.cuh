@@ -155,6 +155,17 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor drains; it must wait before
+// touching global memory the predecessor reads or writes.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // thread-block clusters / distributed shared memory
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cluster_sync() {
