@@ -103,8 +103,45 @@ __global__ void k_solver_energy(const float* __restrict__ C, size_t count, Solve
 // stops shrinking (the fp32 rounding floor) below 1e-4 * ||A||_F; returns
 // false when neither happens within max_sweeps.
 // ---------------------------------------------------------------------------
-__device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int max_sweeps,
-                             float* cs, int* pairs, float* red) {
+__device__ __forceinline__ void jac_pair(int r, int k, int N, int& p, int& q) {
+  if (k == 0) {
+    p = r;
+    q = N - 1;
+  } else {
+    int a = r + k;
+    if (a >= N - 1) a -= N - 1;
+    int b = r - k;
+    if (b < 0) b += N - 1;
+    p = a < b ? a : b;
+    q = a < b ? b : a;
+  }
+  if (p > q) {
+    const int t = p;
+    p = q;
+    q = t;
+  }
+}
+
+__device__ __forceinline__ void jac_rot(const float* A, int ld, int p, int q, float& c, float& s) {
+  c = 1.f;
+  s = 0.f;
+  const float apq = A[p * ld + q];
+  if (fabsf(apq) > 1e-30f) {
+    const float app = A[p * ld + p], aqq = A[q * ld + q];
+    const float tau = (aqq - app) / (2.f * apq);
+    float t;
+    if (fabsf(tau) > 1e18f) {
+      t = 0.5f / tau;
+    } else {
+      t = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+    }
+    c = rsqrtf(1.f + t * t);
+    s = t * c;
+  }
+}
+
+__device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float tol,
+                             int max_sweeps, float* red) {
   const int N = n + (n & 1);
   const int half = N / 2;
   for (int idx = threadIdx.x; idx < N * N; idx += blockDim.x) {
@@ -113,15 +150,17 @@ __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int m
     if (i >= n || j >= n) A[i * ld + j] = 0.f;
   }
   __syncthreads();
+  float* Ao = A;   // current matrix
+  float* An = A2;  // next matrix
   bool converged = false;
   float prev = 0.f;
   for (int sweep = 0; sweep <= max_sweeps; ++sweep) {
     float off = 0.f, tot = 0.f;
     for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
       const int i = idx / n, j = idx - (idx / n) * n;
-      const float a = A[i * ld + j];
-      tot += a * a;
-      if (i != j) off += a * a;
+      const float v = Ao[i * ld + j];
+      tot += v * v;
+      if (i != j) off += v * v;
     }
     off = block_sum_f(off, red);
     tot = block_sum_f(tot, red);
@@ -136,69 +175,46 @@ __device__ bool block_jacobi(float* A, float* V, int n, int ld, float tol, int m
     prev = off;
     if (sweep == max_sweeps) break;
     for (int r = 0; r < N - 1; ++r) {
-      if (threadIdx.x < half) {
-        const int k = threadIdx.x;
-        int p, q;
-        if (k == 0) {
-          p = r;
-          q = N - 1;
-        } else {
-          p = (r + k) % (N - 1);
-          q = (r - k + N - 1) % (N - 1);
-        }
-        if (p > q) {
-          const int t = p;
-          p = q;
-          q = t;
-        }
-        float c = 1.f, s = 0.f;
-        const float apq = A[p * ld + q];
-        if (fabsf(apq) > 1e-30f) {
-          const float app = A[p * ld + p], aqq = A[q * ld + q];
-          const float tau = (aqq - app) / (2.f * apq);
-          float t;
-          if (fabsf(tau) > 1e18f) {
-            t = 0.5f / tau;
-          } else {
-            t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
-          }
-          c = 1.f / sqrtf(1.f + t * t);
-          s = t * c;
-        }
-        pairs[2 * k] = p;
-        pairs[2 * k + 1] = q;
-        cs[2 * k] = c;
-        cs[2 * k + 1] = s;
-      }
-      __syncthreads();
-      // A <- J^T A J, one 2x2 block per work item
+      // every work item recomputes the rotations it needs from the current
+      // matrix, so a round needs a single barrier
       for (int idx = threadIdx.x; idx < half * half; idx += blockDim.x) {
         const int k = idx / half, k2 = idx - (idx / half) * half;
-        const int p = pairs[2 * k], q = pairs[2 * k + 1];
-        const int p2 = pairs[2 * k2], q2 = pairs[2 * k2 + 1];
-        const float c1 = cs[2 * k], s1 = cs[2 * k + 1];
-        const float c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
-        if (s1 == 0.f && s2 == 0.f) continue;
-        const float a = A[p * ld + p2], b = A[p * ld + q2];
-        const float c = A[q * ld + p2], d = A[q * ld + q2];
+        int p, q, p2, q2;
+        jac_pair(r, k, N, p, q);
+        jac_pair(r, k2, N, p2, q2);
+        float c1, s1, c2, s2;
+        jac_rot(Ao, ld, p, q, c1, s1);
+        jac_rot(Ao, ld, p2, q2, c2, s2);
+        const float a = Ao[p * ld + p2], b = Ao[p * ld + q2];
+        const float c = Ao[q * ld + p2], d = Ao[q * ld + q2];
         const float y00 = c1 * a - s1 * c, y01 = c1 * b - s1 * d;
         const float y10 = s1 * a + c1 * c, y11 = s1 * b + c1 * d;
-        A[p * ld + p2] = c2 * y00 - s2 * y01;
-        A[p * ld + q2] = s2 * y00 + c2 * y01;
-        A[q * ld + p2] = c2 * y10 - s2 * y11;
-        A[q * ld + q2] = s2 * y10 + c2 * y11;
+        An[p * ld + p2] = c2 * y00 - s2 * y01;
+        An[p * ld + q2] = s2 * y00 + c2 * y01;
+        An[q * ld + p2] = c2 * y10 - s2 * y11;
+        An[q * ld + q2] = s2 * y10 + c2 * y11;
       }
-      // V <- V J
       for (int idx = threadIdx.x; idx < N * half; idx += blockDim.x) {
         const int k = idx / N, i = idx - (idx / N) * N;
-        const float c = cs[2 * k], s = cs[2 * k + 1];
+        int p, q;
+        jac_pair(r, k, N, p, q);
+        float c, s;
+        jac_rot(Ao, ld, p, q, c, s);
         if (s == 0.f) continue;
-        const int p = pairs[2 * k], q = pairs[2 * k + 1];
         const float vp = V[i * ld + p], vq = V[i * ld + q];
         V[i * ld + p] = c * vp - s * vq;
         V[i * ld + q] = s * vp + c * vq;
       }
       __syncthreads();
+      float* t = Ao;
+      Ao = An;
+      An = t;
+    }
+  }
+  if (Ao != A) {
+    for (int idx = threadIdx.x; idx < N * N; idx += blockDim.x) {
+      const int i = idx / N, j = idx - (idx / N) * N;
+      A[i * ld + j] = Ao[i * ld + j];
     }
   }
   __syncthreads();
@@ -218,6 +234,7 @@ __device__ __forceinline__ int desc_rank(const float* A, int ld, int n, int i) {
 
 struct JacSmem {
   float* A;
+  float* A2;
   float* V;
   float* cs;
   int* pairs;
@@ -230,7 +247,8 @@ __device__ JacSmem jac_carve(uint8_t* smem, int n) {
   const int ld = n + 1;
   const int N = n + (n & 1);
   s.A = reinterpret_cast<float*>(smem);
-  s.V = s.A + N * ld;
+  s.A2 = s.A + N * ld;
+  s.V = s.A2 + N * ld;
   s.cs = s.V + N * ld;
   s.pairs = reinterpret_cast<int*>(s.cs + kMaxBlock + 2);
   s.red = reinterpret_cast<float*>(s.pairs + kMaxBlock + 2);
@@ -241,7 +259,7 @@ __device__ JacSmem jac_carve(uint8_t* smem, int n) {
 size_t jac_smem_bytes(int n) {
   const int ld = n + 1;
   const int N = n + (n & 1);
-  return sizeof(float) * (2 * N * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
+  return sizeof(float) * (3 * N * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
 }
 
 // ---------------------------------------------------------------------------
@@ -258,7 +276,7 @@ __global__ void __launch_bounds__(kJacThreads) k_jacobi_full(const float* __rest
     s.A[i * ld + j] = 0.5f * (C[i * L + j] + C[j * L + i]) * inv_n;
   }
   __syncthreads();
-  const bool ok = block_jacobi(s.A, s.V, L, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, L, ld, 3e-6f, max_sweeps, s.red);
   for (int i = threadIdx.x; i < L; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, L, i);
   __syncthreads();
   for (int i = threadIdx.x; i < L; i += blockDim.x)
@@ -325,10 +343,13 @@ __global__ void k_sub_gram(int L, int m, SolverWs w) {
 // vanishes (Z rank deficient) the symmetric (Lowdin) form T = D W Lambda^(-1/2)
 // from a Jacobi eigensolve is used instead; it zeroes the null directions.
 __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint8_t smem[];
   JacSmem s = jac_carve(smem, m);
   const int ld = m + 1;
   __shared__ float dsc[kMaxBlock];
+  __shared__ float pv[kMaxBlock];
   __shared__ int deficient;
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
     const float g = w.G[i * m + i];
@@ -342,7 +363,9 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.G[idx] = 0.f;
-  // ---- Cholesky (lower, in V so that A survives for the fallback) ----
+  // ---- Cholesky (elimination form in V, so that A survives for the fallback):
+  // step k subtracts a_ik a_jk / a_kk from the trailing block; column k is then
+  // final and L = (column k) / sqrt(a_kk).  One barrier per step.
   float* Lc = s.V;
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
     const int i = idx / m, j = idx - (idx / m) * m;
@@ -350,22 +373,29 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
   }
   __syncthreads();
   for (int k = 0; k < m; ++k) {
-    if (threadIdx.x == 0) {
-      const float d = Lc[k * ld + k];
-      if (!(d > 1e-6f)) deficient = 1;
-      Lc[k * ld + k] = d > 1e-6f ? sqrtf(d) : 1.f;
+    const float d = Lc[k * ld + k];
+    if (!(d > 1e-6f)) {
+      if (threadIdx.x == 0) deficient = 1;
+      break;
     }
-    __syncthreads();
-    const float piv = Lc[k * ld + k];
-    for (int i = k + 1 + threadIdx.x; i < m; i += blockDim.x) Lc[i * ld + k] /= piv;
-    __syncthreads();
     const int rem = m - k - 1;
+    const float inv = 1.f / d;
     for (int idx = threadIdx.x; idx < rem * rem; idx += blockDim.x) {
       const int i = k + 1 + idx / rem, j = k + 1 + idx % rem;
-      if (j <= i) Lc[i * ld + j] -= Lc[i * ld + k] * Lc[j * ld + k];
+      if (j <= i) Lc[i * ld + j] -= Lc[i * ld + k] * Lc[j * ld + k] * inv;
     }
     __syncthreads();
   }
+  __syncthreads();
+  if (!deficient) {
+    for (int j = threadIdx.x; j < m; j += blockDim.x) pv[j] = rsqrtf(Lc[j * ld + j]);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
+      const int i = idx / m, j = idx - (idx / m) * m;
+      if (j <= i) Lc[i * ld + j] *= pv[j];
+    }
+  }
+  __syncthreads();
   if (!deficient) {
     // T = D L^-T.  s.A is free now: X = L^-1 by forward substitution, one
     // thread per column j (each thread reads only the entries it wrote)
@@ -385,7 +415,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     return;
   }
   // ---- fallback: symmetric orthonormalisation (A still holds D G D) ----
-  const bool ok = block_jacobi(s.A, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.red);
   float lmax = 0.f;
   for (int j = 0; j < m; ++j) lmax = fmaxf(lmax, s.A[j * ld + j]);
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
@@ -400,6 +430,8 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
 // out[rows] = in[rows] * M   (M m x m), rows of kRows per CTA
 __global__ void k_sub_apply(const float* __restrict__ in, const float* __restrict__ M, float* out,
                             int L, int m) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sm[];
   float* Ms = sm;            // [m][m]
   float* rs = sm + m * m;    // [kRows][m]
@@ -419,27 +451,22 @@ __global__ void k_sub_apply(const float* __restrict__ in, const float* __restric
   }
 }
 
-// Y[rows] = C[rows, :] V / n ;  H += V[rows]^T Y[rows]
-// 8 warps x 2 rows per CTA.  Tiles of 64 rows of V are staged in shared
-// memory once per CTA; each warp holds its rows' 64 C entries in registers
-// and broadcasts them with shuffles; lane l owns columns l, l+32, ...
-constexpr int kCvRows = 16;
+// Y = C V / n.  One warp per row, 4 warps per CTA (L/4 CTAs).  Tiles of 64
+// rows of V are staged in shared memory once per CTA; each warp holds its
+// row's 64 C entries in registers and broadcasts them with shuffles; lane l
+// owns columns l, l+32, ...
+constexpr int kCvWarps = 4;
 constexpr int kCvTile = 64;
-__global__ void __launch_bounds__(256) k_sub_cv(const float* __restrict__ C, int L, int m,
+__global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int L, int m,
                                                 float inv_n, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sm[];
-  float* vs = sm;                        // [kCvTile][m]
-  float* ys = vs + kCvTile * m;          // [kCvRows][m]
-  float* vr = ys + kCvRows * m;          // [kCvRows][m]
+  float* vs = sm;  // [kCvTile][m]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i0 = blockIdx.x * kCvRows;
-  const int r0 = i0 + 2 * warp;          // this warp's two rows
-  const int mq = (m + 31) / 32;          // columns per lane (<= 4)
-  float acc[2][4];
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[r][q] = 0.f;
+  const int row = blockIdx.x * kCvWarps + warp;
+  const int mq = (m + 31) / 32;  // columns per lane (<= 4)
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int j0 = 0; j0 < L; j0 += kCvTile) {
     const int nj = min(kCvTile, L - j0);
     __syncthreads();
@@ -448,51 +475,54 @@ __global__ void __launch_bounds__(256) k_sub_cv(const float* __restrict__ C, int
       vs[idx] = r < nj ? w.V[static_cast<size_t>(j0 + r) * m + (idx - r * m)] : 0.f;
     }
     __syncthreads();
-    float cr[2][2];
+    float cr[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int j = j0 + h * 32 + lane;
-        cr[r][h] = (r0 + r < L && j < L) ? C[static_cast<size_t>(r0 + r) * L + j] : 0.f;
-      }
-#pragma unroll 4
+    for (int h = 0; h < 2; ++h) {
+      const int j = j0 + h * 32 + lane;
+      cr[h] = (row < L && j < L) ? C[static_cast<size_t>(row) * L + j] : 0.f;
+    }
+#pragma unroll 8
     for (int jj = 0; jj < kCvTile; ++jj) {
-      const float c0 = __shfl_sync(0xffffffffu, cr[0][jj >> 5], jj & 31);
-      const float c1 = __shfl_sync(0xffffffffu, cr[1][jj >> 5], jj & 31);
+      const float c = __shfl_sync(0xffffffffu, cr[jj >> 5], jj & 31);
       const float* vrow = vs + jj * m;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int col = lane + 32 * q;
-        if (q < mq && col < m) {
-          const float v = vrow[col];
-          acc[0][q] = fmaf(c0, v, acc[0][q]);
-          acc[1][q] = fmaf(c1, v, acc[1][q]);
-        }
+        if (q < mq && col < m) acc[q] = fmaf(c, vrow[col], acc[q]);
       }
     }
   }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int row = r0 + r;
+  if (row < L) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int col = lane + 32 * q;
-      if (q < mq && col < m) {
-        const float y = acc[r][q] * inv_n;
-        ys[(2 * warp + r) * m + col] = row < L ? y : 0.f;
-        vr[(2 * warp + r) * m + col] = row < L ? w.V[static_cast<size_t>(row) * m + col] : 0.f;
-        if (row < L) w.Y[static_cast<size_t>(row) * m + col] = y;
-      }
+      if (q < mq && col < m) w.Y[static_cast<size_t>(row) * m + col] = acc[q] * inv_n;
     }
+  }
+}
+
+// H += V[rows]^T Y[rows] over chunks of 64 rows (H is zeroed by the previous
+// Rayleigh-Ritz step and by the start of the iteration)
+constexpr int kHRows = 64;
+__global__ void __launch_bounds__(256) k_sub_h(int L, int m, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ float sm[];
+  float* vr = sm;               // [kHRows][m]
+  float* yr = vr + kHRows * m;  // [kHRows][m]
+  const int i0 = blockIdx.x * kHRows;
+  const int nr = min(kHRows, L - i0);
+  for (int idx = threadIdx.x; idx < kHRows * m; idx += blockDim.x) {
+    const int r = idx / m, c = idx - (idx / m) * m;
+    vr[idx] = r < nr ? w.V[static_cast<size_t>(i0 + r) * m + c] : 0.f;
+    yr[idx] = r < nr ? w.Y[static_cast<size_t>(i0 + r) * m + c] : 0.f;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
     const int a = idx / m, b = idx - (idx / m) * m;
     float h = 0.f;
-#pragma unroll 4
-    for (int r = 0; r < kCvRows; ++r) h = fmaf(vr[r * m + a], ys[r * m + b], h);
+#pragma unroll 8
+    for (int r = 0; r < kHRows; ++r) h = fmaf(vr[r * m + a], yr[r * m + b], h);
     atomicAdd(&w.H[a * m + b], h);
   }
 }
@@ -500,6 +530,8 @@ __global__ void __launch_bounds__(256) k_sub_cv(const float* __restrict__ C, int
 // 1 CTA: Rayleigh-Ritz on H -> W (columns sorted by descending theta), theta;
 // zeroes H and the residual accumulators
 __global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ uint8_t smem[];
   JacSmem s = jac_carve(smem, m);
   const int ld = m + 1;
@@ -509,7 +541,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, S
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.H[idx] = 0.f;
-  const bool ok = block_jacobi(s.A, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.red);
   for (int i = threadIdx.x; i < m; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, m, i);
   __syncthreads();
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
@@ -525,6 +557,8 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, S
 
 // U = V W, Z = Y W; G += Z^T Z; res2_j += |Z_j - theta_j U_j|^2 over this block's rows
 __global__ void k_sub_ritz(int L, int m, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float sm[];
   float* Ws = sm;                 // [m][m]
   float* vs = Ws + m * m;         // [kRows][m]
@@ -735,22 +769,34 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   const int nb = (L + kRows - 1) / kRows;
   const size_t jb = jac_smem_bytes(m);
   const size_t ab = sizeof(float) * (m * m + kRows * m);
-  const size_t cb = sizeof(float) * (kCvTile * m + 2 * kCvRows * m);
+  const size_t cb = sizeof(float) * (kCvTile * m);
+  const size_t hb = sizeof(float) * (2 * kHRows * m);
   const size_t rb = sizeof(float) * (m * m + 4 * kRows * m);
   cudaError_t e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_orth), jb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_rr), jb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_apply), ab)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_cv), cb)) != cudaSuccess) return e;
+  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_h), hb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_ritz), rb)) != cudaSuccess) return e;
   const int jt = m <= 32 ? 128 : (m <= 64 ? 256 : kJacThreads);
-  k_sub_orth<<<1, jt, jb, st>>>(m, max_sweeps, w);
-  k_sub_apply<<<nb, 256, ab, st>>>(w.Z, w.T, w.V, L, m);
-  k_sub_cv<<<(L + kCvRows - 1) / kCvRows, 256, cb, st>>>(C, L, m, static_cast<float>(inv_n), w);
-  k_sub_rr<<<1, jt, jb, st>>>(m, max_sweeps, w);
-  k_sub_ritz<<<nb, 256, rb, st>>>(L, m, w);
-  count_launches(5);
-  return cudaGetLastError();
+  const bool pdl = pdl_enabled();
+  const float fn = static_cast<float>(inv_n);
+  if ((e = launch_ex(k_sub_orth, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, w)) != cudaSuccess)
+    return e;
+  if ((e = launch_ex(k_sub_apply, dim3(nb), dim3(256), ab, st, 1, pdl,
+                     static_cast<const float*>(w.Z), static_cast<const float*>(w.T), w.V, L, m)) !=
+      cudaSuccess)
+    return e;
+  if ((e = launch_ex(k_sub_cv, dim3((L + kCvWarps - 1) / kCvWarps), dim3(128), cb, st, 1, pdl, C, L, m,
+                     fn, w)) != cudaSuccess)
+    return e;
+  if ((e = launch_ex(k_sub_h, dim3((L + kHRows - 1) / kHRows), dim3(256), hb, st, 1, pdl, L, m, w)) !=
+      cudaSuccess)
+    return e;
+  if ((e = launch_ex(k_sub_rr, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, w)) != cudaSuccess)
+    return e;
+  return launch_ex(k_sub_ritz, dim3(nb), dim3(256), rb, st, 1, pdl, L, m, w);
 }
 
 cudaError_t launch_subspace_check(int L, int m, double eps, int p, int r_override, double tol,
