@@ -438,18 +438,21 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
   if (L <= 128) {
     if (launch_jacobi_full(C, L, inv_n, max_sweeps, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
   } else {
+    // block: the needed rank plus a margin for the convergence rate
     const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
-    m = round_up(std::max(2 * r_guess, r_guess + 16), 32);
-    if (m < 32) m = 32;
+    m = round_up(std::max(2 * r_guess, r_guess + 8), 16);
+    if (m < 16) m = 16;
     if (m > 128) m = 128;
     bool converged = false;
     for (;;) {
       if (launch_subspace_init(L, m, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
       bool grow = false;
       for (int it = 0; it < max_iter; ++it) {
-        if (launch_subspace_iteration(C, L, m, inv_n, max_sweeps, w, st) != cudaSuccess)
+        const bool check = (it + 1) % 4 == 0 || it == max_iter - 1;
+        if (launch_subspace_iteration(C, L, m, inv_n, max_sweeps, check ? 1e-5f : 1e-3f, w, st) !=
+            cudaSuccess)
           return INSTANT_ERR_CUDA;
-        if ((it + 1) % 4 != 0 && it != max_iter - 1) continue;
+        if (!check) continue;
         if (launch_subspace_check(L, m, prm->eps, prm->p, prm->r_override, tol, inv_n2, w, st) !=
             cudaSuccess)
           return INSTANT_ERR_CUDA;

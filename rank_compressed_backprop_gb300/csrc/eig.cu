@@ -141,7 +141,7 @@ __device__ __forceinline__ void jac_rot(const float* A, int ld, int p, int q, fl
 }
 
 __device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float tol,
-                             int max_sweeps, float* red) {
+                             int max_sweeps, float* cs, int* pairs, float* red) {
   const int N = n + (n & 1);
   const int half = N / 2;
   for (int idx = threadIdx.x; idx < N * N; idx += blockDim.x) {
@@ -175,16 +175,24 @@ __device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float
     prev = off;
     if (sweep == max_sweeps) break;
     for (int r = 0; r < N - 1; ++r) {
-      // every work item recomputes the rotations it needs from the current
-      // matrix, so a round needs a single barrier
+      for (int k = threadIdx.x; k < half; k += blockDim.x) {
+        int p, q;
+        jac_pair(r, k, N, p, q);
+        float c, sn;
+        jac_rot(Ao, ld, p, q, c, sn);
+        pairs[2 * k] = p;
+        pairs[2 * k + 1] = q;
+        cs[2 * k] = c;
+        cs[2 * k + 1] = sn;
+      }
+      __syncthreads();
+      // A' = J^T A J: disjoint 2x2 blocks, read from Ao, written to An
       for (int idx = threadIdx.x; idx < half * half; idx += blockDim.x) {
         const int k = idx / half, k2 = idx - (idx / half) * half;
-        int p, q, p2, q2;
-        jac_pair(r, k, N, p, q);
-        jac_pair(r, k2, N, p2, q2);
-        float c1, s1, c2, s2;
-        jac_rot(Ao, ld, p, q, c1, s1);
-        jac_rot(Ao, ld, p2, q2, c2, s2);
+        const int p = pairs[2 * k], q = pairs[2 * k + 1];
+        const int p2 = pairs[2 * k2], q2 = pairs[2 * k2 + 1];
+        const float c1 = cs[2 * k], s1 = cs[2 * k + 1];
+        const float c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
         const float a = Ao[p * ld + p2], b = Ao[p * ld + q2];
         const float c = Ao[q * ld + p2], d = Ao[q * ld + q2];
         const float y00 = c1 * a - s1 * c, y01 = c1 * b - s1 * d;
@@ -194,16 +202,15 @@ __device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float
         An[q * ld + p2] = c2 * y10 - s2 * y11;
         An[q * ld + q2] = s2 * y10 + c2 * y11;
       }
+      // V <- V J (each item owns its two entries)
       for (int idx = threadIdx.x; idx < N * half; idx += blockDim.x) {
         const int k = idx / N, i = idx - (idx / N) * N;
-        int p, q;
-        jac_pair(r, k, N, p, q);
-        float c, s;
-        jac_rot(Ao, ld, p, q, c, s);
-        if (s == 0.f) continue;
+        const float c = cs[2 * k], sn = cs[2 * k + 1];
+        if (sn == 0.f) continue;
+        const int p = pairs[2 * k], q = pairs[2 * k + 1];
         const float vp = V[i * ld + p], vq = V[i * ld + q];
-        V[i * ld + p] = c * vp - s * vq;
-        V[i * ld + q] = s * vp + c * vq;
+        V[i * ld + p] = c * vp - sn * vq;
+        V[i * ld + q] = sn * vp + c * vq;
       }
       __syncthreads();
       float* t = Ao;
@@ -219,6 +226,12 @@ __device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float
   }
   __syncthreads();
   return converged;
+}
+
+// threads for a one-CTA Jacobi of order n: barriers are nearly free for a
+// single warp, so small problems run on one warp
+__host__ __device__ inline int jac_threads(int n) {
+  return n <= 24 ? 32 : (n <= 40 ? 64 : (n <= 72 ? 128 : 256));
 }
 
 // rank of diagonal entry i in descending order (ties: lower index first)
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(kJacThreads) k_jacobi_full(const float* __rest
     s.A[i * ld + j] = 0.5f * (C[i * L + j] + C[j * L + i]) * inv_n;
   }
   __syncthreads();
-  const bool ok = block_jacobi(s.A, s.A2, s.V, L, ld, 3e-6f, max_sweeps, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, L, ld, 3e-6f, max_sweeps, s.cs, s.pairs, s.red);
   for (int i = threadIdx.x; i < L; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, L, i);
   __syncthreads();
   for (int i = threadIdx.x; i < L; i += blockDim.x)
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     return;
   }
   // ---- fallback: symmetric orthonormalisation (A still holds D G D) ----
-  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
   float lmax = 0.f;
   for (int j = 0; j < m; ++j) lmax = fmaxf(lmax, s.A[j * ld + j]);
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
@@ -457,6 +470,7 @@ __global__ void k_sub_apply(const float* __restrict__ in, const float* __restric
 // owns columns l, l+32, ...
 constexpr int kCvWarps = 4;
 constexpr int kCvTile = 64;
+template <int MQ>
 __global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int L, int m,
                                                 float inv_n, SolverWs w) {
   pdl_launch_dependents();
@@ -465,8 +479,12 @@ __global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int
   float* vs = sm;  // [kCvTile][m]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kCvWarps + warp;
-  const int mq = (m + 31) / 32;  // columns per lane (<= 4)
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[MQ];
+#pragma unroll
+  for (int q = 0; q < MQ; ++q) acc[q] = 0.f;
+  bool colok[MQ];
+#pragma unroll
+  for (int q = 0; q < MQ; ++q) colok[q] = lane + 32 * q < m;
   for (int j0 = 0; j0 < L; j0 += kCvTile) {
     const int nj = min(kCvTile, L - j0);
     __syncthreads();
@@ -475,30 +493,35 @@ __global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int
       vs[idx] = r < nj ? w.V[static_cast<size_t>(j0 + r) * m + (idx - r * m)] : 0.f;
     }
     __syncthreads();
-    float cr[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = j0 + h * 32 + lane;
-      cr[h] = (row < L && j < L) ? C[static_cast<size_t>(row) * L + j] : 0.f;
-    }
+      const float cr = (row < L && j < L) ? C[static_cast<size_t>(row) * L + j] : 0.f;
 #pragma unroll 8
-    for (int jj = 0; jj < kCvTile; ++jj) {
-      const float c = __shfl_sync(0xffffffffu, cr[jj >> 5], jj & 31);
-      const float* vrow = vs + jj * m;
+      for (int jj = 0; jj < 32; ++jj) {
+        const float c = __shfl_sync(0xffffffffu, cr, jj);
+        const float* vrow = vs + (h * 32 + jj) * m + lane;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int col = lane + 32 * q;
-        if (q < mq && col < m) acc[q] = fmaf(c, vrow[col], acc[q]);
+        for (int q = 0; q < MQ; ++q)
+          if (colok[q]) acc[q] = fmaf(c, vrow[32 * q], acc[q]);
       }
     }
   }
   if (row < L) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int col = lane + 32 * q;
-      if (q < mq && col < m) w.Y[static_cast<size_t>(row) * m + col] = acc[q] * inv_n;
-    }
+    for (int q = 0; q < MQ; ++q)
+      if (colok[q]) w.Y[static_cast<size_t>(row) * m + lane + 32 * q] = acc[q] * inv_n;
   }
+}
+
+template <int MQ>
+cudaError_t launch_cv(const float* C, int L, int m, float inv_n, size_t cb, bool pdl, SolverWs w,
+                      cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(k_sub_cv<MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       200 * 1024);
+  if (e != cudaSuccess) return e;
+  return launch_ex(k_sub_cv<MQ>, dim3((L + kCvWarps - 1) / kCvWarps), dim3(128), cb, st, 1, pdl, C,
+                   L, m, inv_n, w);
 }
 
 // H += V[rows]^T Y[rows] over chunks of 64 rows (H is zeroed by the previous
@@ -529,7 +552,7 @@ __global__ void __launch_bounds__(256) k_sub_h(int L, int m, SolverWs w) {
 
 // 1 CTA: Rayleigh-Ritz on H -> W (columns sorted by descending theta), theta;
 // zeroes H and the residual accumulators
-__global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, SolverWs w) {
+__global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, float tol, SolverWs w) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ uint8_t smem[];
@@ -541,7 +564,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_rr(int m, int max_sweeps, S
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.H[idx] = 0.f;
-  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.red);
+  const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, tol, max_sweeps, s.cs, s.pairs, s.red);
   for (int i = threadIdx.x; i < m; i += blockDim.x) s.rank[i] = desc_rank(s.A, ld, m, i);
   __syncthreads();
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
@@ -750,7 +773,7 @@ cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_swee
   const size_t bytes = jac_smem_bytes(L);
   cudaError_t e = set_smem(reinterpret_cast<const void*>(k_jacobi_full), bytes);
   if (e != cudaSuccess) return e;
-  const int jt = L <= 32 ? 128 : (L <= 64 ? 256 : kJacThreads);
+  const int jt = jac_threads(L);
   k_jacobi_full<<<1, jt, bytes, st>>>(C, L, static_cast<float>(inv_n), max_sweeps, w);
   count_launches(1);
   return cudaGetLastError();
@@ -765,7 +788,7 @@ cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st) {
 }
 
 cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n, int max_sweeps,
-                                      SolverWs w, cudaStream_t st) {
+                                      float rr_tol, SolverWs w, cudaStream_t st) {
   const int nb = (L + kRows - 1) / kRows;
   const size_t jb = jac_smem_bytes(m);
   const size_t ab = sizeof(float) * (m * m + kRows * m);
@@ -776,10 +799,9 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_orth), jb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_rr), jb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_apply), ab)) != cudaSuccess) return e;
-  if ((e = set_smem(reinterpret_cast<const void*>(k_sub_cv), cb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_h), hb)) != cudaSuccess) return e;
   if ((e = set_smem(reinterpret_cast<const void*>(k_sub_ritz), rb)) != cudaSuccess) return e;
-  const int jt = m <= 32 ? 128 : (m <= 64 ? 256 : kJacThreads);
+  const int jt = jac_threads(m);
   const bool pdl = pdl_enabled();
   const float fn = static_cast<float>(inv_n);
   if ((e = launch_ex(k_sub_orth, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, w)) != cudaSuccess)
@@ -788,13 +810,19 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
                      static_cast<const float*>(w.Z), static_cast<const float*>(w.T), w.V, L, m)) !=
       cudaSuccess)
     return e;
-  if ((e = launch_ex(k_sub_cv, dim3((L + kCvWarps - 1) / kCvWarps), dim3(128), cb, st, 1, pdl, C, L, m,
-                     fn, w)) != cudaSuccess)
-    return e;
+  {
+    const int mq = (m + 31) / 32;
+    e = mq == 1 ? launch_cv<1>(C, L, m, fn, cb, pdl, w, st)
+                : mq == 2 ? launch_cv<2>(C, L, m, fn, cb, pdl, w, st)
+                          : mq == 3 ? launch_cv<3>(C, L, m, fn, cb, pdl, w, st)
+                                    : launch_cv<4>(C, L, m, fn, cb, pdl, w, st);
+    if (e != cudaSuccess) return e;
+  }
   if ((e = launch_ex(k_sub_h, dim3((L + kHRows - 1) / kHRows), dim3(256), hb, st, 1, pdl, L, m, w)) !=
       cudaSuccess)
     return e;
-  if ((e = launch_ex(k_sub_rr, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, w)) != cudaSuccess)
+  if ((e = launch_ex(k_sub_rr, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, rr_tol, w)) !=
+      cudaSuccess)
     return e;
   return launch_ex(k_sub_ritz, dim3(nb), dim3(256), rb, st, 1, pdl, L, m, w);
 }

@@ -127,8 +127,10 @@ cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_swee
                                cudaStream_t st);
 // subspace iteration building blocks
 cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st);
+// rr_tol: Jacobi tolerance of the Rayleigh-Ritz step (loose between
+// convergence checks, tight right before one)
 cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n, int max_sweeps,
-                                      SolverWs w, cudaStream_t st);
+                                      float rr_tol, SolverWs w, cudaStream_t st);
 cudaError_t launch_subspace_check(int L, int m, double eps, int p, int r_override,
                                   double tol, double inv_n2, SolverWs w, cudaStream_t st);
 // k, R, s and the projector rows from theta and U (sign-canonical)
