@@ -128,12 +128,13 @@ __device__ __forceinline__ void jac_rot(const float* A, int ld, int p, int q, fl
   const float apq = A[p * ld + q];
   if (fabsf(apq) > 1e-30f) {
     const float app = A[p * ld + p], aqq = A[q * ld + q];
-    const float tau = (aqq - app) / (2.f * apq);
+    const float tau = __fdividef(aqq - app, 2.f * apq);
     float t;
     if (fabsf(tau) > 1e18f) {
-      t = 0.5f / tau;
+      t = __fdividef(0.5f, tau);
     } else {
-      t = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(1.f + tau * tau));
+      const float u = 1.f + tau * tau;
+      t = copysignf(1.f, tau) * __fdividef(1.f, fabsf(tau) + u * rsqrtf(u));
     }
     c = rsqrtf(1.f + t * t);
     s = t * c;
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
 
 // out[rows] = in[rows] * M   (M m x m), rows of kRows per CTA
 __global__ void k_sub_apply(const float* __restrict__ in, const float* __restrict__ M, float* out,
-                            int L, int m) {
+                            float* zero_rows, int L, int m) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ float sm[];
@@ -461,67 +462,48 @@ __global__ void k_sub_apply(const float* __restrict__ in, const float* __restric
     float acc = 0.f;
     for (int k = 0; k < m; ++k) acc = fmaf(rs[r * m + k], Ms[k * m + j], acc);
     out[(i0 + r) * m + j] = acc;
+    if (zero_rows) zero_rows[(i0 + r) * m + j] = 0.f;
   }
 }
 
-// Y = C V / n.  One warp per row, 4 warps per CTA (L/4 CTAs).  Tiles of 64
-// rows of V are staged in shared memory once per CTA; each warp holds its
-// row's 64 C entries in registers and broadcasts them with shuffles; lane l
-// owns columns l, l+32, ...
-constexpr int kCvWarps = 4;
-constexpr int kCvTile = 64;
-template <int MQ>
-__global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int L, int m,
+// Y += C[rows, js] V[js, :] / n over a (32-row x JB-column) block of C per
+// CTA: one global round trip stages the C block and the matching V rows in
+// shared memory, then each thread accumulates its outputs and adds them to Y
+// (zeroed by the preceding apply step) with atomics.
+constexpr int kCvRows = 32;
+__global__ void __launch_bounds__(128) k_sub_cv(const float* __restrict__ C, int L, int m, int JB,
                                                 float inv_n, SolverWs w) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ float sm[];
-  float* vs = sm;  // [kCvTile][m]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kCvWarps + warp;
-  float acc[MQ];
-#pragma unroll
-  for (int q = 0; q < MQ; ++q) acc[q] = 0.f;
-  bool colok[MQ];
-#pragma unroll
-  for (int q = 0; q < MQ; ++q) colok[q] = lane + 32 * q < m;
-  for (int j0 = 0; j0 < L; j0 += kCvTile) {
-    const int nj = min(kCvTile, L - j0);
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kCvTile * m; idx += blockDim.x) {
-      const int r = idx / m;
-      vs[idx] = r < nj ? w.V[static_cast<size_t>(j0 + r) * m + (idx - r * m)] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int j = j0 + h * 32 + lane;
-      const float cr = (row < L && j < L) ? C[static_cast<size_t>(row) * L + j] : 0.f;
-#pragma unroll 8
-      for (int jj = 0; jj < 32; ++jj) {
-        const float c = __shfl_sync(0xffffffffu, cr, jj);
-        const float* vrow = vs + (h * 32 + jj) * m + lane;
-#pragma unroll
-        for (int q = 0; q < MQ; ++q)
-          if (colok[q]) acc[q] = fmaf(c, vrow[32 * q], acc[q]);
-      }
-    }
+  const int ldc = JB + 1;
+  float* cs = sm;                   // [kCvRows][JB + 1]
+  float* vs = cs + kCvRows * ldc;   // [JB][m]
+  const int i0 = blockIdx.x * kCvRows;
+  const int j0 = blockIdx.y * JB;
+  const int nr = min(kCvRows, L - i0);
+  const int nj = min(JB, L - j0);
+  for (int idx = threadIdx.x; idx < kCvRows * JB; idx += blockDim.x) {
+    const int r = idx / JB, j = idx - (idx / JB) * JB;
+    cs[r * ldc + j] = (r < nr && j < nj) ? C[static_cast<size_t>(i0 + r) * L + j0 + j] : 0.f;
   }
-  if (row < L) {
-#pragma unroll
-    for (int q = 0; q < MQ; ++q)
-      if (colok[q]) w.Y[static_cast<size_t>(row) * m + lane + 32 * q] = acc[q] * inv_n;
+  for (int idx = threadIdx.x; idx < JB * m; idx += blockDim.x) {
+    const int j = idx / m;
+    vs[idx] = j < nj ? w.V[static_cast<size_t>(j0 + j) * m + (idx - j * m)] : 0.f;
   }
-}
-
-template <int MQ>
-cudaError_t launch_cv(const float* C, int L, int m, float inv_n, size_t cb, bool pdl, SolverWs w,
-                      cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(k_sub_cv<MQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       200 * 1024);
-  if (e != cudaSuccess) return e;
-  return launch_ex(k_sub_cv<MQ>, dim3((L + kCvWarps - 1) / kCvWarps), dim3(128), cb, st, 1, pdl, C,
-                   L, m, inv_n, w);
+  __syncthreads();
+  for (int o = threadIdx.x; o < nr * m; o += blockDim.x) {
+    const int r = o / m, col = o - (o / m) * m;
+    const float* crow = cs + r * ldc;
+    float acc0 = 0.f, acc1 = 0.f;
+    int j = 0;
+    for (; j + 1 < nj; j += 2) {
+      acc0 = fmaf(crow[j], vs[j * m + col], acc0);
+      acc1 = fmaf(crow[j + 1], vs[(j + 1) * m + col], acc1);
+    }
+    if (j < nj) acc0 = fmaf(crow[j], vs[j * m + col], acc0);
+    atomicAdd(&w.Y[static_cast<size_t>(i0 + r) * m + col], (acc0 + acc1) * inv_n);
+  }
 }
 
 // H += V[rows]^T Y[rows] over chunks of 64 rows (H is zeroed by the previous
@@ -792,7 +774,6 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   const int nb = (L + kRows - 1) / kRows;
   const size_t jb = jac_smem_bytes(m);
   const size_t ab = sizeof(float) * (m * m + kRows * m);
-  const size_t cb = sizeof(float) * (kCvTile * m);
   const size_t hb = sizeof(float) * (2 * kHRows * m);
   const size_t rb = sizeof(float) * (m * m + 4 * kRows * m);
   cudaError_t e;
@@ -807,15 +788,15 @@ cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n
   if ((e = launch_ex(k_sub_orth, dim3(1), dim3(jt), jb, st, 1, pdl, m, max_sweeps, w)) != cudaSuccess)
     return e;
   if ((e = launch_ex(k_sub_apply, dim3(nb), dim3(256), ab, st, 1, pdl,
-                     static_cast<const float*>(w.Z), static_cast<const float*>(w.T), w.V, L, m)) !=
-      cudaSuccess)
+                     static_cast<const float*>(w.Z), static_cast<const float*>(w.T), w.V, w.Y, L,
+                     m)) != cudaSuccess)
     return e;
   {
-    const int mq = (m + 31) / 32;
-    e = mq == 1 ? launch_cv<1>(C, L, m, fn, cb, pdl, w, st)
-                : mq == 2 ? launch_cv<2>(C, L, m, fn, cb, pdl, w, st)
-                          : mq == 3 ? launch_cv<3>(C, L, m, fn, cb, pdl, w, st)
-                                    : launch_cv<4>(C, L, m, fn, cb, pdl, w, st);
+    const int JB = L >= 1024 ? 256 : (L >= 256 ? 64 : 32);
+    const size_t cvb = sizeof(float) * (kCvRows * (JB + 1) + JB * m);
+    if ((e = set_smem(reinterpret_cast<const void*>(k_sub_cv), cvb)) != cudaSuccess) return e;
+    e = launch_ex(k_sub_cv, dim3((L + kCvRows - 1) / kCvRows, (L + JB - 1) / JB), dim3(128), cvb, st,
+                  1, pdl, C, L, m, JB, fn, w);
     if (e != cudaSuccess) return e;
   }
   if ((e = launch_ex(k_sub_h, dim3((L + kHRows - 1) / kHRows), dim3(256), hb, st, 1, pdl, L, m, w)) !=
