@@ -137,7 +137,7 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
 // GEMM plan: N tile and split-K cluster size for an M x N x K product
 // ---------------------------------------------------------------------------
 struct GemmPlan {
-  int BN, splits, cps, nk;
+  int BN, splits, cps, nk, stages;
 };
 
 GemmPlan plan_gemm(int M, int N, int K) {
@@ -160,6 +160,7 @@ GemmPlan plan_gemm(int M, int N, int K) {
     }
   }
   p.cps = cdiv(p.nk, p.splits);
+  p.stages = p.cps < 4 ? p.cps : 4;
   return p;
 }
 
@@ -235,6 +236,7 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
     g.nk = cdiv(g.K, 64);
     g.splits = 1;
     g.chunks_per_split = g.nk;
+    g.stages = 1;
     return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sx),
                                      static_cast<const float*>(xhat), st));
   }
@@ -245,6 +247,7 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   g.nk = p.nk;
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
+  g.stages = p.stages;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.K)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
@@ -284,6 +287,7 @@ instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size
     g.nk = cdiv(g.K, 64);
     g.splits = 1;
     g.chunks_per_split = g.nk;
+    g.stages = 1;
     return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sq), static_cast<const float*>(w), st));
   }
   if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
@@ -294,6 +298,7 @@ instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size
   g.nk = p.nk;
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
+  g.stages = p.stages;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.M)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
@@ -348,6 +353,61 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
   return from_cuda(launch_expand_bf16(mq, mg, mo, e, st));
 }
 
+// fused single-kernel input gradient when every CTA can afford to recompute
+// its g_hat_x tile (small Cy); otherwise grad_x_core + expand
+bool use_fused_grad_x(int B, int Cy, int Ry, instant_dtype dt) {
+  (void)B;
+  if (dt != INSTANT_BF16 || Ry > 64) return false;
+  if (std::getenv("INSTANT_NO_FUSED_GRAD_X")) return false;
+  return cdiv(Cy, 64) <= 16;
+}
+
+instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
+                            int Cx, int Cy, int Ry, cudaStream_t st) {
+  FusedArgs f;
+  f.B = B;
+  f.L = L;
+  f.Cx = Cx;
+  f.Cy = Cy;
+  f.Ry = Ry;
+  f.KR = round_up(Ry, 16);
+  f.spt = 128 / Ry;
+  f.BN = 64;
+  f.nk = cdiv(Cy, 64);
+  f.stages = f.nk < 3 ? f.nk : 3;  // ~92 KB of shared memory: two CTAs per SM
+  f.nlt = cdiv(L, 128);
+  // smaller sample tiles when the grid would not cover the SMs
+  while (f.spt > 1 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.nlt < 200) f.spt /= 2;
+  const int base = cdiv(Cx, f.BN) * cdiv(B, f.spt);
+  int ls = cdiv(228, base);
+  if (ls > f.nlt) ls = f.nlt;
+  if (ls < 1) ls = 1;
+  f.lt_per = cdiv(f.nlt, ls);
+  f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
+  f.Q = Q;
+  CUtensorMap ms, mw, mq, mo;
+  std::memset(&mq, 0, sizeof(mq));
+  const uint64_t ds[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(B) * Ry};
+  const uint64_t ss[1] = {static_cast<uint64_t>(Cy) * 2};
+  const uint32_t bs[2] = {64, 128};
+  const uint64_t dw[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
+  const uint64_t sw[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bw[2] = {64, 64};
+  const uint64_t dout[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t sout[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(L) * Cx * 2};
+  const uint32_t bout[3] = {64, 128, 1};
+  if (!make_map(&ms, Sq, 2, ds, ss, bs) || !make_map(&mw, w, 2, dw, sw, bw) ||
+      !make_map(&mo, gx, 3, dout, sout, bout))
+    return INSTANT_ERR_CUDA;
+  if (f.q_tma) {
+    const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
+    const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
+    const uint32_t b2[2] = {64, static_cast<uint32_t>(f.KR)};
+    if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+  }
+  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, f, st));
+}
+
 instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
                               size_t ws_bytes, int B, int L, int Cx, int Cy, int Ry,
                               instant_dtype dt, void* stream) {
@@ -358,6 +418,8 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
   if (dt == INSTANT_BF16 && (!aligned16(Sq) || !aligned16(w) || !aligned16(gx) || !aligned16(ws) ||
                              Cx % 8 != 0 || Cy % 8 != 0))
     return INSTANT_ERR_ALIGN;
+  if (use_fused_grad_x(B, Cy, Ry, dt))
+    return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, static_cast<cudaStream_t>(stream));
   const instant_status s = instant_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, stream);
   if (s != INSTANT_OK) return s;
   return instant_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
@@ -507,6 +569,8 @@ instant_status instant_device_status(int clear, void* stream) {
   if (read_fault_syrk(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   if (read_fault_eig(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_fused(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   return total ? INSTANT_ERR_DEVICE : INSTANT_OK;
 }

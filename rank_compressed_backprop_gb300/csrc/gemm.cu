@@ -36,14 +36,15 @@ __global__ void __launch_bounds__(128, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr uint32_t STAGE = A_BYTES + BN * BK * 2;
   constexpr int RED_LD = BN + 4;  // fp32 reduction tile row pitch (bank spread)
-  constexpr uint32_t RING = kGemmStages * STAGE;
+  const int NS = g.stages;  // ring depth: min(4, chunks per CTA)
+  const uint32_t RING = NS * STAGE;
   constexpr uint32_t REDB = BM * RED_LD * 4;
-  constexpr uint32_t BAR_OFF = RING > REDB ? RING : REDB;
+  const uint32_t BAR_OFF = RING > REDB ? RING : REDB;
   uint8_t* sbase = smem;
   float* red = reinterpret_cast<float*>(smem);  // reuses the stages after the K loop
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
-  uint64_t* empty = full + kGemmStages;
-  uint64_t* done = empty + kGemmStages;
+  uint64_t* empty = full + NS;
+  uint64_t* done = empty + NS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -57,7 +58,7 @@ __global__ void __launch_bounds__(128, 1)
   const int nkc = kc_end > kc_begin ? kc_end - kc_begin : 0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kGemmStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -81,8 +82,8 @@ __global__ void __launch_bounds__(128, 1)
     // ---------------- TMA producer ----------------
     int issued = 0;
     for (int i = 0; i < nkc; ++i) {
-      const int s = i % kGemmStages;
-      if (i >= kGemmStages && !mbar_wait(&empty[s], ((i / kGemmStages) - 1) & 1)) {
+      const int s = i % NS;
+      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
@@ -105,15 +106,15 @@ __global__ void __launch_bounds__(128, 1)
       }
       ++issued;
     }
-    for (int i = issued - kGemmStages < 0 ? 0 : issued - kGemmStages; i < issued; ++i)
-      if (!mbar_wait(&full[i % kGemmStages], (i / kGemmStages) & 1)) raise_fault(FAULT_WAIT_FULL);
+    for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
+      if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, B_MN);
     bool ok = true;
     for (int i = 0; i < nkc; ++i) {
-      const int s = i % kGemmStages;
-      if (!mbar_wait(&full[s], (i / kGemmStages) & 1)) {
+      const int s = i % NS;
+      if (!mbar_wait(&full[s], (i / NS) & 1)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;
@@ -254,7 +255,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmAr
 }  // namespace
 
 size_t gemm_bf16_smem_bytes(const GemmArgs& g) {
-  const size_t ring = kGemmStages * static_cast<size_t>(stage_bytes(g.BN));
+  const size_t ring = static_cast<size_t>(g.stages) * stage_bytes(g.BN);
   const size_t red = static_cast<size_t>(BM) * (g.BN + 4) * sizeof(float);
   return (ring > red ? ring : red) + 256 + 1024;
 }
@@ -262,6 +263,7 @@ size_t gemm_bf16_smem_bytes(const GemmArgs& g) {
 cudaError_t launch_gemm_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                              cudaStream_t st) {
   if (g.splits != 1 && g.splits != 2 && g.splits != 4 && g.splits != 8) return cudaErrorInvalidValue;
+  if (g.stages < 1 || g.stages > kGemmStages) return cudaErrorInvalidValue;
   if (g.a_mn_major && g.b_mn_major) return launch_bn<1, 1>(ta, tb, g, st);
   if (!g.a_mn_major && g.b_mn_major) return launch_bn<0, 1>(ta, tb, g, st);
   if (g.a_mn_major && !g.b_mn_major) return launch_bn<1, 0>(ta, tb, g, st);

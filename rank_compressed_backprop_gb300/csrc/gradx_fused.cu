@@ -1,0 +1,342 @@
+// gradx_fused.cu -- input gradient in one kernel (page "INSTANT: Compressing
+// Gradients and Activations for Resource-Efficient Training", 关键设计 3:
+// g_hat_x = g_hat_y2 w, g_tilde_x = Q^T g_hat_x), so that g_hat_x never
+// leaves the SM.
+//
+// A CTA owns a tile of `spt` whole samples (spt * Ry <= 128 rows of g_hat_x),
+// a BN-column strip of the output, and a range of 128-token tiles:
+//   phase 1  TMEM acc1[128 x BN] = Sq[tile rows, :] w[:, strip]  (tcgen05, K = Cy
+//            streamed through a TMA ring: Sq K-major, w MN-major);
+//   phase 2  the epilogue warps turn acc1 into bf16 and write, per sample, the
+//            MN-major B operand [Ry (padded to 16) x BN] of the expansion
+//            straight into shared memory;
+//   phase 3  for every (sample, token tile): TMEM acc2 = Q^T[tile] B_s (one
+//            K = Ry MMA chain, two accumulators in flight) -> bf16 -> swizzled
+//            staging (reusing the phase-1 ring) -> TMA bulk store.
+// Used when Cy is small enough that every CTA can afford to recompute its
+// g_hat_x tile (the token range is split across CTAs for parallelism).
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace instant {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int BOX = BM * 128;         // staging box: 128 rows x 64 bf16
+
+struct FLay {
+  uint32_t ring, stage, qt, qt_tile, bs, bs_sample, stg, bar, total;
+};
+
+__host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_per, int spt) {
+  FLay l;
+  l.stage = A_BYTES + BN * BK * 2;
+  l.ring = 0;
+  const uint32_t ring_bytes = stages * l.stage;
+  const uint32_t stg_bytes = 2 * (BN / 64) * BOX;  // staging reuses the ring after phase 1
+  const uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
+  l.stg = 0;
+  l.qt = first;
+  l.qt_tile = 2 * KR * 128;
+  l.bs = l.qt + lt_per * l.qt_tile;
+  l.bs_sample = (BN / 64) * KR * 128;
+  l.bar = l.bs + spt * l.bs_sample;
+  l.total = l.bar + 256;
+  return l;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    k_gradx_fused(const __grid_constant__ CUtensorMap tmap_sq,
+                  const __grid_constant__ CUtensorMap tmap_w,
+                  const __grid_constant__ CUtensorMap tmap_q,
+                  const __grid_constant__ CUtensorMap tmap_out, FusedArgs f) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int KR = f.KR;
+  const int NS = f.stages;
+  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt);
+  uint8_t* ring = smem + lay.ring;
+  uint8_t* stg = smem + lay.stg;
+  uint8_t* sQ = smem + lay.qt;
+  uint8_t* sB = smem + lay.bs;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar);
+  uint64_t* empty = full + NS;
+  uint64_t* acc1_full = empty + NS;
+  uint64_t* b_ready = acc1_full + 1;
+  uint64_t* q_full = b_ready + 1;
+  uint64_t* t_full = q_full + 1;
+  uint64_t* t_empty = t_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BN;
+  const int s0 = blockIdx.y * f.spt;             // first sample of the tile
+  const int m0 = s0 * f.Ry;                      // first g_hat_x row of the tile
+  const int lt0 = blockIdx.z * f.lt_per;         // first token tile
+  int nlt = f.nlt - lt0;
+  if (nlt > f.lt_per) nlt = f.lt_per;
+  int nsamp = f.B - s0;
+  if (nsamp > f.spt) nsamp = f.spt;
+  const int njobs = nsamp * (nlt > 0 ? nlt : 0);
+  constexpr uint32_t kCols = BN == 64 ? 256 : 512;  // acc1 + two acc2 buffers
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc1_full, 1);
+    mbar_init(b_ready, 1);
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&t_full[i], 1);
+      mbar_init(&t_empty[i], 1);
+    }
+    fence_barrier_init();
+    prefetch_tmap(&tmap_sq);
+    prefetch_tmap(&tmap_w);
+    if (f.q_tma) prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_out);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kCols);
+    tmem_relinquish();
+  }
+  // zero the expansion operands: rows Ry..KR-1 of every sample stay zero
+  for (uint32_t i = threadIdx.x * 16; i < static_cast<uint32_t>(f.spt) * lay.bs_sample;
+       i += blockDim.x * 16)
+    *reinterpret_cast<uint4*>(sB + i) = make_uint4(0, 0, 0, 0);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t acc1 = tmem;
+  pdl_launch_dependents();
+  pdl_wait();
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    const uint16_t* Q = static_cast<const uint16_t*>(f.Q);
+    if (f.q_tma) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, nlt * lay.qt_tile);
+        for (int t = 0; t < nlt; ++t) {
+          uint8_t* dst = sQ + t * lay.qt_tile;
+          tma_load_2d(dst, &tmap_q, q_full, (lt0 + t) * BM, 0);
+          tma_load_2d(dst + KR * 128, &tmap_q, q_full, (lt0 + t) * BM + 64, 0);
+        }
+      }
+    } else {
+      for (int t = 0; t < nlt; ++t) {
+        uint8_t* dst = sQ + t * lay.qt_tile;
+        for (int idx = lane; idx < KR * BM; idx += 32) {
+          const int r = idx / BM;
+          const int ll = idx - r * BM;
+          const int l = (lt0 + t) * BM + ll;
+          const uint16_t v = (r < f.Ry && l < f.L) ? Q[static_cast<size_t>(r) * f.L + l] : 0;
+          *reinterpret_cast<uint16_t*>(dst + (ll >> 6) * KR * 128 + sw128_offset(r, ll & 63)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_full);
+    }
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < f.nk; ++i) {
+        const int s = i % NS;
+        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
+          raise_fault(FAULT_WAIT_EMPTY);
+          break;
+        }
+        uint8_t* sa = ring + s * lay.stage;
+        uint8_t* sb = sa + A_BYTES;
+        mbar_arrive_expect_tx(&full[s], lay.stage);
+        tma_load_2d(sa, &tmap_sq, &full[s], i * BK, m0);
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h)
+          tma_load_2d(sb + h * (64 * BK * 2), &tmap_w, &full[s], n0 + 64 * h, i * BK);
+        ++issued;
+      }
+      for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
+        if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
+      if (!mbar_wait(q_full, 0)) raise_fault(FAULT_WAIT_FULL);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc1 = idesc_bf16_f32(128, BN, /*a_mn=*/0, /*b_mn=*/1);
+      constexpr uint32_t idesc2 = idesc_bf16_f32(128, BN, /*a_mn=*/1, /*b_mn=*/1);
+      bool ok = true;
+      for (int i = 0; i < f.nk; ++i) {
+        const int s = i % NS;
+        if (!mbar_wait(&full[s], (i / NS) & 1)) {
+          raise_fault(FAULT_WAIT_FULL);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(ring + s * lay.stage);
+        const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(b_base + kk * 2048, 64 * BK * 2, 1024);
+          umma_bf16(acc1, ad, bd, idesc1, (i | kk) != 0);
+        }
+        umma_commit(&empty[s]);
+      }
+      if (ok) umma_commit(acc1_full);
+      if (ok && !mbar_wait(b_ready, 0)) {
+        raise_fault(FAULT_WAIT_DONE);
+        ok = false;
+      }
+      if (ok && !mbar_wait(q_full, 0)) {
+        raise_fault(FAULT_WAIT_FULL);
+        ok = false;
+      }
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      const uint32_t b_base = smem_u32(sB);
+      for (int j = 0; ok && j < njobs; ++j) {
+        const int s = j / nlt;
+        const int t = j - s * nlt;
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait(&t_empty[buf], ((j >> 1) - 1) & 1)) {
+          raise_fault(FAULT_WAIT_EMPTY);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t ab = q_base + t * lay.qt_tile;
+        const uint32_t bb = b_base + s * lay.bs_sample;
+        for (int kk = 0; kk < KR / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(ab + kk * 2048, KR * 128, 1024);
+          const uint64_t bd = sdesc_sw128(bb + kk * 2048, KR * 128, 1024);
+          umma_bf16(tmem + BN + buf * BN, ad, bd, idesc2, kk != 0);
+        }
+        umma_commit(&t_full[buf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int et = threadIdx.x - 64;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    // phase 2: acc1 row (s*Ry + r) -> B_s[r][:] in bf16 (MN-major, swizzled)
+    if (!mbar_wait(acc1_full, 0)) raise_fault(FAULT_WAIT_DONE);
+    tc_fence_after();
+    const int s_row = row / f.Ry;
+    const int r_row = row - s_row * f.Ry;
+    const bool keep = s_row < f.spt;
+    const uint32_t t1 = acc1 + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+    for (int j0 = 0; j0 < BN; j0 += 16) {
+      float v[16];
+      tmem_ld16(t1 + j0, v);
+      if (keep) {
+        uint32_t p[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
+                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
+        uint8_t* base = sB + s_row * lay.bs_sample + (j0 >> 6) * KR * 128;
+        const int c = j0 & 63;
+        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c + 8)) =
+            make_uint4(p[4], p[5], p[6], p[7]);
+      }
+    }
+    tc_fence_before();
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (et == 0) mbar_arrive(b_ready);
+    // phase 3: expansion tiles -> TMA stores (staging reuses the phase-1 ring,
+    // whose TMA writes all completed before acc1 did)
+    fence_proxy_async_smem();
+    for (int j = 0; j < njobs; ++j) {
+      const int s = j / nlt;
+      const int t = j - s * nlt;
+      const int buf = j & 1;
+      uint8_t* st = stg + buf * (BN / 64) * BOX;
+      if (et == 0 && j >= 2) tma_store_wait_read<1>();
+      named_barrier(1, 128);
+      if (!mbar_wait(&t_full[buf], (j >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
+      tc_fence_after();
+      const uint32_t taddr = tmem + BN + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+#pragma unroll 1
+      for (int j0 = 0; j0 < BN; j0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + j0, v);
+        uint32_t p[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
+                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
+        uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
+        const int c8 = (j0 & 63) >> 3;
+        *reinterpret_cast<uint4*>(box + ((c8 ^ (row & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<uint4*>(box + (((c8 + 1) ^ (row & 7)) << 4)) =
+            make_uint4(p[4], p[5], p[6], p[7]);
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (et == 0) {
+        mbar_arrive(&t_empty[buf]);
+        for (int h = 0; h < BN / 64; ++h)
+          if (n0 + 64 * h < f.Cx)
+            tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, (lt0 + t) * BM, s0 + s);
+        tma_store_commit();
+      }
+    }
+    if (et == 0) tma_store_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kCols);
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtensorMap& tq,
+                      const CUtensorMap& to, const FusedArgs& f, cudaStream_t st) {
+  const size_t bytes = gradx_fused_smem_bytes(f);
+  static size_t configured_ = 0;
+  if (bytes > configured_) {
+    cudaError_t e = cudaFuncSetAttribute(k_gradx_fused<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bytes));
+    if (e != cudaSuccess) return e;
+    configured_ = bytes;
+  }
+  const dim3 grid((f.Cx + BN - 1) / BN, (f.B + f.spt - 1) / f.spt,
+                  (f.nlt + f.lt_per - 1) / f.lt_per);
+  return launch_ex(k_gradx_fused<BN>, grid, dim3(192), bytes, st, 1, pdl_enabled(), ts, tw, tq, to,
+                   f);
+}
+
+}  // namespace
+
+size_t gradx_fused_smem_bytes(const FusedArgs& f) {
+  return fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt).total + 1024;
+}
+
+cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
+                               const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
+                               const FusedArgs& f, cudaStream_t st) {
+  if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
+  switch (f.BN) {
+    case 64: return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);
+    case 128: return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+INSTANT_FAULT_READER(read_fault_fused)
+
+}  // namespace instant

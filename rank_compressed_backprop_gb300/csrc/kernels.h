@@ -41,6 +41,7 @@ struct GemmArgs {
   int splits;        // split-K factor = cluster size along grid z (1, 2, 4 or 8);
                      // partial tiles are reduced through distributed shared memory
   int chunks_per_split;
+  int stages;        // TMA ring depth, 1..kGemmStages
   int accumulate;    // fp32 output only: out += D
   int out_bf16;      // 1: bf16 output (round to nearest even); 0: fp32
   void* out;         // [M][N]
@@ -71,6 +72,27 @@ size_t expand_bf16_smem_bytes(const ExpandArgs& e);
 cudaError_t launch_expand_bf16(const CUtensorMap& tmap_q, const CUtensorMap& tmap_g,
                                const CUtensorMap& tmap_out, const ExpandArgs& e, cudaStream_t st);
 cudaError_t launch_expand_f32(const ExpandArgs& e, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// fused input gradient: out[b] = Q^T (Sq[b] w) with g_hat_x kept on chip
+// ---------------------------------------------------------------------------
+struct FusedArgs {
+  int B, L, Cx, Cy, Ry;
+  int KR;            // Ry rounded up to a multiple of 16
+  int spt;           // samples per g_hat_x tile (spt * Ry <= 128)
+  int BN;            // column strip (64 or 128)
+  int nk;            // ceil(Cy / 64)
+  int stages;        // phase-1 TMA ring depth (1..4)
+  int nlt;           // ceil(L / 128)
+  int lt_per;        // token tiles per CTA
+  int q_tma;         // 1: Q^T tiles by TMA (L % 8 == 0); 0: threads fill them
+  const void* Q;     // [Ry, L]
+};
+
+size_t gradx_fused_smem_bytes(const FusedArgs& f);
+cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
+                               const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
+                               const FusedArgs& f, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // autocorrelation accumulation: Cout[i, j] += sum_b sum_c t[b,i,c] t[b,j,c]
@@ -182,5 +204,6 @@ cudaError_t read_fault_gemm(unsigned int* out, int clear);
 cudaError_t read_fault_expand(unsigned int* out, int clear);
 cudaError_t read_fault_syrk(unsigned int* out, int clear);
 cudaError_t read_fault_eig(unsigned int* out, int clear);
+cudaError_t read_fault_fused(unsigned int* out, int clear);
 
 }  // namespace instant
