@@ -160,7 +160,7 @@ GemmPlan plan_gemm(int M, int N, int K) {
     }
   }
   p.cps = cdiv(p.nk, p.splits);
-  p.stages = p.cps < 4 ? p.cps : 4;
+  p.stages = 4;
   return p;
 }
 
@@ -355,11 +355,19 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
 
 // fused single-kernel input gradient when every CTA can afford to recompute
 // its g_hat_x tile (small Cy); otherwise grad_x_core + expand
-bool use_fused_grad_x(int B, int Cy, int Ry, instant_dtype dt) {
-  (void)B;
+// token-axis cluster of the fused kernel: up to 8 CTAs, a power of two
+int fused_cluster(int L) {
+  const int nlt = cdiv(L, 128);
+  int cl = 1;
+  while (cl * 2 <= nlt && cl < 8) cl *= 2;
+  return cl;
+}
+
+bool use_fused_grad_x(int L, int Cy, int Ry, instant_dtype dt) {
   if (dt != INSTANT_BF16 || Ry > 64) return false;
   if (std::getenv("INSTANT_NO_FUSED_GRAD_X")) return false;
-  return cdiv(Cy, 64) <= 16;
+  // each CTA recomputes a K-slice of its g_hat_x tile: keep that slice short
+  return cdiv(cdiv(Cy, 64), fused_cluster(L)) <= 16;
 }
 
 instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
@@ -374,15 +382,13 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
   f.spt = 128 / Ry;
   f.BN = 64;
   f.nk = cdiv(Cy, 64);
-  f.stages = f.nk < 3 ? f.nk : 3;  // ~92 KB of shared memory: two CTAs per SM
   f.nlt = cdiv(L, 128);
+  f.cl = fused_cluster(L);
+  f.lt_per = cdiv(f.nlt, f.cl);
+  const int kper = cdiv(f.nk, f.cl);
+  f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;
   // smaller sample tiles when the grid would not cover the SMs
-  while (f.spt > 1 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.nlt < 200) f.spt /= 2;
-  const int base = cdiv(Cx, f.BN) * cdiv(B, f.spt);
-  int ls = cdiv(228, base);
-  if (ls > f.nlt) ls = f.nlt;
-  if (ls < 1) ls = 1;
-  f.lt_per = cdiv(f.nlt, ls);
+  while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < 152) f.spt /= 2;
   f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
   f.Q = Q;
   CUtensorMap ms, mw, mq, mo;
@@ -418,7 +424,7 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
   if (dt == INSTANT_BF16 && (!aligned16(Sq) || !aligned16(w) || !aligned16(gx) || !aligned16(ws) ||
                              Cx % 8 != 0 || Cy % 8 != 0))
     return INSTANT_ERR_ALIGN;
-  if (use_fused_grad_x(B, Cy, Ry, dt))
+  if (use_fused_grad_x(L, Cy, Ry, dt))
     return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, static_cast<cudaStream_t>(stream));
   const instant_status s = instant_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, stream);
   if (s != INSTANT_OK) return s;

@@ -37,7 +37,10 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   l.ring = 0;
   const uint32_t ring_bytes = stages * l.stage;
   const uint32_t stg_bytes = 2 * (BN / 64) * BOX;  // staging reuses the ring after phase 1
-  const uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
+  const uint32_t red_bytes = BM * (BN + 4) * 4;     // so does the cluster reduction tile
+  uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
+  if (red_bytes > first) first = red_bytes;
+  first = (first + 1023u) & ~1023u;
   l.stg = 0;
   l.qt = first;
   l.qt_tile = 2 * KR * 128;
@@ -79,8 +82,15 @@ __global__ void __launch_bounds__(192, 1)
   const int s0 = blockIdx.y * f.spt;             // first sample of the tile
   const int m0 = s0 * f.Ry;                      // first g_hat_x row of the tile
   const int lt0 = blockIdx.z * f.lt_per;         // first token tile
+  const int crank = blockIdx.z;                  // rank in the cluster (dims 1 x 1 x cl)
+  const int kper = (f.nk + f.cl - 1) / f.cl;     // phase-1 chunks per cluster rank
+  const int kc0 = crank * kper;
+  int nkc = f.nk - kc0;
+  if (nkc > kper) nkc = kper;
+  if (nkc < 0) nkc = 0;
   int nlt = f.nlt - lt0;
   if (nlt > f.lt_per) nlt = f.lt_per;
+  if (nlt < 0) nlt = 0;
   int nsamp = f.B - s0;
   if (nsamp > f.spt) nsamp = f.spt;
   const int njobs = nsamp * (nlt > 0 ? nlt : 0);
@@ -149,7 +159,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     if (lane == 0) {
       int issued = 0;
-      for (int i = 0; i < f.nk; ++i) {
+      for (int i = 0; i < nkc; ++i) {
         const int s = i % NS;
         if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
           raise_fault(FAULT_WAIT_EMPTY);
@@ -157,24 +167,25 @@ __global__ void __launch_bounds__(192, 1)
         }
         uint8_t* sa = ring + s * lay.stage;
         uint8_t* sb = sa + A_BYTES;
+        const int k0 = (kc0 + i) * BK;
         mbar_arrive_expect_tx(&full[s], lay.stage);
-        tma_load_2d(sa, &tmap_sq, &full[s], i * BK, m0);
+        tma_load_2d(sa, &tmap_sq, &full[s], k0, m0);
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h)
-          tma_load_2d(sb + h * (64 * BK * 2), &tmap_w, &full[s], n0 + 64 * h, i * BK);
+          tma_load_2d(sb + h * (64 * BK * 2), &tmap_w, &full[s], n0 + 64 * h, k0);
         ++issued;
       }
       for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
         if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
       if (!mbar_wait(q_full, 0)) raise_fault(FAULT_WAIT_FULL);
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  }
+  if (warp == 1) {
+    // ---------------- MMA issuer, phase 1 ----------------
     if (lane == 0) {
       constexpr uint32_t idesc1 = idesc_bf16_f32(128, BN, /*a_mn=*/0, /*b_mn=*/1);
-      constexpr uint32_t idesc2 = idesc_bf16_f32(128, BN, /*a_mn=*/1, /*b_mn=*/1);
       bool ok = true;
-      for (int i = 0; i < f.nk; ++i) {
+      for (int i = 0; i < nkc; ++i) {
         const int s = i % NS;
         if (!mbar_wait(&full[s], (i / NS) & 1)) {
           raise_fault(FAULT_WAIT_FULL);
@@ -193,10 +204,103 @@ __global__ void __launch_bounds__(192, 1)
         umma_commit(&empty[s]);
       }
       if (ok) umma_commit(acc1_full);
-      if (ok && !mbar_wait(b_ready, 0)) {
-        raise_fault(FAULT_WAIT_DONE);
-        ok = false;
+    }
+  }
+  __syncwarp();
+
+  // ---------------- phase 2: g_hat_x tile -> bf16 expansion operands ----------------
+  const bool epi = warp >= 2;
+  const int et = threadIdx.x - 64;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+  const int s_row = row / f.Ry;
+  const int r_row = row - s_row * f.Ry;
+  const bool keep = s_row < f.spt;
+  const uint32_t t1 = acc1 + (static_cast<uint32_t>(quarter * 32) << 16);
+  constexpr int LDR = BN + 4;
+  float* red = reinterpret_cast<float*>(ring);  // the ring is idle once acc1 is complete
+  if (epi) {
+    if (nkc > 0 && !mbar_wait(acc1_full, 0)) raise_fault(FAULT_WAIT_DONE);
+    tc_fence_after();
+    fence_proxy_async_smem();
+  }
+  if (f.cl > 1) {
+    // every CTA of the cluster holds a K-slice of the tile: park it, then each
+    // CTA sums all slices for all rows through distributed shared memory
+    if (epi) {
+#pragma unroll 1
+      for (int j0 = 0; j0 < BN; j0 += 16) {
+        float v[16];
+        if (nkc > 0) {
+          tmem_ld16(t1 + j0, v);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] = 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(red + row * LDR + j0 + 4 * q) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
+      tc_fence_before();
+    }
+    cluster_sync();
+    if (epi) {
+#pragma unroll 1
+      for (int c4 = 0; c4 < BN; c4 += 4) {
+        const float* src = red + row * LDR + c4;
+        float4 acc = *reinterpret_cast<const float4*>(src);
+        float4 part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < f.cl && q != crank) part[q] = dsmem_ld_f4(dsmem_addr(src, q));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < f.cl && q != crank) {
+            acc.x += part[q].x; acc.y += part[q].y; acc.z += part[q].z; acc.w += part[q].w;
+          }
+        if (keep) {
+          uint2 pk;
+          pk.x = static_cast<uint32_t>(bf16_bits(acc.x)) | (static_cast<uint32_t>(bf16_bits(acc.y)) << 16);
+          pk.y = static_cast<uint32_t>(bf16_bits(acc.z)) | (static_cast<uint32_t>(bf16_bits(acc.w)) << 16);
+          uint8_t* base = sB + s_row * lay.bs_sample + (c4 >> 6) * KR * 128;
+          *reinterpret_cast<uint2*>(base + sw128_offset(r_row, c4 & 63)) = pk;
+        }
+      }
+    }
+    cluster_sync();  // peers have read this CTA's slice
+  } else if (epi) {
+#pragma unroll 1
+    for (int j0 = 0; j0 < BN; j0 += 16) {
+      float v[16];
+      tmem_ld16(t1 + j0, v);
+      if (keep) {
+        uint32_t p[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
+                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
+        uint8_t* base = sB + s_row * lay.bs_sample + (j0 >> 6) * KR * 128;
+        const int c = j0 & 63;
+        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c)) = make_uint4(p[0], p[1], p[2], p[3]);
+        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c + 8)) =
+            make_uint4(p[4], p[5], p[6], p[7]);
+      }
+    }
+    tc_fence_before();
+  }
+  if (epi) {
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (et == 0) mbar_arrive(b_ready);
+  }
+
+  if (warp == 1) {
+    // ---------------- MMA issuer, phase 3 ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc2 = idesc_bf16_f32(128, BN, /*a_mn=*/1, /*b_mn=*/1);
+      bool ok = mbar_wait(b_ready, 0);
+      if (!ok) raise_fault(FAULT_WAIT_DONE);
       if (ok && !mbar_wait(q_full, 0)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
@@ -223,39 +327,7 @@ __global__ void __launch_bounds__(192, 1)
         umma_commit(&t_full[buf]);
       }
     }
-  } else {
-    // ---------------- epilogue warps 2..5 ----------------
-    const int et = threadIdx.x - 64;
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    // phase 2: acc1 row (s*Ry + r) -> B_s[r][:] in bf16 (MN-major, swizzled)
-    if (!mbar_wait(acc1_full, 0)) raise_fault(FAULT_WAIT_DONE);
-    tc_fence_after();
-    const int s_row = row / f.Ry;
-    const int r_row = row - s_row * f.Ry;
-    const bool keep = s_row < f.spt;
-    const uint32_t t1 = acc1 + (static_cast<uint32_t>(quarter * 32) << 16);
-#pragma unroll 1
-    for (int j0 = 0; j0 < BN; j0 += 16) {
-      float v[16];
-      tmem_ld16(t1 + j0, v);
-      if (keep) {
-        uint32_t p[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
-                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
-        uint8_t* base = sB + s_row * lay.bs_sample + (j0 >> 6) * KR * 128;
-        const int c = j0 & 63;
-        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c)) = make_uint4(p[0], p[1], p[2], p[3]);
-        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c + 8)) =
-            make_uint4(p[4], p[5], p[6], p[7]);
-      }
-    }
-    tc_fence_before();
-    fence_proxy_async_smem();
-    named_barrier(1, 128);
-    if (et == 0) mbar_arrive(b_ready);
+  } else if (epi) {
     // phase 3: expansion tiles -> TMA stores (staging reuses the phase-1 ring,
     // whose TMA writes all completed before acc1 did)
     fence_proxy_async_smem();
@@ -314,10 +386,9 @@ cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtens
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  const dim3 grid((f.Cx + BN - 1) / BN, (f.B + f.spt - 1) / f.spt,
-                  (f.nlt + f.lt_per - 1) / f.lt_per);
-  return launch_ex(k_gradx_fused<BN>, grid, dim3(192), bytes, st, 1, pdl_enabled(), ts, tw, tq, to,
-                   f);
+  const dim3 grid((f.Cx + BN - 1) / BN, (f.B + f.spt - 1) / f.spt, f.cl);
+  return launch_ex(k_gradx_fused<BN>, grid, dim3(192), bytes, st, f.cl, pdl_enabled(), ts, tw, tq,
+                   to, f);
 }
 
 }  // namespace
@@ -330,6 +401,8 @@ cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tm
                                const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
                                const FusedArgs& f, cudaStream_t st) {
   if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
+  if (f.cl != 1 && f.cl != 2 && f.cl != 4 && f.cl != 8) return cudaErrorInvalidValue;
+  if (f.lt_per * f.cl < f.nlt) return cudaErrorInvalidValue;
   switch (f.BN) {
     case 64: return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);
     case 128: return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);

@@ -85,6 +85,8 @@ struct FusedArgs {
   int stages;        // phase-1 TMA ring depth (1..4)
   int nlt;           // ceil(L / 128)
   int lt_per;        // token tiles per CTA
+  int cl;            // cluster size along the token axis (1, 2, 4, 8): phase 1's K
+                     // range is split across the cluster and reduced through DSMEM
   int q_tma;         // 1: Q^T tiles by TMA (L % 8 == 0); 0: threads fill them
   const void* Q;     // [Ry, L]
 };
