@@ -14,9 +14,10 @@
 //           through a 4-stage ring;
 //   warp 1  MMA issuer: one K = Ry (padded to 16) tcgen05 MMA chain per tile
 //           into one of two TMEM accumulators (double buffered);
-//   warps 2-5  epilogue: TMEM -> bf16 -> 128-byte-swizzled staging tile ->
-//           TMA bulk store, two staging buffers in flight, so the MMA of tile
-//           t+1 and the store of tile t overlap.
+//   warps 2-9  epilogue (two warps per TMEM lane quarter, split by columns):
+//           TMEM -> bf16 -> 128-byte-swizzled staging tile -> TMA bulk store,
+//           two staging buffers in flight, so the MMA of tile t+1 and the
+//           store of tile t overlap.
 // Full 128-byte lines leave the SM through the TMA engine; rows past L are
 // clipped by the tensor map.
 #include "kernels.h"
@@ -46,7 +47,7 @@ __host__ __device__ inline Lay expand_layout(int BN, int KR) {
 }
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_expand_bf16(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_g,
                   const __grid_constant__ CUtensorMap tmap_out, ExpandArgs e) {
@@ -174,36 +175,37 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int et = threadIdx.x - 64;       // 0..127
+    // ---------------- epilogue (warps 2..9) ----------------
+    // two warps per TMEM lane quarter, each converting half of the columns
+    const int et = threadIdx.x - 64;       // 0..255
+    const int ew = warp - 2;
     const int quarter = warp & 3;          // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;   // token row within the tile
+    const int c_lo = (ew >> 2) * (BN / 2);
     for (int lt = 0; lt < e.nlt; ++lt) {
       const int buf = lt & 1;
       uint8_t* st = stg + buf * (BN / 64) * BOX;
       if (et == 0 && lt >= 2) tma_store_wait_read<1>();
-      named_barrier(1, 128);
+      named_barrier(1, 256);
       if (!mbar_wait(&t_full[buf], (lt >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
       const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + j0, v);
-        uint32_t p[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
-                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
+      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + j0, v);
         uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
         const int c8 = (j0 & 63) >> 3;
-        *reinterpret_cast<uint4*>(box + ((c8 ^ (row & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
-        *reinterpret_cast<uint4*>(box + (((c8 + 1) ^ (row & 7)) << 4)) =
-            make_uint4(p[4], p[5], p[6], p[7]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(box + (((c8 + q) ^ (row & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                         pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      named_barrier(1, 128);
+      named_barrier(1, 256);
       if (et == 0) {
         mbar_arrive(&t_empty[buf]);
         for (int h = 0; h < BN / 64; ++h)
@@ -245,7 +247,7 @@ cudaError_t launch_bn(const CUtensorMap& tq, const CUtensorMap& tg, const CUtens
     if (err != cudaSuccess) return err;
     configured_ = bytes;
   }
-  return launch_ex(k_expand_bf16<BN>, dim3((e.Cx + BN - 1) / BN, e.B), dim3(192), bytes, st, 1,
+  return launch_ex(k_expand_bf16<BN>, dim3((e.Cx + BN - 1) / BN, e.B), dim3(320), bytes, st, 1,
                    pdl_enabled(), tq, tg, to, e);
 }
 

@@ -52,7 +52,7 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
 }
 
 template <int BN>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     k_gradx_fused(const __grid_constant__ CUtensorMap tmap_sq,
                   const __grid_constant__ CUtensorMap tmap_w,
                   const __grid_constant__ CUtensorMap tmap_q,
@@ -209,14 +209,14 @@ __global__ void __launch_bounds__(192, 1)
   __syncwarp();
 
   // ---------------- phase 2: g_hat_x tile -> bf16 expansion operands ----------------
+  // epilogue warps 2..9: two per TMEM lane quarter, each owning half the columns
   const bool epi = warp >= 2;
-  const int et = threadIdx.x - 64;
+  const int et = threadIdx.x - 64;   // 0..255 for the epilogue warps
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
-  const int s_row = row / f.Ry;
-  const int r_row = row - s_row * f.Ry;
-  const bool keep = s_row < f.spt;
+  const int c_lo = ((warp - 2) >> 2) * (BN / 2);
   const uint32_t t1 = acc1 + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int real_rows = f.spt * f.Ry;
   constexpr int LDR = BN + 4;
   float* red = reinterpret_cast<float*>(ring);  // the ring is idle once acc1 is complete
   if (epi) {
@@ -225,20 +225,21 @@ __global__ void __launch_bounds__(192, 1)
     fence_proxy_async_smem();
   }
   if (f.cl > 1) {
-    // every CTA of the cluster holds a K-slice of the tile: park it, then each
-    // CTA sums all slices for all rows through distributed shared memory
+    // every CTA of the cluster holds a K-slice of the tile.  Reduce-scatter:
+    // CTA r sums rows [r*rows_per, ...) over all slices; all-gather: it writes
+    // the bf16 result into the expansion operands of every CTA of the cluster.
     if (epi) {
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 16) {
-        float v[16];
+      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+        float v[32];
         if (nkc > 0) {
-          tmem_ld16(t1 + j0, v);
+          tmem_ld32(t1 + j0, v);
         } else {
 #pragma unroll
-          for (int q = 0; q < 16; ++q) v[q] = 0.f;
+          for (int q = 0; q < 32; ++q) v[q] = 0.f;
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 8; ++q)
           *reinterpret_cast<float4*>(red + row * LDR + j0 + 4 * q) =
               make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
@@ -246,9 +247,14 @@ __global__ void __launch_bounds__(192, 1)
     }
     cluster_sync();
     if (epi) {
-#pragma unroll 1
-      for (int c4 = 0; c4 < BN; c4 += 4) {
-        const float* src = red + row * LDR + c4;
+      const int rows_per = (real_rows + f.cl - 1) / f.cl;
+      const int r_begin = crank * rows_per;
+      constexpr int C4 = BN / 4;
+      for (int idx = et; idx < rows_per * C4; idx += 256) {
+        const int rr = r_begin + idx / C4;
+        if (rr >= real_rows) break;
+        const int c4 = (idx % C4) * 4;
+        const float* src = red + rr * LDR + c4;
         float4 acc = *reinterpret_cast<const float4*>(src);
         float4 part[8];
 #pragma unroll
@@ -259,39 +265,43 @@ __global__ void __launch_bounds__(192, 1)
           if (q < f.cl && q != crank) {
             acc.x += part[q].x; acc.y += part[q].y; acc.z += part[q].z; acc.w += part[q].w;
           }
-        if (keep) {
-          uint2 pk;
-          pk.x = static_cast<uint32_t>(bf16_bits(acc.x)) | (static_cast<uint32_t>(bf16_bits(acc.y)) << 16);
-          pk.y = static_cast<uint32_t>(bf16_bits(acc.z)) | (static_cast<uint32_t>(bf16_bits(acc.w)) << 16);
-          uint8_t* base = sB + s_row * lay.bs_sample + (c4 >> 6) * KR * 128;
-          *reinterpret_cast<uint2*>(base + sw128_offset(r_row, c4 & 63)) = pk;
-        }
-      }
-    }
-    cluster_sync();  // peers have read this CTA's slice
-  } else if (epi) {
-#pragma unroll 1
-    for (int j0 = 0; j0 < BN; j0 += 16) {
-      float v[16];
-      tmem_ld16(t1 + j0, v);
-      if (keep) {
-        uint32_t p[8];
+        const uint2 pk = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+        const int s_r = rr / f.Ry;
+        const int r_r = rr - s_r * f.Ry;
+        uint8_t* dst = sB + s_r * lay.bs_sample + (c4 >> 6) * KR * 128 + sw128_offset(r_r, c4 & 63);
+        *reinterpret_cast<uint2*>(dst) = pk;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
-                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
-        uint8_t* base = sB + s_row * lay.bs_sample + (j0 >> 6) * KR * 128;
-        const int c = j0 & 63;
-        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c)) = make_uint4(p[0], p[1], p[2], p[3]);
-        *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c + 8)) =
-            make_uint4(p[4], p[5], p[6], p[7]);
+          if (q < f.cl && q != crank) dsmem_st_u2(dsmem_addr(dst, q), pk);
+      }
+      fence_proxy_async_cluster();  // the operands feed the tensor cores of every CTA
+    }
+    cluster_sync();  // operands gathered everywhere; peers are done with this CTA's slice
+  } else if (epi) {
+    const int s_row = row / f.Ry;
+    const int r_row = row - s_row * f.Ry;
+    {
+#pragma unroll 1
+      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+        float v[32];
+        tmem_ld32(t1 + j0, v);
+        if (row < real_rows) {
+          uint8_t* base = sB + s_row * lay.bs_sample + (j0 >> 6) * KR * 128;
+          const int c = j0 & 63;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(base + sw128_offset(r_row, c + 8 * q)) =
+                make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        }
       }
     }
     tc_fence_before();
   }
   if (epi) {
     fence_proxy_async_smem();
-    named_barrier(1, 128);
+    named_barrier(1, 256);
     if (et == 0) mbar_arrive(b_ready);
   }
 
@@ -337,28 +347,26 @@ __global__ void __launch_bounds__(192, 1)
       const int buf = j & 1;
       uint8_t* st = stg + buf * (BN / 64) * BOX;
       if (et == 0 && j >= 2) tma_store_wait_read<1>();
-      named_barrier(1, 128);
+      named_barrier(1, 256);
       if (!mbar_wait(&t_full[buf], (j >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
       const uint32_t taddr = tmem + BN + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 16) {
-        float v[16];
-        tmem_ld16(taddr + j0, v);
-        uint32_t p[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p[q] = static_cast<uint32_t>(bf16_bits(v[2 * q])) |
-                 (static_cast<uint32_t>(bf16_bits(v[2 * q + 1])) << 16);
+      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + j0, v);
         uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
         const int c8 = (j0 & 63) >> 3;
-        *reinterpret_cast<uint4*>(box + ((c8 ^ (row & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
-        *reinterpret_cast<uint4*>(box + (((c8 + 1) ^ (row & 7)) << 4)) =
-            make_uint4(p[4], p[5], p[6], p[7]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(box + (((c8 + q) ^ (row & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                         pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      named_barrier(1, 128);
+      named_barrier(1, 256);
       if (et == 0) {
         mbar_arrive(&t_empty[buf]);
         for (int h = 0; h < BN / 64; ++h)
@@ -387,7 +395,7 @@ cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtens
     configured_ = bytes;
   }
   const dim3 grid((f.Cx + BN - 1) / BN, (f.B + f.spt - 1) / f.spt, f.cl);
-  return launch_ex(k_gradx_fused<BN>, grid, dim3(192), bytes, st, f.cl, pdl_enabled(), ts, tw, tq,
+  return launch_ex(k_gradx_fused<BN>, grid, dim3(320), bytes, st, f.cl, pdl_enabled(), ts, tw, tq,
                    to, f);
 }
 
