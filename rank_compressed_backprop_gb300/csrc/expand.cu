@@ -37,7 +37,7 @@ struct Lay {
 __host__ __device__ inline Lay expand_layout(int BN, int KR) {
   Lay l;
   l.stg = 0;
-  l.b = 2 * (BN / 64) * BOX;
+  l.b = 4 * (BN / 64) * BOX;
   l.b_bytes = (BN / 64) * KR * 128;
   l.a = l.b + l.b_bytes;
   l.a_stage = 2 * KR * 128;
@@ -176,22 +176,23 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..9) ----------------
-    // two warps per TMEM lane quarter, each converting half of the columns
-    const int et = threadIdx.x - 64;       // 0..255
-    const int ew = warp - 2;
+    // two groups of four warps (one per TMEM lane quarter); group g handles
+    // tiles g, g+2, ... from accumulator g, so two tiles are converted at once.
+    // Each group double-buffers its staging and tracks its own store groups.
+    const int grp = (warp - 2) >> 2;       // 0 or 1
+    const int gt = (threadIdx.x - 64) & 127;  // thread index within the group
     const int quarter = warp & 3;          // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;   // token row within the tile
-    const int c_lo = (ew >> 2) * (BN / 2);
-    for (int lt = 0; lt < e.nlt; ++lt) {
-      const int buf = lt & 1;
-      uint8_t* st = stg + buf * (BN / 64) * BOX;
-      if (et == 0 && lt >= 2) tma_store_wait_read<1>();
-      named_barrier(1, 256);
-      if (!mbar_wait(&t_full[buf], (lt >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
+    int it = 0;
+    for (int lt = grp; lt < e.nlt; lt += 2, ++it) {
+      uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
+      if (gt == 0 && it >= 2) tma_store_wait_read<1>();
+      named_barrier(1 + grp, 128);
+      if (!mbar_wait(&t_full[grp], it & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
-      const uint32_t taddr = tmem + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t taddr = tmem + grp * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+      for (int j0 = 0; j0 < BN; j0 += 32) {
         float v[32];
         tmem_ld32(taddr + j0, v);
         uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
@@ -205,14 +206,15 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      named_barrier(1, 256);
-      if (et == 0) {
-        mbar_arrive(&t_empty[buf]);
+      named_barrier(1 + grp, 128);
+      if (gt == 0) {
+        mbar_arrive(&t_empty[grp]);
         for (int h = 0; h < BN / 64; ++h)
           if (n0 + 64 * h < e.Cx) tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, lt * BM, b);
         tma_store_commit();
       }
     }
+    const int et = gt;
     if (et == 0) tma_store_wait_all();
   }
   tc_fence_before();

@@ -36,7 +36,7 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   l.stage = A_BYTES + BN * BK * 2;
   l.ring = 0;
   const uint32_t ring_bytes = stages * l.stage;
-  const uint32_t stg_bytes = 2 * (BN / 64) * BOX;  // staging reuses the ring after phase 1
+  const uint32_t stg_bytes = 4 * (BN / 64) * BOX;  // staging reuses the ring after phase 1
   const uint32_t red_bytes = BM * (BN + 4) * 4;     // so does the cluster reduction tile
   uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
   if (red_bytes > first) first = red_bytes;
@@ -339,20 +339,24 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (epi) {
     // phase 3: expansion tiles -> TMA stores (staging reuses the phase-1 ring,
-    // whose TMA writes all completed before acc1 did)
+    // whose TMA writes all completed before acc1 did).  Two groups of four
+    // warps: group g converts jobs g, g+2, ... from accumulator g into its own
+    // two staging buffers and tracks its own store groups.
     fence_proxy_async_smem();
-    for (int j = 0; j < njobs; ++j) {
+    const int grp = (warp - 2) >> 2;
+    const int gt = et & 127;
+    int it = 0;
+    for (int j = grp; j < njobs; j += 2, ++it) {
       const int s = j / nlt;
       const int t = j - s * nlt;
-      const int buf = j & 1;
-      uint8_t* st = stg + buf * (BN / 64) * BOX;
-      if (et == 0 && j >= 2) tma_store_wait_read<1>();
-      named_barrier(1, 256);
-      if (!mbar_wait(&t_full[buf], (j >> 1) & 1)) raise_fault(FAULT_WAIT_DONE);
+      uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
+      if (gt == 0 && it >= 2) tma_store_wait_read<1>();
+      named_barrier(2 + grp, 128);
+      if (!mbar_wait(&t_full[grp], it & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
-      const uint32_t taddr = tmem + BN + buf * BN + (static_cast<uint32_t>(quarter * 32) << 16);
+      const uint32_t taddr = tmem + BN + grp * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int j0 = c_lo; j0 < c_lo + BN / 2; j0 += 32) {
+      for (int j0 = 0; j0 < BN; j0 += 32) {
         float v[32];
         tmem_ld32(taddr + j0, v);
         uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
@@ -366,16 +370,16 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      named_barrier(1, 256);
-      if (et == 0) {
-        mbar_arrive(&t_empty[buf]);
+      named_barrier(2 + grp, 128);
+      if (gt == 0) {
+        mbar_arrive(&t_empty[grp]);
         for (int h = 0; h < BN / 64; ++h)
           if (n0 + 64 * h < f.Cx)
             tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, (lt0 + t) * BM, s0 + s);
         tma_store_commit();
       }
     }
-    if (et == 0) tma_store_wait_all();
+    if (gt == 0) tma_store_wait_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -67,7 +67,7 @@ struct ExpandArgs {
   void* out;         // [B, L, Cx]
 };
 
-constexpr int kExpandStages = 4;
+constexpr int kExpandStages = 2;
 size_t expand_bf16_smem_bytes(const ExpandArgs& e);
 cudaError_t launch_expand_bf16(const CUtensorMap& tmap_q, const CUtensorMap& tmap_g,
                                const CUtensorMap& tmap_out, const ExpandArgs& e, cudaStream_t st);
