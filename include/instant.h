@@ -62,6 +62,8 @@ typedef struct {
   int scale_on;     /* 1: rows scaled by (sum_{i<=R} sigma_i^2)^(-1/2); 0: off   */
   int max_iter;     /* subspace-iteration cap; 0 selects 300                     */
   double tol;       /* Ritz residual tolerance relative to sigma_1; 0 selects 2e-5 */
+  int warm_start;   /* 1: rows_out already holds a projector of this statistic   */
+                    /* (e.g. the previous calibration); its rows seed the solve  */
 } instant_calib_params;
 
 /*

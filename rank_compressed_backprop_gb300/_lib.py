@@ -37,6 +37,7 @@ class CalibParams(ctypes.Structure):
         ("scale_on", ctypes.c_int),
         ("max_iter", ctypes.c_int),
         ("tol", ctypes.c_double),
+        ("warm_start", ctypes.c_int),
     ]
 
 

@@ -184,8 +184,11 @@ class CalibResult:
 def calib_solve(C: torch.Tensor, n_samples: int, rows_out: torch.Tensor, *, eps: float = 0.95,
                 p: int = 0, r_override: int = 0, scale_on: bool = True, max_iter: int = 0,
                 tol: float = 0.0, ws: torch.Tensor | None = None, stream=None,
-                raise_on_error: bool = True):
+                raise_on_error: bool = True, warm_start: bool = False):
     """Projector rows from an accumulated statistic; synchronises the stream.
+
+    With ``warm_start`` the rows already in ``rows_out`` (a previous projector
+    of the same statistic) seed the eigensolver.
 
     Returns a :class:`CalibResult` (and the raw status when ``raise_on_error``
     is False)."""
@@ -195,7 +198,7 @@ def calib_solve(C: torch.Tensor, n_samples: int, rows_out: torch.Tensor, *, eps:
         raise ValueError("calib_solve: inconsistent shapes")
     if ws is None:
         ws = torch.empty(calib_workspace_bytes(L, r_cap), dtype=torch.uint8, device=C.device)
-    prm = CalibParams(eps, p, r_override, int(bool(scale_on)), max_iter, tol)
+    prm = CalibParams(eps, p, r_override, int(bool(scale_on)), max_iter, tol, int(bool(warm_start)))
     k = ctypes.c_int(0)
     R = ctypes.c_int(0)
     s = ctypes.c_float(0)

@@ -512,11 +512,16 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
     if (m < 16) m = 16;
     if (m > 128) m = 128;
     bool converged = false;
+    // warm start: the previous projector rows seed the block; the subspace has
+    // usually moved little, so convergence is checked early and often
+    const bool warm = prm->warm_start != 0;
     for (;;) {
-      if (launch_subspace_init(L, m, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+      const int n_seed = warm ? std::min(r_cap, m) : 0;
+      if (launch_subspace_init(L, m, rows_out, n_seed, out_bf16, w, st) != cudaSuccess)
+        return INSTANT_ERR_CUDA;
       bool grow = false;
       for (int it = 0; it < max_iter; ++it) {
-        const bool check = (it + 1) % 4 == 0 || it == max_iter - 1;
+        const bool check = (warm ? (it + 1) % 2 == 1 : (it + 1) % 4 == 0) || it == max_iter - 1;
         if (launch_subspace_iteration(C, L, m, inv_n, max_sweeps, check ? 1e-5f : 1e-3f, w, st) !=
             cudaSuccess)
           return INSTANT_ERR_CUDA;

@@ -319,10 +319,18 @@ __device__ __forceinline__ float hash_uniform(uint32_t i, uint32_t j) {
   return static_cast<float>(h) * (2.0f / 4294967296.0f) - 1.0f;
 }
 
-__global__ void k_sub_init(int L, int m, SolverWs w) {
+// starting block: columns j < n_seed are the seed rows (a previous projector,
+// row j = column j), the rest deterministic pseudo-random
+__global__ void k_sub_init(int L, int m, const void* seed, int n_seed, int seed_bf16, SolverWs w) {
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < L * m; idx += gridDim.x * blockDim.x) {
     const int i = idx / m, j = idx - (idx / m) * m;
-    w.Z[idx] = hash_uniform(i, j);
+    float v = hash_uniform(i, j);
+    if (j < n_seed) {
+      const size_t o = static_cast<size_t>(j) * L + i;
+      v = seed_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(seed)[o])
+                    : static_cast<const float*>(seed)[o];
+    }
+    w.Z[idx] = v;
   }
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < m * m; idx += gridDim.x * blockDim.x) {
     w.G[idx] = 0.f;
@@ -761,8 +769,9 @@ cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_swee
   return cudaGetLastError();
 }
 
-cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st) {
-  k_sub_init<<<64, 256, 0, st>>>(L, m, w);
+cudaError_t launch_subspace_init(int L, int m, const void* seed, int n_seed, int seed_bf16,
+                                 SolverWs w, cudaStream_t st) {
+  k_sub_init<<<64, 256, 0, st>>>(L, m, seed, n_seed, seed_bf16, w);
   const size_t gb = sizeof(float) * kRows * m;
   k_sub_gram<<<(L + kRows - 1) / kRows, 256, gb, st>>>(L, m, w);
   count_launches(2);

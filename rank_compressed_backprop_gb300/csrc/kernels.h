@@ -150,7 +150,10 @@ cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t
 cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_sweeps, SolverWs w,
                                cudaStream_t st);
 // subspace iteration building blocks
-cudaError_t launch_subspace_init(int L, int m, SolverWs w, cudaStream_t st);
+// seed: optional [n_seed, L] rows (bf16 when seed_bf16) used as the first
+// block columns; the rest is pseudo-random
+cudaError_t launch_subspace_init(int L, int m, const void* seed, int n_seed, int seed_bf16,
+                                 SolverWs w, cudaStream_t st);
 // rr_tol: Jacobi tolerance of the Rayleigh-Ritz step (loose between
 // convergence checks, tight right before one)
 cudaError_t launch_subspace_iteration(const float* C, int L, int m, double inv_n, int max_sweeps,

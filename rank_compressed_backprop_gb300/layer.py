@@ -44,7 +44,6 @@ class InstantLinear:
         self.ws_cal = torch.empty(api.calib_workspace_bytes(L, max(Rx, Ry)), dtype=torch.uint8,
                                   device=dev)
         self.last_calibration = None
-        self._side = torch.cuda.Stream(device=dev)
 
     # views of the stacked projector
     @property
@@ -68,15 +67,9 @@ class InstantLinear:
         gw = self.gw if gw is None else gw
         gx = self.gx if gx is None else gx
         B = g_y.shape[0]
-        main = torch.cuda.current_stream()
         api.project_grad(g_y, self.PQ, self.Sx, self.Sq, self.Rx, self.Ry)
-        # g_w and g_tilde_x only share the projection's outputs: run them
-        # concurrently (fork/join; also valid inside CUDA-graph capture)
-        self._side.wait_stream(main)
-        with torch.cuda.stream(self._side):
-            api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
+        api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
         api.grad_x(self.Sq, self.w, self.Q, gx, self.ws_gx)
-        main.wait_stream(self._side)
         return gw, gx
 
     # ---- calibration --------------------------------------------------------
@@ -96,12 +89,13 @@ class InstantLinear:
         ``k`` and ``k + p`` are still reported."""
         if self.n_x == 0 or self.n_g == 0:
             raise RuntimeError("recalibrate: no statistics accumulated")
+        warm = self.last_calibration is not None
         rx = api.calib_solve(self.C_X, self.n_x, self.P, eps=self.eps, p=self.p,
                              r_override=self.Rx if r_override else 0, scale_on=self.scale_on,
-                             ws=self.ws_cal)
+                             ws=self.ws_cal, warm_start=warm)
         rg = api.calib_solve(self.C_G, self.n_g, self.Q, eps=self.eps, p=self.p,
                              r_override=self.Ry if r_override else 0, scale_on=self.scale_on,
-                             ws=self.ws_cal)
+                             ws=self.ws_cal, warm_start=warm)
         self.C_X.zero_()
         self.C_G.zero_()
         self.n_x = self.n_g = 0

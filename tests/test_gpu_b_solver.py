@@ -93,3 +93,23 @@ def test_flat_tail_needs_more_rank(torch):
     C = _planted_C(41, L, lam, n=4)
     _check(torch, C, 4, eps=0.9, p=2, r_override=0, scale_on=True, r_cap=32,
            out_dtype=torch.float32)
+
+
+def test_warm_start_reproduces_the_cold_solve(torch):
+    from rank_compressed_backprop_gb300 import api
+
+    L = 512
+    lam = 1e5 * np.arange(1, L + 1, dtype=np.float64) ** -3.0 + 7.0
+    C = to_dev(_planted_C(77, L, lam, n=64))
+    cold = torch.empty(8, L, dtype=torch.bfloat16, device="cuda")
+    r0 = api.calib_solve(C, 64, cold, eps=0.95, p=2, r_override=8)
+    warm = cold.clone()
+    r1 = api.calib_solve(C, 64, warm, eps=0.95, p=2, r_override=8, warm_start=True)
+    assert (r1.k, r1.R) == (r0.k, r0.R)
+    assert abs(r1.scale - r0.scale) <= 1e-5 * r0.scale
+    assert float((warm.float() - cold.float()).abs().max()) <= 2e-2 * float(cold.float().abs().max())
+    # a warm start from an unrelated projector still converges to the same answer
+    other = torch.randn(8, L, device="cuda").to(torch.bfloat16)
+    r2 = api.calib_solve(C, 64, other, eps=0.95, p=2, r_override=8, warm_start=True)
+    assert (r2.k, r2.R) == (r0.k, r0.R)
+    assert float((other.float() - cold.float()).abs().max()) <= 2e-2 * float(cold.float().abs().max())
