@@ -137,6 +137,34 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
                               instant_dtype dt, void* stream);
 
 /*
+ * instant_grad_x without a workspace argument.  The page has no counterpart:
+ * this is a convenience of the library for callers that cannot allocate
+ * device memory -- a C host linking only this library, with no device
+ * allocator of its own, or a training loop whose device memory is planned at
+ * start-up and must not grow (or synchronise on a cudaMalloc) afterwards.
+ *
+ * Same arguments, result and limits as instant_grad_x, minus ws/ws_bytes.  It
+ * always runs the two-kernel form (instant_grad_x_core, then instant_expand)
+ * with g_hat_x in a fixed device array of INSTANT_GRAD_X_STATIC_SCRATCH_BYTES
+ * bytes that belongs to the library's CUDA module; no device memory is
+ * allocated or freed by the call.
+ *   - Returns INSTANT_ERR_WORKSPACE when the intermediate,
+ *     instant_grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt) bytes, is larger
+ *     than INSTANT_GRAD_X_STATIC_SCRATCH_BYTES; nothing is launched then.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current (this may load the module there); make that first
+ *     call before any stream capture begins.
+ *   - There is one array per device, shared by every call on it: two calls
+ *     whose executions overlap on one device (other streams, other host
+ *     threads) race on it and both results are undefined.  Serialise them,
+ *     e.g. by issuing them on one stream.
+ */
+#define INSTANT_GRAD_X_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+instant_status instant_grad_x_static(const void* Sq, const void* w, const void* Q, void* gx,
+                                     int B, int L, int Cx, int Cy, int Ry,
+                                     instant_dtype dt, void* stream);
+
+/*
  * Autocorrelation statistic (关键设计 1: C = E[t t^T], only statistics are
  * accumulated during calibration, not the batch):
  *   C += sum_b t_b t_b^T

@@ -15,6 +15,9 @@ LIB_PATH = os.path.join(_HERE, "libinstant.so")
 INSTANT_F32 = 0
 INSTANT_BF16 = 1
 
+# size of the library's fixed g_hat_x array (INSTANT_GRAD_X_STATIC_SCRATCH_BYTES)
+GRAD_X_STATIC_SCRATCH_BYTES = 8 << 20
+
 STATUS_NAMES = {
     0: "INSTANT_OK",
     1: "INSTANT_ERR_ARG",
@@ -60,6 +63,7 @@ _PROTOS = {
     "instant_grad_x_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "instant_grad_x_core": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _vp]),
     "instant_expand": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
+    "instant_grad_x_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_calib_accumulate": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),
     "instant_calib_solve": (_i, [_vp, ctypes.c_longlong, _i, ctypes.POINTER(CalibParams), _vp, _i,
                                  _i, ctypes.POINTER(_i), ctypes.POINTER(_i),

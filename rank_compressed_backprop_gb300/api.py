@@ -12,7 +12,7 @@ import dataclasses
 
 import torch
 
-from ._lib import INSTANT_BF16, INSTANT_F32, CalibParams, check, lib
+from ._lib import GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, CalibParams, check, lib
 
 __all__ = [
     "compress_act",
@@ -22,6 +22,7 @@ __all__ = [
     "grad_x_workspace_bytes",
     "grad_x_core",
     "expand",
+    "grad_x_static",
     "launch_count",
     "calib_accumulate",
     "calib_solve",
@@ -138,6 +139,29 @@ def grad_x_core(Sq: torch.Tensor, w: torch.Tensor, ws: torch.Tensor, B: int, str
                                     ws.numel() * ws.element_size(), B, Cx, Cy, Ry,
                                     dtype_code(Sq.dtype), _stream(stream)), "instant_grad_x_core")
     return ws
+
+
+def grad_x_static(Sq: torch.Tensor, w: torch.Tensor, Q: torch.Tensor, gx: torch.Tensor,
+                  stream=None) -> torch.Tensor:
+    """:func:`grad_x` for callers that cannot allocate device memory: no
+    workspace argument; ``g_hat_x`` lives in a fixed array of the library
+    (``GRAD_X_STATIC_SCRATCH_BYTES`` per device) that every call on a device
+    shares, so calls must not overlap in time.  The first call on a device
+    looks the array up and should come before any stream capture."""
+    B, L, Cx = gx.shape
+    Ry = Q.shape[0]
+    Cy = w.shape[0]
+    if Q.shape != (Ry, L) or w.shape != (Cy, Cx) or Sq.shape != (B * Ry, Cy):
+        raise ValueError("grad_x_static: inconsistent shapes")
+    _same_dtype(Sq.dtype, ("w", w), ("Q", Q), ("gx", gx))
+    status = lib().instant_grad_x_static(_dev(Sq, "Sq"), _dev(w, "w"), _dev(Q, "Q"), _dev(gx, "gx"),
+                                         B, L, Cx, Cy, Ry, dtype_code(Sq.dtype), _stream(stream))
+    if status == 5:
+        need = grad_x_workspace_bytes(B, L, Cx, Cy, Ry, Sq.dtype)
+        raise ValueError(f"grad_x_static: g_hat_x needs {need} bytes, more than the "
+                         f"{GRAD_X_STATIC_SCRATCH_BYTES}-byte fixed array; use grad_x with a workspace")
+    check(status, "instant_grad_x_static")
+    return gx
 
 
 def expand(Q: torch.Tensor, gx: torch.Tensor, ws: torch.Tensor, Cy: int, stream=None):
