@@ -111,13 +111,11 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   }
   a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
-  // split the token axis over a 2-CTA cluster when that balances the SMs better
+  // one CTA per (128-column tile, sample) over the whole token axis: three
+  // CTAs fit on an SM, so the grid is resident at once, and a token split's
+  // cluster reduction costs more than the balance it buys (measured on GB300
+  // from 2 to 64 samples of a BERT-base block)
   a.splits = 1;
-  if (a.NT <= 64 && a.nk >= 4) {
-    const int units = cdiv(C, 128) * B;
-    auto eff = [](int u) { return static_cast<double>(u) / (152.0 * cdiv(u, 152)); };
-    if (eff(2 * units) > eff(units) + 0.05) a.splits = 2;
-  }
   CUtensorMap mt, mpq;
   std::memset(&mpq, 0, sizeof(mpq));
   const uint64_t dt3[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&t_full[i], 1);
-      mbar_init(&t_empty[i], 1);
+      mbar_init(&t_empty[i], 4);  // one arrival per warp of the epilogue group
     }
     fence_barrier_init();
     prefetch_tmap(&tmap_sq);
@@ -356,23 +356,27 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const uint32_t taddr = tmem + BN + grp * BN + (static_cast<uint32_t>(quarter * 32) << 16);
 #pragma unroll 1
-      for (int j0 = 0; j0 < BN; j0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + j0, v);
-        uint8_t* box = st + (j0 >> 6) * BOX + row * 128;
-        const int c8 = (j0 & 63) >> 3;
+      for (int h = 0; h < BN / 64; ++h) {
+        float v[64];
+        tmem_ld64(taddr + 64 * h, v);
+        if (h == BN / 64 - 1) {
+          // this warp has read its lanes of the accumulator: hand it back to
+          // the MMA issuer before converting
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&t_empty[grp]);
+        }
+        uint8_t* box = st + h * BOX + row * 128;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(box + (((c8 + q) ^ (row & 7)) << 4)) =
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(box + ((q ^ (row & 7)) << 4)) =
               make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
-      tc_fence_before();
       fence_proxy_async_smem();
       named_barrier(2 + grp, 128);
       if (gt == 0) {
-        mbar_arrive(&t_empty[grp]);
         for (int h = 0; h < BN / 64; ++h)
           if (n0 + 64 * h < f.Cx)
             tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, (lt0 + t) * BM, s0 + s);
