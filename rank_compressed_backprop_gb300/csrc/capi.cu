@@ -491,8 +491,58 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
   const int out_bf16 = dt == INSTANT_BF16 ? 1 : 0;
 
   SolverWs w = solver_carve(ws, L);
-  if (launch_solver_energy(C, L, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
   SolverResult res;
+  // block: the needed rank plus a margin for the convergence rate
+  const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
+  int m_block = std::min(128, std::max(16, round_up(std::max(2 * r_guess, r_guess + 8), 16)));
+  const bool warm = prm->warm_start != 0;
+  if (L > 128 && cluster_solve_fits(L, m_block) && !std::getenv("INSTANT_SOLVER_MULTI")) {
+    // the whole iteration in one launch of an 8-CTA cluster, checked on the device
+    ClusterSolveArgs ca;
+    ca.C = C;
+    ca.L = L;
+    ca.m = m_block;
+    ca.rp = 0;
+    ca.inv_n = static_cast<float>(inv_n);
+    ca.inv_n2 = inv_n2;
+    ca.eps = prm->eps;
+    ca.p = prm->p;
+    ca.r_override = prm->r_override;
+    ca.scale_on = prm->scale_on ? 1 : 0;
+    ca.tol = tol;
+    ca.max_iter = max_iter;
+    ca.max_sweeps = max_sweeps;
+    ca.rr_tol = 1e-5f;
+    ca.seed = rows_out;
+    ca.n_seed = warm ? std::min(r_cap, m_block) : 0;
+    ca.seed_bf16 = out_bf16;
+    ca.rows_out = rows_out;
+    ca.r_cap = r_cap;
+    ca.out_bf16 = out_bf16;
+    ca.res = w.res;
+    if (launch_cluster_solve(ca, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+    if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return INSTANT_ERR_CUDA;
+    const double E1 = res.energy_sum * inv_n2;
+    if (res.nonfinite || !std::isfinite(E1) || !(E1 > 0.0)) return INSTANT_ERR_NONFINITE;
+    if (!res.block_short) {
+      instant_status st1 = res.converged ? INSTANT_OK : INSTANT_ERR_NOT_CONVERGED;
+      if (res.jacobi_failed) st1 = INSTANT_ERR_NOT_CONVERGED;
+      if (res.R > r_cap) st1 = INSTANT_ERR_SHAPE;
+      *k_out = res.k;
+      *r_out = res.R < r_cap ? res.R : r_cap;
+      *scale_out = res.scale;
+      if (energy_out) *energy_out = E1;
+      if (eig_out)
+        for (int i = 0; i < r_cap; ++i) eig_out[i] = i < m_block ? res.theta[i] : 0.0;
+      return st1;
+    }
+    // k + p did not fit the block: continue below with a larger one (rows_out
+    // still holds the caller's seed)
+    m_block = std::min(128, 2 * m_block);
+  }
+  if (launch_solver_energy(C, L, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
   if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
       cudaStreamSynchronize(st) != cudaSuccess)
     return INSTANT_ERR_CUDA;
@@ -504,15 +554,10 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
   if (L <= 128) {
     if (launch_jacobi_full(C, L, inv_n, max_sweeps, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
   } else {
-    // block: the needed rank plus a margin for the convergence rate
-    const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
-    m = round_up(std::max(2 * r_guess, r_guess + 8), 16);
-    if (m < 16) m = 16;
-    if (m > 128) m = 128;
+    m = m_block;
     bool converged = false;
     // warm start: the previous projector rows seed the block; the subspace has
     // usually moved little, so convergence is checked early and often
-    const bool warm = prm->warm_start != 0;
     for (;;) {
       const int n_seed = warm ? std::min(r_cap, m) : 0;
       if (launch_subspace_init(L, m, rows_out, n_seed, out_bf16, w, st) != cudaSuccess)

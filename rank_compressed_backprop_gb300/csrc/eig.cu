@@ -270,7 +270,7 @@ __device__ JacSmem jac_carve(uint8_t* smem, int n) {
   return s;
 }
 
-size_t jac_smem_bytes(int n) {
+__host__ __device__ inline size_t jac_smem_bytes(int n) {
   const int ld = n + 1;
   const int N = n + (n & 1);
   return sizeof(float) * (3 * N * ld + kMaxBlock + 2 + 32) + sizeof(int) * (kMaxBlock + 2 + kMaxBlock);
@@ -358,33 +358,29 @@ __global__ void k_sub_gram(int L, int m, SolverWs w) {
   }
 }
 
-// 1 CTA: T with Z T orthonormal, from the Gram matrix G = Z^T Z; zeroes G.
+// T with Z T orthonormal, from the Gram matrix G = Z^T Z (m x m, row stride
+// ldg), written to T (row stride ldt); the whole CTA takes part.
 // Columns are first normalised (D = diag(G)^(-1/2)); the normalised Gram
 // matrix of near-orthogonal Ritz directions is close to I, so a Cholesky
 // factorisation D G D = L L^T is stable and T = D L^(-T).  When a pivot
 // vanishes (Z rank deficient) the symmetric (Lowdin) form T = D W Lambda^(-1/2)
 // from a Jacobi eigensolve is used instead; it zeroes the null directions.
-__global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps, SolverWs w) {
-  pdl_launch_dependents();
-  pdl_wait();
-  extern __shared__ uint8_t smem[];
-  JacSmem s = jac_carve(smem, m);
+// Returns false when that Jacobi solve hit its sweep cap.  G before the first Cholesky step and T is written last, so G and
+// T may share storage.
+__device__ bool orth_core(const float* G, int ldg, int m, int max_sweeps, JacSmem s, float* T,
+                          int ldt, float* dsc, float* pv, int* deficient) {
   const int ld = m + 1;
-  __shared__ float dsc[kMaxBlock];
-  __shared__ float pv[kMaxBlock];
-  __shared__ int deficient;
   for (int i = threadIdx.x; i < m; i += blockDim.x) {
-    const float g = w.G[i * m + i];
+    const float g = G[i * ldg + i];
     dsc[i] = g > 0.f ? 1.f / sqrtf(g) : 0.f;
   }
-  if (threadIdx.x == 0) deficient = 0;
+  if (threadIdx.x == 0) *deficient = 0;
   __syncthreads();
   for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
     const int i = idx / m, j = idx - (idx / m) * m;
-    s.A[i * ld + j] = 0.5f * (w.G[i * m + j] + w.G[j * m + i]) * dsc[i] * dsc[j];
+    s.A[i * ld + j] = 0.5f * (G[i * ldg + j] + G[j * ldg + i]) * dsc[i] * dsc[j];
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.G[idx] = 0.f;
   // ---- Cholesky (elimination form in V, so that A survives for the fallback):
   // step k subtracts a_ik a_jk / a_kk from the trailing block; column k is then
   // final and L = (column k) / sqrt(a_kk).  One barrier per step.
@@ -397,7 +393,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
   for (int k = 0; k < m; ++k) {
     const float d = Lc[k * ld + k];
     if (!(d > 1e-6f)) {
-      if (threadIdx.x == 0) deficient = 1;
+      if (threadIdx.x == 0) *deficient = 1;
       break;
     }
     const int rem = m - k - 1;
@@ -409,7 +405,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     __syncthreads();
   }
   __syncthreads();
-  if (!deficient) {
+  if (!*deficient) {
     for (int j = threadIdx.x; j < m; j += blockDim.x) pv[j] = rsqrtf(Lc[j * ld + j]);
     __syncthreads();
     for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
@@ -418,7 +414,7 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     }
   }
   __syncthreads();
-  if (!deficient) {
+  if (!*deficient) {
     // T = D L^-T.  s.A is free now: X = L^-1 by forward substitution, one
     // thread per column j (each thread reads only the entries it wrote)
     for (int j = threadIdx.x; j < m; j += blockDim.x) {
@@ -432,9 +428,10 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     // T[a][c] = D_a * (L^-T)[a][c] = D_a * X[c][a]
     for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) {
       const int a = idx / m, c = idx - (idx / m) * m;
-      w.T[a * m + c] = dsc[a] * s.A[c * ld + a];
+      T[a * ldt + c] = dsc[a] * s.A[c * ld + a];
     }
-    return;
+    __syncthreads();
+    return true;
   }
   // ---- fallback: symmetric orthonormalisation (A still holds D G D) ----
   const bool ok = block_jacobi(s.A, s.A2, s.V, m, ld, 1e-5f, max_sweeps, s.cs, s.pairs, s.red);
@@ -444,8 +441,23 @@ __global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps,
     const int a = idx / m, j = idx - (idx / m) * m;
     const float lam = s.A[j * ld + j];
     const float f = lam > 1e-10f * lmax ? 1.f / sqrtf(lam) : 0.f;
-    w.T[a * m + j] = dsc[a] * s.V[a * ld + j] * f;
+    T[a * ldt + j] = dsc[a] * s.V[a * ld + j] * f;
   }
+  __syncthreads();
+  return ok;
+}
+
+// 1 CTA: T from the Gram matrix G (see orth_core); zeroes G for the next step
+__global__ void __launch_bounds__(kJacThreads) k_sub_orth(int m, int max_sweeps, SolverWs w) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ uint8_t smem[];
+  JacSmem s = jac_carve(smem, m);
+  __shared__ float dsc[kMaxBlock];
+  __shared__ float pv[kMaxBlock];
+  __shared__ int deficient;
+  const bool ok = orth_core(w.G, m, m, max_sweeps, s, w.T, m, dsc, pv, &deficient);
+  for (int idx = threadIdx.x; idx < m * m; idx += blockDim.x) w.G[idx] = 0.f;
   if (threadIdx.x == 0 && !ok) w.res->jacobi_failed = 1;
 }
 
@@ -712,6 +724,601 @@ __global__ void k_finalize(int L, int m, double eps, int p, int r_override, int 
   }
 }
 
+// ---------------------------------------------------------------------------
+// whole subspace iteration in one launch: a cluster of 8 CTAs (128 < L <= 512,
+// block m <= 32).  CTA q owns rows [q*rp, (q+1)*rp) of every tall matrix and
+// streams the same rows of C for Y = C V / n, gathering the rest of V from its
+// peers' shared memory.  The m x m steps (Rayleigh-Ritz Jacobi, Cholesky-QR,
+// convergence test) run in every CTA on partial sums that each CTA adds in
+// rank order, so all CTAs hold identical copies; the decision to stop is
+// still taken from rank 0 so that every CTA leaves the loop together.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ double dsmem_ld_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// Jacobi of order M (even, <= 32) with one barrier per round: every thread
+// recomputes, from the matrix at the start of the round, the rotations of the
+// pairs it touches (the same values block_jacobi computes once per pair), so
+// no rotation table and no second barrier are needed.  Rotation formula,
+// ordering and stopping rule are block_jacobi's; A is double-buffered in A/A2.
+template <int M>
+__device__ bool jacobi_fast(float* A, float* A2, float* V, int ld, float tol, int max_sweeps,
+                            float* red) {
+  constexpr int H = M / 2;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  for (int idx = tid; idx < M * M; idx += nthr) {
+    const int i = idx / M, j = idx % M;
+    V[i * ld + j] = (i == j) ? 1.f : 0.f;
+  }
+  __syncthreads();
+  float* Ao = A;
+  float* An = A2;
+  bool converged = false;
+  float prev = 0.f;
+  for (int sweep = 0; sweep <= max_sweeps; ++sweep) {
+    float off = 0.f, tot = 0.f;
+    for (int idx = tid; idx < M * M; idx += nthr) {
+      const int i = idx / M, j = idx % M;
+      const float v = Ao[i * ld + j];
+      tot += v * v;
+      if (i != j) off += v * v;
+    }
+    off = block_sum_f(off, red);
+    tot = block_sum_f(tot, red);
+    if (off <= tol * tol * tot || tot == 0.f) {
+      converged = true;
+      break;
+    }
+    if (sweep >= 3 && off > 0.25f * prev && off <= 1e-8f * tot) {
+      converged = true;
+      break;
+    }
+    prev = off;
+    if (sweep == max_sweeps) break;
+    for (int r = 0; r < M - 1; ++r) {
+      for (int idx = tid; idx < H * H; idx += nthr) {
+        const int k = idx / H, k2 = idx % H;
+        int p, q, p2, q2;
+        jac_pair(r, k, M, p, q);
+        jac_pair(r, k2, M, p2, q2);
+        float c1, s1, c2, s2;
+        jac_rot(Ao, ld, p, q, c1, s1);
+        jac_rot(Ao, ld, p2, q2, c2, s2);
+        const float a = Ao[p * ld + p2], b = Ao[p * ld + q2];
+        const float c = Ao[q * ld + p2], d = Ao[q * ld + q2];
+        const float y00 = c1 * a - s1 * c, y01 = c1 * b - s1 * d;
+        const float y10 = s1 * a + c1 * c, y11 = s1 * b + c1 * d;
+        An[p * ld + p2] = c2 * y00 - s2 * y01;
+        An[p * ld + q2] = s2 * y00 + c2 * y01;
+        An[q * ld + p2] = c2 * y10 - s2 * y11;
+        An[q * ld + q2] = s2 * y10 + c2 * y11;
+      }
+      for (int idx = tid; idx < M * H; idx += nthr) {
+        const int k = idx / M, i = idx % M;
+        int p, q;
+        jac_pair(r, k, M, p, q);
+        float c, sn;
+        jac_rot(Ao, ld, p, q, c, sn);
+        if (sn == 0.f) continue;
+        const float vp = V[i * ld + p], vq = V[i * ld + q];
+        V[i * ld + p] = c * vp - sn * vq;
+        V[i * ld + q] = sn * vp + c * vq;
+      }
+      __syncthreads();
+      float* t = Ao;
+      Ao = An;
+      An = t;
+    }
+  }
+  if (Ao != A) {
+    for (int idx = tid; idx < M * M; idx += nthr) {
+      const int i = idx / M, j = idx % M;
+      A[i * ld + j] = Ao[i * ld + j];
+    }
+  }
+  __syncthreads();
+  return converged;
+}
+
+// Cholesky factor of the column-normalised Gram matrix: D = diag(G)^(-1/2)
+// into dsc, L (lower, D G D = L L^T) into Lf.  Whole CTA, one barrier per
+// column.  Returns false (uniformly) when a pivot vanishes; G is only read.
+template <int M>
+__device__ bool chol_block(const float* G, int ld, float* Lf, float* dsc, float* pv, int* flag) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  for (int i = tid; i < M; i += nthr) {
+    const float g = G[i * ld + i];
+    dsc[i] = g > 0.f ? 1.f / sqrtf(g) : 0.f;
+  }
+  if (tid == 0) *flag = 0;
+  __syncthreads();
+  for (int idx = tid; idx < M * M; idx += nthr) {
+    const int i = idx / M, j = idx % M;
+    Lf[i * ld + j] = j <= i ? 0.5f * (G[i * ld + j] + G[j * ld + i]) * dsc[i] * dsc[j] : 0.f;
+  }
+  __syncthreads();
+  for (int k = 0; k < M; ++k) {
+    const float d = Lf[k * ld + k];
+    if (!(d > 1e-6f)) {
+      if (tid == 0) *flag = 1;
+      break;
+    }
+    const float inv = 1.f / d;
+    for (int idx = tid; idx < M * M; idx += nthr) {
+      const int i = idx / M, j = idx % M;
+      if (k < j && j <= i) Lf[i * ld + j] -= Lf[i * ld + k] * Lf[j * ld + k] * inv;
+    }
+    __syncthreads();
+  }
+  __syncthreads();
+  if (*flag) return false;
+  for (int j = tid; j < M; j += nthr) pv[j] = rsqrtf(Lf[j * ld + j]);
+  __syncthreads();
+  for (int idx = tid; idx < M * M; idx += nthr) {
+    const int i = idx / M, j = idx % M;
+    if (j <= i) Lf[i * ld + j] *= pv[j];
+  }
+  __syncthreads();
+  return true;
+}
+
+// error-free sum of two floats (Knuth's two-sum): a + b = s + e exactly
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// one exact square added to a double-float (hi, lo) accumulator
+__device__ __forceinline__ void add_square(float v, float& hi, float& lo, int& bad) {
+  if (!isfinite(v)) bad = 1;
+  const float sq = v * v;
+  const float sq_err = fmaf(v, v, -sq);
+  float sum, err;
+  two_sum(hi, sq, sum, err);
+  hi = sum;
+  lo += err + sq_err;
+}
+
+constexpr int kCvTileRows = 64;  // rows of C per CTA (L <= 512)
+constexpr int kCvTileL = 64;     // columns of C per staged tile
+constexpr int kCvTileLd = 68;    // padded row stride: 16-byte rows, conflict-free column reads
+
+// stage columns [t * 64, t * 64 + 64) of the CTA's rows of C into a tile
+__device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int nr, int L, int t,
+                                             bool vec) {
+  const int l0 = t * kCvTileL;
+  for (int i = threadIdx.x; i < kCvTileRows * (kCvTileL / 4); i += blockDim.x) {
+    const int rr = i / (kCvTileL / 4), c4 = (i - rr * (kCvTileL / 4)) * 4;
+    float* d = dst + rr * kCvTileLd + c4;
+    if (vec && rr < nr && l0 + c4 + 4 <= L) {
+      cp_async16(d, Cown + static_cast<size_t>(rr) * L + l0 + c4);
+    } else {
+      for (int e = 0; e < 4; ++e)
+        d[e] = (rr < nr && l0 + c4 + e < L) ? Cown[static_cast<size_t>(rr) * L + l0 + c4 + e] : 0.f;
+    }
+  }
+  cp_async_commit();
+}
+
+struct ClusterLay {
+  uint32_t V, Y, Z, U, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
+      ct, total;
+};
+
+__host__ __device__ inline uint32_t lay_take(uint32_t& o, size_t bytes) {
+  const uint32_t r = o;
+  o = static_cast<uint32_t>((o + bytes + 15u) & ~static_cast<size_t>(15u));
+  return r;
+}
+
+__host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
+  ClusterLay c;
+  uint32_t o = 0;
+  c.V = lay_take(o, 4u * L * m);       // the whole basis, gathered each iteration
+  c.Y = lay_take(o, 4u * rp * m);      // own rows of Y = C V / n
+  c.Z = lay_take(o, 4u * rp * m);      // own rows of Z = Y W (or Y)
+  c.U = lay_take(o, 4u * rp * m);      // own rows of the Ritz vectors U = V W
+  c.Hp = lay_take(o, 4u * m * m);      // partial V^T Y (read by the peers)
+  c.Gp = lay_take(o, 4u * m * m);      // partial Z^T Z (read by the peers)
+  c.resp = lay_take(o, 4u * m);        // partial residual norms (read by the peers)
+  c.r2 = lay_take(o, 4u * m);          // summed residual norms
+  c.W = lay_take(o, 4u * m * (m + 1)); // Ritz rotation, columns by descending theta
+  c.T = lay_take(o, 4u * m * (m + 1)); // summed Gram matrix; Z -> V transform on the fallback
+  c.Lf = lay_take(o, 4u * m * (m + 1)); // Cholesky factor of the normalised Gram matrix
+  c.th = lay_take(o, 8u * m);          // Ritz values (descending)
+  c.dpart = lay_take(o, 8u);           // partial energy (read by the peers)
+  c.ipart = lay_take(o, 16u);          // partial non-finite flag (read by the peers)
+  c.aval = lay_take(o, 4u * m);        // per column: entry of largest magnitude (peers)
+  c.aidx = lay_take(o, 4u * m);        // ... and its row (peers)
+  c.flag = lay_take(o, 16u);           // rank 0's decision (read by the peers)
+  c.dsc = lay_take(o, 4u * kMaxBlock);
+  c.pv = lay_take(o, 4u * kMaxBlock);
+  c.jac = lay_take(o, jac_smem_bytes(m));
+  c.ct = lay_take(o, 4u * 2 * kCvTileRows * kCvTileLd);  // two C tiles for Y = C V
+  c.total = o;
+  return c;
+}
+
+constexpr int kClusterCtas = 8;
+constexpr int kClusterThreads = 256;
+
+template <int M>
+__global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSolveArgs a) {
+  extern __shared__ __align__(16) uint8_t csm[];
+  constexpr int m = M;
+  const int L = a.L, rp = a.rp;
+  const ClusterLay lay = cluster_layout(L, m, rp);
+  float* Vall = reinterpret_cast<float*>(csm + lay.V);
+  float* Y = reinterpret_cast<float*>(csm + lay.Y);
+  float* Z = reinterpret_cast<float*>(csm + lay.Z);
+  float* U = reinterpret_cast<float*>(csm + lay.U);
+  float* Hp = reinterpret_cast<float*>(csm + lay.Hp);
+  float* Gp = reinterpret_cast<float*>(csm + lay.Gp);
+  float* resp = reinterpret_cast<float*>(csm + lay.resp);
+  float* r2 = reinterpret_cast<float*>(csm + lay.r2);
+  float* W = reinterpret_cast<float*>(csm + lay.W);
+  float* T = reinterpret_cast<float*>(csm + lay.T);
+  float* Lf = reinterpret_cast<float*>(csm + lay.Lf);
+  double* th = reinterpret_cast<double*>(csm + lay.th);
+  double* dpart = reinterpret_cast<double*>(csm + lay.dpart);
+  int* ipart = reinterpret_cast<int*>(csm + lay.ipart);
+  float* aval = reinterpret_cast<float*>(csm + lay.aval);
+  int* aidx = reinterpret_cast<int*>(csm + lay.aidx);
+  int* flag = reinterpret_cast<int*>(csm + lay.flag);
+  float* dsc = reinterpret_cast<float*>(csm + lay.dsc);
+  float* pv = reinterpret_cast<float*>(csm + lay.pv);
+  JacSmem js = jac_carve(csm + lay.jac, m);
+  float* Ct = reinterpret_cast<float*>(csm + lay.ct);
+  __shared__ double s_E;
+  __shared__ int s_bad, s_dec, s_jfail, s_deficient, s_cflag, s_useT, s_k, s_R;
+  __shared__ float s_scale;
+  __shared__ double wred[kClusterThreads / 32];
+
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int rank = blockIdx.z;  // == rank in the cluster (dims 1 x 1 x 8)
+  const int r0 = rank * rp;
+  const int nr = min(rp, L - r0);  // >= 1 for 128 < L (host guarantees rp * 7 < L)
+  constexpr int ld = m + 1;
+  const float* Cown = a.C + static_cast<size_t>(r0) * L;
+
+  // ---- energy ||C||_F^2 and finiteness, summed over the cluster ----
+  {
+    // per thread a double-float (hi, lo) sum of exact squares: fp32 arithmetic
+    // only (fp64 units are scarce), about fp64 accuracy
+    float hi = 0.f, lo = 0.f;
+    int bad = 0;
+    const int count = nr * L;
+    if ((count & 3) == 0 && (reinterpret_cast<uintptr_t>(Cown) & 15) == 0) {
+      const float4* c4 = reinterpret_cast<const float4*>(Cown);
+#pragma unroll 8
+      for (int i = tid; i < count / 4; i += nthr) {
+        const float4 v = __ldg(c4 + i);
+        add_square(v.x, hi, lo, bad);
+        add_square(v.y, hi, lo, bad);
+        add_square(v.z, hi, lo, bad);
+        add_square(v.w, hi, lo, bad);
+      }
+    } else {
+#pragma unroll 8
+      for (int i = tid; i < count; i += nthr) add_square(__ldg(Cown + i), hi, lo, bad);
+    }
+    double acc = static_cast<double>(hi) + static_cast<double>(lo);
+    acc = warp_sum_d(acc);
+    bad = __syncthreads_or(bad);
+    if ((tid & 31) == 0) wred[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int i = 0; i < nthr / 32; ++i) t += wred[i];
+      dpart[0] = t;
+      ipart[0] = bad;
+      s_jfail = 0;
+    }
+  }
+  cluster_sync();
+  if (tid == 0) {
+    double t = 0.0;
+    int bad = 0;
+    for (int q = 0; q < kClusterCtas; ++q) {
+      t += dsmem_ld_f64(dsmem_addr(dpart, q));
+      bad |= dsmem_ld_s32(dsmem_addr(ipart, q));
+    }
+    s_E = t;
+    s_bad = bad;
+  }
+  __syncthreads();
+  const double E = s_E * a.inv_n2;
+  if (rank == 0 && tid == 0) {
+    a.res->energy_sum = s_E;
+    a.res->nonfinite = s_bad;
+  }
+  if (s_bad || !isfinite(E) || !(E > 0.0)) {
+    cluster_sync();
+    return;
+  }
+
+  // ---- starting block (own rows): seed rows first, then pseudo-random ----
+  for (int idx = tid; idx < nr * m; idx += nthr) {
+    const int r = idx / m, j = idx % m;
+    const int i = r0 + r;
+    float v = hash_uniform(i, j);
+    if (j < a.n_seed) {
+      const size_t o = static_cast<size_t>(j) * L + i;
+      v = a.seed_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(a.seed)[o])
+                      : static_cast<const float*>(a.seed)[o];
+    }
+    Z[idx] = v;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < m * m; idx += nthr) {
+    const int p = idx / m, q = idx % m;
+    float g = 0.f;
+    for (int r = 0; r < nr; ++r) g = fmaf(Z[r * m + p], Z[r * m + q], g);
+    Gp[idx] = g;
+  }
+
+  int dec = 0;  // 1 converged, 2 block too short, 3 iteration cap
+  constexpr int cpg = m / 4;  // columns per thread group in C V
+  float* Vown = Vall + static_cast<size_t>(r0) * m;
+  for (int it = 0;; ++it) {
+    // ---- orthonormalise Z (Gram partials in Gp): V = Z D L^-T ----
+    cluster_sync();
+    for (int idx = tid; idx < m * m; idx += nthr) {
+      float g = 0.f;
+      for (int q = 0; q < kClusterCtas; ++q) g += dsmem_ld_f32(dsmem_addr(Gp + idx, q));
+      T[(idx / m) * ld + idx % m] = g;
+    }
+    __syncthreads();
+    if (chol_block<M>(T, ld, Lf, dsc, pv, &s_cflag)) {
+      // each row v of V solves v L^T = z D by forward substitution
+      for (int r = tid; r < nr; r += nthr) {
+        float v[M];
+#pragma unroll
+        for (int j = 0; j < M; ++j) {
+          float acc = Z[r * m + j] * dsc[j];
+#pragma unroll
+          for (int k = 0; k < j; ++k) acc = fmaf(-v[k], Lf[j * ld + k], acc);
+          v[j] = acc / Lf[j * ld + j];
+        }
+#pragma unroll
+        for (int j = 0; j < M; ++j) Vown[r * m + j] = v[j];
+      }
+    } else {
+      // rank-deficient block: symmetric orthonormalisation with Jacobi
+      if (!orth_core(T, ld, m, a.max_sweeps, js, T, ld, dsc, pv, &s_deficient) && tid == 0)
+        s_jfail = 1;
+      for (int idx = tid; idx < nr * m; idx += nthr) {
+        const int r = idx / m, j = idx % m;
+        float v = 0.f;
+        for (int k = 0; k < m; ++k) v = fmaf(Z[r * m + k], T[k * ld + j], v);
+        Vown[idx] = v;
+      }
+    }
+    // ---- gather the other rows of V from the peers ----
+    cluster_sync();
+    for (int q = 0; q < kClusterCtas; ++q) {
+      if (q == rank) continue;
+      const int q0 = q * rp;
+      const int nq = min(rp, L - q0);
+      float* dst = Vall + static_cast<size_t>(q0) * m;
+      for (int i4 = tid; i4 < nq * m / 4; i4 += nthr)
+        reinterpret_cast<float4*>(dst)[i4] = dsmem_ld_f4(dsmem_addr(dst + 4 * i4, q));
+    }
+    __syncthreads();
+    // ---- Y = C[own rows, :] V / n through double-buffered cp.async tiles of C ----
+    {
+      const int r = tid >> 2, cg = tid & 3;
+      const int ntile = (L + kCvTileL - 1) / kCvTileL;
+      const bool vec = (L & 3) == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
+      float acc[cpg];
+#pragma unroll
+      for (int c = 0; c < cpg; ++c) acc[c] = 0.f;
+      stage_c_tile(Ct, Cown, nr, L, 0, vec);
+      for (int t = 0; t < ntile; ++t) {
+        if (t + 1 < ntile) {
+          stage_c_tile(Ct + ((t + 1) & 1) * kCvTileRows * kCvTileLd, Cown, nr, L, t + 1, vec);
+          cp_async_wait<1>();
+        } else {
+          cp_async_wait<0>();
+        }
+        __syncthreads();
+        const float* crow = Ct + (t & 1) * kCvTileRows * kCvTileLd + r * kCvTileLd;
+        const int l0 = t * kCvTileL;
+        const int nl = min(kCvTileL, L - l0);
+        const float* vb = Vall + static_cast<size_t>(l0) * m + cg * cpg;
+        for (int l = 0; l < nl; ++l) {
+          const float cv = crow[l];
+#pragma unroll
+          for (int c4 = 0; c4 < cpg; c4 += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(vb + l * m + c4);
+            acc[c4] = fmaf(cv, v.x, acc[c4]);
+            acc[c4 + 1] = fmaf(cv, v.y, acc[c4 + 1]);
+            acc[c4 + 2] = fmaf(cv, v.z, acc[c4 + 2]);
+            acc[c4 + 3] = fmaf(cv, v.w, acc[c4 + 3]);
+          }
+        }
+        __syncthreads();  // the buffer is refilled two tiles later
+      }
+      if (r < nr)
+#pragma unroll
+        for (int c = 0; c < cpg; ++c) Y[r * m + cg * cpg + c] = acc[c] * a.inv_n;
+    }
+    __syncthreads();
+    // ---- H = V^T Y summed over the cluster, symmetrised, into the Jacobi matrix ----
+    for (int idx = tid; idx < m * m; idx += nthr) {
+      const int p = idx / m, q = idx % m;
+      float h = 0.f;
+      for (int r = 0; r < nr; ++r) h = fmaf(Vown[r * m + p], Y[r * m + q], h);
+      Hp[idx] = h;
+    }
+    cluster_sync();
+    for (int idx = tid; idx < m * m; idx += nthr) {
+      const int i = idx / m, j = idx % m;
+      float hij = 0.f, hji = 0.f;
+      for (int q = 0; q < kClusterCtas; ++q) {
+        hij += dsmem_ld_f32(dsmem_addr(Hp + i * m + j, q));
+        hji += dsmem_ld_f32(dsmem_addr(Hp + j * m + i, q));
+      }
+      js.A[i * ld + j] = 0.5f * (hij + hji);
+    }
+    __syncthreads();
+    // ---- Rayleigh-Ritz: H = W Theta W^T, columns by descending theta ----
+    if (!jacobi_fast<M>(js.A, js.A2, js.V, ld, a.rr_tol, a.max_sweeps, js.red) && tid == 0)
+      s_jfail = 1;
+    for (int i = tid; i < m; i += nthr) js.rank[i] = desc_rank(js.A, ld, m, i);
+    __syncthreads();
+    for (int i = tid; i < m; i += nthr) th[js.rank[i]] = static_cast<double>(js.A[i * ld + i]);
+    for (int idx = tid; idx < m * m; idx += nthr) {
+      const int row = idx / m, col = idx % m;
+      W[row * ld + js.rank[col]] = js.V[row * ld + col];
+    }
+    __syncthreads();
+    // ---- U = V W, Z = Y W (own rows); residual and Gram partials ----
+    for (int idx = tid; idx < nr * m; idx += nthr) {
+      const int r = idx / m, j = idx % m;
+      float u = 0.f, z = 0.f;
+#pragma unroll
+      for (int k = 0; k < m; ++k) {
+        const float wk = W[k * ld + j];
+        u = fmaf(Vown[r * m + k], wk, u);
+        z = fmaf(Y[r * m + k], wk, z);
+      }
+      U[idx] = u;
+      Z[idx] = z;
+    }
+    __syncthreads();
+    for (int j = tid; j < m; j += nthr) {
+      const float t = static_cast<float>(th[j]);
+      float acc = 0.f;
+      for (int r = 0; r < nr; ++r) {
+        const float d = Z[r * m + j] - t * U[r * m + j];
+        acc = fmaf(d, d, acc);
+      }
+      resp[j] = acc;
+    }
+    for (int idx = tid; idx < m * m; idx += nthr) {
+      const int p = idx / m, q = idx % m;
+      float g = 0.f;
+      for (int r = 0; r < nr; ++r) g = fmaf(Z[r * m + p], Z[r * m + q], g);
+      Gp[idx] = g;
+    }
+    cluster_sync();
+    for (int j = tid; j < m; j += nthr) {
+      float t = 0.f;
+      for (int q = 0; q < kClusterCtas; ++q) t += dsmem_ld_f32(dsmem_addr(resp + j, q));
+      r2[j] = t;
+    }
+    __syncthreads();
+    // ---- convergence test (as in the multi-launch path), decided by rank 0 ----
+    if (rank == 0 && tid == 0) {
+      const int k = k_rule(th, m, a.eps * E);
+      int R = a.r_override > 0 ? a.r_override : k + a.p;
+      if (R > L) R = L;
+      const bool fits = k <= m && R <= m - 1;
+      int conv = fits ? 1 : 0;
+      const double lim = a.tol * a.tol * th[0] * th[0];
+      for (int i = 0; i < R && i < m && conv; ++i)
+        if (!(static_cast<double>(r2[i]) <= lim)) conv = 0;
+      int d = conv ? 1 : 0;
+      if (!d && !fits && it >= 15) d = 2;
+      if (!d && it >= a.max_iter - 1) d = 3;
+      flag[0] = d;
+    }
+    cluster_sync();
+    if (tid == 0) s_dec = dsmem_ld_s32(dsmem_addr(flag, 0));
+    __syncthreads();
+    dec = s_dec;
+    if (dec != 0) break;
+  }
+
+  // ---- projector rows: sign-canonical, scaled Ritz vectors ----
+  if (tid == 0) {
+    int k = k_rule(th, m, a.eps * E);
+    if (k > L) k = L;
+    int R = a.r_override > 0 ? a.r_override : k + a.p;
+    if (R > L) R = L;
+    if (R > m) R = m;
+    double cum = 0.0;
+    for (int i = 0; i < R; ++i) cum += th[i] * th[i];
+    s_k = k;
+    s_R = R;
+    s_scale = static_cast<float>(a.scale_on ? 1.0 / sqrt(cum) : 1.0);
+  }
+  // largest-magnitude entry of each column over the own rows (lowest row on ties)
+  for (int j = tid; j < m; j += nthr) {
+    float best = -1.f, val = 0.f;
+    int bi = 0x7fffffff;
+    for (int r = 0; r < nr; ++r) {
+      const float u = U[r * m + j];
+      if (fabsf(u) > best) {
+        best = fabsf(u);
+        val = u;
+        bi = r0 + r;
+      }
+    }
+    aval[j] = val;
+    aidx[j] = bi;
+  }
+  cluster_sync();
+  const int R = s_R;
+  const float sc = s_scale;
+  if (dec != 2) {
+    for (int j = tid; j < m; j += nthr) {
+      float best = -1.f, val = 0.f;
+      int bi = 0x7fffffff;
+      for (int q = 0; q < kClusterCtas; ++q) {
+        const float v = dsmem_ld_f32(dsmem_addr(aval + j, q));
+        const int ix = dsmem_ld_s32(dsmem_addr(aidx + j, q));
+        if (fabsf(v) > best || (fabsf(v) == best && ix < bi)) {
+          best = fabsf(v);
+          val = v;
+          bi = ix;
+        }
+      }
+      pv[j] = val < 0.f ? -sc : sc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < a.r_cap * nr; idx += nthr) {
+      const int i = idx / nr, r = idx - (idx / nr) * nr;
+      const float v = i < R ? pv[i] * U[r * m + i] : 0.f;
+      const size_t o = static_cast<size_t>(i) * L + r0 + r;
+      if (a.out_bf16)
+        static_cast<uint16_t*>(a.rows_out)[o] = bf16_bits(v);
+      else
+        static_cast<float*>(a.rows_out)[o] = v;
+    }
+  }
+  if (rank == 0 && tid == 0) {
+    SolverResult* res = a.res;
+    res->k = s_k;
+    res->R = R;
+    res->scale = sc;
+    res->converged = dec == 1 ? 1 : 0;
+    res->block_short = dec == 2 ? 1 : 0;
+    res->jacobi_failed = s_jfail;
+    for (int i = 0; i < m; ++i) {
+      res->theta[i] = th[i];
+      res->res2[i] = r2[i];
+    }
+  }
+  cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 }  // namespace
@@ -831,6 +1438,23 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
                                 inv_n2, w);
   count_launches(1);
   return cudaGetLastError();
+}
+
+bool cluster_solve_fits(int L, int m) {
+  if (L <= 128 || L > 512 || (m != 16 && m != 32)) return false;
+  const int rp = (L + kClusterCtas - 1) / kClusterCtas;
+  return cluster_layout(L, m, rp).total <= 200 * 1024;
+}
+
+cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st) {
+  if (!cluster_solve_fits(a.L, a.m)) return cudaErrorInvalidValue;
+  a.rp = (a.L + kClusterCtas - 1) / kClusterCtas;
+  const size_t bytes = cluster_layout(a.L, a.m, a.rp).total;
+  auto kern = a.m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  return launch_ex(kern, dim3(1, 1, kClusterCtas), dim3(kClusterThreads), bytes, st, kClusterCtas,
+                   false, a);
 }
 
 INSTANT_FAULT_READER(read_fault_eig)

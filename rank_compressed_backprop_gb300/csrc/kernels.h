@@ -165,6 +165,27 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
                                    int scale_on, void* rows_out, int r_cap, int out_bf16,
                                    double inv_n2, SolverWs w, cudaStream_t st);
 
+// the whole subspace iteration + projector rows in one launch of an 8-CTA
+// cluster (128 < L <= 512, block m <= 32); rp is set by the launcher
+struct ClusterSolveArgs {
+  const float* C;
+  int L, m, rp;
+  float inv_n;
+  double inv_n2;
+  double eps;
+  int p, r_override, scale_on;
+  double tol;
+  int max_iter, max_sweeps;
+  float rr_tol;
+  const void* seed;      // [n_seed, L] rows seeding the block (bf16 when seed_bf16)
+  int n_seed, seed_bf16;
+  void* rows_out;        // [r_cap, L]; written unless the block proved too short
+  int r_cap, out_bf16;
+  SolverResult* res;
+};
+bool cluster_solve_fits(int L, int m);
+cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st);
+
 // host-side count of kernel launches issued by the library
 void count_launches(unsigned int n);
 

@@ -113,3 +113,45 @@ def test_warm_start_reproduces_the_cold_solve(torch):
     r2 = api.calib_solve(C, 64, other, eps=0.95, p=2, r_override=8, warm_start=True)
     assert (r2.k, r2.R) == (r0.k, r0.R)
     assert float((other.float() - cold.float()).abs().max()) <= 2e-2 * float(cold.float().abs().max())
+
+
+@pytest.mark.parametrize("path", ["one_launch", "multi_launch"])
+@pytest.mark.parametrize("L", [200, 512])
+def test_mid_size_solvers_match_the_oracle(torch, monkeypatch, path, L):
+    """Both solvers for 128 < L <= 512 -- the whole iteration in one cluster
+    launch, and the multi-launch host loop -- against the oracle."""
+    if path == "multi_launch":
+        monkeypatch.setenv("INSTANT_SOLVER_MULTI", "1")
+    lam = 2e4 * np.arange(1, L + 1, dtype=np.float64) ** -2.5 + 3.0
+    C = _planted_C(60 + L, L, lam, n=32)
+    _check(torch, C, 32, eps=0.95, p=2, r_override=16, scale_on=True, r_cap=16,
+           out_dtype=torch.bfloat16)
+    _check(torch, C, 32, eps=0.9, p=3, r_override=0, scale_on=True, r_cap=24,
+           out_dtype=torch.float32)
+
+
+def test_block_too_short_hands_over_to_a_larger_block(torch):
+    # k + p beyond the first block (32 columns): the one-launch solve stops and
+    # the multi-launch loop carries on with 64 columns
+    L = 300
+    lam = np.concatenate([np.linspace(10.0, 6.0, 40), np.full(L - 40, 0.02)])
+    C = _planted_C(43, L, lam, n=4)
+    res, ref = _check(torch, C, 4, eps=0.9, p=2, r_override=0, scale_on=True, r_cap=48,
+                      out_dtype=torch.float32)
+    assert res.R > 31
+
+
+def test_one_launch_solver_rejects_bad_statistics(torch):
+    from rank_compressed_backprop_gb300 import api
+    from rank_compressed_backprop_gb300._lib import InstantError
+
+    L = 300
+    rows = torch.full((8, L), 5.0, dtype=torch.float32, device="cuda")
+    for C in (torch.zeros(L, L, device="cuda"), torch.eye(L, device="cuda")):
+        if C[0, 0] == 1:
+            C[7, 11] = float("nan")
+        with pytest.raises(InstantError) as e:
+            api.calib_solve(C, 4, rows, r_override=8)
+        assert e.value.status == 8
+        assert bool((rows == 5.0).all())   # nothing written
+    assert api.device_status() == 0
