@@ -749,14 +749,28 @@ __device__ __forceinline__ int dsmem_ld_s32(uint32_t addr) {
   return v;
 }
 
-// Jacobi of order M (even, <= 32) with one barrier per round: every thread
-// recomputes, from the matrix at the start of the round, the rotations of the
-// pairs it touches (the same values block_jacobi computes once per pair), so
-// no rotation table and no second barrier are needed.  Rotation formula,
-// ordering and stopping rule are block_jacobi's; A is double-buffered in A/A2.
+// Rotation annihilating a_pq of a symmetric 2x2 block, branch-free:
+// theta = a_qq - a_pp, t = sign(theta) 2 a_pq / (|theta| + sqrt(theta^2 + 4 a_pq^2))
+// (the smaller root of the classical tangent equation, Golub & Van Loan
+// sec. 8.5, multiplied through by |2 a_pq|), c = 1 / sqrt(1 + t^2), s = t c.
+__device__ __forceinline__ void jac_rot_bf(float app, float aqq, float apq, float& c, float& s) {
+  const float th = aqq - app;
+  const float two = 2.f * apq;
+  const float r2 = fmaf(th, th, two * two);
+  const float r = r2 * rsqrtf(fmaxf(r2, 1e-38f));
+  float t = __fdividef(copysignf(1.f, th) * two, fabsf(th) + r);
+  t = fabsf(apq) > 1e-30f ? t : 0.f;
+  c = rsqrtf(fmaf(t, t, 1.f));
+  s = t * c;
+}
+
+// Jacobi of order M (even, <= 32) for the whole CTA: per round, the M/2
+// rotations are computed once (one thread each), then the disjoint 2x2 blocks
+// of A' = J^T A J (double-buffered in A/A2) and the pairs of columns of V J
+// are updated.  Round-robin ordering and stopping rule as block_jacobi.
 template <int M>
 __device__ bool jacobi_fast(float* A, float* A2, float* V, int ld, float tol, int max_sweeps,
-                            float* red) {
+                            float* red, float* cs) {
   constexpr int H = M / 2;
   const int tid = threadIdx.x, nthr = blockDim.x;
   for (int idx = tid; idx < M * M; idx += nthr) {
@@ -789,14 +803,22 @@ __device__ bool jacobi_fast(float* A, float* A2, float* V, int ld, float tol, in
     prev = off;
     if (sweep == max_sweeps) break;
     for (int r = 0; r < M - 1; ++r) {
+      if (tid < H) {
+        int p, q;
+        jac_pair(r, tid, M, p, q);
+        float c, sn;
+        jac_rot_bf(Ao[p * ld + p], Ao[q * ld + q], Ao[p * ld + q], c, sn);
+        cs[2 * tid] = c;
+        cs[2 * tid + 1] = sn;
+      }
+      __syncthreads();
       for (int idx = tid; idx < H * H; idx += nthr) {
         const int k = idx / H, k2 = idx % H;
         int p, q, p2, q2;
         jac_pair(r, k, M, p, q);
         jac_pair(r, k2, M, p2, q2);
-        float c1, s1, c2, s2;
-        jac_rot(Ao, ld, p, q, c1, s1);
-        jac_rot(Ao, ld, p2, q2, c2, s2);
+        const float c1 = cs[2 * k], s1 = cs[2 * k + 1];
+        const float c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
         const float a = Ao[p * ld + p2], b = Ao[p * ld + q2];
         const float c = Ao[q * ld + p2], d = Ao[q * ld + q2];
         const float y00 = c1 * a - s1 * c, y01 = c1 * b - s1 * d;
@@ -808,11 +830,10 @@ __device__ bool jacobi_fast(float* A, float* A2, float* V, int ld, float tol, in
       }
       for (int idx = tid; idx < M * H; idx += nthr) {
         const int k = idx / M, i = idx % M;
+        const float c = cs[2 * k], sn = cs[2 * k + 1];
+        if (sn == 0.f) continue;
         int p, q;
         jac_pair(r, k, M, p, q);
-        float c, sn;
-        jac_rot(Ao, ld, p, q, c, sn);
-        if (sn == 0.f) continue;
         const float vp = V[i * ld + p], vq = V[i * ld + q];
         V[i * ld + p] = c * vp - sn * vq;
         V[i * ld + q] = sn * vp + c * vq;
@@ -914,6 +935,10 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
   cp_async_commit();
 }
 
+// row stride of the resident C rows: 4 mod 32 words, so that the eight rows a
+// warp reads at one column fall in distinct banks; rows stay 16-byte aligned
+__host__ __device__ inline int cres_ld(int L) { return (L + 31) / 32 * 32 + 4; }
+
 struct ClusterLay {
   uint32_t V, Y, Z, U, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
       ct, total;
@@ -948,7 +973,12 @@ __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   c.dsc = lay_take(o, 4u * kMaxBlock);
   c.pv = lay_take(o, 4u * kMaxBlock);
   c.jac = lay_take(o, jac_smem_bytes(m));
-  c.ct = lay_take(o, 4u * 2 * kCvTileRows * kCvTileLd);  // two C tiles for Y = C V
+  if (m == 16) {
+    // the CTA's rows of C stay in shared memory for the whole solve
+    c.ct = lay_take(o, 4u * rp * cres_ld(L));
+  } else {
+    c.ct = lay_take(o, 4u * 2 * kCvTileRows * kCvTileLd);  // two C tiles for Y = C V
+  }
   c.total = o;
   return c;
 }
@@ -996,8 +1026,48 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
   constexpr int ld = m + 1;
   const float* Cown = a.C + static_cast<size_t>(r0) * L;
 
+  constexpr bool kResident = (M == 16);
+  const bool vecC = (L & 3) == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
+  if (kResident) {
+    // load the own rows of C once (cp.async when rows are 16-byte aligned)
+    const int ldc = cres_ld(L);
+    const int l4 = (L + 3) / 4;
+    for (int i = tid; i < nr * l4; i += nthr) {
+      const int r = i / l4, c4 = (i - r * l4) * 4;
+      float* d = Ct + r * ldc + c4;
+      if (vecC && c4 + 4 <= L) {
+        cp_async16(d, Cown + static_cast<size_t>(r) * L + c4);
+      } else {
+        for (int e = 0; e < 4; ++e) d[e] = c4 + e < L ? Cown[static_cast<size_t>(r) * L + c4 + e] : 0.f;
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+  }
   // ---- energy ||C||_F^2 and finiteness, summed over the cluster ----
-  {
+  if (kResident) {
+    float hi = 0.f, lo = 0.f;
+    int bad = 0;
+    const int ldc = cres_ld(L);
+#pragma unroll 4
+    for (int i = tid; i < nr * L; i += nthr) {
+      const int r = i / L, l = i - r * L;
+      add_square(Ct[r * ldc + l], hi, lo, bad);
+    }
+    double acc = static_cast<double>(hi) + static_cast<double>(lo);
+    acc = warp_sum_d(acc);
+    bad = __syncthreads_or(bad);
+    if ((tid & 31) == 0) wred[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+      double t = 0.0;
+      for (int i = 0; i < nthr / 32; ++i) t += wred[i];
+      dpart[0] = t;
+      ipart[0] = bad;
+      s_jfail = 0;
+    }
+  } else {
     // per thread a double-float (hi, lo) sum of exact squares: fp32 arithmetic
     // only (fp64 units are scarce), about fp64 accuracy
     float hi = 0.f, lo = 0.f;
@@ -1120,11 +1190,35 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
         reinterpret_cast<float4*>(dst)[i4] = dsmem_ld_f4(dsmem_addr(dst + 4 * i4, q));
     }
     __syncthreads();
-    // ---- Y = C[own rows, :] V / n through double-buffered cp.async tiles of C ----
-    {
+    // ---- Y = C[own rows, :] V / n ----
+    if (kResident) {
+      const int r = tid >> 2, cg = tid & 3;
+      const float* crow = Ct + r * cres_ld(L);
+      const float* vb = Vall + cg * cpg;
+      float acc[cpg];
+#pragma unroll
+      for (int c = 0; c < cpg; ++c) acc[c] = 0.f;
+      if (r < nr) {
+#pragma unroll 4
+        for (int l = 0; l < L; ++l) {
+          const float cv = crow[l];
+#pragma unroll
+          for (int c4 = 0; c4 < cpg; c4 += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(vb + l * m + c4);
+            acc[c4] = fmaf(cv, v.x, acc[c4]);
+            acc[c4 + 1] = fmaf(cv, v.y, acc[c4 + 1]);
+            acc[c4 + 2] = fmaf(cv, v.z, acc[c4 + 2]);
+            acc[c4 + 3] = fmaf(cv, v.w, acc[c4 + 3]);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < cpg; ++c) Y[r * m + cg * cpg + c] = acc[c] * a.inv_n;
+      }
+    } else {
+      // C streamed through double-buffered cp.async tiles
       const int r = tid >> 2, cg = tid & 3;
       const int ntile = (L + kCvTileL - 1) / kCvTileL;
-      const bool vec = (L & 3) == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
+      const bool vec = vecC;
       float acc[cpg];
 #pragma unroll
       for (int c = 0; c < cpg; ++c) acc[c] = 0.f;
@@ -1178,7 +1272,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
     }
     __syncthreads();
     // ---- Rayleigh-Ritz: H = W Theta W^T, columns by descending theta ----
-    if (!jacobi_fast<M>(js.A, js.A2, js.V, ld, a.rr_tol, a.max_sweeps, js.red) && tid == 0)
+    if (!jacobi_fast<M>(js.A, js.A2, js.V, ld, a.rr_tol, a.max_sweeps, js.red, js.cs) && tid == 0)
       s_jfail = 1;
     for (int i = tid; i < m; i += nthr) js.rank[i] = desc_rank(js.A, ld, m, i);
     __syncthreads();

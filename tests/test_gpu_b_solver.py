@@ -155,3 +155,22 @@ def test_one_launch_solver_rejects_bad_statistics(torch):
         assert e.value.status == 8
         assert bool((rows == 5.0).all())   # nothing written
     assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("r_override", [8, 16])
+def test_mid_size_solve_converges_in_one_launch(torch, r_override):
+    """For 128 < L <= 512 and blocks of 16 or 32 columns the whole solve is one
+    cluster launch: no hand-over to the multi-launch loop on a planted spectrum."""
+    from rank_compressed_backprop_gb300 import api
+
+    L = 512
+    lam = 1e5 * np.arange(1, L + 1, dtype=np.float64) ** -2.0 + 5.0
+    C = to_dev(_planted_C(88, L, lam, n=64))
+    rows = torch.empty(r_override, L, dtype=torch.bfloat16, device="cuda")
+    n0 = api.launch_count()
+    res = api.calib_solve(C, 64, rows, eps=0.95, p=2, r_override=r_override)
+    assert api.launch_count() - n0 == 1
+    assert res.R == r_override
+    n0 = api.launch_count()
+    api.calib_solve(C, 64, rows, eps=0.95, p=2, r_override=r_override, warm_start=True)
+    assert api.launch_count() - n0 == 1
