@@ -121,13 +121,28 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
 size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt);
 
 /*
+ * Both products of the low-rank backward (关键设计 3: g_w ~ g_hat_y1 x_hat and
+ * g_tilde_x = Q^T g_hat_y2 w) in one call: the same results as
+ * instant_grad_w(Sx, xhat, gw, accumulate, ...) followed by
+ * instant_grad_x(Sq, w, Q, gx, ws, ...), with the same arguments, layouts and
+ * limits.  Where the single-kernel input gradient applies (bf16, short Cy) the
+ * weight-gradient tiles run inside the same launch, on the SMs the input
+ * gradient leaves free; otherwise the two calls are made in turn.
+ */
+instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int accumulate,
+                                const void* Sq, const void* w, const void* Q, void* gx,
+                                void* ws, size_t ws_bytes,
+                                int B, int L, int Cx, int Cy, int Rx, int Ry,
+                                instant_dtype dt, void* stream);
+
+/*
  * The two halves of instant_grad_x, for callers that schedule or time them
  * separately.  instant_grad_x_core computes g_hat_x = Sq w (关键设计 3,
- * g_hat_x = g_hat_y2 w) into `ws` as fp32 split-K partial planes whose number
- * depends only on (B, Cx, Cy, Ry, dt); instant_expand sums those planes and
- * writes g_tilde_x,b = Q^T g_hat_x,b.  Call them with the same sizes and the
- * same workspace (of instant_grad_x_workspace_bytes bytes), in that order on
- * one stream; the layout of `ws` between the two calls is private.
+ * g_hat_x = g_hat_y2 w) into `ws` as [B*Ry, Cx] in dtype dt (its split-K
+ * partial sums are reduced on chip); instant_expand reads it back and writes
+ * g_tilde_x,b = Q^T g_hat_x,b.  Call them with the same sizes and the same
+ * workspace (of instant_grad_x_workspace_bytes bytes), in that order on one
+ * stream.
  */
 instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes,
                                    int B, int Cx, int Cy, int Ry,

@@ -61,6 +61,8 @@ _PROTOS = {
     "instant_grad_w": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x": (_i, [_vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "instant_grad_w_x": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i,
+                              _i, _vp]),
     "instant_grad_x_core": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _vp]),
     "instant_expand": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),

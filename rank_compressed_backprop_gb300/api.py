@@ -20,6 +20,7 @@ __all__ = [
     "grad_w",
     "grad_x",
     "grad_x_workspace_bytes",
+    "grad_w_x",
     "grad_x_core",
     "expand",
     "grad_x_static",
@@ -126,6 +127,28 @@ def grad_x(Sq: torch.Tensor, w: torch.Tensor, Q: torch.Tensor, gx: torch.Tensor,
                                _dev(ws, "ws"), ws.numel() * ws.element_size(), B, L, Cx, Cy, Ry,
                                dtype_code(Sq.dtype), _stream(stream)), "instant_grad_x")
     return gx
+
+
+def grad_w_x(Sx: torch.Tensor, xhat: torch.Tensor, gw: torch.Tensor, Sq: torch.Tensor,
+             w: torch.Tensor, Q: torch.Tensor, gx: torch.Tensor, ws: torch.Tensor, B: int, *,
+             accumulate: bool = False, stream=None):
+    """:func:`grad_w` and :func:`grad_x` in one call (one launch where the
+    single-kernel input gradient applies).  Returns ``(gw, gx)``."""
+    Bg, L, Cx = gx.shape
+    Ry = Q.shape[0]
+    Cy = w.shape[0]
+    Rx = Sx.shape[0] // B
+    if (Bg != B or Q.shape != (Ry, L) or w.shape != (Cy, Cx) or Sq.shape != (B * Ry, Cy)
+            or Sx.shape != (B * Rx, Cy) or xhat.numel() != B * Rx * Cx or gw.shape != (Cy, Cx)):
+        raise ValueError("grad_w_x: inconsistent shapes")
+    if gw.dtype != torch.float32:
+        raise TypeError("grad_w_x: gw must be float32")
+    _same_dtype(Sq.dtype, ("Sx", Sx), ("xhat", xhat), ("w", w), ("Q", Q), ("gx", gx))
+    check(lib().instant_grad_w_x(_dev(Sx, "Sx"), _dev(xhat, "xhat"), _dev(gw, "gw"), int(bool(accumulate)),
+                                 _dev(Sq, "Sq"), _dev(w, "w"), _dev(Q, "Q"), _dev(gx, "gx"),
+                                 _dev(ws, "ws"), ws.numel() * ws.element_size(), B, L, Cx, Cy, Rx,
+                                 Ry, dtype_code(Sq.dtype), _stream(stream)), "instant_grad_w_x")
+    return gw, gx
 
 
 def grad_x_core(Sq: torch.Tensor, w: torch.Tensor, ws: torch.Tensor, B: int, stream=None):

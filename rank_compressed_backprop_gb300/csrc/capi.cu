@@ -368,8 +368,17 @@ bool use_fused_grad_x(int L, int Cy, int Ry, instant_dtype dt) {
   return cdiv(cdiv(Cy, 64), fused_cluster(L)) <= 16;
 }
 
+// weight-gradient operands riding along in the fused launch (Sx == nullptr: none)
+struct GradWPart {
+  const void* Sx;
+  const void* xhat;
+  float* gw;
+  int accumulate;
+  int Rx;
+};
+
 instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
-                            int Cx, int Cy, int Ry, cudaStream_t st) {
+                            int Cx, int Cy, int Ry, const GradWPart& gwp, cudaStream_t st) {
   FusedArgs f;
   f.B = B;
   f.L = L;
@@ -389,8 +398,26 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
   while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < 152) f.spt /= 2;
   f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
   f.Q = Q;
-  CUtensorMap ms, mw, mq, mo;
+  f.gw_y0 = cdiv(B, f.spt);
+  f.gw_mt = gwp.Sx ? cdiv(Cy, 128) : 0;
+  f.gw_nk = gwp.Sx ? cdiv(B * gwp.Rx, 64) : 0;
+  f.gw_acc = gwp.accumulate ? 1 : 0;
+  f.gw = gwp.gw;
+  CUtensorMap ms, mw, mq, mo, msx, mxh;
   std::memset(&mq, 0, sizeof(mq));
+  std::memset(&msx, 0, sizeof(msx));
+  std::memset(&mxh, 0, sizeof(mxh));
+  if (gwp.Sx) {
+    // Sx [B*Rx, Cy] and x_hat [B*Rx, Cx], both read MN-major in 64 x 64 boxes
+    const uint64_t K = static_cast<uint64_t>(B) * gwp.Rx;
+    const uint64_t da[2] = {static_cast<uint64_t>(Cy), K};
+    const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
+    const uint64_t db[2] = {static_cast<uint64_t>(Cx), K};
+    const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
+    const uint32_t bx[2] = {64, 64};
+    if (!make_map(&msx, gwp.Sx, 2, da, sa, bx) || !make_map(&mxh, gwp.xhat, 2, db, sb, bx))
+      return INSTANT_ERR_CUDA;
+  }
   const uint64_t ds[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(B) * Ry};
   const uint64_t ss[1] = {static_cast<uint64_t>(Cy) * 2};
   const uint32_t bs[2] = {64, 128};
@@ -409,7 +436,7 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
     const uint32_t b2[2] = {64, static_cast<uint32_t>(f.KR)};
     if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
   }
-  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, f, st));
+  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, f, st));
 }
 
 instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
@@ -423,10 +450,31 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
                              Cx % 8 != 0 || Cy % 8 != 0))
     return INSTANT_ERR_ALIGN;
   if (use_fused_grad_x(L, Cy, Ry, dt))
-    return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, static_cast<cudaStream_t>(stream));
+    return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{nullptr, nullptr, nullptr, 0, 0},
+                        static_cast<cudaStream_t>(stream));
   const instant_status s = instant_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, stream);
   if (s != INSTANT_OK) return s;
   return instant_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
+}
+
+instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int accumulate,
+                                const void* Sq, const void* w, const void* Q, void* gx, void* ws,
+                                size_t ws_bytes, int B, int L, int Cx, int Cy, int Rx, int Ry,
+                                instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!Sx || !xhat || !gw || !Sq || !w || !Q || !gx) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Rx < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
+  if (dt == INSTANT_BF16 &&
+      (!aligned16(Sx) || !aligned16(xhat) || !aligned16(gw) || !aligned16(Sq) || !aligned16(w) ||
+       !aligned16(gx) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0))
+    return INSTANT_ERR_ALIGN;
+  if (use_fused_grad_x(L, Cy, Ry, dt))
+    return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{Sx, xhat, gw, accumulate, Rx},
+                        static_cast<cudaStream_t>(stream));
+  const instant_status s = instant_grad_w(Sx, xhat, gw, accumulate, B, Rx, Cx, Cy, dt, stream);
+  if (s != INSTANT_OK) return s;
+  return instant_grad_x(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
 }
 
 instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, int Cdim,

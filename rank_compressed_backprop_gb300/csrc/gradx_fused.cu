@@ -15,6 +15,12 @@
 //            staging (reusing the phase-1 ring) -> TMA bulk store.
 // Used when Cy is small enough that every CTA can afford to recompute its
 // g_hat_x tile (the token range is split across CTAs for parallelism).
+//
+// The same launch can also compute the weight gradient g_w = Sx^T x_hat
+// (关键设计 3): extra grid rows of CTAs (clusters of their own, no cluster
+// barrier) each produce one 128 x 64 fp32 tile of g_w, so that both products
+// of the backward pass share one launch and fill the SMs the input gradient
+// leaves free.
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -31,7 +37,9 @@ struct FLay {
   uint32_t ring, stage, qt, qt_tile, bs, bs_sample, stg, bar, total;
 };
 
-__host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_per, int spt) {
+// gw: the launch also runs weight-gradient tiles, whose 3-stage ring needs 72 KB
+__host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_per, int spt,
+                                             bool gw) {
   FLay l;
   l.stage = A_BYTES + BN * BK * 2;
   l.ring = 0;
@@ -40,6 +48,7 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   const uint32_t red_bytes = BM * (BN + 4) * 4;     // so does the cluster reduction tile
   uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
   if (red_bytes > first) first = red_bytes;
+  if (gw && first < 3u * (A_BYTES + 64 * BK * 2)) first = 3u * (A_BYTES + 64 * BK * 2);
   first = (first + 1023u) & ~1023u;
   l.stg = 0;
   l.qt = first;
@@ -51,18 +60,130 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   return l;
 }
 
+// One 128 x 64 tile of g_w[Cy, Cx] = Sx^T x_hat (K = B * Rx): Sx [K, Cy] and
+// x_hat [K, Cx] both arrive MN-major by TMA through a 3-stage ring (the first
+// 72 KB of shared memory); warps 2..9 store the fp32 tile (or add it to g_w).
+__device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CUtensorMap* tmap_xh,
+                                            const FusedArgs& f, uint8_t* smem, uint32_t bar_off,
+                                            int m0, int n0) {
+  constexpr uint32_t STAGE = A_BYTES + 64 * BK * 2;  // 24 KB
+  const int nk = f.gw_nk;
+  const int NS = nk < 3 ? (nk < 1 ? 1 : nk) : 3;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + bar_off);
+  uint64_t* empty = full + 3;
+  uint64_t* done = empty + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+    prefetch_tmap(tmap_sx);
+    prefetch_tmap(tmap_xh);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 64);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (warp == 0 && lane == 0) {
+    int issued = 0;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % NS;
+      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
+        raise_fault(FAULT_WAIT_EMPTY);
+        break;
+      }
+      uint8_t* sa = smem + s * STAGE;
+      const int k0 = i * BK;
+      mbar_arrive_expect_tx(&full[s], STAGE);
+      tma_load_2d(sa, tmap_sx, &full[s], m0, k0);
+      tma_load_2d(sa + A_BYTES / 2, tmap_sx, &full[s], m0 + 64, k0);
+      tma_load_2d(sa + A_BYTES, tmap_xh, &full[s], n0, k0);
+      ++issued;
+    }
+    for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
+      if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, /*a_mn=*/1, /*b_mn=*/1);
+    bool ok = true;
+    for (int i = 0; i < nk; ++i) {
+      const int s = i % NS;
+      if (!mbar_wait(&full[s], (i / NS) & 1)) {
+        raise_fault(FAULT_WAIT_FULL);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(smem + s * STAGE);
+      const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t ad = sdesc_sw128(a_base + kk * 2048, A_BYTES / 2, 1024);
+        const uint64_t bd = sdesc_sw128(b_base + kk * 2048, 64 * BK * 2, 1024);
+        umma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
+      }
+      umma_commit(&empty[s]);
+    }
+    if (ok && nk > 0) umma_commit(done);
+  }
+  __syncwarp();
+  if (warp >= 2) {
+    if (nk > 0 && !mbar_wait(done, 0)) raise_fault(FAULT_WAIT_DONE);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const int c0 = ((warp - 2) >> 2) * 32;
+    float v[32];
+    if (nk > 0) {
+      tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 32; ++q) v[q] = 0.f;
+    }
+    const int m = m0 + quarter * 32 + lane;
+    if (m < f.Cy) {
+      float* dst = f.gw + static_cast<size_t>(m) * f.Cx + n0 + c0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (n0 + c0 + 4 * q < f.Cx) {
+          float4 o = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          if (f.gw_acc) {
+            const float4 p = *reinterpret_cast<const float4*>(dst + 4 * q);
+            o.x += p.x; o.y += p.y; o.z += p.z; o.w += p.w;
+          }
+          *reinterpret_cast<float4*>(dst + 4 * q) = o;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
 template <int BN>
 __global__ void __launch_bounds__(320, 1)
     k_gradx_fused(const __grid_constant__ CUtensorMap tmap_sq,
                   const __grid_constant__ CUtensorMap tmap_w,
                   const __grid_constant__ CUtensorMap tmap_q,
-                  const __grid_constant__ CUtensorMap tmap_out, FusedArgs f) {
+                  const __grid_constant__ CUtensorMap tmap_out,
+                  const __grid_constant__ CUtensorMap tmap_sx,
+                  const __grid_constant__ CUtensorMap tmap_xh, FusedArgs f) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int KR = f.KR;
   const int NS = f.stages;
-  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt);
+  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt, f.gw_mt > 0);
   uint8_t* ring = smem + lay.ring;
   uint8_t* stg = smem + lay.stg;
   uint8_t* sQ = smem + lay.qt;
@@ -76,6 +197,12 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* t_empty = t_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
 
+  if (BN == 64 && static_cast<int>(blockIdx.y) >= f.gw_y0) {
+    // weight-gradient rows of the grid (clusters of their own)
+    const int mt = (static_cast<int>(blockIdx.y) - f.gw_y0) * f.cl + static_cast<int>(blockIdx.z);
+    if (mt < f.gw_mt) grad_w_tile(&tmap_sx, &tmap_xh, f, smem, lay.bar, mt * BM, blockIdx.x * BN);
+    return;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
@@ -392,7 +519,8 @@ __global__ void __launch_bounds__(320, 1)
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtensorMap& tq,
-                      const CUtensorMap& to, const FusedArgs& f, cudaStream_t st) {
+                      const CUtensorMap& to, const CUtensorMap& tsx, const CUtensorMap& txh,
+                      const FusedArgs& f, cudaStream_t st) {
   const size_t bytes = gradx_fused_smem_bytes(f);
   static size_t configured_ = 0;
   if (bytes > configured_) {
@@ -402,26 +530,30 @@ cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtens
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  const dim3 grid((f.Cx + BN - 1) / BN, (f.B + f.spt - 1) / f.spt, f.cl);
+  const int gw_rows = f.gw_mt > 0 ? (f.gw_mt + f.cl - 1) / f.cl : 0;
+  const dim3 grid((f.Cx + BN - 1) / BN, f.gw_y0 + gw_rows, f.cl);
   return launch_ex(k_gradx_fused<BN>, grid, dim3(320), bytes, st, f.cl, pdl_enabled(), ts, tw, tq,
-                   to, f);
+                   to, tsx, txh, f);
 }
 
 }  // namespace
 
 size_t gradx_fused_smem_bytes(const FusedArgs& f) {
-  return fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt).total + 1024;
+  return fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt, f.gw_mt > 0).total + 1024;
 }
 
 cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
                                const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
+                               const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
                                const FusedArgs& f, cudaStream_t st) {
   if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
   if (f.cl != 1 && f.cl != 2 && f.cl != 4 && f.cl != 8) return cudaErrorInvalidValue;
   if (f.lt_per * f.cl < f.nlt) return cudaErrorInvalidValue;
+  if (f.gw_y0 != (f.B + f.spt - 1) / f.spt) return cudaErrorInvalidValue;
+  if (f.gw_mt > 0 && (f.BN != 64 || !f.gw || f.gw_nk < 1)) return cudaErrorInvalidValue;
   switch (f.BN) {
-    case 64: return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);
-    case 128: return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, f, st);
+    case 64: return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, f, st);
+    case 128: return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, f, st);
     default: return cudaErrorInvalidValue;
   }
 }

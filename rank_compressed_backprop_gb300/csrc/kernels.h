@@ -89,11 +89,19 @@ struct FusedArgs {
                      // range is split across the cluster and reduced through DSMEM
   int q_tma;         // 1: Q^T tiles by TMA (L % 8 == 0); 0: threads fill them
   const void* Q;     // [Ry, L]
+  // weight gradient in the same launch (gw_mt > 0): grid rows gw_y0.. run the
+  // 128 x 64 tiles of g_w[Cy, Cx] = Sx^T x_hat over K = B * Rx
+  int gw_y0;         // first weight-gradient grid row (= ceil(B / spt))
+  int gw_mt;         // ceil(Cy / 128) row tiles, 0: none
+  int gw_nk;         // ceil(B * Rx / 64)
+  int gw_acc;        // 1: g_w += result
+  float* gw;         // [Cy, Cx] fp32
 };
 
 size_t gradx_fused_smem_bytes(const FusedArgs& f);
 cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
                                const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
+                               const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
                                const FusedArgs& f, cudaStream_t st);
 
 // ---------------------------------------------------------------------------

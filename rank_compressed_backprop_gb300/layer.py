@@ -68,8 +68,8 @@ class InstantLinear:
         gx = self.gx if gx is None else gx
         B = g_y.shape[0]
         api.project_grad(g_y, self.PQ, self.Sx, self.Sq, self.Rx, self.Ry)
-        api.grad_w(self.Sx, xhat, gw, B, accumulate=accumulate)
-        api.grad_x(self.Sq, self.w, self.Q, gx, self.ws_gx)
+        api.grad_w_x(self.Sx, xhat, gw, self.Sq, self.w, self.Q, gx, self.ws_gx, B,
+                     accumulate=accumulate)
         return gw, gx
 
     # ---- calibration --------------------------------------------------------

@@ -132,3 +132,40 @@ def test_calib_accumulate(torch, dtype, B, L, C):
 
 def test_device_status_clean(torch):
     assert _api().device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# grad_w_x: both products of the backward in one call
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("dtype,B,L,Cx,Cy,Rx,Ry", [
+    ("bf16", 32, 512, 768, 768, 8, 8),     # BERT-base block: one launch
+    ("bf16", 5, 300, 200, 264, 6, 5),      # ragged g_w tiles (Cy % 128, Cx % 64) in one launch
+    ("bf16", 3, 130, 136, 64, 16, 16),     # one K chunk each, a half-filled g_w row tile
+    ("bf16", 2, 49, 448, 1792, 8, 8),      # long Cy: two launches
+    ("f32", 2, 72, 40, 48, 4, 4),
+])
+def test_grad_w_x_matches_the_oracle(torch, dtype, B, L, Cx, Cy, Rx, Ry, accumulate):
+    api = _api()
+    g = rng(1300 + B + L + Cy)
+    Sx = stored(g.standard_normal((B * Rx, Cy)), dtype)
+    xh = stored(g.standard_normal((B, Rx, Cx)), dtype)
+    Sq = stored(g.standard_normal((B * Ry, Cy)), dtype)
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), dtype)
+    Q = stored(orthonormal_rows(g, Ry, L), dtype)
+    gw0 = g.standard_normal((Cy, Cx)).astype(np.float32)
+    dt = _tdt(torch, dtype)
+    gw = torch.from_numpy(gw0.copy()).cuda() if accumulate else torch.full(
+        (Cy, Cx), float("nan"), dtype=torch.float32, device="cuda")
+    gx = torch.full((B, L, Cx), float("nan"), dtype=dt, device="cuda")
+    ws = torch.empty(max(api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt), 16), dtype=torch.uint8,
+                     device="cuda")
+    api.grad_w_x(to_dev(Sx), to_dev(xh), gw, to_dev(Sq), to_dev(w), to_dev(Q), gx, ws, B,
+                 accumulate=accumulate)
+    torch.cuda.synchronize()
+    ref_w = O.grad_w(O.decode(Sx).reshape(B, Rx, Cy), O.decode(xh))
+    if accumulate:
+        ref_w = ref_w + gw0.astype(np.float64)
+    ref_x = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
+    assert rel(to_np(gw), ref_w) <= (1e-5 if dtype == "f32" else 2e-3)
+    assert rel(to_np(gx), ref_x) <= tol(dtype)
