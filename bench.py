@@ -44,11 +44,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-iters", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--mode", choices=["bench", "kernels"], default="bench",
+    ap.add_argument("--mode", choices=["bench", "kernels", "drift"], default="bench",
                     help="kernels: after a first (cold) calibration, run one recalibration "
                          "period of the timed loop eagerly -- a warm-started calibration and "
                          "N_t steps -- and exit (the case ncu captures); prints the number of "
-                         "library launches before the period as 'skip=N'")
+                         "library launches before the period as 'skip=N'; drift: the "
+                         "oversampling study on the drifting ViT-MLP workload (reconstruction "
+                         "error per step for p in 0,2,4 and N_t in 5,10,100)")
     return ap.parse_args()
 
 
@@ -622,9 +624,73 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_drift(args):
+    """Oversampling under subspace drift: per-step ||g - Q^T Q g|| / ||g|| on the
+    first layer of the drifting ViT-MLP workload, for p in {0, 2, 4} and
+    N_t in {5, 10, 100}, every computation in the CUDA library."""
+    import torch
+    import workloads as W
+    from rank_compressed_backprop_gb300.build import build
+
+    build()
+    from rank_compressed_backprop_gb300 import api
+    from rank_compressed_backprop_gb300.drift import drift_errors
+
+    wl = W.workload(4)
+    li = W.LayerInputs(wl)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    steps = wl.steps
+    batches = [to_dev(li.g_y(t), dev) for t in range(steps)]
+    B, L, C = batches[0].shape
+    table = {}
+    for p in (0, 2, 4):
+        for n_t in (5, 10, 100):
+            drift_errors(lambda t: batches[t], 2, n_t, p, eps=wl.eps)  # warm-up
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            run = drift_errors(lambda t: batches[t], steps, n_t, p, eps=wl.eps)
+            torch.cuda.synchronize()
+            el = time.perf_counter() - t0
+            table[f"p={p},N_t={n_t}"] = {
+                "errors": [round(e, 5) for e in run.errors],
+                "mean": round(sum(run.errors) / len(run.errors), 5),
+                "last": round(run.errors[-1], 5),
+                "calibrations": [list(c) for c in run.calibrations],
+                "ms_per_step": round(el * 1e3 / steps, 3),
+            }
+    # the reconstruction-error kernel alone (reads g once plus the projected rows)
+    Q = torch.zeros(8, L, dtype=batches[0].dtype, device=dev)
+    Q[:, :8] = torch.eye(8, dtype=batches[0].dtype, device=dev)
+    S = torch.empty(B, 8, C, dtype=batches[0].dtype, device=dev)
+    ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    api.compress_act(batches[0], Q, S)
+    reps = 20
+    for i in range(3):
+        api.reconstruction_error(batches[i], Q, S.view(B * 8, C), ws)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(reps):
+        api.reconstruction_error(batches[i % steps], Q, S.view(B * 8, C), ws)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    nbytes = B * L * C * 2 + B * 8 * C * 2
+    print(json.dumps({
+        "mode": "drift",
+        "workload": f"ViT-MLP first layer g_y [{B}, {L}, {C}] bf16, planted rank-6 spectrum plus "
+                    f"noise, token basis rotated by a seeded Givens angle of {wl.drift_angle} rad "
+                    f"per step, {steps} steps, eps={wl.eps}",
+        "table": table,
+        "recon_kernel": {"us_per_call_incl_sync": round(us, 2), "bytes": nbytes,
+                         "gbs_incl_sync": round(nbytes / (us * 1e-6) / 1e9, 1)},
+    }), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.mode == "drift":
+        run_drift(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

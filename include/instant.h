@@ -223,6 +223,25 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
 
 size_t instant_calib_workspace_bytes(int L, int r_cap);
 
+/*
+ * How much of a tensor a projector keeps (关键设计 2: the oversampling p guards
+ * the compression against the subspace drifting between recalibrations):
+ *   err2   = sum_b ||t_b - Q^T S_b||_F^2        energy = sum_b ||t_b||_F^2
+ * with S_b = Q t_b already computed, e.g. by instant_compress_act(t, Q, S, ...).
+ * For orthonormal rows of Q (a projector solved with scale_on = 0),
+ * sqrt(err2 / energy) = ||t - Q^T Q t|| / ||t||.
+ *   t   [B, L, C]   dtype dt (read)
+ *   Q   [R, L]      dtype dt (read)
+ *   S   [B*R, C]    dtype dt (read), row b*R + r
+ *   err2_out, energy_out: HOST doubles
+ *   ws  device scratch of at least 16 bytes, 8-byte aligned (two fp64 totals)
+ * Limits: 1 <= R <= 64, R * L <= 12288.  Synchronises `stream`.
+ */
+instant_status instant_reconstruction_error(const void* t, const void* Q, const void* S,
+                                           int B, int L, int C, int R, instant_dtype dt,
+                                           double* err2_out, double* energy_out,
+                                           void* ws, size_t ws_bytes, void* stream);
+
 /* Reads (and clears when clear != 0) the sticky device status word after
  * synchronising `stream`; INSTANT_OK when no device-side wait ran out. */
 instant_status instant_device_status(int clear, void* stream);

@@ -72,6 +72,9 @@ _PROTOS = {
                                  ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
     "instant_calib_workspace_bytes": (_sz, [_i, _i]),
+    "instant_reconstruction_error": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                          ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
     "instant_device_status": (_i, [_i, _vp]),
     "instant_status_string": (ctypes.c_char_p, [_i]),
     "instant_version": (_i, []),

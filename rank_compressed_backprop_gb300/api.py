@@ -29,6 +29,7 @@ __all__ = [
     "calib_solve",
     "calib_workspace_bytes",
     "device_status",
+    "reconstruction_error",
     "CalibResult",
     "dtype_code",
 ]
@@ -261,6 +262,26 @@ def calib_solve(C: torch.Tensor, n_samples: int, rows_out: torch.Tensor, *, eps:
         check(st, "instant_calib_solve")
         return res
     return res, st
+
+
+def reconstruction_error(t: torch.Tensor, Q: torch.Tensor, S: torch.Tensor, ws: torch.Tensor,
+                         stream=None) -> tuple[float, float]:
+    """``(sum_b ||t_b - Q^T S_b||^2, sum_b ||t_b||^2)`` for ``S = Q t`` per sample
+    (t ``[B, L, C]``, Q ``[R, L]``, S ``[B*R, C]``); synchronises the stream.
+    ``ws`` is at least 16 bytes of device scratch."""
+    B, L, C = t.shape
+    R = Q.shape[0]
+    if Q.shape != (R, L) or S.shape != (B * R, C):
+        raise ValueError("reconstruction_error: inconsistent shapes")
+    _same_dtype(t.dtype, ("Q", Q), ("S", S))
+    e2 = ctypes.c_double(0)
+    n2 = ctypes.c_double(0)
+    check(lib().instant_reconstruction_error(_dev(t, "t"), _dev(Q, "Q"), _dev(S, "S"), B, L, C, R,
+                                             dtype_code(t.dtype), ctypes.byref(e2),
+                                             ctypes.byref(n2), _dev(ws, "ws"),
+                                             ws.numel() * ws.element_size(), _stream(stream)),
+          "instant_reconstruction_error")
+    return e2.value, n2.value
 
 
 def device_status(clear: bool = True, stream=None) -> int:

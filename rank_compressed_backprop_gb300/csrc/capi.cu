@@ -658,6 +658,29 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
   return status;
 }
 
+instant_status instant_reconstruction_error(const void* t, const void* Q, const void* S, int B,
+                                           int L, int C, int R, instant_dtype dt,
+                                           double* err2_out, double* energy_out, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!t || !Q || !S || !err2_out || !energy_out) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || C < 1 || R < 1 || R > 64 || static_cast<long long>(R) * L > 12288)
+    return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < 2 * sizeof(double)) return INSTANT_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 7u) return INSTANT_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  double* totals = static_cast<double*>(ws);
+  if (launch_recon(t, Q, S, B, L, C, R, dt == INSTANT_BF16 ? 1 : 0, totals, st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  double h[2];
+  if (cudaMemcpyAsync(h, totals, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  *err2_out = h[0];
+  *energy_out = h[1];
+  return INSTANT_OK;
+}
+
 instant_status instant_device_status(int clear, void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return INSTANT_ERR_CUDA;

@@ -194,6 +194,11 @@ struct ClusterSolveArgs {
 bool cluster_solve_fits(int L, int m);
 cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st);
 
+// ||t - Q^T S||^2 and ||t||^2 over a batch (S = Q t per sample, [B*R, C]) into
+// totals[0..1] (fp64 device, zeroed by the launch)
+cudaError_t launch_recon(const void* t, const void* Q, const void* S, int B, int L, int C, int R,
+                         int bf16, double* totals, cudaStream_t st);
+
 // host-side count of kernel launches issued by the library
 void count_launches(unsigned int n);
 
