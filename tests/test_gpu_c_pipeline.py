@@ -69,8 +69,15 @@ def _run_layer(torch, wl, layer, calib_batches):
     api.grad_w(Sx, xhat, gw, B)
     api.grad_x(Sq, wd, PQd[Rx:], gx, ws)
     torch.cuda.synchronize()
+    # both products again through the one-call entry point (one launch where the
+    # single-kernel input gradient applies)
+    gw1 = torch.full((Cy, Cx), float("nan"), dtype=torch.float32, device="cuda")
+    gx1 = torch.full((B, L, Cx), float("nan"), dtype=dt, device="cuda")
+    api.grad_w_x(Sx, xhat, gw1, Sq, wd, PQd[Rx:], gx1, ws, B)
+    torch.cuda.synchronize()
     errs = {"x_hat": rel(to_np(xhat), ref["x_hat"]), "g_w": rel(to_np(gw), ref["g_w"]),
-            "g_x": rel(to_np(gx), ref["g_x"])}
+            "g_x": rel(to_np(gx), ref["g_x"]), "g_w (one call)": rel(to_np(gw1), ref["g_w"]),
+            "g_x (one call)": rel(to_np(gx1), ref["g_x"])}
     for k, v in errs.items():
         assert v <= tol(wl.dtype), (k, errs)
     assert api.device_status() == 0
@@ -93,3 +100,20 @@ def test_config4_vit_mlp_pair(torch):
     wl = W.workload(4)
     for layer in (0, 1):
         _run_layer(torch, wl, layer, lambda li: [(li.x(), li.g_y())])
+
+
+def test_config3_bert_ffn_pair(torch):
+    # rank 16: 32-column solver blocks; layer 0 (Cy = 3072) takes the cluster-split
+    # single-kernel input gradient, layer 1 (Cy = 768) the short one
+    wl = W.workload(3)
+    for layer in (0, 1):
+        _run_layer(torch, wl, layer, lambda li: [(li.calib_x(j, 32), li.calib_g(j, 32))
+                                                 for j in range(2)])
+
+
+def test_config5_long_sequence_wide_linear(torch):
+    # L = 2048 (multi-launch solver), Cy = 11008 (g_hat_x GEMM + expansion).  The
+    # statistic is the step's own 4-sample batch: the configured 64 samples would
+    # cost the float64 oracle about 2 TFLOP.
+    wl = W.workload(5)
+    _run_layer(torch, wl, 0, lambda li: [(li.x(), li.g_y())])
