@@ -939,6 +939,18 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
 // warp reads at one column fall in distinct banks; rows stay 16-byte aligned
 __host__ __device__ inline int cres_ld(int L) { return (L + 31) / 32 * 32 + 4; }
 
+// sum over the 8 CTAs of the cluster of the float at `p` (the same shared
+// address in every CTA), in rank order; every load is issued before the adds
+__device__ __forceinline__ float cluster_sum8(const float* p) {
+  float v[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) v[q] = dsmem_ld_f32(dsmem_addr(p, q));
+  float t = v[0];
+#pragma unroll
+  for (int q = 1; q < 8; ++q) t += v[q];
+  return t;
+}
+
 struct ClusterLay {
   uint32_t V, Y, Z, U, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
       ct, total;
@@ -1050,11 +1062,10 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
     float hi = 0.f, lo = 0.f;
     int bad = 0;
     const int ldc = cres_ld(L);
+    // warp w takes rows w, w + 8, ...; its lanes stride along the row
+    for (int r = tid >> 5; r < nr; r += nthr >> 5)
 #pragma unroll 4
-    for (int i = tid; i < nr * L; i += nthr) {
-      const int r = i / L, l = i - r * L;
-      add_square(Ct[r * ldc + l], hi, lo, bad);
-    }
+      for (int l = tid & 31; l < L; l += 32) add_square(Ct[r * ldc + l], hi, lo, bad);
     double acc = static_cast<double>(hi) + static_cast<double>(lo);
     acc = warp_sum_d(acc);
     bad = __syncthreads_or(bad);
@@ -1150,7 +1161,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
     cluster_sync();
     for (int idx = tid; idx < m * m; idx += nthr) {
       float g = 0.f;
-      for (int q = 0; q < kClusterCtas; ++q) g += dsmem_ld_f32(dsmem_addr(Gp + idx, q));
+      g = cluster_sum8(Gp + idx);
       T[(idx / m) * ld + idx % m] = g;
     }
     __syncthreads();
@@ -1263,11 +1274,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
     cluster_sync();
     for (int idx = tid; idx < m * m; idx += nthr) {
       const int i = idx / m, j = idx % m;
-      float hij = 0.f, hji = 0.f;
-      for (int q = 0; q < kClusterCtas; ++q) {
-        hij += dsmem_ld_f32(dsmem_addr(Hp + i * m + j, q));
-        hji += dsmem_ld_f32(dsmem_addr(Hp + j * m + i, q));
-      }
+      const float hij = cluster_sum8(Hp + i * m + j);
+      const float hji = cluster_sum8(Hp + j * m + i);
       js.A[i * ld + j] = 0.5f * (hij + hji);
     }
     __syncthreads();
@@ -1314,7 +1322,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSol
     cluster_sync();
     for (int j = tid; j < m; j += nthr) {
       float t = 0.f;
-      for (int q = 0; q < kClusterCtas; ++q) t += dsmem_ld_f32(dsmem_addr(resp + j, q));
+      t = cluster_sum8(resp + j);
       r2[j] = t;
     }
     __syncthreads();
