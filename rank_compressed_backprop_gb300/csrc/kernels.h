@@ -117,7 +117,7 @@ struct SyrkArgs {
   float* Cout;       // [L, L]
 };
 
-constexpr int kSyrkStages = 4;
+constexpr int kSyrkStages = 3;  // 96 KB of stages: two CTAs per SM
 size_t syrk_bf16_smem_bytes();
 cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st);
 cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st);
