@@ -107,3 +107,22 @@ def test_python_binding_refuses_cpu_tensors():
     with pytest.raises(ValueError):
         api.compress_act(x, torch.zeros(4, 8, dtype=torch.bfloat16),
                          torch.zeros(1, 4, 8, dtype=torch.bfloat16))
+
+
+def test_empty_extents_are_rejected_without_gpu(L):
+    fake = ctypes.c_void_p(0x1000)
+    null = ctypes.c_void_p(0)
+    for B, Lr, C in ((0, 8, 64), (1, 0, 64), (1, 8, 0)):
+        assert L.instant_compress_act(fake, fake, fake, B, Lr, C, 4, 1, null) == 2
+        assert L.instant_project_grad(fake, fake, fake, fake, B, Lr, C, 4, 4, 1, null) == 2
+        assert L.instant_calib_accumulate(fake, fake, B, Lr, C, 1, null) == 2
+        assert L.instant_grad_x(fake, fake, fake, fake, fake, 1 << 20, B, Lr, C, 64, 4, 1, null) == 2
+        assert L.instant_grad_w_x(fake, fake, fake, 0, fake, fake, fake, fake, fake, 1 << 20,
+                                  B, Lr, C, 64, 4, 4, 1, null) == 2
+        assert L.instant_grad_x_static(fake, fake, fake, fake, B, Lr, C, 64, 4, 1, null) == 2
+    assert L.instant_grad_w(fake, fake, fake, 0, 0, 4, 64, 64, 1, null) == 2
+    e2, n2 = ctypes.c_double(), ctypes.c_double()
+    assert L.instant_reconstruction_error(fake, fake, fake, 0, 8, 64, 4, 1, ctypes.byref(e2),
+                                          ctypes.byref(n2), fake, 16, null) == 2
+    assert L.instant_reconstruction_error(fake, fake, fake, 1, 8, 64, 4, 1, ctypes.byref(e2),
+                                          ctypes.byref(n2), fake, 8, null) == 5
