@@ -20,7 +20,8 @@
  *     innermost extent of every 2-D/3-D operand read by TMA (L for PQ/P/Q is
  *     exempt) must be a multiple of 8 elements; otherwise INSTANT_ERR_ALIGN.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
- *     asynchronous on that stream except instant_calib_solve and
+ *     asynchronous on that stream except instant_calib_solve,
+ *     instant_calib_solve_batch, instant_reconstruction_error and
  *     instant_device_status, which synchronise it.
  *   - Argument, shape and dtype errors are reported before anything is
  *     launched; nothing is written in that case.  A launch error returns
@@ -34,6 +35,10 @@
 #define INSTANT_H_
 
 #include <stddef.h>
+
+#if defined(__GNUC__)
+#pragma GCC visibility push(default) /* the library exports exactly these names */
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -224,6 +229,53 @@ instant_status instant_calib_solve(const float* C, long long n_samples, int L,
 size_t instant_calib_workspace_bytes(int L, int r_cap);
 
 /*
+ * Several statistics of one token length L solved in one call (关键设计 1
+ * and 2: a layer calibrates P from its activations and Q from its output
+ * gradients at the same step, and a model calibrates all its layers at the
+ * same step).  Each problem gets what instant_calib_solve would give it
+ * alone (same kernels, same arithmetic: bit for bit on the one-launch solver;
+ * the multi-launch path adds some partial sums with atomics, so any two of its
+ * runs agree only up to that rounding order); the problems that the
+ * one-launch solver takes (128 < L <= 512, block of 16 or 32 columns) run
+ * together, one 8-CTA cluster each, up to 16 per launch, with one
+ * synchronisation for all of them.
+ *
+ * instant_calib_problem: one statistic.
+ *   C, n_samples, prm, rows_out, r_cap, eig_out   as for instant_calib_solve
+ *                 (C, rows_out: device; eig_out: HOST or NULL)
+ *   k, R, scale, energy   outputs (host struct, written by the call)
+ *   status        this problem's own result
+ * Arguments
+ *   problems   HOST array of `count` problems (count >= 1)
+ *   dt         dtype of every rows_out
+ *   ws         device scratch of instant_calib_batch_workspace_bytes(L, count)
+ *              bytes; problem i uses its own slice
+ * Returns INSTANT_OK when every problem succeeded, else the first failing
+ * problem's status.  Argument, shape, dtype, alignment or workspace errors of
+ * any problem are reported before anything is launched, with that error in
+ * every problem's `status`.  Synchronises `stream`.
+ */
+typedef struct {
+  const float* C;
+  long long n_samples;
+  instant_calib_params prm;
+  void* rows_out;
+  int r_cap;
+  double* eig_out;
+  int k;
+  int R;
+  float scale;
+  double energy;
+  instant_status status;
+} instant_calib_problem;
+
+instant_status instant_calib_solve_batch(instant_calib_problem* problems, int count, int L,
+                                         instant_dtype dt, void* ws, size_t ws_bytes,
+                                         void* stream);
+
+size_t instant_calib_batch_workspace_bytes(int L, int count);
+
+/*
  * How much of a tensor a projector keeps (关键设计 2: the oversampling p guards
  * the compression against the subspace drifting between recalibrations):
  *   err2   = sum_b ||t_b - Q^T S_b||_F^2        energy = sum_b ||t_b||_F^2
@@ -257,5 +309,9 @@ unsigned long long instant_launch_count(void);
 
 #ifdef __cplusplus
 }
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
 #endif
 #endif /* INSTANT_H_ */

@@ -44,6 +44,22 @@ class CalibParams(ctypes.Structure):
     ]
 
 
+class CalibProblem(ctypes.Structure):
+    _fields_ = [
+        ("C", ctypes.c_void_p),
+        ("n_samples", ctypes.c_longlong),
+        ("prm", CalibParams),
+        ("rows_out", ctypes.c_void_p),
+        ("r_cap", ctypes.c_int),
+        ("eig_out", ctypes.POINTER(ctypes.c_double)),
+        ("k", ctypes.c_int),
+        ("R", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("energy", ctypes.c_double),
+        ("status", ctypes.c_int),
+    ]
+
+
 class InstantError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
@@ -72,6 +88,8 @@ _PROTOS = {
                                  ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),
                                  ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
     "instant_calib_workspace_bytes": (_sz, [_i, _i]),
+    "instant_calib_solve_batch": (_i, [ctypes.POINTER(CalibProblem), _i, _i, _i, _vp, _sz, _vp]),
+    "instant_calib_batch_workspace_bytes": (_sz, [_i, _i]),
     "instant_reconstruction_error": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i,
                                           ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),

@@ -12,7 +12,8 @@ import dataclasses
 
 import torch
 
-from ._lib import GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, CalibParams, check, lib
+from ._lib import (GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, CalibParams,
+                   CalibProblem, check, lib)
 
 __all__ = [
     "compress_act",
@@ -27,7 +28,9 @@ __all__ = [
     "launch_count",
     "calib_accumulate",
     "calib_solve",
+    "calib_solve_batch",
     "calib_workspace_bytes",
+    "calib_batch_workspace_bytes",
     "device_status",
     "reconstruction_error",
     "CalibResult",
@@ -262,6 +265,52 @@ def calib_solve(C: torch.Tensor, n_samples: int, rows_out: torch.Tensor, *, eps:
         check(st, "instant_calib_solve")
         return res
     return res, st
+
+
+def calib_batch_workspace_bytes(L: int, count: int) -> int:
+    return int(lib().instant_calib_batch_workspace_bytes(L, count))
+
+
+def calib_solve_batch(problems, *, ws: torch.Tensor | None = None, stream=None,
+                      raise_on_error: bool = True):
+    """Several statistics of one token length in one call; synchronises the stream.
+
+    ``problems`` is a sequence of dicts with the keys ``C`` (``[L, L]`` fp32),
+    ``n_samples`` and ``rows_out`` (``[r_cap, L]``, one dtype for all), and
+    optionally the keyword parameters of :func:`calib_solve` (``eps``, ``p``,
+    ``r_override``, ``scale_on``, ``max_iter``, ``tol``, ``warm_start``).
+    Returns a list of :class:`CalibResult` (and the list of per-problem
+    statuses when ``raise_on_error`` is False)."""
+    n = len(problems)
+    if n < 1:
+        raise ValueError("calib_solve_batch: no problems")
+    L = problems[0]["C"].shape[0]
+    dt = problems[0]["rows_out"].dtype
+    arr = (CalibProblem * n)()
+    eigs = []
+    for i, q in enumerate(problems):
+        C, rows = q["C"], q["rows_out"]
+        if C.shape != (L, L) or C.dtype != torch.float32 or rows.shape[1] != L or rows.dtype != dt:
+            raise ValueError("calib_solve_batch: inconsistent shapes or dtypes")
+        r_cap = rows.shape[0]
+        eig = (ctypes.c_double * r_cap)()
+        eigs.append(eig)
+        prm = CalibParams(q.get("eps", 0.95), q.get("p", 0), q.get("r_override", 0),
+                          int(bool(q.get("scale_on", True))), q.get("max_iter", 0), q.get("tol", 0.0),
+                          int(bool(q.get("warm_start", False))))
+        arr[i] = CalibProblem(_dev(C, "C"), int(q["n_samples"]), prm, _dev(rows, "rows_out"), r_cap,
+                              ctypes.cast(eig, ctypes.POINTER(ctypes.c_double)), 0, 0, 0.0, 0.0, 0)
+    if ws is None:
+        ws = torch.empty(calib_batch_workspace_bytes(L, n), dtype=torch.uint8,
+                         device=problems[0]["C"].device)
+    st = lib().instant_calib_solve_batch(arr, n, L, dtype_code(dt), _dev(ws, "ws"),
+                                         ws.numel() * ws.element_size(), _stream(stream))
+    res = [CalibResult(arr[i].k, arr[i].R, arr[i].scale, arr[i].energy, list(eigs[i]))
+           for i in range(n)]
+    if raise_on_error:
+        check(st, "instant_calib_solve_batch")
+        return res
+    return res, [arr[i].status for i in range(n)]
 
 
 def reconstruction_error(t: torch.Tensor, Q: torch.Tensor, S: torch.Tensor, ws: torch.Tensor,

@@ -22,7 +22,8 @@ LIB = os.path.join(PKG, "libinstant.so")
 SOURCES = ["capi.cu", "project.cu", "gemm.cu", "expand.cu", "gradx_fused.cu", "syrk.cu", "eig.cu",
            "static_scratch.cu", "recon.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+         "-I", INCLUDE, "-I", CSRC]
 
 
 def nvcc() -> str:

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -172,6 +173,289 @@ size_t grad_x_ws(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
 // ===========================================================================
 // C ABI
 // ===========================================================================
+namespace {
+
+// fused single-kernel input gradient when every CTA can afford to recompute
+// its g_hat_x tile (small Cy); otherwise grad_x_core + expand
+// token-axis cluster of the fused kernel: up to 8 CTAs, a power of two
+int fused_cluster(int L) {
+  const int nlt = cdiv(L, 128);
+  int cl = 1;
+  while (cl * 2 <= nlt && cl < 8) cl *= 2;
+  return cl;
+}
+
+bool use_fused_grad_x(int L, int Cy, int Ry, instant_dtype dt) {
+  if (dt != INSTANT_BF16 || Ry > 64) return false;
+  if (std::getenv("INSTANT_NO_FUSED_GRAD_X")) return false;
+  // each CTA recomputes a K-slice of its g_hat_x tile: keep that slice short
+  return cdiv(cdiv(Cy, 64), fused_cluster(L)) <= 16;
+}
+
+// weight-gradient operands riding along in the fused launch (Sx == nullptr: none)
+struct GradWPart {
+  const void* Sx;
+  const void* xhat;
+  float* gw;
+  int accumulate;
+  int Rx;
+};
+
+instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
+                            int Cx, int Cy, int Ry, const GradWPart& gwp, cudaStream_t st) {
+  FusedArgs f;
+  f.B = B;
+  f.L = L;
+  f.Cx = Cx;
+  f.Cy = Cy;
+  f.Ry = Ry;
+  f.KR = round_up(Ry, 16);
+  f.spt = 128 / Ry;
+  f.BN = 64;
+  f.nk = cdiv(Cy, 64);
+  f.nlt = cdiv(L, 128);
+  f.cl = fused_cluster(L);
+  f.lt_per = cdiv(f.nlt, f.cl);
+  const int kper = cdiv(f.nk, f.cl);
+  f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;
+  // smaller sample tiles when the grid would not cover the SMs
+  while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < 152) f.spt /= 2;
+  f.a_rows = std::min(128, round_up(f.spt * Ry, 8));
+  f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
+  f.Q = Q;
+  f.gw_y0 = cdiv(B, f.spt);
+  f.gw_mt = gwp.Sx ? cdiv(Cy, 128) : 0;
+  f.gw_nk = gwp.Sx ? cdiv(B * gwp.Rx, 64) : 0;
+  f.gw_acc = gwp.accumulate ? 1 : 0;
+  f.gw = gwp.gw;
+  CUtensorMap ms, mw, mq, mo, msx, mxh;
+  std::memset(&mq, 0, sizeof(mq));
+  std::memset(&msx, 0, sizeof(msx));
+  std::memset(&mxh, 0, sizeof(mxh));
+  if (gwp.Sx) {
+    // Sx [B*Rx, Cy] and x_hat [B*Rx, Cx], both read MN-major in 64 x 64 boxes
+    const uint64_t K = static_cast<uint64_t>(B) * gwp.Rx;
+    const uint64_t da[2] = {static_cast<uint64_t>(Cy), K};
+    const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
+    const uint64_t db[2] = {static_cast<uint64_t>(Cx), K};
+    const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
+    const uint32_t bx[2] = {64, 64};
+    if (!make_map(&msx, gwp.Sx, 2, da, sa, bx) || !make_map(&mxh, gwp.xhat, 2, db, sb, bx))
+      return INSTANT_ERR_CUDA;
+  }
+  const uint64_t ds[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(B) * Ry};
+  const uint64_t ss[1] = {static_cast<uint64_t>(Cy) * 2};
+  const uint32_t bs[2] = {64, static_cast<uint32_t>(f.a_rows)};
+  const uint64_t dw[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
+  const uint64_t sw[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bw[2] = {64, 64};
+  const uint64_t dout[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+  const uint64_t sout[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(L) * Cx * 2};
+  const uint32_t bout[3] = {64, 128, 1};
+  if (!make_map(&ms, Sq, 2, ds, ss, bs) || !make_map(&mw, w, 2, dw, sw, bw) ||
+      !make_map(&mo, gx, 3, dout, sout, bout))
+    return INSTANT_ERR_CUDA;
+  if (f.q_tma) {
+    const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
+    const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
+    const uint32_t b2[2] = {64, static_cast<uint32_t>(f.KR)};
+    if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+  }
+  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, f, st));
+}
+
+// ---------------------------------------------------------------------------
+// calibration solve of one statistic (instant_calib_solve and the batch call)
+// ---------------------------------------------------------------------------
+struct SolveJob {
+  const float* C;
+  int L;
+  instant_calib_params prm;
+  void* rows_out;
+  int r_cap;
+  int out_bf16;
+  int max_iter, max_sweeps;
+  double tol, inv_n, inv_n2;
+  int m_block;  // subspace block of the first attempt
+  bool warm;
+  SolverWs w;
+};
+
+struct SolveOut {
+  int k = 0, R = 0;
+  float scale = 0.f;
+  double energy = 0.0;
+};
+
+size_t solve_ws_stride(int L) { return (solver_workspace_bytes(L) + 255) & ~static_cast<size_t>(255); }
+
+instant_status solve_prepare(const float* C, long long n_samples, int L,
+                             const instant_calib_params* prm, void* rows_out, int r_cap,
+                             instant_dtype dt, void* ws, size_t ws_bytes, SolveJob* j) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!C || !prm || !rows_out) return INSTANT_ERR_ARG;
+  if (n_samples < 1 || !(prm->eps > 0.0 && prm->eps <= 1.0) || prm->p < 0 || prm->r_override < 0)
+    return INSTANT_ERR_ARG;
+  if (L < 1 || L > 8192 || r_cap < 1 || r_cap > 128 || r_cap > L) return INSTANT_ERR_SHAPE;
+  if (prm->r_override > r_cap) return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < solver_workspace_bytes(L)) return INSTANT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return INSTANT_ERR_ALIGN;
+  const bool noconv = fault_injected("solve_noconv");
+  j->C = C;
+  j->L = L;
+  j->prm = *prm;
+  j->rows_out = rows_out;
+  j->r_cap = r_cap;
+  j->out_bf16 = dt == INSTANT_BF16 ? 1 : 0;
+  j->max_iter = noconv ? 1 : (prm->max_iter > 0 ? prm->max_iter : 300);
+  j->max_sweeps = noconv ? 0 : 60;
+  j->tol = prm->tol > 0.0 ? prm->tol : 2e-5;
+  j->inv_n = 1.0 / static_cast<double>(n_samples);
+  j->inv_n2 = j->inv_n * j->inv_n;
+  // block: the needed rank plus a margin for the convergence rate
+  const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
+  j->m_block = std::min(128, std::max(16, round_up(std::max(2 * r_guess, r_guess + 8), 16)));
+  j->warm = prm->warm_start != 0;
+  j->w = solver_carve(ws, L);
+  return INSTANT_OK;
+}
+
+// the whole iteration in one launch of an 8-CTA cluster, checked on the device
+bool solve_uses_cluster(const SolveJob& j) {
+  return j.L > 128 && cluster_solve_fits(j.L, j.m_block) && !std::getenv("INSTANT_SOLVER_MULTI");
+}
+
+ClusterSolveArgs cluster_args(const SolveJob& j) {
+  ClusterSolveArgs ca;
+  ca.C = j.C;
+  ca.L = j.L;
+  ca.m = j.m_block;
+  ca.rp = 0;
+  ca.inv_n = static_cast<float>(j.inv_n);
+  ca.inv_n2 = j.inv_n2;
+  ca.eps = j.prm.eps;
+  ca.p = j.prm.p;
+  ca.r_override = j.prm.r_override;
+  ca.scale_on = j.prm.scale_on ? 1 : 0;
+  ca.tol = j.tol;
+  ca.max_iter = j.max_iter;
+  ca.max_sweeps = j.max_sweeps;
+  ca.rr_tol = 1e-5f;
+  ca.seed = j.rows_out;
+  ca.n_seed = j.warm ? std::min(j.r_cap, j.m_block) : 0;
+  ca.seed_bf16 = j.out_bf16;
+  ca.rows_out = j.rows_out;
+  ca.r_cap = j.r_cap;
+  ca.out_bf16 = j.out_bf16;
+  ca.res = j.w.res;
+  return ca;
+}
+
+// outcome of a one-launch solve; false: k + p did not fit the block, and the
+// multi-launch loop continues with twice the columns (rows_out still holds
+// the caller's seed)
+bool cluster_finish(SolveJob& j, const SolverResult& res, SolveOut* o, double* eig_out,
+                    instant_status* status) {
+  const double E = res.energy_sum * j.inv_n2;
+  if (res.nonfinite || !std::isfinite(E) || !(E > 0.0)) {
+    *status = INSTANT_ERR_NONFINITE;
+    return true;
+  }
+  if (res.block_short) {
+    j.m_block = std::min(128, 2 * j.m_block);
+    return false;
+  }
+  instant_status st1 = res.converged ? INSTANT_OK : INSTANT_ERR_NOT_CONVERGED;
+  if (res.jacobi_failed) st1 = INSTANT_ERR_NOT_CONVERGED;
+  if (res.R > j.r_cap) st1 = INSTANT_ERR_SHAPE;
+  o->k = res.k;
+  o->R = res.R < j.r_cap ? res.R : j.r_cap;
+  o->scale = res.scale;
+  o->energy = E;
+  if (eig_out)
+    for (int i = 0; i < j.r_cap; ++i) eig_out[i] = i < j.m_block ? res.theta[i] : 0.0;
+  *status = st1;
+  return true;
+}
+
+// energy, then full Jacobi (L <= 128) or the multi-launch subspace iteration
+// with host-side convergence checks, then the projector rows
+instant_status solve_multi(SolveJob& j, SolveOut* o, double* eig_out, cudaStream_t st) {
+  const int L = j.L;
+  SolverWs& w = j.w;
+  SolverResult res;
+  if (launch_solver_energy(j.C, L, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  const double E = res.energy_sum * j.inv_n2;
+  if (res.nonfinite || !std::isfinite(E) || !(E > 0.0)) return INSTANT_ERR_NONFINITE;
+
+  instant_status status = INSTANT_OK;
+  int m = L;
+  if (L <= 128) {
+    if (launch_jacobi_full(j.C, L, j.inv_n, j.max_sweeps, w, st) != cudaSuccess)
+      return INSTANT_ERR_CUDA;
+  } else {
+    m = j.m_block;
+    bool converged = false;
+    // warm start: the previous projector rows seed the block; the subspace has
+    // usually moved little, so convergence is checked early and often
+    for (;;) {
+      const int n_seed = j.warm ? std::min(j.r_cap, m) : 0;
+      if (launch_subspace_init(L, m, j.rows_out, n_seed, j.out_bf16, w, st) != cudaSuccess)
+        return INSTANT_ERR_CUDA;
+      bool grow = false;
+      for (int it = 0; it < j.max_iter; ++it) {
+        const bool check =
+            (j.warm ? (it + 1) % 2 == 1 : (it + 1) % 4 == 0) || it == j.max_iter - 1;
+        if (launch_subspace_iteration(j.C, L, m, j.inv_n, j.max_sweeps, check ? 1e-5f : 1e-3f, w,
+                                      st) != cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if (!check) continue;
+        if (launch_subspace_check(L, m, j.prm.eps, j.prm.p, j.prm.r_override, j.tol, j.inv_n2, w,
+                                  st) != cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+          return INSTANT_ERR_CUDA;
+        if (res.converged) {
+          converged = true;
+          break;
+        }
+        if (res.block_short && it >= 15 && m < 128) {
+          grow = true;
+          break;
+        }
+      }
+      if (grow) {
+        m = std::min(128, 2 * m);
+        continue;
+      }
+      break;
+    }
+    if (!converged) status = INSTANT_ERR_NOT_CONVERGED;
+  }
+  if (launch_solver_finalize(L, m, j.prm.eps, j.prm.p, j.prm.r_override, j.prm.scale_on ? 1 : 0,
+                             j.rows_out, j.r_cap, j.out_bf16, j.inv_n2, w, st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
+  if (res.jacobi_failed) status = INSTANT_ERR_NOT_CONVERGED;
+  if (L > 128 && res.R > j.r_cap) status = INSTANT_ERR_SHAPE;
+  o->k = res.k;
+  o->R = res.R < j.r_cap ? res.R : j.r_cap;
+  o->scale = res.scale;
+  o->energy = E;
+  if (eig_out)
+    for (int i = 0; i < j.r_cap; ++i) eig_out[i] = i < m ? res.theta[i] : 0.0;
+  if (L <= 128 && res.R > j.r_cap && status == INSTANT_OK) status = INSTANT_ERR_SHAPE;
+  return status;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* instant_status_string(instant_status s) {
@@ -351,94 +635,6 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
   return from_cuda(launch_expand_bf16(mq, mg, mo, e, st));
 }
 
-// fused single-kernel input gradient when every CTA can afford to recompute
-// its g_hat_x tile (small Cy); otherwise grad_x_core + expand
-// token-axis cluster of the fused kernel: up to 8 CTAs, a power of two
-int fused_cluster(int L) {
-  const int nlt = cdiv(L, 128);
-  int cl = 1;
-  while (cl * 2 <= nlt && cl < 8) cl *= 2;
-  return cl;
-}
-
-bool use_fused_grad_x(int L, int Cy, int Ry, instant_dtype dt) {
-  if (dt != INSTANT_BF16 || Ry > 64) return false;
-  if (std::getenv("INSTANT_NO_FUSED_GRAD_X")) return false;
-  // each CTA recomputes a K-slice of its g_hat_x tile: keep that slice short
-  return cdiv(cdiv(Cy, 64), fused_cluster(L)) <= 16;
-}
-
-// weight-gradient operands riding along in the fused launch (Sx == nullptr: none)
-struct GradWPart {
-  const void* Sx;
-  const void* xhat;
-  float* gw;
-  int accumulate;
-  int Rx;
-};
-
-instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
-                            int Cx, int Cy, int Ry, const GradWPart& gwp, cudaStream_t st) {
-  FusedArgs f;
-  f.B = B;
-  f.L = L;
-  f.Cx = Cx;
-  f.Cy = Cy;
-  f.Ry = Ry;
-  f.KR = round_up(Ry, 16);
-  f.spt = 128 / Ry;
-  f.BN = 64;
-  f.nk = cdiv(Cy, 64);
-  f.nlt = cdiv(L, 128);
-  f.cl = fused_cluster(L);
-  f.lt_per = cdiv(f.nlt, f.cl);
-  const int kper = cdiv(f.nk, f.cl);
-  f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;
-  // smaller sample tiles when the grid would not cover the SMs
-  while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < 152) f.spt /= 2;
-  f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
-  f.Q = Q;
-  f.gw_y0 = cdiv(B, f.spt);
-  f.gw_mt = gwp.Sx ? cdiv(Cy, 128) : 0;
-  f.gw_nk = gwp.Sx ? cdiv(B * gwp.Rx, 64) : 0;
-  f.gw_acc = gwp.accumulate ? 1 : 0;
-  f.gw = gwp.gw;
-  CUtensorMap ms, mw, mq, mo, msx, mxh;
-  std::memset(&mq, 0, sizeof(mq));
-  std::memset(&msx, 0, sizeof(msx));
-  std::memset(&mxh, 0, sizeof(mxh));
-  if (gwp.Sx) {
-    // Sx [B*Rx, Cy] and x_hat [B*Rx, Cx], both read MN-major in 64 x 64 boxes
-    const uint64_t K = static_cast<uint64_t>(B) * gwp.Rx;
-    const uint64_t da[2] = {static_cast<uint64_t>(Cy), K};
-    const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
-    const uint64_t db[2] = {static_cast<uint64_t>(Cx), K};
-    const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
-    const uint32_t bx[2] = {64, 64};
-    if (!make_map(&msx, gwp.Sx, 2, da, sa, bx) || !make_map(&mxh, gwp.xhat, 2, db, sb, bx))
-      return INSTANT_ERR_CUDA;
-  }
-  const uint64_t ds[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(B) * Ry};
-  const uint64_t ss[1] = {static_cast<uint64_t>(Cy) * 2};
-  const uint32_t bs[2] = {64, 128};
-  const uint64_t dw[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
-  const uint64_t sw[1] = {static_cast<uint64_t>(Cx) * 2};
-  const uint32_t bw[2] = {64, 64};
-  const uint64_t dout[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
-  const uint64_t sout[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(L) * Cx * 2};
-  const uint32_t bout[3] = {64, 128, 1};
-  if (!make_map(&ms, Sq, 2, ds, ss, bs) || !make_map(&mw, w, 2, dw, sw, bw) ||
-      !make_map(&mo, gx, 3, dout, sout, bout))
-    return INSTANT_ERR_CUDA;
-  if (f.q_tma) {
-    const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
-    const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
-    const uint32_t b2[2] = {64, static_cast<uint32_t>(f.KR)};
-    if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
-  }
-  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, f, st));
-}
-
 instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
                               size_t ws_bytes, int B, int L, int Cx, int Cy, int Ry,
                               instant_dtype dt, void* stream) {
@@ -516,146 +712,102 @@ size_t instant_calib_workspace_bytes(int L, int r_cap) {
   return solver_workspace_bytes(L);
 }
 
+size_t instant_calib_batch_workspace_bytes(int L, int count) {
+  if (L < 1 || count < 1) return 0;
+  return static_cast<size_t>(count) * solve_ws_stride(L);
+}
+
 instant_status instant_calib_solve(const float* C, long long n_samples, int L,
                                    const instant_calib_params* prm, void* rows_out, int r_cap,
                                    instant_dtype dt, int* k_out, int* r_out, float* scale_out,
                                    double* energy_out, double* eig_out, void* ws, size_t ws_bytes,
                                    void* stream) {
   if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
-  if (!C || !prm || !rows_out || !k_out || !r_out || !scale_out) return INSTANT_ERR_ARG;
-  if (n_samples < 1 || !(prm->eps > 0.0 && prm->eps <= 1.0) || prm->p < 0 || prm->r_override < 0)
-    return INSTANT_ERR_ARG;
-  if (L < 1 || L > 8192 || r_cap < 1 || r_cap > 128 || r_cap > L) return INSTANT_ERR_SHAPE;
-  if (prm->r_override > r_cap) return INSTANT_ERR_SHAPE;
-  if (!ws || ws_bytes < solver_workspace_bytes(L)) return INSTANT_ERR_WORKSPACE;
-  if (!aligned16(ws)) return INSTANT_ERR_ALIGN;
+  if (!k_out || !r_out || !scale_out) return INSTANT_ERR_ARG;
+  SolveJob j;
+  const instant_status v = solve_prepare(C, n_samples, L, prm, rows_out, r_cap, dt, ws, ws_bytes, &j);
+  if (v != INSTANT_OK) return v;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool noconv = fault_injected("solve_noconv");
-  const int max_iter = noconv ? 1 : (prm->max_iter > 0 ? prm->max_iter : 300);
-  const int max_sweeps = noconv ? 0 : 60;
-  const double tol = prm->tol > 0.0 ? prm->tol : 2e-5;
-  const double inv_n = 1.0 / static_cast<double>(n_samples);
-  const double inv_n2 = inv_n * inv_n;
-  const int out_bf16 = dt == INSTANT_BF16 ? 1 : 0;
-
-  SolverWs w = solver_carve(ws, L);
-  SolverResult res;
-  // block: the needed rank plus a margin for the convergence rate
-  const int r_guess = prm->r_override > 0 ? prm->r_override : prm->p + 8;
-  int m_block = std::min(128, std::max(16, round_up(std::max(2 * r_guess, r_guess + 8), 16)));
-  const bool warm = prm->warm_start != 0;
-  if (L > 128 && cluster_solve_fits(L, m_block) && !std::getenv("INSTANT_SOLVER_MULTI")) {
-    // the whole iteration in one launch of an 8-CTA cluster, checked on the device
-    ClusterSolveArgs ca;
-    ca.C = C;
-    ca.L = L;
-    ca.m = m_block;
-    ca.rp = 0;
-    ca.inv_n = static_cast<float>(inv_n);
-    ca.inv_n2 = inv_n2;
-    ca.eps = prm->eps;
-    ca.p = prm->p;
-    ca.r_override = prm->r_override;
-    ca.scale_on = prm->scale_on ? 1 : 0;
-    ca.tol = tol;
-    ca.max_iter = max_iter;
-    ca.max_sweeps = max_sweeps;
-    ca.rr_tol = 1e-5f;
-    ca.seed = rows_out;
-    ca.n_seed = warm ? std::min(r_cap, m_block) : 0;
-    ca.seed_bf16 = out_bf16;
-    ca.rows_out = rows_out;
-    ca.r_cap = r_cap;
-    ca.out_bf16 = out_bf16;
-    ca.res = w.res;
-    if (launch_cluster_solve(ca, st) != cudaSuccess) return INSTANT_ERR_CUDA;
-    if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+  SolveOut o;
+  instant_status status = INSTANT_OK;
+  bool done = false;
+  if (solve_uses_cluster(j)) {
+    if (launch_cluster_solve(cluster_args(j), st) != cudaSuccess) return INSTANT_ERR_CUDA;
+    SolverResult res;
+    if (cudaMemcpyAsync(&res, j.w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
       return INSTANT_ERR_CUDA;
-    const double E1 = res.energy_sum * inv_n2;
-    if (res.nonfinite || !std::isfinite(E1) || !(E1 > 0.0)) return INSTANT_ERR_NONFINITE;
-    if (!res.block_short) {
-      instant_status st1 = res.converged ? INSTANT_OK : INSTANT_ERR_NOT_CONVERGED;
-      if (res.jacobi_failed) st1 = INSTANT_ERR_NOT_CONVERGED;
-      if (res.R > r_cap) st1 = INSTANT_ERR_SHAPE;
-      *k_out = res.k;
-      *r_out = res.R < r_cap ? res.R : r_cap;
-      *scale_out = res.scale;
-      if (energy_out) *energy_out = E1;
-      if (eig_out)
-        for (int i = 0; i < r_cap; ++i) eig_out[i] = i < m_block ? res.theta[i] : 0.0;
-      return st1;
-    }
-    // k + p did not fit the block: continue below with a larger one (rows_out
-    // still holds the caller's seed)
-    m_block = std::min(128, 2 * m_block);
+    done = cluster_finish(j, res, &o, eig_out, &status);
   }
-  if (launch_solver_energy(C, L, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
-  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaStreamSynchronize(st) != cudaSuccess)
-    return INSTANT_ERR_CUDA;
-  const double E = res.energy_sum * inv_n2;
-  if (res.nonfinite || !std::isfinite(E) || !(E > 0.0)) return INSTANT_ERR_NONFINITE;
-
-  instant_status status = INSTANT_OK;
-  int m = L;
-  if (L <= 128) {
-    if (launch_jacobi_full(C, L, inv_n, max_sweeps, w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
-  } else {
-    m = m_block;
-    bool converged = false;
-    // warm start: the previous projector rows seed the block; the subspace has
-    // usually moved little, so convergence is checked early and often
-    for (;;) {
-      const int n_seed = warm ? std::min(r_cap, m) : 0;
-      if (launch_subspace_init(L, m, rows_out, n_seed, out_bf16, w, st) != cudaSuccess)
-        return INSTANT_ERR_CUDA;
-      bool grow = false;
-      for (int it = 0; it < max_iter; ++it) {
-        const bool check = (warm ? (it + 1) % 2 == 1 : (it + 1) % 4 == 0) || it == max_iter - 1;
-        if (launch_subspace_iteration(C, L, m, inv_n, max_sweeps, check ? 1e-5f : 1e-3f, w, st) !=
-            cudaSuccess)
-          return INSTANT_ERR_CUDA;
-        if (!check) continue;
-        if (launch_subspace_check(L, m, prm->eps, prm->p, prm->r_override, tol, inv_n2, w, st) !=
-            cudaSuccess)
-          return INSTANT_ERR_CUDA;
-        if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-          return INSTANT_ERR_CUDA;
-        if (res.converged) {
-          converged = true;
-          break;
-        }
-        if (res.block_short && it >= 15 && m < 128) {
-          grow = true;
-          break;
-        }
-      }
-      if (grow) {
-        m = std::min(128, 2 * m);
-        continue;
-      }
-      break;
-    }
-    if (!converged) status = INSTANT_ERR_NOT_CONVERGED;
-  }
-  if (launch_solver_finalize(L, m, prm->eps, prm->p, prm->r_override, prm->scale_on ? 1 : 0,
-                             rows_out, r_cap, out_bf16, inv_n2, w, st) != cudaSuccess)
-    return INSTANT_ERR_CUDA;
-  if (cudaMemcpyAsync(&res, w.res, sizeof(res), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-      cudaStreamSynchronize(st) != cudaSuccess)
-    return INSTANT_ERR_CUDA;
-  if (res.jacobi_failed) status = INSTANT_ERR_NOT_CONVERGED;
-  if (L > 128 && res.R > r_cap) status = INSTANT_ERR_SHAPE;
-  *k_out = res.k;
-  *r_out = res.R < r_cap ? res.R : r_cap;
-  *scale_out = res.scale;
-  if (energy_out) *energy_out = E;
-  if (eig_out)
-    for (int i = 0; i < r_cap; ++i) eig_out[i] = i < m ? res.theta[i] : 0.0;
-  if (L <= 128 && res.R > r_cap && status == INSTANT_OK) status = INSTANT_ERR_SHAPE;
+  if (!done) status = solve_multi(j, &o, eig_out, st);
+  *k_out = o.k;
+  *r_out = o.R;
+  *scale_out = o.scale;
+  if (energy_out) *energy_out = o.energy;
   return status;
+}
+
+instant_status instant_calib_solve_batch(instant_calib_problem* problems, int count, int L,
+                                         instant_dtype dt, void* ws, size_t ws_bytes,
+                                         void* stream) {
+  if (!problems || count < 1) return INSTANT_ERR_ARG;
+  if (L < 1 || L > 8192) return INSTANT_ERR_SHAPE;
+  const size_t stride = solve_ws_stride(L);
+  instant_status v = INSTANT_OK;
+  if (!ws || ws_bytes < static_cast<size_t>(count) * stride) v = INSTANT_ERR_WORKSPACE;
+  std::vector<SolveJob> jobs(count);
+  for (int i = 0; i < count && v == INSTANT_OK; ++i) {
+    const instant_calib_problem& q = problems[i];
+    v = solve_prepare(q.C, q.n_samples, L, &q.prm, q.rows_out, q.r_cap, dt,
+                      static_cast<uint8_t*>(ws) + i * stride, stride, &jobs[i]);
+  }
+  if (v != INSTANT_OK) {
+    for (int i = 0; i < count; ++i) problems[i].status = v;
+    return v;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // every problem that the one-launch solver takes: one cluster each, all in
+  // as few launches as the block sizes allow, one synchronisation
+  std::vector<SolverResult> res(count);
+  std::vector<char> launched(count, 0);
+  for (int m : {16, 32}) {
+    ClusterSolveBatch batch;
+    int idx[kMaxSolveBatch];
+    int n = 0;
+    for (int i = 0; i <= count; ++i) {
+      const bool take = i < count && solve_uses_cluster(jobs[i]) && jobs[i].m_block == m;
+      if (take) {
+        batch.s[n] = cluster_args(jobs[i]);
+        idx[n++] = i;
+      }
+      if (n == kMaxSolveBatch || (i == count && n > 0)) {
+        if (launch_cluster_solve_batch(batch, n, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+        for (int u = 0; u < n; ++u) {
+          if (cudaMemcpyAsync(&res[idx[u]], jobs[idx[u]].w.res, sizeof(SolverResult),
+                              cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return INSTANT_ERR_CUDA;
+          launched[idx[u]] = 1;
+        }
+        n = 0;
+      }
+    }
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  instant_status first = INSTANT_OK;
+  for (int i = 0; i < count; ++i) {
+    instant_calib_problem& q = problems[i];
+    SolveOut o;
+    instant_status s1 = INSTANT_OK;
+    const bool done = launched[i] && cluster_finish(jobs[i], res[i], &o, q.eig_out, &s1);
+    if (!done) s1 = solve_multi(jobs[i], &o, q.eig_out, st);
+    q.k = o.k;
+    q.R = o.R;
+    q.scale = o.scale;
+    q.energy = o.energy;
+    q.status = s1;
+    if (first == INSTANT_OK) first = s1;
+  }
+  return first;
 }
 
 instant_status instant_reconstruction_error(const void* t, const void* Q, const void* S, int B,

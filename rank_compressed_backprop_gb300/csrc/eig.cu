@@ -999,8 +999,10 @@ constexpr int kClusterCtas = 8;
 constexpr int kClusterThreads = 256;
 
 template <int M>
-__global__ void __launch_bounds__(kClusterThreads, 1) k_solve_cluster(ClusterSolveArgs a) {
+__global__ void __launch_bounds__(kClusterThreads, 1)
+    k_solve_cluster(const __grid_constant__ ClusterSolveBatch batch) {
   extern __shared__ __align__(16) uint8_t csm[];
+  const ClusterSolveArgs& a = batch.s[blockIdx.y];  // one statistic per cluster
   constexpr int m = M;
   const int L = a.L, rp = a.rp;
   const ClusterLay lay = cluster_layout(L, m, rp);
@@ -1548,15 +1550,27 @@ bool cluster_solve_fits(int L, int m) {
   return cluster_layout(L, m, rp).total <= 200 * 1024;
 }
 
-cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st) {
-  if (!cluster_solve_fits(a.L, a.m)) return cudaErrorInvalidValue;
-  a.rp = (a.L + kClusterCtas - 1) / kClusterCtas;
-  const size_t bytes = cluster_layout(a.L, a.m, a.rp).total;
-  auto kern = a.m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
+cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStream_t st) {
+  if (count < 1 || count > kMaxSolveBatch) return cudaErrorInvalidValue;
+  const int L = b.s[0].L, m = b.s[0].m;
+  if (!cluster_solve_fits(L, m)) return cudaErrorInvalidValue;
+  const int rp = (L + kClusterCtas - 1) / kClusterCtas;
+  for (int i = 0; i < count; ++i) {
+    if (b.s[i].L != L || b.s[i].m != m) return cudaErrorInvalidValue;
+    b.s[i].rp = rp;
+  }
+  const size_t bytes = cluster_layout(L, m, rp).total;
+  auto kern = m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
-  return launch_ex(kern, dim3(1, 1, kClusterCtas), dim3(kClusterThreads), bytes, st, kClusterCtas,
-                   false, a);
+  return launch_ex(kern, dim3(1, count, kClusterCtas), dim3(kClusterThreads), bytes, st,
+                   kClusterCtas, false, b);
+}
+
+cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st) {
+  ClusterSolveBatch b;
+  b.s[0] = a;
+  return launch_cluster_solve_batch(b, 1, st);
 }
 
 INSTANT_FAULT_READER(read_fault_eig)

@@ -6,7 +6,9 @@
 // A CTA owns a tile of `spt` whole samples (spt * Ry <= 128 rows of g_hat_x),
 // a BN-column strip of the output, and a range of 128-token tiles:
 //   phase 1  TMEM acc1[128 x BN] = Sq[tile rows, :] w[:, strip]  (tcgen05, K = Cy
-//            streamed through a TMA ring: Sq K-major, w MN-major);
+//            streamed through a TMA ring: Sq K-major, w MN-major; only the
+//            tile's spt * Ry rows of Sq are copied, the MMA rows past them read
+//            whatever the stage holds and are never used);
 //   phase 2  the epilogue warps turn acc1 into bf16 and write, per sample, the
 //            MN-major B operand [Ry (padded to 16) x BN] of the expansion
 //            straight into shared memory;
@@ -295,7 +297,7 @@ __global__ void __launch_bounds__(320, 1)
         uint8_t* sa = ring + s * lay.stage;
         uint8_t* sb = sa + A_BYTES;
         const int k0 = (kc0 + i) * BK;
-        mbar_arrive_expect_tx(&full[s], lay.stage);
+        mbar_arrive_expect_tx(&full[s], f.a_rows * BK * 2 + BN * BK * 2);
         tma_load_2d(sa, &tmap_sq, &full[s], k0, m0);
 #pragma unroll
         for (int h = 0; h < BN / 64; ++h)
@@ -547,6 +549,7 @@ cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tm
                                const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
                                const FusedArgs& f, cudaStream_t st) {
   if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
+  if (f.a_rows < f.spt * f.Ry || f.a_rows > BM || f.a_rows % 8 != 0) return cudaErrorInvalidValue;
   if (f.cl != 1 && f.cl != 2 && f.cl != 4 && f.cl != 8) return cudaErrorInvalidValue;
   if (f.lt_per * f.cl < f.nlt) return cudaErrorInvalidValue;
   if (f.gw_y0 != (f.B + f.spt - 1) / f.spt) return cudaErrorInvalidValue;

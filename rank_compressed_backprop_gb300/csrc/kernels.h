@@ -88,6 +88,8 @@ struct FusedArgs {
   int cl;            // cluster size along the token axis (1, 2, 4, 8): phase 1's K
                      // range is split across the cluster and reduced through DSMEM
   int q_tma;         // 1: Q^T tiles by TMA (L % 8 == 0); 0: threads fill them
+  int a_rows;        // Sq rows per phase-1 TMA box (spt * Ry rounded up to 8, <= 128):
+                     // the MMA still reads 128 rows, the ones past the box are unused
   const void* Q;     // [Ry, L]
   // weight gradient in the same launch (gw_mt > 0): grid rows gw_y0.. run the
   // 128 x 64 tiles of g_w[Cy, Cx] = Sx^T x_hat over K = B * Rx
@@ -193,6 +195,13 @@ struct ClusterSolveArgs {
 };
 bool cluster_solve_fits(int L, int m);
 cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st);
+// up to kMaxSolveBatch statistics of one size (same L and m) in one launch,
+// one cluster each (grid 1 x count x 8); rp is set by the launcher
+constexpr int kMaxSolveBatch = 16;
+struct ClusterSolveBatch {
+  ClusterSolveArgs s[kMaxSolveBatch];
+};
+cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStream_t st);
 
 // ||t - Q^T S||^2 and ||t||^2 over a batch (S = Q t per sample, [B*R, C]) into
 // totals[0..1] (fp64 device, zeroed by the launch)

@@ -41,7 +41,7 @@ class InstantLinear:
         self.gx = torch.empty(B, L, self.Cx, dtype=self.dtype, device=dev)
         nbytes = api.grad_x_workspace_bytes(B, L, self.Cx, self.Cy, Ry, self.dtype)
         self.ws_gx = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
-        self.ws_cal = torch.empty(api.calib_workspace_bytes(L, max(Rx, Ry)), dtype=torch.uint8,
+        self.ws_cal = torch.empty(api.calib_batch_workspace_bytes(L, 2), dtype=torch.uint8,
                                   device=dev)
         self.last_calibration = None
 
@@ -83,19 +83,20 @@ class InstantLinear:
             self.n_g += g_y.shape[0]
 
     def recalibrate(self, r_override: bool = True):
-        """Solves both statistics into ``P`` and ``Q`` and clears them.
+        """Solves both statistics into ``P`` and ``Q`` (one call) and clears them.
 
         With ``r_override`` the ranks stay at the buffer sizes ``Rx``/``Ry``;
         ``k`` and ``k + p`` are still reported."""
         if self.n_x == 0 or self.n_g == 0:
             raise RuntimeError("recalibrate: no statistics accumulated")
         warm = self.last_calibration is not None
-        rx = api.calib_solve(self.C_X, self.n_x, self.P, eps=self.eps, p=self.p,
-                             r_override=self.Rx if r_override else 0, scale_on=self.scale_on,
-                             ws=self.ws_cal, warm_start=warm)
-        rg = api.calib_solve(self.C_G, self.n_g, self.Q, eps=self.eps, p=self.p,
-                             r_override=self.Ry if r_override else 0, scale_on=self.scale_on,
-                             ws=self.ws_cal, warm_start=warm)
+        common = dict(eps=self.eps, p=self.p, scale_on=self.scale_on, warm_start=warm)
+        rx, rg = api.calib_solve_batch(
+            [dict(C=self.C_X, n_samples=self.n_x, rows_out=self.P,
+                  r_override=self.Rx if r_override else 0, **common),
+             dict(C=self.C_G, n_samples=self.n_g, rows_out=self.Q,
+                  r_override=self.Ry if r_override else 0, **common)],
+            ws=self.ws_cal)
         self.C_X.zero_()
         self.C_G.zero_()
         self.n_x = self.n_g = 0

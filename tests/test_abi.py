@@ -126,3 +126,25 @@ def test_empty_extents_are_rejected_without_gpu(L):
                                           ctypes.byref(n2), fake, 16, null) == 2
     assert L.instant_reconstruction_error(fake, fake, fake, 1, 8, 64, 4, 1, ctypes.byref(e2),
                                           ctypes.byref(n2), fake, 8, null) == 5
+
+
+def test_batch_solve_validation_without_gpu(L):
+    from rank_compressed_backprop_gb300._lib import CalibParams, CalibProblem
+
+    assert L.instant_calib_batch_workspace_bytes(512, 2) >= 2 * L.instant_calib_workspace_bytes(512, 8)
+    assert L.instant_calib_batch_workspace_bytes(0, 2) == 0
+    assert L.instant_calib_solve_batch(None, 1, 64, 1, ctypes.c_void_p(0x1000), 1 << 30, None) == 1
+    arr = (CalibProblem * 2)()
+    for i in range(2):
+        arr[i] = CalibProblem(0x1000 + 4096 * i, 4, CalibParams(0.95, 0, 8, 1, 0, 0.0, 0),
+                              0x100000 + 4096 * i, 8, None, 0, 0, 0.0, 0.0, -1)
+    fake = ctypes.c_void_p(0x200000)
+    assert L.instant_calib_solve_batch(arr, 0, 64, 1, fake, 1 << 30, None) == 1
+    need = L.instant_calib_batch_workspace_bytes(64, 2)
+    assert L.instant_calib_solve_batch(arr, 2, 64, 1, fake, need - 1, None) == 5
+    assert [arr[i].status for i in range(2)] == [5, 5]
+    arr[1].prm.r_override = 9                 # beyond r_cap
+    assert L.instant_calib_solve_batch(arr, 2, 64, 1, fake, need, None) == 2
+    assert [arr[i].status for i in range(2)] == [2, 2]
+    arr[1].prm.r_override = 8
+    assert L.instant_calib_solve_batch(arr, 2, 64, 7, fake, need, None) == 3   # dtype
