@@ -110,6 +110,10 @@ def layer_bytes(B, L, Cx, Cy, Rx, Ry):
         "grad_x": B * Ry * Cy * 2 + Cy * Cx * 2 + Ry * L * 2 + B * L * Cx * 2,
         "grad_w_x": (B * Rx * (Cy + Cx) * 2 + Cy * Cx * 4
                      + B * Ry * Cy * 2 + Cy * Cx * 2 + Ry * L * 2 + B * L * Cx * 2),
+        # the whole backward (one call): inputs g_y, [P; Q], x_hat, w; outputs
+        # Sx, Sq, g_w, g_x
+        "backward": (B * L * Cy * 2 + (Rx + Ry) * L * 2 + B * (Rx + Ry) * Cy * 2
+                     + B * Rx * Cx * 2 + Cy * Cx * 2 + Cy * Cx * 4 + B * L * Cx * 2),
     }
 
 
@@ -122,6 +126,8 @@ def layer_flops(B, L, Cx, Cy, Rx, Ry):
         "expand": 2 * B * Ry * L * Cx,
         "grad_x": 2 * B * Ry * Cy * Cx + 2 * B * Ry * L * Cx,
         "grad_w_x": 2 * B * Rx * Cy * Cx + 2 * B * Ry * Cy * Cx + 2 * B * Ry * L * Cx,
+        "backward": (2 * B * (Rx + Ry) * L * Cy + 2 * B * Rx * Cy * Cx + 2 * B * Ry * Cy * Cx
+                     + 2 * B * Ry * L * Cx),
     }
 
 
@@ -135,16 +141,19 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = {
-    "compress_act": "project.cu", "project_grad": "project.cu", "grad_w": "gemm.cu",
-    "grad_x_core": "gemm.cu", "expand": "expand.cu", "grad_x": "gradx_fused.cu",
-    "grad_w_x": "gradx_fused.cu",
+    "compress_act": ("project.cu", "project_tile.cuh"),
+    "project_grad": ("project.cu", "project_tile.cuh"),
+    "grad_w": ("gemm.cu",), "grad_x_core": ("gemm.cu",), "expand": ("expand.cu",),
+    "grad_x": ("gradx_fused.cu", "project_tile.cuh"),
+    "grad_w_x": ("gradx_fused.cu", "project_tile.cuh"),
+    "backward": ("gradx_fused.cu", "project_tile.cuh"),
 }
 
 
 def source_hash(kernel: str) -> str:
     d = os.path.join(ROOT, "rank_compressed_backprop_gb300", "csrc")
     h = hashlib.sha256()
-    for f in (KERNEL_SOURCES[kernel], "tc.cuh", "kernels.h"):
+    for f in (*KERNEL_SOURCES[kernel], "tc.cuh", "kernels.h"):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -372,6 +381,8 @@ def run_ours(args):
         "grad_x": lambda s: api.grad_x(lay.Sq, w, lay.Q, s["gx"], ws),
         "grad_w_x": lambda s: api.grad_w_x(lay.Sx, s["xhat"], s["gw"], lay.Sq, w, lay.Q, s["gx"], ws,
                                            B),
+        "backward": lambda s: api.backward(s["g"], lay.PQ, s["xhat"], w, lay.Sx, lay.Sq, s["gw"],
+                                           s["gx"], lay.ws_bw, Rx),
         "grad_x_core": lambda s: api.grad_x_core(lay.Sq, w, ws, B),
         "expand": lambda s: api.expand(lay.Q, s["gx"], ws, Cy),
     }
@@ -441,7 +452,7 @@ def run_ours(args):
         "config": {
             "workload": "BERT-base-block linear, B=32 L=512 Cx=Cy=768 Rx=Ry=8, sigma_i ~ i^-1.5",
             "B": B, "L": L, "Cx": Cx, "Cy": Cy, "Rx": Rx, "Ry": Ry,
-            "step": "compress_act + project_grad + grad_w_x (g_w and g_x in one launch); CUDA graphs of 8 steps "
+            "step": "compress_act + backward (project_grad, then g_w and g_x in one launch); CUDA graphs of 8 steps "
                     "(one per rotating buffer set); calibration (2x accumulate over 64 samples "
                     "+ 2 solves) every N_t steps",
             "calibration_every": args.nt, "calibrations_timed": n_cal,

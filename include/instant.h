@@ -141,6 +141,40 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
                                 instant_dtype dt, void* stream);
 
 /*
+ * The layer's whole low-rank backward in one call (关键设计 3): the same
+ * results, bit for bit, as instant_project_grad(gy, PQ, Sx, Sq, ...) followed
+ * by instant_grad_w_x(Sx, xhat, gw, accumulate, Sq, w, Q = rows Rx.. of PQ,
+ * gx, ...), which is what it runs.  With the environment variable
+ * INSTANT_ONE_LAUNCH_BACKWARD set, and where the single-kernel input gradient
+ * applies (bf16, short Cy), it is ONE launch instead: clusters take tickets
+ * as they start; the first tickets project (sample, 128-column) tiles of g_y
+ * and signal each finished tile through counters in `ws`, the input-gradient
+ * items of a sample group wait for their group's tiles and the
+ * weight-gradient tiles for all of them (a consumer only waits for smaller
+ * tickets, so the waits end whatever the scheduling).  That launch measured
+ * slower than the two on a BERT-base block, hence opt-in.
+ *   gy    [B, L, Cy]     dtype dt (read)
+ *   PQ    [Rx+Ry, L]     dtype dt (read)
+ *   xhat  [B, Rx, Cx]    dtype dt (read)
+ *   w     [Cy, Cx]       dtype dt (read)
+ *   Sx    [B*Rx, Cy], Sq [B*Ry, Cy]  dtype dt (written: the projections)
+ *   gw    [Cy, Cx]       fp32 (written, or added to when accumulate = 1)
+ *   gx    [B, L, Cx]     dtype dt (written)
+ *   ws    device scratch of instant_backward_workspace_bytes(...) bytes,
+ *         16-byte aligned.  ZERO IT ONCE after allocating it: its first bytes
+ *         are the counters, which every call leaves zero again; zero it again
+ *         after instant_device_status has reported INSTANT_ERR_DEVICE.  Calls
+ *         that may run at the same time need separate workspaces.
+ * Limits: 1 <= Ry <= 64, Rx + Ry <= 128.
+ */
+instant_status instant_backward(const void* gy, const void* PQ, const void* xhat, const void* w,
+                                void* Sx, void* Sq, float* gw, int accumulate, void* gx,
+                                void* ws, size_t ws_bytes, int B, int L, int Cx, int Cy,
+                                int Rx, int Ry, instant_dtype dt, void* stream);
+
+size_t instant_backward_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt);
+
+/*
  * The two halves of instant_grad_x, for callers that schedule or time them
  * separately.  instant_grad_x_core computes g_hat_x = Sq w (关键设计 3,
  * g_hat_x = g_hat_y2 w) into `ws` as [B*Ry, Cx] in dtype dt (its split-K

@@ -79,6 +79,9 @@ _PROTOS = {
     "instant_grad_x_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "instant_grad_w_x": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i,
                               _i, _vp]),
+    "instant_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _i, _i, _i, _i,
+                              _i, _i, _i, _vp]),
+    "instant_backward_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "instant_grad_x_core": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _vp]),
     "instant_expand": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),

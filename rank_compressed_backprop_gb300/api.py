@@ -22,6 +22,9 @@ __all__ = [
     "grad_x",
     "grad_x_workspace_bytes",
     "grad_w_x",
+    "backward",
+    "backward_workspace",
+    "backward_workspace_bytes",
     "grad_x_core",
     "expand",
     "grad_x_static",
@@ -152,6 +155,41 @@ def grad_w_x(Sx: torch.Tensor, xhat: torch.Tensor, gw: torch.Tensor, Sq: torch.T
                                  _dev(Sq, "Sq"), _dev(w, "w"), _dev(Q, "Q"), _dev(gx, "gx"),
                                  _dev(ws, "ws"), ws.numel() * ws.element_size(), B, L, Cx, Cy, Rx,
                                  Ry, dtype_code(Sq.dtype), _stream(stream)), "instant_grad_w_x")
+    return gw, gx
+
+
+def backward_workspace_bytes(B: int, L: int, Cx: int, Cy: int, Ry: int, dtype: torch.dtype) -> int:
+    return int(lib().instant_backward_workspace_bytes(B, L, Cx, Cy, Ry, dtype_code(dtype)))
+
+
+def backward_workspace(B: int, L: int, Cx: int, Cy: int, Ry: int, dtype: torch.dtype,
+                       device) -> torch.Tensor:
+    """A zeroed workspace for :func:`backward` (its counters must start at zero)."""
+    return torch.zeros(backward_workspace_bytes(B, L, Cx, Cy, Ry, dtype), dtype=torch.uint8,
+                       device=device)
+
+
+def backward(g_y: torch.Tensor, PQ: torch.Tensor, xhat: torch.Tensor, w: torch.Tensor,
+             Sx: torch.Tensor, Sq: torch.Tensor, gw: torch.Tensor, gx: torch.Tensor,
+             ws: torch.Tensor, Rx: int, *, accumulate: bool = False, stream=None):
+    """:func:`project_grad` then :func:`grad_w_x` in one call (one launch where
+    the single-kernel input gradient applies).  ``ws`` comes from
+    :func:`backward_workspace`.  Returns ``(gw, gx)``."""
+    B, L, Cy = g_y.shape
+    Ry = PQ.shape[0] - Rx
+    Cx = w.shape[1]
+    if (PQ.shape[1] != L or Ry < 1 or w.shape != (Cy, Cx) or xhat.numel() != B * Rx * Cx
+            or Sx.shape != (B * Rx, Cy) or Sq.shape != (B * Ry, Cy) or gw.shape != (Cy, Cx)
+            or gx.shape != (B, L, Cx)):
+        raise ValueError("backward: inconsistent shapes")
+    if gw.dtype != torch.float32:
+        raise TypeError("backward: gw must be float32")
+    _same_dtype(g_y.dtype, ("PQ", PQ), ("xhat", xhat), ("w", w), ("Sx", Sx), ("Sq", Sq), ("gx", gx))
+    check(lib().instant_backward(_dev(g_y, "g_y"), _dev(PQ, "PQ"), _dev(xhat, "xhat"), _dev(w, "w"),
+                                 _dev(Sx, "Sx"), _dev(Sq, "Sq"), _dev(gw, "gw"),
+                                 int(bool(accumulate)), _dev(gx, "gx"), _dev(ws, "ws"),
+                                 ws.numel() * ws.element_size(), B, L, Cx, Cy, Rx, Ry,
+                                 dtype_code(g_y.dtype), _stream(stream)), "instant_backward")
     return gw, gx
 
 

@@ -105,18 +105,12 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   a.pq = pq;
   a.out0 = out0;
   a.out1 = out1;
-  a.splits = 1;
   if (dt == INSTANT_F32) {
     a.pq_tma = 0;
     return from_cuda(launch_project_f32(a, static_cast<const float*>(t), st));
   }
   a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
-  // one CTA per (128-column tile, sample) over the whole token axis: three
-  // CTAs fit on an SM, so the grid is resident at once, and a token split's
-  // cluster reduction costs more than the balance it buys (measured on GB300
-  // from 2 to 64 samples of a BERT-base block)
-  a.splits = 1;
   CUtensorMap mt, mpq;
   std::memset(&mpq, 0, sizeof(mpq));
   const uint64_t dt3[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
@@ -201,8 +195,20 @@ struct GradWPart {
   int Rx;
 };
 
+// projection of g_y riding along in the fused launch (instant_backward)
+struct ProjPart {
+  const void* gy;    // [B, L, Cy]
+  const void* PQ;    // [Rx + Ry, L]
+  void* Sx;          // [B * Rx, Cy]
+  int Rx;
+  unsigned int* sync;  // zeroed counters, at least B + 3
+};
+
+// *no_room: the projector does not fit the projection phase's shared memory
+// (nothing launched; the caller takes two launches)
 instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* gx, int B, int L,
-                            int Cx, int Cy, int Ry, const GradWPart& gwp, cudaStream_t st) {
+                            int Cx, int Cy, int Ry, const GradWPart& gwp, cudaStream_t st,
+                            const ProjPart* pp = nullptr, bool* no_room = nullptr) {
   FusedArgs f;
   f.B = B;
   f.L = L;
@@ -261,8 +267,46 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
     const uint32_t b2[2] = {64, static_cast<uint32_t>(f.KR)};
     if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
   }
-  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, f, st));
+  CUtensorMap mgy, mpq;
+  std::memset(&mgy, 0, sizeof(mgy));
+  std::memset(&mpq, 0, sizeof(mpq));
+  f.proj = pp ? 1 : 0;
+  f.nct = cdiv(Cy, 128);
+  f.sync = pp ? pp->sync : nullptr;
+  std::memset(&f.pa, 0, sizeof(f.pa));
+  if (pp) {
+    ProjectArgs& a = f.pa;
+    a.B = B;
+    a.L = L;
+    a.C = Cy;
+    a.Rx = pp->Rx;
+    a.Ry = Ry;
+    a.NT = round_up(pp->Rx + Ry, 16);
+    a.nk = cdiv(L, 64);
+    a.pq = pp->PQ;
+    a.out0 = pp->Sx;
+    a.out1 = const_cast<void*>(Sq);
+    a.pq_tma = (L % 8 == 0 && aligned16(pp->PQ)) ? 1 : 0;
+    if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) {
+      if (no_room) *no_room = true;
+      return INSTANT_ERR_SHAPE;
+    }
+    const uint64_t dt3[3] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
+    const uint64_t st3[2] = {static_cast<uint64_t>(Cy) * 2, static_cast<uint64_t>(L) * Cy * 2};
+    const uint32_t bx3[3] = {64, 64, 1};
+    if (!make_map(&mgy, pp->gy, 3, dt3, st3, bx3)) return INSTANT_ERR_CUDA;
+    if (a.pq_tma) {
+      const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(pp->Rx + Ry)};
+      const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
+      const uint32_t b2[2] = {64, static_cast<uint32_t>(a.NT)};
+      if (!make_map(&mpq, pp->PQ, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+    }
+  }
+  return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, mgy, mpq, f, st));
 }
+
+// counters of the fused backward: per sample group (at most B), total, done, ticket
+size_t backward_sync_bytes(int B) { return (static_cast<size_t>(B + 3) * 4 + 255) & ~static_cast<size_t>(255); }
 
 // ---------------------------------------------------------------------------
 // calibration solve of one statistic (instant_calib_solve and the batch call)
@@ -671,6 +715,49 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
   const instant_status s = instant_grad_w(Sx, xhat, gw, accumulate, B, Rx, Cx, Cy, dt, stream);
   if (s != INSTANT_OK) return s;
   return instant_grad_x(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
+}
+
+size_t instant_backward_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt) {
+  (void)L;
+  if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || !dtype_ok(dt)) return 0;
+  return backward_sync_bytes(B) + grad_x_ws(B, Cx, Cy, Ry, dt);
+}
+
+instant_status instant_backward(const void* gy, const void* PQ, const void* xhat, const void* w,
+                                void* Sx, void* Sq, float* gw, int accumulate, void* gx, void* ws,
+                                size_t ws_bytes, int B, int L, int Cx, int Cy, int Rx, int Ry,
+                                instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!gy || !PQ || !xhat || !w || !Sx || !Sq || !gw || !gx) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Rx < 1 || Ry < 1 || Ry > 64 || Rx + Ry > 128)
+    return INSTANT_ERR_SHAPE;
+  if (!ws || ws_bytes < instant_backward_workspace_bytes(B, L, Cx, Cy, Ry, dt))
+    return INSTANT_ERR_WORKSPACE;
+  if (!aligned16(ws)) return INSTANT_ERR_ALIGN;
+  if (dt == INSTANT_BF16 &&
+      (!aligned16(gy) || !aligned16(xhat) || !aligned16(w) || !aligned16(Sx) || !aligned16(Sq) ||
+       !aligned16(gw) || !aligned16(gx) || Cx % 8 != 0 || Cy % 8 != 0))
+    return INSTANT_ERR_ALIGN;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t elt = dt == INSTANT_BF16 ? 2 : 4;
+  const void* Q = static_cast<const uint8_t*>(PQ) + static_cast<size_t>(Rx) * L * elt;
+  const size_t sync_bytes = backward_sync_bytes(B);
+  void* ws_gx = static_cast<uint8_t*>(ws) + sync_bytes;
+  // one launch on request: correct, but measured slower than the two launches
+  // below on a BERT-base block (23.9 against 18.9 us: the projection tiles
+  // finish late and the input-gradient items still take ~9 us after their signal)
+  if (use_fused_grad_x(L, Cy, Ry, dt) && std::getenv("INSTANT_ONE_LAUNCH_BACKWARD")) {
+    const ProjPart pp{gy, PQ, Sx, Rx, static_cast<unsigned int*>(ws)};
+    bool no_room = false;
+    const instant_status s = grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry,
+                                          GradWPart{Sx, xhat, gw, accumulate, Rx}, st, &pp, &no_room);
+    if (!no_room) return s;
+  }
+  // two launches: the projection, then the weight and input gradients
+  const instant_status s = project(gy, PQ, Sx, Sq, B, L, Cy, Rx, Ry, dt, st);
+  if (s != INSTANT_OK) return s;
+  return instant_grad_w_x(Sx, xhat, gw, accumulate, Sq, w, Q, gx, ws_gx, ws_bytes - sync_bytes, B, L,
+                          Cx, Cy, Rx, Ry, dt, stream);
 }
 
 instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, int Cdim,

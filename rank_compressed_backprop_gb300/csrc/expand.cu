@@ -47,7 +47,9 @@ __host__ __device__ inline Lay expand_layout(int BN, int KR) {
 }
 
 template <int BN>
-__global__ void __launch_bounds__(320, 1)
+// two CTAs per SM: at most 102 registers a thread (with more, as an
+// instrumented build once had, the SM held one CTA and the grid ran in two waves)
+__global__ void __launch_bounds__(320, 2)
     k_expand_bf16(const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_g,
                   const __grid_constant__ CUtensorMap tmap_out, ExpandArgs e) {
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int lt = grp; lt < e.nlt; lt += 2, ++it) {
       uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
       if (gt == 0 && it >= 2) tma_store_wait_read<1>();
-      named_barrier(1 + grp, 128);
+      if (grp == 0) named_barrier<1>(128); else named_barrier<2>(128);
       if (!mbar_wait(&t_full[grp], it & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
       const uint32_t taddr = tmem + grp * BN + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(320, 1)
                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       fence_proxy_async_smem();
-      named_barrier(1 + grp, 128);
+      if (grp == 0) named_barrier<1>(128); else named_barrier<2>(128);
       if (gt == 0) {
         for (int h = 0; h < BN / 64; ++h)
           if (n0 + 64 * h < e.Cx) tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, lt * BM, b);

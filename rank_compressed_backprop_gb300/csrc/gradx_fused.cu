@@ -23,7 +23,21 @@
 // barrier) each produce one 128 x 64 fp32 tile of g_w, so that both products
 // of the backward pass share one launch and fill the SMs the input gradient
 // leaves free.
+//
+// And it can start one step earlier, from g_y itself (the whole backward of
+// the layer in one launch): clusters take tickets as they start; the first
+// tickets are projection tiles (sample, 128 columns of g_y -> Sx, Sq, one per
+// CTA), then the input-gradient items of the sample groups in order, then the
+// weight-gradient tiles.  Each projection tile adds to its group's counter and
+// to a total (release); phase 1 of a group waits for its group's count, the
+// weight-gradient tiles for the total (acquire, bounded).  A consumer only
+// waits for smaller tickets, held by clusters that are running and never
+// wait themselves, so the waits end whatever the scheduling; the last CTA
+// zeroes the counters for the next launch.
+#include <mutex>
+
 #include "kernels.h"
+#include "project_tile.cuh"
 #include "tc.cuh"
 
 namespace instant {
@@ -36,12 +50,13 @@ constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int BOX = BM * 128;         // staging box: 128 rows x 64 bf16
 
 struct FLay {
-  uint32_t ring, stage, qt, qt_tile, bs, bs_sample, stg, bar, total;
+  uint32_t ring, stage, qt, qt_tile, bs, bs_sample, stg, bar, pbar, total;
 };
 
-// gw: the launch also runs weight-gradient tiles, whose 3-stage ring needs 72 KB
+// gw: the launch also runs weight-gradient tiles, whose 3-stage ring needs 72 KB;
+// proj_bytes: the projection phase's ring (0: none), also at the start
 __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_per, int spt,
-                                             bool gw) {
+                                             bool gw, uint32_t proj_bytes) {
   FLay l;
   l.stage = A_BYTES + BN * BK * 2;
   l.ring = 0;
@@ -51,6 +66,7 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   uint32_t first = ring_bytes > stg_bytes ? ring_bytes : stg_bytes;
   if (red_bytes > first) first = red_bytes;
   if (gw && first < 3u * (A_BYTES + 64 * BK * 2)) first = 3u * (A_BYTES + 64 * BK * 2);
+  if (first < proj_bytes) first = proj_bytes;
   first = (first + 1023u) & ~1023u;
   l.stg = 0;
   l.qt = first;
@@ -58,8 +74,87 @@ __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_
   l.bs = l.qt + lt_per * l.qt_tile;
   l.bs_sample = (BN / 64) * KR * 128;
   l.bar = l.bs + spt * l.bs_sample;
-  l.total = l.bar + 256;
+  l.pbar = l.bar + 256;
+  l.total = l.pbar + 128;
   return l;
+}
+
+__host__ __device__ inline uint32_t fused_proj_bytes(const FusedArgs& f) {
+  return f.proj ? proj_layout(f.pa.NT, f.pa.nk, f.pa.pq_tma).bytes : 0u;
+}
+
+// last action of every CTA of a launch with the projection phase: the CTA
+// that finishes last (all others are past all their waits) zeroes the
+// counters for the next launch
+__device__ __forceinline__ void proj_launch_done(const FusedArgs& f) {
+  if (threadIdx.x != 0) return;
+  unsigned int* done = f.sync + f.gw_y0 + 1;
+  const unsigned int ctas = gridDim.x * gridDim.y * gridDim.z;
+  if (atomicAdd(done, 1u) == ctas - 1) {
+    for (int i = 0; i < f.gw_y0 + 3; ++i) f.sync[i] = 0u;
+  }
+}
+
+// Work items of a launch with the projection phase, in ticket order: first
+// the projection tiles (cl per cluster), then the input-gradient items (one
+// (sample group, column strip) per cluster, groups in order), then the
+// weight-gradient tiles (cl per cluster).  Consumers only wait for items with
+// smaller tickets, which running clusters hold and finish without waiting.
+struct ProjItems {
+  int nstrips, n_tiles, n_pc, n_xc, n_gc;
+};
+
+__host__ __device__ inline ProjItems proj_items(const FusedArgs& f) {
+  ProjItems w;
+  w.nstrips = (f.Cx + f.BN - 1) / f.BN;
+  w.n_tiles = f.B * f.nct;
+  w.n_pc = (w.n_tiles + f.cl - 1) / f.cl;
+  w.n_xc = f.gw_y0 * w.nstrips;
+  w.n_gc = (f.gw_mt * w.nstrips + f.cl - 1) / f.cl;
+  return w;
+}
+
+// one projection tile of g_y (u = sample * nct + column tile; none when u is
+// past the last tile) into Sx and Sq, then its signals: one for the sample's
+// group and one in total
+__device__ __forceinline__ void proj_item(const CUtensorMap* tmap_gy, const CUtensorMap* tmap_pq,
+                                          const FusedArgs& f, uint8_t* smem, uint32_t pbar_off,
+                                          int u) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pbar_off);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kProjBarriers);
+  const uint32_t cols = f.pa.NT <= 32 ? 32 : (f.pa.NT <= 64 ? 64 : 128);
+  ProjPipe pipe = proj_pipe(smem, bars, f.pa.NT, f.pa.nk, f.pa.pq_tma, 0);
+  if (threadIdx.x == 0) {
+    proj_init_barriers(pipe);
+    fence_barrier_init();
+    prefetch_tmap(tmap_gy);
+    if (f.pa.pq_tma) prefetch_tmap(tmap_pq);
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(tmem_slot, cols);
+    tmem_relinquish();
+  }
+  if (!f.pa.pq_tma) proj_fill_pq(f.pa, pipe, f.pa.NT, threadIdx.x, blockDim.x);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();  // after the allocation
+  pipe.tmem = *tmem_slot;
+  if (u < f.B * f.nct && threadIdx.x < 128) {
+    const int b = u / f.nct;
+    proj_tile<2>(tmap_gy, tmap_pq, f.pa, f.pa.NT, b, (u % f.nct) * kProjBM, pipe);
+    // publish: the tile's stores, then the signals
+    __threadfence();
+    fence_proxy_async_global();
+    named_barrier<3>(128);
+    if (threadIdx.x == 0) {
+      signal_add(f.sync + b / f.spt, 1u);
+      signal_add(f.sync + f.gw_y0, 1u);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) tmem_dealloc(pipe.tmem, cols);
 }
 
 // One 128 x 64 tile of g_w[Cy, Cx] = Sx^T x_hat (K = B * Rx): Sx [K, Cy] and
@@ -98,6 +193,12 @@ __device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CU
   pdl_launch_dependents();
   pdl_wait();
   if (warp == 0 && lane == 0) {
+    if (f.proj) {
+      // Sx comes from the projection phase of this launch: all of its tiles
+      if (!wait_signal(f.sync + f.gw_y0, static_cast<unsigned>(f.B * f.nct)))
+        raise_fault(FAULT_WAIT_SIGNAL);
+      fence_proxy_async_global();
+    }
     int issued = 0;
     for (int i = 0; i < nk; ++i) {
       const int s = i % NS;
@@ -173,19 +274,23 @@ __device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CU
 }
 
 template <int BN>
-__global__ void __launch_bounds__(320, 1)
+// two CTAs per SM: at most 102 registers a thread (with more, as an
+// instrumented build once had, the SM held one CTA and the grid ran in two waves)
+__global__ void __launch_bounds__(320, 2)
     k_gradx_fused(const __grid_constant__ CUtensorMap tmap_sq,
                   const __grid_constant__ CUtensorMap tmap_w,
                   const __grid_constant__ CUtensorMap tmap_q,
                   const __grid_constant__ CUtensorMap tmap_out,
                   const __grid_constant__ CUtensorMap tmap_sx,
-                  const __grid_constant__ CUtensorMap tmap_xh, FusedArgs f) {
+                  const __grid_constant__ CUtensorMap tmap_xh,
+                  const __grid_constant__ CUtensorMap tmap_gy,
+                  const __grid_constant__ CUtensorMap tmap_pq, FusedArgs f) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int KR = f.KR;
   const int NS = f.stages;
-  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt, f.gw_mt > 0);
+  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f));
   uint8_t* ring = smem + lay.ring;
   uint8_t* stg = smem + lay.stg;
   uint8_t* sQ = smem + lay.qt;
@@ -199,19 +304,53 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t* t_empty = t_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
 
-  if (BN == 64 && static_cast<int>(blockIdx.y) >= f.gw_y0) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int crank = blockIdx.z;                  // rank in the cluster (dims 1 x 1 x cl)
+  int item_x = blockIdx.x;                       // column strip
+  int item_y = blockIdx.y;                       // sample group
+  __shared__ unsigned int s_ticket;
+  if (f.proj) {
+    // (every path below lets the next kernel launch only after its own TMEM
+    // allocation: a CTA of the next kernel holding TMEM while it waits for
+    // this grid must never be what an allocation here waits for)
+    pdl_wait();  // the counters are this launch's only once its predecessor has finished
+    if (crank == 0 && threadIdx.x == 0) {
+      const unsigned int t = atomicAdd(f.sync + f.gw_y0 + 2, 1u);
+      for (int q = 0; q < f.cl; ++q) dsmem_st_u32(dsmem_addr(&s_ticket, q), t);
+    }
+    cluster_sync();
+    const int T = static_cast<int>(s_ticket);
+    const ProjItems w = proj_items(f);
+    if (T < w.n_pc) {
+      proj_item(&tmap_gy, &tmap_pq, f, smem, lay.pbar, T * f.cl + crank);
+      proj_launch_done(f);
+      return;
+    }
+    if (T >= w.n_pc + w.n_xc) {
+      const int u = (T - w.n_pc - w.n_xc) * f.cl + crank;  // weight-gradient tile
+      if (BN == 64 && u < f.gw_mt * w.nstrips) {
+        grad_w_tile(&tmap_sx, &tmap_xh, f, smem, lay.bar, (u / w.nstrips) * BM,
+                    (u % w.nstrips) * BN);
+      } else {
+        pdl_launch_dependents();
+        __syncthreads();
+      }
+      proj_launch_done(f);
+      return;
+    }
+    item_y = (T - w.n_pc) / w.nstrips;
+    item_x = (T - w.n_pc) % w.nstrips;
+  } else if (BN == 64 && static_cast<int>(blockIdx.y) >= f.gw_y0) {
     // weight-gradient rows of the grid (clusters of their own)
     const int mt = (static_cast<int>(blockIdx.y) - f.gw_y0) * f.cl + static_cast<int>(blockIdx.z);
     if (mt < f.gw_mt) grad_w_tile(&tmap_sx, &tmap_xh, f, smem, lay.bar, mt * BM, blockIdx.x * BN);
     return;
   }
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN;
-  const int s0 = blockIdx.y * f.spt;             // first sample of the tile
+  const int n0 = item_x * BN;
+  const int s0 = item_y * f.spt;                 // first sample of the tile
   const int m0 = s0 * f.Ry;                      // first g_hat_x row of the tile
-  const int lt0 = blockIdx.z * f.lt_per;         // first token tile
-  const int crank = blockIdx.z;                  // rank in the cluster (dims 1 x 1 x cl)
+  const int lt0 = crank * f.lt_per;              // first token tile
   const int kper = (f.nk + f.cl - 1) / f.cl;     // phase-1 chunks per cluster rank
   const int kc0 = crank * kper;
   int nkc = f.nk - kc0;
@@ -287,6 +426,12 @@ __global__ void __launch_bounds__(320, 1)
       if (lane == 0) mbar_arrive(q_full);
     }
     if (lane == 0) {
+      if (f.proj) {
+        // the group's Sq rows come from the projection phase of its CTAs
+        if (!wait_signal(f.sync + item_y, static_cast<unsigned>(nsamp * f.nct)))
+          raise_fault(FAULT_WAIT_SIGNAL);
+        fence_proxy_async_global();
+      }
       int issued = 0;
       for (int i = 0; i < nkc; ++i) {
         const int s = i % NS;
@@ -430,7 +575,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   if (epi) {
     fence_proxy_async_smem();
-    named_barrier(1, 256);
+    named_barrier<1>(256);
     if (et == 0) mbar_arrive(b_ready);
   }
 
@@ -480,7 +625,7 @@ __global__ void __launch_bounds__(320, 1)
       const int t = j - s * nlt;
       uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
       if (gt == 0 && it >= 2) tma_store_wait_read<1>();
-      named_barrier(2 + grp, 128);
+      if (grp == 0) named_barrier<2>(128); else named_barrier<3>(128);
       if (!mbar_wait(&t_full[grp], it & 1)) raise_fault(FAULT_WAIT_DONE);
       tc_fence_after();
       const uint32_t taddr = tmem + BN + grp * BN + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -504,7 +649,7 @@ __global__ void __launch_bounds__(320, 1)
                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
       }
       fence_proxy_async_smem();
-      named_barrier(2 + grp, 128);
+      if (grp == 0) named_barrier<2>(128); else named_barrier<3>(128);
       if (gt == 0) {
         for (int h = 0; h < BN / 64; ++h)
           if (n0 + 64 * h < f.Cx)
@@ -517,36 +662,63 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kCols);
+  if (f.proj) proj_launch_done(f);
+}
+
+dim3 fused_grid(const FusedArgs& f) {
+  if (f.proj) {
+    const ProjItems w = proj_items(f);
+    return dim3(w.n_pc + w.n_xc + w.n_gc, 1, f.cl);
+  }
+  const int gw_rows = f.gw_mt > 0 ? (f.gw_mt + f.cl - 1) / f.cl : 0;
+  return dim3((f.Cx + f.BN - 1) / f.BN, f.gw_y0 + gw_rows, f.cl);
+}
+
+size_t fused_smem_bytes(const FusedArgs& f) {
+  size_t b = fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f))
+                 .total +
+             1024;
+  // with the projection phase at most two CTAs share an SM, so that two
+  // CTAs' TMEM (256 columns each) always fits and no allocation waits on a
+  // CTA that waits for a signal
+  if (f.proj && b < 80 * 1024) b = 80 * 1024;
+  return b;
+}
+
+template <int BN>
+cudaError_t configure_smem(size_t bytes) {
+  static std::mutex mu;
+  static size_t configured = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (bytes <= configured) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(
+      k_gradx_fused<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) configured = bytes;
+  return e;
 }
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap& ts, const CUtensorMap& tw, const CUtensorMap& tq,
                       const CUtensorMap& to, const CUtensorMap& tsx, const CUtensorMap& txh,
-                      const FusedArgs& f, cudaStream_t st) {
-  const size_t bytes = gradx_fused_smem_bytes(f);
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_gradx_fused<BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
-  const int gw_rows = f.gw_mt > 0 ? (f.gw_mt + f.cl - 1) / f.cl : 0;
-  const dim3 grid((f.Cx + BN - 1) / BN, f.gw_y0 + gw_rows, f.cl);
+                      const CUtensorMap& tgy, const CUtensorMap& tpq, const FusedArgs& f,
+                      cudaStream_t st) {
+  const size_t bytes = fused_smem_bytes(f);
+  const cudaError_t e = configure_smem<BN>(bytes);
+  if (e != cudaSuccess) return e;
+  const dim3 grid = fused_grid(f);
   return launch_ex(k_gradx_fused<BN>, grid, dim3(320), bytes, st, f.cl, pdl_enabled(), ts, tw, tq,
-                   to, tsx, txh, f);
+                   to, tsx, txh, tgy, tpq, f);
 }
+
 
 }  // namespace
 
-size_t gradx_fused_smem_bytes(const FusedArgs& f) {
-  return fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt, f.gw_mt > 0).total + 1024;
-}
+size_t gradx_fused_smem_bytes(const FusedArgs& f) { return fused_smem_bytes(f); }
 
 cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
                                const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
                                const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
+                               const CUtensorMap& tmap_gy, const CUtensorMap& tmap_pq,
                                const FusedArgs& f, cudaStream_t st) {
   if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
   if (f.a_rows < f.spt * f.Ry || f.a_rows > BM || f.a_rows % 8 != 0) return cudaErrorInvalidValue;
@@ -554,9 +726,17 @@ cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tm
   if (f.lt_per * f.cl < f.nlt) return cudaErrorInvalidValue;
   if (f.gw_y0 != (f.B + f.spt - 1) / f.spt) return cudaErrorInvalidValue;
   if (f.gw_mt > 0 && (f.BN != 64 || !f.gw || f.gw_nk < 1)) return cudaErrorInvalidValue;
+  if (f.proj && (!f.sync || f.BN != 64 || f.nct != (f.Cy + kProjBM - 1) / kProjBM ||
+                 f.pa.C != f.Cy || f.pa.B != f.B || f.pa.NT < 16 || f.pa.NT > 128 ||
+                 f.pa.NT % 16 != 0))
+    return cudaErrorInvalidValue;
   switch (f.BN) {
-    case 64: return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, f, st);
-    case 128: return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, f, st);
+    case 64:
+      return launch_bn<64>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, tmap_gy, tmap_pq,
+                           f, st);
+    case 128:
+      return launch_bn<128>(tmap_sq, tmap_w, tmap_q, tmap_out, tmap_sx, tmap_xh, tmap_gy, tmap_pq,
+                            f, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -17,7 +17,6 @@ struct ProjectArgs {
   int NT;            // MMA N: Rx + Ry rounded up to a multiple of 16
   int nk;            // ceil(L / 64)
   int pq_tma;        // 1: PQ tiles arrive by TMA; 0: threads fill all of PQ up front
-  int splits;        // token-axis split = cluster size along grid z (1 or 2)
   const void* pq;    // [Rx+Ry, L]
   void* out0;        // [B*Rx, C]
   void* out1;        // [B*Ry, C] or null
@@ -98,13 +97,25 @@ struct FusedArgs {
   int gw_nk;         // ceil(B * Rx / 64)
   int gw_acc;        // 1: g_w += result
   float* gw;         // [Cy, Cx] fp32
+  // projection of g_y in the same launch (proj = 1): the input-gradient CTAs
+  // of a sample group first compute the group's (sample, 128-column) tiles of
+  // Sx and Sq, each tile followed by a signal; phase 1 of the group waits for
+  // its own tiles, the weight-gradient CTAs for all of them
+  int proj;
+  int nct;           // ceil(Cy / 128): projection tiles per sample
+  ProjectArgs pa;    // the projection of g_y [B, L, Cy] by [P; Q]
+  unsigned int* sync;  // [gw_y0] per-group tile counts, total, finished CTAs,
+                       // next ticket; zero before the launch, zeroed again by
+                       // its last CTA
 };
 
 size_t gradx_fused_smem_bytes(const FusedArgs& f);
 cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tmap_w,
                                const CUtensorMap& tmap_q, const CUtensorMap& tmap_out,
                                const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
+                               const CUtensorMap& tmap_gy, const CUtensorMap& tmap_pq,
                                const FusedArgs& f, cudaStream_t st);
+
 
 // ---------------------------------------------------------------------------
 // autocorrelation accumulation: Cout[i, j] += sum_b sum_c t[b,i,c] t[b,j,c]

@@ -33,6 +33,7 @@ enum : unsigned int {
   FAULT_WAIT_EMPTY = 1u << 1,  // producer gave up waiting for a free stage
   FAULT_WAIT_DONE = 1u << 2,   // epilogue gave up waiting for the accumulator
   FAULT_SOLVER = 1u << 3,
+  FAULT_WAIT_SIGNAL = 1u << 4,  // a CTA gave up waiting for other CTAs' signal
 };
 
 __device__ __forceinline__ void raise_fault(unsigned int bit) { atomicOr(&g_device_fault, bit); }
@@ -90,6 +91,39 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
     if (((++n) & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// signals between the CTAs of one launch: counters in global memory, added to
+// with release semantics after the producer's stores and read with acquire
+// semantics before the consumer's loads (all CTAs of such a launch are
+// resident together, so a wait ends unless a kernel fault stopped a producer)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void signal_add(unsigned int* counter, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(counter), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int load_acquire(const unsigned int* counter) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  return v;
+}
+
+// generic-proxy global writes seen so far -> this thread's later async-proxy
+// (TMA) accesses
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *counter >= target; gives up after kWaitLimitNs and returns false.
+__device__ __forceinline__ bool wait_signal(const unsigned int* counter, unsigned int target) {
+  if (load_acquire(counter) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (load_acquire(counter) < target) {
+    __nanosleep(32);
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   }
   return true;
 }
@@ -165,8 +199,13 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // named barrier among `count` threads (ids 1..15; 0 is __syncthreads)
-__device__ __forceinline__ void named_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+// The barrier id is an immediate: ptxas then reserves ids 0..ID only.  (With
+// the id in a register it reserves all 16 hardware barriers of the CTA, which
+// limits the kernel to one CTA per SM.)
+template <int ID>
+__device__ __forceinline__ void named_barrier(int count) {
+  static_assert(ID >= 1 && ID < 16, "named barrier ids are 1..15 (0 is __syncthreads)");
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -198,6 +237,10 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
 __device__ __forceinline__ void dsmem_st_u2(uint32_t addr, uint2 v) {
   asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y)
                : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {

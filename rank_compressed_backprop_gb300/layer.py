@@ -41,6 +41,7 @@ class InstantLinear:
         self.gx = torch.empty(B, L, self.Cx, dtype=self.dtype, device=dev)
         nbytes = api.grad_x_workspace_bytes(B, L, self.Cx, self.Cy, Ry, self.dtype)
         self.ws_gx = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        self.ws_bw = api.backward_workspace(B, L, self.Cx, self.Cy, Ry, self.dtype, dev)
         self.ws_cal = torch.empty(api.calib_batch_workspace_bytes(L, 2), dtype=torch.uint8,
                                   device=dev)
         self.last_calibration = None
@@ -66,9 +67,7 @@ class InstantLinear:
         xhat = self.xhat if xhat is None else xhat
         gw = self.gw if gw is None else gw
         gx = self.gx if gx is None else gx
-        B = g_y.shape[0]
-        api.project_grad(g_y, self.PQ, self.Sx, self.Sq, self.Rx, self.Ry)
-        api.grad_w_x(self.Sx, xhat, gw, self.Sq, self.w, self.Q, gx, self.ws_gx, B,
+        api.backward(g_y, self.PQ, xhat, self.w, self.Sx, self.Sq, gw, gx, self.ws_bw, self.Rx,
                      accumulate=accumulate)
         return gw, gx
 

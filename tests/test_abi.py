@@ -148,3 +148,20 @@ def test_batch_solve_validation_without_gpu(L):
     assert [arr[i].status for i in range(2)] == [2, 2]
     arr[1].prm.r_override = 8
     assert L.instant_calib_solve_batch(arr, 2, 64, 7, fake, need, None) == 3   # dtype
+
+
+def test_backward_validation_without_gpu(L):
+    fake = ctypes.c_void_p(0x1000)
+    need = L.instant_backward_workspace_bytes(32, 512, 768, 768, 8, 1)
+    assert need >= 256 + L.instant_grad_x_workspace_bytes(32, 512, 768, 768, 8, 1)
+    args = lambda B=32, Lr=512, Cx=768, Cy=768, Rx=8, Ry=8, dt=1, ws_bytes=need, ws=fake: (  # noqa: E731
+        fake, fake, fake, fake, fake, fake, fake, 0, fake, ws, ws_bytes, B, Lr, Cx, Cy, Rx, Ry, dt,
+        None)
+    assert L.instant_backward(*args(dt=7)) == 3
+    assert L.instant_backward(*args(B=0)) == 2
+    assert L.instant_backward(*args(Lr=0)) == 2
+    assert L.instant_backward(*args(Rx=70, Ry=64)) == 2
+    assert L.instant_backward(*args(Ry=65)) == 2
+    assert L.instant_backward(*args(ws_bytes=need - 1)) == 5
+    assert L.instant_backward(*args(ws=ctypes.c_void_p(0x1008))) == 4
+    assert L.instant_backward(*args(Cx=764)) == 4            # Cx % 8 != 0 for bf16
