@@ -776,15 +776,20 @@ instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, i
   s.Cout = C;
   if (dt == INSTANT_F32) {
     s.splits = 1;
-    s.b_per_split = B;
+    s.it_per_split = B * s.nkc;
     return from_cuda(launch_syrk_f32(s, static_cast<const float*>(t), st));
   }
   if (!aligned16(t) || !aligned16(C) || Cdim % 8 != 0) return INSTANT_ERR_ALIGN;
-  int splits = cdiv(kTargetCtas, s.ntiles);
-  if (splits > B) splits = B;
-  if (splits < 1) splits = 1;
-  s.b_per_split = cdiv(B, splits);
-  s.splits = cdiv(B, s.b_per_split);
+  // two CTAs per SM over all tiles, each with at least 4 channel chunks, and
+  // at most 64 CTAs adding into one tile (measured on GB300: BERT-base batch
+  // 19.5 -> 16.8 us against whole-sample splits; more splits than 64 per tile
+  // lose to the atomic adds, e.g. 256 ViT samples of 197 tokens)
+  const int iters = B * s.nkc;
+  int splits = std::max(1, kTargetCtas / s.ntiles);
+  splits = std::min(splits, 64);
+  splits = std::min(splits, std::max(1, iters / 4));
+  s.it_per_split = cdiv(iters, splits);
+  s.splits = cdiv(iters, s.it_per_split);
   CUtensorMap mt;
   const uint64_t d3[3] = {static_cast<uint64_t>(Cdim), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
   const uint64_t s3[2] = {static_cast<uint64_t>(Cdim) * 2, static_cast<uint64_t>(L) * Cdim * 2};

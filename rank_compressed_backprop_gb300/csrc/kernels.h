@@ -124,8 +124,8 @@ struct SyrkArgs {
   int B, L, C;
   int nblk;          // ceil(L / 128)
   int ntiles;        // nblk * (nblk + 1) / 2 upper-triangle tiles
-  int splits;        // sample splits (grid y)
-  int b_per_split;
+  int splits;        // splits of the (sample, channel chunk) iterations (grid y)
+  int it_per_split;  // consecutive iterations per split (a split may cross samples)
   int nkc;           // ceil(C / 64)
   float* Cout;       // [L, L]
 };

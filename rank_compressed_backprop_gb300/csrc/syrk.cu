@@ -5,9 +5,11 @@
 // storing the batch.  This is the one truly tensor-bound step (2L flops per
 // byte of t), so it is a tcgen05 GEMM over the upper-triangle 128x128 tiles of
 // C: both operands are K-major row blocks of the same sample (K = channels),
-// streamed by TMA; the sum over samples continues the K loop.  Samples are
-// split across grid y for parallelism and every CTA adds its tile (and, off
-// the diagonal, the mirrored tile) into C with fp32 atomics.
+// streamed by TMA; the sum over samples continues the K loop.  The (sample,
+// 64-channel chunk) iterations are split into equal ranges across grid y (a
+// range may cross samples), sized so that two CTAs per SM cover the GPU, and
+// every CTA adds its tile (and, off the diagonal, the mirrored tile) into C
+// with fp32 atomics.
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -49,10 +51,10 @@ __global__ void __launch_bounds__(128, 1)
   const bool diag = bi == bj;
   const int i0 = bi * BT;
   const int j0 = bj * BT;
-  const int b_begin = blockIdx.y * a.b_per_split;
-  int b_end = b_begin + a.b_per_split;
-  if (b_end > a.B) b_end = a.B;
-  const int niter = b_end > b_begin ? (b_end - b_begin) * a.nkc : 0;
+  const int it_begin = blockIdx.y * a.it_per_split;
+  int it_end = it_begin + a.it_per_split;
+  if (it_end > a.B * a.nkc) it_end = a.B * a.nkc;
+  const int niter = it_end > it_begin ? it_end - it_begin : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSyrkStages; ++s) {
@@ -83,8 +85,8 @@ __global__ void __launch_bounds__(128, 1)
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
-      const int b = b_begin + it / a.nkc;
-      const int c0 = (it % a.nkc) * BK;
+      const int b = (it_begin + it) / a.nkc;
+      const int c0 = ((it_begin + it) % a.nkc) * BK;
       uint8_t* dst = smem + s * STAGE;
       mbar_arrive_expect_tx(&full[s], bytes);
       tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
