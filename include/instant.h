@@ -231,6 +231,26 @@ instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, i
                                         instant_dtype dt, void* stream);
 
 /*
+ * Several statistics of one token length L accumulated in one call (关键设计
+ * 1: a layer accumulates C_X from its activations and C_G from its output
+ * gradients at the same step): for each item, C += sum_b t_b t_b^T exactly
+ * as instant_calib_accumulate does (the fp32 sums may add in another order).
+ * Up to four statistics share one launch.
+ *   items  HOST array of `count` items: t [B, L, Cdim] (device, dtype dt),
+ *          C [L, L] fp32 (device, accumulated in place), B, Cdim
+ * Limits: L <= 8192; the items' C must not overlap.
+ */
+typedef struct {
+  const void* t;
+  float* C;
+  int B;
+  int Cdim;
+} instant_accumulate_item;
+
+instant_status instant_calib_accumulate_batch(const instant_accumulate_item* items, int count,
+                                              int L, instant_dtype dt, void* stream);
+
+/*
  * Projector from an accumulated statistic (关键设计 1 and 2):
  *   C/n = U Sigma U^T (symmetric PSD, so the SVD is the eigendecomposition);
  *   E = ||C/n||_F^2 (fp64, from C directly);

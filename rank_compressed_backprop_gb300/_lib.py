@@ -44,6 +44,15 @@ class CalibParams(ctypes.Structure):
     ]
 
 
+class AccumulateItem(ctypes.Structure):
+    _fields_ = [
+        ("t", ctypes.c_void_p),
+        ("C", ctypes.c_void_p),
+        ("B", ctypes.c_int),
+        ("Cdim", ctypes.c_int),
+    ]
+
+
 class CalibProblem(ctypes.Structure):
     _fields_ = [
         ("C", ctypes.c_void_p),
@@ -86,6 +95,7 @@ _PROTOS = {
     "instant_expand": (_i, [_vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_calib_accumulate": (_i, [_vp, _vp, _i, _i, _i, _i, _vp]),
+    "instant_calib_accumulate_batch": (_i, [ctypes.POINTER(AccumulateItem), _i, _i, _i, _vp]),
     "instant_calib_solve": (_i, [_vp, ctypes.c_longlong, _i, ctypes.POINTER(CalibParams), _vp, _i,
                                  _i, ctypes.POINTER(_i), ctypes.POINTER(_i),
                                  ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_double),

@@ -12,8 +12,8 @@ import dataclasses
 
 import torch
 
-from ._lib import (GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, CalibParams,
-                   CalibProblem, check, lib)
+from ._lib import (GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, AccumulateItem,
+                   CalibParams, CalibProblem, check, lib)
 
 __all__ = [
     "compress_act",
@@ -30,6 +30,7 @@ __all__ = [
     "grad_x_static",
     "launch_count",
     "calib_accumulate",
+    "calib_accumulate_batch",
     "calib_solve",
     "calib_solve_batch",
     "calib_workspace_bytes",
@@ -255,6 +256,25 @@ def calib_accumulate(t: torch.Tensor, C: torch.Tensor, stream=None) -> torch.Ten
     check(lib().instant_calib_accumulate(_dev(t, "t"), _dev(C, "C"), B, L, Cd, dtype_code(t.dtype),
                                          _stream(stream)), "instant_calib_accumulate")
     return C
+
+
+def calib_accumulate_batch(pairs, stream=None) -> None:
+    """``C += sum_b t[b] t[b]^T`` for every ``(t, C)`` in ``pairs`` (one token
+    length L; t ``[B, L, Cdim]`` of one dtype, C ``[L, L]`` fp32), up to four
+    statistics per launch."""
+    pairs = list(pairs)
+    if not pairs:
+        raise ValueError("calib_accumulate_batch: nothing to accumulate")
+    L = pairs[0][0].shape[1]
+    dt = pairs[0][0].dtype
+    arr = (AccumulateItem * len(pairs))()
+    for i, (t, C) in enumerate(pairs):
+        B, Lt, Cd = t.shape
+        if Lt != L or t.dtype != dt or C.shape != (L, L) or C.dtype != torch.float32:
+            raise ValueError("calib_accumulate_batch: inconsistent shapes or dtypes")
+        arr[i] = AccumulateItem(_dev(t, "t"), _dev(C, "C"), B, Cd)
+    check(lib().instant_calib_accumulate_batch(arr, len(pairs), L, dtype_code(dt), _stream(stream)),
+          "instant_calib_accumulate_batch")
 
 
 def calib_workspace_bytes(L: int, r_cap: int) -> int:

@@ -762,40 +762,84 @@ instant_status instant_backward(const void* gy, const void* PQ, const void* xhat
 
 instant_status instant_calib_accumulate(const void* t, float* C, int B, int L, int Cdim,
                                         instant_dtype dt, void* stream) {
+  const instant_accumulate_item item{t, C, B, Cdim};
+  return instant_calib_accumulate_batch(&item, 1, L, dt, stream);
+}
+
+instant_status instant_calib_accumulate_batch(const instant_accumulate_item* items, int count, int L,
+                                              instant_dtype dt, void* stream) {
   if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
-  if (!t || !C) return INSTANT_ERR_ARG;
-  if (B < 1 || L < 1 || L > 8192 || Cdim < 1) return INSTANT_ERR_SHAPE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  SyrkArgs s;
-  s.B = B;
-  s.L = L;
-  s.C = Cdim;
-  s.nblk = cdiv(L, 128);
-  s.ntiles = s.nblk * (s.nblk + 1) / 2;
-  s.nkc = cdiv(Cdim, 64);
-  s.Cout = C;
-  if (dt == INSTANT_F32) {
-    s.splits = 1;
-    s.it_per_split = B * s.nkc;
-    return from_cuda(launch_syrk_f32(s, static_cast<const float*>(t), st));
+  if (!items || count < 1) return INSTANT_ERR_ARG;
+  if (L < 1 || L > 8192) return INSTANT_ERR_SHAPE;
+  for (int i = 0; i < count; ++i) {
+    const instant_accumulate_item& it = items[i];
+    if (!it.t || !it.C) return INSTANT_ERR_ARG;
+    if (it.B < 1 || it.Cdim < 1) return INSTANT_ERR_SHAPE;
+    if (dt == INSTANT_BF16 && (!aligned16(it.t) || !aligned16(it.C) || it.Cdim % 8 != 0))
+      return INSTANT_ERR_ALIGN;
   }
-  if (!aligned16(t) || !aligned16(C) || Cdim % 8 != 0) return INSTANT_ERR_ALIGN;
-  // two CTAs per SM over all tiles, each with at least 4 channel chunks, and
-  // at most 64 CTAs adding into one tile (measured on GB300: BERT-base batch
-  // 19.5 -> 16.8 us against whole-sample splits; more splits than 64 per tile
-  // lose to the atomic adds, e.g. 256 ViT samples of 197 tokens)
-  const int iters = B * s.nkc;
-  int splits = std::max(1, kTargetCtas / s.ntiles);
-  splits = std::min(splits, 64);
-  splits = std::min(splits, std::max(1, iters / 4));
-  s.it_per_split = cdiv(iters, splits);
-  s.splits = cdiv(iters, s.it_per_split);
-  CUtensorMap mt;
-  const uint64_t d3[3] = {static_cast<uint64_t>(Cdim), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
-  const uint64_t s3[2] = {static_cast<uint64_t>(Cdim) * 2, static_cast<uint64_t>(L) * Cdim * 2};
-  const uint32_t b3[3] = {64, 128, 1};
-  if (!make_map(&mt, t, 3, d3, s3, b3)) return INSTANT_ERR_CUDA;
-  return from_cuda(launch_syrk_bf16(mt, s, st));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int nblk = cdiv(L, 128);
+  const int ntiles = nblk * (nblk + 1) / 2;
+  if (dt == INSTANT_F32) {
+    for (int i = 0; i < count; ++i) {
+      SyrkArgs s;
+      s.B = items[i].B;
+      s.L = L;
+      s.C = items[i].Cdim;
+      s.nblk = nblk;
+      s.ntiles = ntiles;
+      s.nkc = cdiv(s.C, 64);
+      s.Cout = items[i].C;
+      s.splits = 1;
+      s.it_per_split = s.B * s.nkc;
+      if (launch_syrk_f32(s, static_cast<const float*>(items[i].t), st) != cudaSuccess)
+        return INSTANT_ERR_CUDA;
+    }
+    return INSTANT_OK;
+  }
+  // groups of up to kMaxSyrkBatch statistics per launch; within a launch the
+  // (sample, channel chunk) iterations of every statistic are split evenly so
+  // that the whole grid fills two CTAs per SM, each CTA with at least 4 chunks
+  // and at most 64 CTAs adding into one tile (measured on GB300: BERT-base
+  // batch 19.5 -> 16.8 us against whole-sample splits; more splits than 64 per
+  // tile lose to the atomic adds, e.g. 256 ViT samples of 197 tokens)
+  for (int g0 = 0; g0 < count; g0 += kMaxSyrkBatch) {
+    const int n = std::min(kMaxSyrkBatch, count - g0);
+    long long total = 0;
+    for (int i = 0; i < n; ++i)
+      total += static_cast<long long>(items[g0 + i].B) * cdiv(items[g0 + i].Cdim, 64);
+    SyrkBatch b;
+    CUtensorMap maps[kMaxSyrkBatch];
+    b.count = n;
+    b.split0[0] = 0;
+    for (int i = 0; i < n; ++i) {
+      const instant_accumulate_item& it = items[g0 + i];
+      SyrkArgs& s = b.s[i];
+      s.B = it.B;
+      s.L = L;
+      s.C = it.Cdim;
+      s.nblk = nblk;
+      s.ntiles = ntiles;
+      s.nkc = cdiv(it.Cdim, 64);
+      s.Cout = it.C;
+      const int iters = s.B * s.nkc;
+      const double share = static_cast<double>(iters) / static_cast<double>(total);
+      int splits = std::max(1, static_cast<int>(kTargetCtas * share / ntiles));
+      splits = std::min(splits, 64);
+      splits = std::min(splits, std::max(1, iters / 4));
+      s.it_per_split = cdiv(iters, splits);
+      s.splits = cdiv(iters, s.it_per_split);
+      b.split0[i + 1] = b.split0[i] + s.splits;
+      const uint64_t d3[3] = {static_cast<uint64_t>(it.Cdim), static_cast<uint64_t>(L),
+                              static_cast<uint64_t>(it.B)};
+      const uint64_t s3[2] = {static_cast<uint64_t>(it.Cdim) * 2, static_cast<uint64_t>(L) * it.Cdim * 2};
+      const uint32_t b3[3] = {64, 128, 1};
+      if (!make_map(&maps[i], it.t, 3, d3, s3, b3)) return INSTANT_ERR_CUDA;
+    }
+    if (launch_syrk_bf16_batch(maps, b, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  }
+  return INSTANT_OK;
 }
 
 size_t instant_calib_workspace_bytes(int L, int r_cap) {

@@ -133,6 +133,15 @@ struct SyrkArgs {
 constexpr int kSyrkStages = 3;  // 96 KB of stages: two CTAs per SM
 size_t syrk_bf16_smem_bytes();
 cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st);
+// up to kMaxSyrkBatch statistics of one token length in one launch: problem p
+// owns grid rows [split0[p], split0[p + 1])
+constexpr int kMaxSyrkBatch = 4;
+struct SyrkBatch {
+  SyrkArgs s[kMaxSyrkBatch];
+  int split0[kMaxSyrkBatch + 1];
+  int count;
+};
+cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b, cudaStream_t st);
 cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st);
 
 // ---------------------------------------------------------------------------

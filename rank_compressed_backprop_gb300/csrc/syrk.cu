@@ -35,7 +35,15 @@ __device__ __forceinline__ void tile_coords(int t, int nblk, int& bi, int& bj) {
 }
 
 __global__ void __launch_bounds__(128, 1)
-    k_syrk_bf16(const __grid_constant__ CUtensorMap tmap_t, SyrkArgs a) {
+    k_syrk_bf16(const __grid_constant__ CUtensorMap tmap0, const __grid_constant__ CUtensorMap tmap1,
+                const __grid_constant__ CUtensorMap tmap2, const __grid_constant__ CUtensorMap tmap3,
+                const __grid_constant__ SyrkBatch batch) {
+  // the problem of this grid row
+  int p = 0;
+  while (p + 1 < batch.count && static_cast<int>(blockIdx.y) >= batch.split0[p + 1]) ++p;
+  const SyrkArgs& a = batch.s[p];
+  const CUtensorMap& tmap_t = p == 0 ? tmap0 : (p == 1 ? tmap1 : (p == 2 ? tmap2 : tmap3));
+  const int split = static_cast<int>(blockIdx.y) - batch.split0[p];
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -51,7 +59,7 @@ __global__ void __launch_bounds__(128, 1)
   const bool diag = bi == bj;
   const int i0 = bi * BT;
   const int j0 = bj * BT;
-  const int it_begin = blockIdx.y * a.it_per_split;
+  const int it_begin = split * a.it_per_split;
   int it_end = it_begin + a.it_per_split;
   if (it_end > a.B * a.nkc) it_end = a.B * a.nkc;
   const int niter = it_end > it_begin ? it_end - it_begin : 0;
@@ -177,7 +185,11 @@ __global__ void k_syrk_f32(const float* __restrict__ t, SyrkArgs a) {
 
 size_t syrk_bf16_smem_bytes() { return kSyrkStages * STAGE + 256 + 1024; }
 
-cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st) {
+cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b, cudaStream_t st) {
+  if (b.count < 1 || b.count > kMaxSyrkBatch || b.split0[0] != 0) return cudaErrorInvalidValue;
+  for (int p = 0; p < b.count; ++p)
+    if (b.s[p].L != b.s[0].L || b.split0[p + 1] != b.split0[p] + b.s[p].splits || b.s[p].splits < 1)
+      return cudaErrorInvalidValue;
   const size_t bytes = syrk_bf16_smem_bytes();
   static size_t configured_ = 0;
   if (bytes > configured_) {
@@ -186,8 +198,21 @@ cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaS
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  return launch_ex(k_syrk_bf16, dim3(s.ntiles, s.splits), dim3(128), bytes, st, 1, pdl_enabled(),
-                   tmap_t, s);
+  const CUtensorMap& m0 = tmaps[0];
+  const CUtensorMap& m1 = tmaps[b.count > 1 ? 1 : 0];
+  const CUtensorMap& m2 = tmaps[b.count > 2 ? 2 : 0];
+  const CUtensorMap& m3 = tmaps[b.count > 3 ? 3 : 0];
+  return launch_ex(k_syrk_bf16, dim3(b.s[0].ntiles, b.split0[b.count]), dim3(128), bytes, st, 1,
+                   pdl_enabled(), m0, m1, m2, m3, b);
+}
+
+cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st) {
+  SyrkBatch b;
+  b.s[0] = s;
+  b.split0[0] = 0;
+  b.split0[1] = s.splits;
+  b.count = 1;
+  return launch_syrk_bf16_batch(&tmap_t, b, st);
 }
 
 cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st) {

@@ -74,12 +74,15 @@ class InstantLinear:
     # ---- calibration --------------------------------------------------------
     def accumulate(self, x: torch.Tensor | None = None, g_y: torch.Tensor | None = None) -> None:
         """Adds the autocorrelation statistics of a batch (no batch is stored)."""
+        pairs = []
         if x is not None:
-            api.calib_accumulate(x, self.C_X)
+            pairs.append((x, self.C_X))
             self.n_x += x.shape[0]
         if g_y is not None:
-            api.calib_accumulate(g_y, self.C_G)
+            pairs.append((g_y, self.C_G))
             self.n_g += g_y.shape[0]
+        if pairs:
+            api.calib_accumulate_batch(pairs)   # both statistics in one launch
 
     def recalibrate(self, r_override: bool = True):
         """Solves both statistics into ``P`` and ``Q`` (one call) and clears them.

@@ -165,3 +165,25 @@ def test_backward_validation_without_gpu(L):
     assert L.instant_backward(*args(ws_bytes=need - 1)) == 5
     assert L.instant_backward(*args(ws=ctypes.c_void_p(0x1008))) == 4
     assert L.instant_backward(*args(Cx=764)) == 4            # Cx % 8 != 0 for bf16
+
+
+def test_accumulate_batch_validation_without_gpu(L):
+    from rank_compressed_backprop_gb300._lib import AccumulateItem
+
+    items = (AccumulateItem * 2)(AccumulateItem(0x1000, 0x2000, 4, 64),
+                                 AccumulateItem(0x3000, 0x4000, 4, 128))
+    assert L.instant_calib_accumulate_batch(None, 1, 64, 1, None) == 1
+    assert L.instant_calib_accumulate_batch(items, 0, 64, 1, None) == 1
+    assert L.instant_calib_accumulate_batch(items, 2, 64, 7, None) == 3
+    assert L.instant_calib_accumulate_batch(items, 2, 0, 1, None) == 2
+    assert L.instant_calib_accumulate_batch(items, 2, 8193, 1, None) == 2
+    items[1].B = 0
+    assert L.instant_calib_accumulate_batch(items, 2, 64, 1, None) == 2
+    items[1].B = 4
+    items[1].Cdim = 60                      # not a multiple of 8 for bf16
+    assert L.instant_calib_accumulate_batch(items, 2, 64, 1, None) == 4
+    items[1].Cdim = 128
+    items[1].t = 0x3008                     # misaligned
+    assert L.instant_calib_accumulate_batch(items, 2, 64, 1, None) == 4
+    items[1].t = None
+    assert L.instant_calib_accumulate_batch(items, 2, 64, 1, None) == 1

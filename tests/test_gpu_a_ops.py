@@ -130,6 +130,32 @@ def test_calib_accumulate(torch, dtype, B, L, C):
     assert np.array_equal(got, got.T) or rel(got, got.T) < 1e-6
 
 
+@pytest.mark.parametrize("dtype,L,dims", [
+    ("bf16", 512, [(32, 768), (32, 3072)]),                    # a layer's C_X and C_G, one launch
+    ("bf16", 300, [(3, 200), (5, 264), (2, 64), (4, 136), (1, 8)]),   # five: two launches
+    ("f32", 72, [(2, 40), (3, 48)]),
+])
+def test_calib_accumulate_batch(torch, dtype, L, dims):
+    g = rng(700 + L + len(dims))
+    ts = [stored(g.standard_normal((B, L, C)), dtype) for B, C in dims]
+    api = _api()
+    Cb = [torch.zeros(L, L, dtype=torch.float32, device="cuda") for _ in dims]
+    Cs = [torch.zeros(L, L, dtype=torch.float32, device="cuda") for _ in dims]
+    n0 = api.launch_count()
+    api.calib_accumulate_batch([(to_dev(t), C) for t, C in zip(ts, Cb)])
+    torch.cuda.synchronize()
+    if dtype == "bf16":
+        assert api.launch_count() - n0 == (len(dims) + 3) // 4
+    for t, C in zip(ts, Cs):
+        api.calib_accumulate(to_dev(t), C)
+    torch.cuda.synchronize()
+    for t, cb, cs in zip(ts, Cb, Cs):
+        ref = O.accumulate_autocorrelation(t)
+        assert rel(to_np(cb), ref) <= (1e-5 if dtype == "f32" else 1e-4)
+        # the same fp32 sums in another order: up to ~sqrt(B * Cdim) * 2^-24 apart
+        assert rel(to_np(cb), to_np(cs)) <= 5e-5
+
+
 def test_device_status_clean(torch):
     assert _api().device_status() == 0
 
