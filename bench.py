@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-iters", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-baseline-only", action="store_true",
+                    help="print the oracle's cpu_baseline object and exit (no GPU)")
     ap.add_argument("--mode", choices=["bench", "kernels", "drift"], default="bench",
                     help="kernels: after a first (cold) calibration, run one recalibration "
                          "period of the timed loop eagerly -- a warm-started calibration and "
@@ -422,6 +424,21 @@ def run_ours(args):
         calibrate(sets[i % NSETS])
     torch.cuda.synchronize()
     cal_ms = (time.perf_counter() - t0) * 1e3 / 5
+    # its parts: the batched accumulation of both statistics (one launch, the
+    # tensor-bound step), and the solve of both (one launch + a synchronisation)
+    s0 = sets[0]
+    for _ in range(3):
+        lay.accumulate(s0["x"], s0["g"])
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(20):
+        lay.accumulate(s0["x"], s0["g"])
+    b.record(stream)
+    torch.cuda.synchronize()
+    acc_us = a.elapsed_time(b) * 1e3 / 20
+    t0 = time.perf_counter()
+    lay.recalibrate()
+    solve_ms = (time.perf_counter() - t0) * 1e3
 
     peaks = measured_peaks()
     nbytes = layer_bytes(B, L, Cx, Cy, Rx, Ry)
@@ -438,9 +455,10 @@ def run_ours(args):
     e2e = run_e2e(args, lay, data, dev, xc, gc)
 
     # ---- CPU baseline (the oracle as it stands) ----
-    cpu = None
+    cpu = cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, data, args.nt)
+        cpu1 = cpu_baseline_1thread(args.nt)
 
     clocks = clk.summary()
     step_bytes = sum(nbytes[k] for k in step_kernels)
@@ -475,6 +493,14 @@ def run_ours(args):
             "step_algorithmic_bytes": step_bytes,
             "step_graph_hbm_gbs": round(step_bytes / (step_only_us * 1e-6) / 1e9, 1),
             "calibration_ms": round(cal_ms, 3),
+            "cpu_baseline_1thread": cpu1,
+            "calibration_parts": {
+                "accumulate_x_and_g_us": round(acc_us, 2),
+                # upper triangle incl. the diagonal: L(L+1) flops per channel and sample
+                "accumulate_tflops": round(B * L * (L + 1) * (Cx + Cy) / (acc_us * 1e-6) / 1e12, 1),
+                "accumulate_tensor_frac": round(B * L * (L + 1) * (Cx + Cy) / (acc_us * 1e-6) / 1e12
+                                                / peaks["bf16_tflops"], 4),
+                "solve_both_wall_ms": round(solve_ms, 3)},
             "launches_per_step": launches_per_step,
             "calibration_k": [cal0[0].k, cal0[1].k],
             "flops_vanilla_per_layer": 4 * B * L * Cx * Cy,
@@ -625,6 +651,22 @@ def cpu_baseline(wl, data, nt, budget_s: float = 15.0):
                       f"({t_cal:.2f} s) amortised over N_t={nt}; scaled to whole layers"}
 
 
+def cpu_baseline_1thread(nt: int):
+    """The same oracle sample on one host thread (BLAS and OpenMP pinned to
+    one thread in a child process, so that the parent's pools are untouched)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--nt", str(nt)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+        line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+        d = json.loads(line)
+        d["cores"] = 1
+        return d
+    except Exception as e:  # reported, not fatal: the all-core figure is the baseline
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 def run_reference(args):
     """The oracle arm: same metric, config and unit, on the host cores."""
     rank, world, _ = dist_env()
@@ -738,6 +780,10 @@ def run_drift(args):
 
 def main():
     args = parse()
+    if args.cpu_baseline_only:
+        wl, _, data = make_workload()
+        print(json.dumps(cpu_baseline(wl, data, args.nt, budget_s=8.0)))
+        return
     if args.mode == "drift":
         run_drift(args)
     elif args.impl == "reference":
