@@ -303,7 +303,8 @@ size_t instant_calib_workspace_bytes(int L, int r_cap);
  *   problems   HOST array of `count` problems (count >= 1)
  *   dt         dtype of every rows_out
  *   ws         device scratch of instant_calib_batch_workspace_bytes(L, count)
- *              bytes; problem i uses its own slice
+ *              bytes: the one-launch results of all problems side by side (one
+ *              copy to the host), then one slice per problem
  * Returns INSTANT_OK when every problem succeeded, else the first failing
  * problem's status.  Argument, shape, dtype, alignment or workspace errors of
  * any problem are reported before anything is launched, with that error in

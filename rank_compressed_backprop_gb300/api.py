@@ -33,6 +33,7 @@ __all__ = [
     "calib_accumulate_batch",
     "calib_solve",
     "calib_solve_batch",
+    "CalibBatch",
     "calib_workspace_bytes",
     "calib_batch_workspace_bytes",
     "device_status",
@@ -369,6 +370,58 @@ def calib_solve_batch(problems, *, ws: torch.Tensor | None = None, stream=None,
         check(st, "instant_calib_solve_batch")
         return res
     return res, [arr[i].status for i in range(n)]
+
+
+class CalibBatch:
+    """The same statistics solved together again and again (a layer's C_X into
+    P and C_G into Q, every N_t steps): the argument block of
+    ``instant_calib_solve_batch`` is built once; :meth:`solve` updates the
+    sample counts and the warm-start flag and passes it.  The tensors given
+    here must stay alive and in place."""
+
+    def __init__(self, problems, ws: torch.Tensor):
+        self.n = len(problems)
+        if self.n < 1:
+            raise ValueError("CalibBatch: no problems")
+        self.L = problems[0]["C"].shape[0]
+        self.dt = problems[0]["rows_out"].dtype
+        self.arr = (CalibProblem * self.n)()
+        self.eigs = []
+        for i, q in enumerate(problems):
+            C, rows = q["C"], q["rows_out"]
+            if (C.shape != (self.L, self.L) or C.dtype != torch.float32 or rows.shape[1] != self.L
+                    or rows.dtype != self.dt):
+                raise ValueError("CalibBatch: inconsistent shapes or dtypes")
+            eig = (ctypes.c_double * rows.shape[0])()
+            self.eigs.append(eig)
+            prm = CalibParams(q.get("eps", 0.95), q.get("p", 0), q.get("r_override", 0),
+                              int(bool(q.get("scale_on", True))), q.get("max_iter", 0),
+                              q.get("tol", 0.0), 0)
+            self.arr[i] = CalibProblem(_dev(C, "C"), 1, prm, _dev(rows, "rows_out"), rows.shape[0],
+                                       ctypes.cast(eig, ctypes.POINTER(ctypes.c_double)), 0, 0, 0.0,
+                                       0.0, 0)
+        need = calib_batch_workspace_bytes(self.L, self.n)
+        if ws.numel() * ws.element_size() < need:
+            raise ValueError("CalibBatch: workspace too small")
+        self.ws_ptr = _dev(ws, "ws")
+        self.ws_bytes = ws.numel() * ws.element_size()
+        self.dcode = dtype_code(self.dt)
+
+    def solve(self, n_samples, warm_start: bool = False, r_override=None, stream=None):
+        """Solves every problem (``n_samples[i]`` samples in statistic i);
+        ``r_override``: optional per-problem overrides.  Returns the list of
+        :class:`CalibResult`; raises on the first failing problem."""
+        for i in range(self.n):
+            q = self.arr[i]
+            q.n_samples = int(n_samples[i])
+            q.prm.warm_start = int(bool(warm_start))
+            if r_override is not None:
+                q.prm.r_override = int(r_override[i])
+        st = lib().instant_calib_solve_batch(self.arr, self.n, self.L, self.dcode, self.ws_ptr,
+                                             self.ws_bytes, _stream(stream))
+        check(st, "instant_calib_solve_batch")
+        return [CalibResult(self.arr[i].k, self.arr[i].R, self.arr[i].scale, self.arr[i].energy,
+                            list(self.eigs[i])) for i in range(self.n)]
 
 
 def reconstruction_error(t: torch.Tensor, Q: torch.Tensor, S: torch.Tensor, ws: torch.Tensor,

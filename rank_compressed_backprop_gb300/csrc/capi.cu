@@ -848,9 +848,15 @@ size_t instant_calib_workspace_bytes(int L, int r_cap) {
   return solver_workspace_bytes(L);
 }
 
+// batch workspace: the one-launch results of all problems side by side (one
+// copy to the host), then one solver workspace per problem
+size_t batch_results_bytes(int count) {
+  return (static_cast<size_t>(count) * sizeof(SolverResult) + 255) & ~static_cast<size_t>(255);
+}
+
 size_t instant_calib_batch_workspace_bytes(int L, int count) {
   if (L < 1 || count < 1) return 0;
-  return static_cast<size_t>(count) * solve_ws_stride(L);
+  return batch_results_bytes(count) + static_cast<size_t>(count) * solve_ws_stride(L);
 }
 
 instant_status instant_calib_solve(const float* C, long long n_samples, int L,
@@ -889,14 +895,16 @@ instant_status instant_calib_solve_batch(instant_calib_problem* problems, int co
   if (!problems || count < 1) return INSTANT_ERR_ARG;
   if (L < 1 || L > 8192) return INSTANT_ERR_SHAPE;
   const size_t stride = solve_ws_stride(L);
+  const size_t res_bytes = batch_results_bytes(count);
   instant_status v = INSTANT_OK;
-  if (!ws || ws_bytes < static_cast<size_t>(count) * stride) v = INSTANT_ERR_WORKSPACE;
+  if (!ws || ws_bytes < res_bytes + static_cast<size_t>(count) * stride) v = INSTANT_ERR_WORKSPACE;
   std::vector<SolveJob> jobs(count);
   for (int i = 0; i < count && v == INSTANT_OK; ++i) {
     const instant_calib_problem& q = problems[i];
     v = solve_prepare(q.C, q.n_samples, L, &q.prm, q.rows_out, q.r_cap, dt,
-                      static_cast<uint8_t*>(ws) + i * stride, stride, &jobs[i]);
+                      static_cast<uint8_t*>(ws) + res_bytes + i * stride, stride, &jobs[i]);
   }
+  SolverResult* res_dev = static_cast<SolverResult*>(ws);
   if (v != INSTANT_OK) {
     for (int i = 0; i < count; ++i) problems[i].status = v;
     return v;
@@ -914,20 +922,21 @@ instant_status instant_calib_solve_batch(instant_calib_problem* problems, int co
       const bool take = i < count && solve_uses_cluster(jobs[i]) && jobs[i].m_block == m;
       if (take) {
         batch.s[n] = cluster_args(jobs[i]);
+        batch.s[n].res = res_dev + i;  // results side by side
         idx[n++] = i;
       }
       if (n == kMaxSolveBatch || (i == count && n > 0)) {
         if (launch_cluster_solve_batch(batch, n, st) != cudaSuccess) return INSTANT_ERR_CUDA;
-        for (int u = 0; u < n; ++u) {
-          if (cudaMemcpyAsync(&res[idx[u]], jobs[idx[u]].w.res, sizeof(SolverResult),
-                              cudaMemcpyDeviceToHost, st) != cudaSuccess)
-            return INSTANT_ERR_CUDA;
-          launched[idx[u]] = 1;
-        }
+        for (int u = 0; u < n; ++u) launched[idx[u]] = 1;
         n = 0;
       }
     }
   }
+  bool any = false;
+  for (int i = 0; i < count; ++i) any = any || launched[i];
+  if (any && cudaMemcpyAsync(res.data(), res_dev, sizeof(SolverResult) * count,
+                             cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return INSTANT_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return INSTANT_ERR_CUDA;
   instant_status first = INSTANT_OK;
   for (int i = 0; i < count; ++i) {

@@ -45,6 +45,7 @@ class InstantLinear:
         self.ws_cal = torch.empty(api.calib_batch_workspace_bytes(L, 2), dtype=torch.uint8,
                                   device=dev)
         self.last_calibration = None
+        self._cal = None   # the solve's argument block, built on first use
 
     # views of the stacked projector
     @property
@@ -92,13 +93,13 @@ class InstantLinear:
         if self.n_x == 0 or self.n_g == 0:
             raise RuntimeError("recalibrate: no statistics accumulated")
         warm = self.last_calibration is not None
-        common = dict(eps=self.eps, p=self.p, scale_on=self.scale_on, warm_start=warm)
-        rx, rg = api.calib_solve_batch(
-            [dict(C=self.C_X, n_samples=self.n_x, rows_out=self.P,
-                  r_override=self.Rx if r_override else 0, **common),
-             dict(C=self.C_G, n_samples=self.n_g, rows_out=self.Q,
-                  r_override=self.Ry if r_override else 0, **common)],
-            ws=self.ws_cal)
+        if self._cal is None:
+            common = dict(eps=self.eps, p=self.p, scale_on=self.scale_on)
+            self._cal = api.CalibBatch([dict(C=self.C_X, rows_out=self.P, **common),
+                                        dict(C=self.C_G, rows_out=self.Q, **common)], self.ws_cal)
+        rx, rg = self._cal.solve(
+            (self.n_x, self.n_g), warm_start=warm,
+            r_override=(self.Rx if r_override else 0, self.Ry if r_override else 0))
         self.C_X.zero_()
         self.C_G.zero_()
         self.n_x = self.n_g = 0
