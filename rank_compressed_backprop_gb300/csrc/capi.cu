@@ -105,6 +105,13 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   a.pq = pq;
   a.out0 = out0;
   a.out1 = out1;
+  // L2 prefetch: the whole tile while the grid's prefetches stay within a
+  // quarter of L2 (all of a BERT-base batch), else the ring's worth
+  {
+    const long long ctas = static_cast<long long>(B) * cdiv(C, 128);
+    const long long budget = (32ll << 20) / std::max(1ll, ctas) / (128 * 64 * 2);
+    a.pf_chunks = static_cast<int>(std::min<long long>(a.nk, std::max<long long>(kProjectStages, budget)));
+  }
   if (dt == INSTANT_F32) {
     a.pq_tma = 0;
     return from_cuda(launch_project_f32(a, static_cast<const float*>(t), st));
@@ -287,6 +294,7 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
     a.out0 = pp->Sx;
     a.out1 = const_cast<void*>(Sq);
     a.pq_tma = (L % 8 == 0 && aligned16(pp->PQ)) ? 1 : 0;
+    a.pf_chunks = 0;  // its tiles start after the wait
     if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) {
       if (no_room) *no_room = true;
       return INSTANT_ERR_SHAPE;

@@ -381,6 +381,10 @@ __global__ void __launch_bounds__(320, 2)
     prefetch_tmap(&tmap_w);
     if (f.q_tma) prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_out);
+    // this CTA's K-slice of the w strip into L2 while the predecessor finishes
+    for (int i = 0; i < nkc; ++i)
+      for (int h = 0; h < BN / 64; ++h)
+        if (n0 + 64 * h < f.Cx) tma_prefetch_l2_2d(&tmap_w, n0 + 64 * h, (kc0 + i) * BK);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kCols);

@@ -17,6 +17,7 @@ struct ProjectArgs {
   int NT;            // MMA N: Rx + Ry rounded up to a multiple of 16
   int nk;            // ceil(L / 64)
   int pq_tma;        // 1: PQ tiles arrive by TMA; 0: threads fill all of PQ up front
+  int pf_chunks;     // leading 64-token chunks of its tile a CTA prefetches into L2
   const void* pq;    // [Rx+Ry, L]
   void* out0;        // [B*Rx, C]
   void* out1;        // [B*Ry, C] or null

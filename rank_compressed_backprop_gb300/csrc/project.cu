@@ -54,6 +54,8 @@ __global__ void __launch_bounds__(128, 1)
     tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
+  // the input tile streams into L2 while the predecessor finishes
+  if (threadIdx.x == 0) proj_prefetch(&tmap_t, a, blockIdx.y, blockIdx.x * kProjBM);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

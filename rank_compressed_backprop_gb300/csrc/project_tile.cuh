@@ -101,6 +101,18 @@ __device__ __forceinline__ void proj_fill_pq(const ProjectArgs& a, const ProjPip
   fence_proxy_async_smem();
 }
 
+// The leading a.pf_chunks chunks of the t tile of (sample b, columns c0 ..)
+// into L2, by one thread, before the wait for the predecessor (the CTA is
+// resident early under programmatic dependent launch, and its first loads
+// then hit L2).
+__device__ __forceinline__ void proj_prefetch(const CUtensorMap* tmap_t, const ProjectArgs& a, int b,
+                                              int c0) {
+  for (int i = 0; i < a.pf_chunks && i < a.nk; ++i) {
+    tma_prefetch_l2_3d(tmap_t, c0, i * kProjBK, b);
+    if (c0 + 64 < a.C) tma_prefetch_l2_3d(tmap_t, c0 + 64, i * kProjBK, b);
+  }
+}
+
 // One tile (sample b, columns c0 .. c0+127), run by threads 0..127 (the other
 // threads of the CTA must not touch the ring meanwhile).  On return every
 // store of the tile has been issued by its thread and the accumulator is free
