@@ -14,8 +14,9 @@
 // mbarrier ring; PQ is the K-major B operand.  The fp32 accumulator lives in
 // TMEM and the epilogue writes both planes as bf16 (the tile itself is in
 // project_tile.cuh).  One CTA per (128-column tile, sample) over the whole
-// token axis; 72 KB of shared memory lets three CTAs share an SM so that the
-// HBM stream stays busy while other CTAs drain.  (A token split over a 2-CTA
+// token axis; a 4-stage ring (73 KB of shared memory) lets three CTAs share
+// an SM.  Before waiting for its predecessor, each CTA prefetches its tile
+// into L2, so the ring mostly refills from L2.  (A token split over a 2-CTA
 // cluster with a DSMEM reduction measured slower at every batch from 2 to 64
 // samples of a BERT-base block: its two cluster barriers cost more than the
 // balance it bought.)
@@ -49,13 +50,15 @@ __global__ void __launch_bounds__(128, 1)
     fence_barrier_init();
     prefetch_tmap(&tmap_t);
     if (a.pq_tma) prefetch_tmap(&tmap_pq);
+    // the input tile streams into L2 while the predecessor finishes (issued
+    // before the TMEM allocation, which may wait for TMEM the predecessor's
+    // CTAs on this SM still hold)
+    proj_prefetch(&tmap_t, a, blockIdx.y, blockIdx.x * kProjBM);
   }
   if (threadIdx.x < 32) {
     tmem_alloc(tmem_slot, tmem_cols);
     tmem_relinquish();
   }
-  // the input tile streams into L2 while the predecessor finishes
-  if (threadIdx.x == 0) proj_prefetch(&tmap_t, a, blockIdx.y, blockIdx.x * kProjBM);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
