@@ -22,6 +22,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -185,8 +186,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/instant_clocks_{os.getpid()}.csv"
+        # raw samples: $INSTANT_BENCH_CLOCKS_DIR if set (to keep them), else a temp file
+        d = os.environ.get("INSTANT_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"instant_clocks_rank{index}_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
