@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 
 METRIC = "low-rank linear-backward layers/s and achieved HBM GB/s (% of roofline) on 1 GB300"
 UNIT = "layers/s"
-CONFIG = 2
+WORKLOAD = "bert_base_block"
 NSETS = 8
 
 
@@ -237,7 +237,7 @@ class ClockSampler:
 def make_workload():
     import workloads as W
 
-    wl = W.workload(CONFIG)
+    wl = W.workload(WORKLOAD)
     li = W.LayerInputs(wl)
     B = wl.B
     return wl, li, {"x": li.x(), "g": li.g_y(), "w": li.w(),
@@ -730,7 +730,7 @@ def run_drift(args):
     from rank_compressed_backprop_gb300 import api
     from rank_compressed_backprop_gb300.drift import drift_errors
 
-    wl = W.workload(4)
+    wl = W.workload("vit_mlp_pair_49")
     li = W.LayerInputs(wl)
     dev = torch.device("cuda", torch.cuda.current_device())
     steps = wl.steps

@@ -84,36 +84,36 @@ def _run_layer(torch, wl, layer, calib_batches):
     return out, errs
 
 
-def test_config1_fp32_single_linear(torch):
-    wl = W.workload(1)
+def test_fp32_linear_64(torch):
+    wl = W.workload("fp32_linear_64")
     out, errs = _run_layer(torch, wl, 0, lambda li: [(li.calib_x(0, 8), li.calib_g(0, 8))])
-    # planted 2^-i spectrum: k = 2 and k + p = 4 = the configured rank
+    # planted 2^-i spectrum: k = 2 and k + p = 4 = the workload's rank
     assert out["P"][0].k == 2 and out["Q"][0].k == 2
 
 
-def test_config2_bert_block(torch):
-    wl = W.workload(2)
+def test_bert_base_block(torch):
+    wl = W.workload("bert_base_block")
     _run_layer(torch, wl, 0, lambda li: [(li.calib_x(j, 32), li.calib_g(j, 32)) for j in range(2)])
 
 
-def test_config4_vit_mlp_pair(torch):
-    wl = W.workload(4)
+def test_vit_mlp_pair_49(torch):
+    wl = W.workload("vit_mlp_pair_49")
     for layer in (0, 1):
         _run_layer(torch, wl, layer, lambda li: [(li.x(), li.g_y())])
 
 
-def test_config3_bert_ffn_pair(torch):
+def test_bert_ffn_pair(torch):
     # rank 16: 32-column solver blocks; layer 0 (Cy = 3072) takes the cluster-split
     # single-kernel input gradient, layer 1 (Cy = 768) the short one
-    wl = W.workload(3)
+    wl = W.workload("bert_ffn_pair")
     for layer in (0, 1):
         _run_layer(torch, wl, layer, lambda li: [(li.calib_x(j, 32), li.calib_g(j, 32))
                                                  for j in range(2)])
 
 
-def test_config5_long_sequence_wide_linear(torch):
+def test_long_seq_4096_11008(torch):
     # L = 2048 (multi-launch solver), Cy = 11008 (g_hat_x GEMM + expansion).  The
-    # statistic is the step's own 4-sample batch: the configured 64 samples would
+    # statistic is the step's own 4-sample batch: the workload's 64 calibration samples would
     # cost the float64 oracle about 2 TFLOP.
-    wl = W.workload(5)
+    wl = W.workload("long_seq_4096_11008")
     _run_layer(torch, wl, 0, lambda li: [(li.x(), li.g_y())])

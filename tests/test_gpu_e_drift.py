@@ -41,7 +41,7 @@ def test_reconstruction_error_kernel(torch, dtype, B, L, C, R):
 def test_drift_loop_matches_the_oracle(torch, p, n_t):
     from rank_compressed_backprop_gb300.drift import drift_errors
 
-    wl = W.workload(4)
+    wl = W.workload("vit_mlp_pair_49")
     li = W.LayerInputs(wl)          # first layer: g_y [256, 49, 1792], planted rank-6 spectrum
     steps = 4
     host = [li.g_y(t) for t in range(steps)]

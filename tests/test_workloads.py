@@ -22,7 +22,7 @@ def test_bf16_rounding_matches_torch_rne():
 
 
 def test_generators_are_deterministic_and_shaped():
-    wl = W.workload(1)
+    wl = W.workload("fp32_linear_64")
     a = W.LayerInputs(wl)
     b = W.LayerInputs(wl)
     assert np.array_equal(a.x(), b.x())
@@ -35,7 +35,7 @@ def test_generators_are_deterministic_and_shaped():
 def test_planted_spectrum_shape():
     # rank-6 pow2 spectrum plus 1e-3 noise; a 64x64 noise matrix has its top
     # singular value near 1e-3 * (8 + 8) = 0.016, comparable to sigma_6 = 2^-6
-    wl = W.workload(1)
+    wl = W.workload("fp32_linear_64")
     li = W.LayerInputs(wl)
     x = li.calib_x(0, 8).astype(np.float64)
     s = np.linalg.svd(x[0], compute_uv=False)

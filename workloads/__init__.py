@@ -8,7 +8,7 @@ any code of the method.
 """
 
 from .gen import (  # noqa: F401
-    CONFIGS,
+    WORKLOADS,
     LayerInputs,
     Workload,
     bf16_bits_to_f32,

@@ -19,7 +19,8 @@ Recipe (all readings of the workload descriptions):
 * bf16 tensors are rounded once, round-to-nearest-even, from the fp32 value;
   both the oracle and the CUDA path consume the same 16-bit patterns.
 
-Seeds: ``0xC0FFEE + 1000 * config + 500 * layer + tensor_id`` with tensor ids
+Seeds: ``0xC0FFEE + 1000 * seed_id + 500 * layer + tensor_id`` (each workload
+has its own ``seed_id``) with tensor ids
 x=1, g_y=2, w=3, calibration batch j: x=4+2j, g_y=5+2j; planted bases
 U_x=400, U_g=401; drift planes 402.
 """
@@ -37,8 +38,8 @@ TID_X, TID_G, TID_W = 1, 2, 3
 TID_UX, TID_UG, TID_DRIFT = 400, 401, 402
 
 
-def seed_for(config: int, tensor_id: int, layer: int = 0) -> int:
-    return SEED_BASE + 1000 * config + 500 * layer + tensor_id
+def seed_for(seed_id: int, tensor_id: int, layer: int = 0) -> int:
+    return SEED_BASE + 1000 * seed_id + 500 * layer + tensor_id
 
 
 def _rng(seed: int) -> np.random.Generator:
@@ -146,7 +147,7 @@ def givens_rotate(U: np.ndarray, seed: int, step: int, angle: float) -> np.ndarr
 # --------------------------------------------------------------------------
 @dataclasses.dataclass(frozen=True)
 class Workload:
-    config: int
+    seed_id: int               # enters every seed of the workload's tensors
     name: str
     dtype: str                 # "f32" or "bf16"
     B: int
@@ -180,27 +181,27 @@ class Workload:
         return (1.0 / Cx) if self.w_var is None else self.w_var
 
 
-CONFIGS = {
-    1: Workload(1, "fp32 single linear 64x64", "f32", B=1, L=64, layers=((64, 64),),
+WORKLOADS = {
+    "fp32_linear_64": Workload(1, "fp32 single linear 64x64", "f32", B=1, L=64, layers=((64, 64),),
                 Rx=4, Ry=4, x_kind="planted", x_sigma="pow2", x_alpha=0.0,
                 g_sigma="pow2", g_alpha=0.0, m_x=6, m_g=6, unit_rms=False,
                 orth_v=True, noise_std=1e-3, w_var=None, calib_samples=8, p=2),
-    2: Workload(2, "BERT-base block linear 768x768", "bf16", B=32, L=512,
+    "bert_base_block": Workload(2, "BERT-base block linear 768x768", "bf16", B=32, L=512,
                 layers=((768, 768),), Rx=8, Ry=8, x_kind="planted", x_sigma="power",
                 x_alpha=1.5, g_sigma="power", g_alpha=1.5, m_x=512, m_g=512,
                 unit_rms=True, orth_v=False, noise_std=0.1, w_var=0.02,
                 calib_samples=64, p=2),
-    3: Workload(3, "transformer FFN pair 768-3072-768", "bf16", B=32, L=512,
+    "bert_ffn_pair": Workload(3, "transformer FFN pair 768-3072-768", "bf16", B=32, L=512,
                 layers=((768, 3072), (3072, 768)), Rx=16, Ry=16, x_kind="planted",
                 x_sigma="power", x_alpha=1.2, g_sigma="power", g_alpha=1.2,
                 m_x=512, m_g=512, unit_rms=True, orth_v=False, noise_std=0.1,
                 w_var=0.02, calib_samples=64, p=2),
-    4: Workload(4, "ViT last-stage MLP pair 448-1792-448, 49 tokens", "bf16", B=256,
+    "vit_mlp_pair_49": Workload(4, "ViT last-stage MLP pair 448-1792-448, 49 tokens", "bf16", B=256,
                 L=49, layers=((448, 1792), (1792, 448)), Rx=8, Ry=8, x_kind="gelu",
                 x_sigma="power", x_alpha=0.0, g_sigma="pow2", g_alpha=0.0, m_x=0,
                 m_g=6, unit_rms=True, orth_v=False, noise_std=0.1, w_var=0.02,
                 calib_samples=256, p=2, n_t=100, steps=20, drift_angle=0.05),
-    5: Workload(5, "long-sequence wide linear 4096->11008, L=2048", "bf16", B=4,
+    "long_seq_4096_11008": Workload(5, "long-sequence wide linear 4096->11008, L=2048", "bf16", B=4,
                 L=2048, layers=((4096, 11008),), Rx=16, Ry=16, x_kind="planted",
                 x_sigma="power", x_alpha=1.0, g_sigma="power", g_alpha=1.0,
                 m_x=512, m_g=512, unit_rms=True, orth_v=False, noise_std=0.1,
@@ -208,8 +209,12 @@ CONFIGS = {
 }
 
 
-def workload(config: int, **overrides) -> Workload:
-    wl = CONFIGS[config]
+def workload(name: str, **overrides) -> Workload:
+    """A workload by name: fp32_linear_64 (fp32, B=1, L=64, 64x64, R=4),
+    bert_base_block (B=32, L=512, 768x768, R=8), bert_ffn_pair (768-3072-768,
+    R=16), vit_mlp_pair_49 (B=256, L=49, 448-1792-448, R=8, drifting g_y) and
+    long_seq_4096_11008 (B=4, L=2048, 4096->11008, R=16)."""
+    wl = WORKLOADS[name]
     return dataclasses.replace(wl, **overrides) if overrides else wl
 
 
@@ -238,9 +243,9 @@ class LayerInputs:
         L = wl.L
         self.Ux = None
         if wl.x_kind == "planted":
-            self.Ux = planted_basis(seed_for(wl.config, TID_UX, layer), L, wl.m_x)
+            self.Ux = planted_basis(seed_for(wl.seed_id, TID_UX, layer), L, wl.m_x)
             self.sx = sigma_profile(wl.x_sigma, wl.m_x, L, self.Cx, wl.unit_rms, wl.x_alpha)
-        self.Ug = planted_basis(seed_for(wl.config, TID_UG, layer), L, wl.m_g)
+        self.Ug = planted_basis(seed_for(wl.seed_id, TID_UG, layer), L, wl.m_g)
         self.sg = sigma_profile(wl.g_sigma, wl.m_g, L, self.Cy, wl.unit_rms, wl.g_alpha)
 
     def _x(self, seed: int, B: int) -> np.ndarray:
@@ -255,26 +260,26 @@ class LayerInputs:
         U = self.Ug
         if wl.drift_angle and step:
             for t in range(1, step + 1):
-                U = givens_rotate(U, seed_for(wl.config, TID_DRIFT, self.layer), t,
+                U = givens_rotate(U, seed_for(wl.seed_id, TID_DRIFT, self.layer), t,
                                   wl.drift_angle)
         dt = _gen_dtype(wl)
         return planted_batch(seed, U, self.sg, B, self.Cy, wl.noise_std, wl.orth_v, dt)
 
     def x(self) -> np.ndarray:
-        return _store(self.wl, self._x(seed_for(self.wl.config, TID_X, self.layer), self.B))
+        return _store(self.wl, self._x(seed_for(self.wl.seed_id, TID_X, self.layer), self.B))
 
     def g_y(self, step: int = 0) -> np.ndarray:
-        s = seed_for(self.wl.config, TID_G, self.layer) + 100_000 * step
+        s = seed_for(self.wl.seed_id, TID_G, self.layer) + 100_000 * step
         return _store(self.wl, self._g(s, self.B, step))
 
     def w(self) -> np.ndarray:
         wl = self.wl
-        return _store(wl, weight(seed_for(wl.config, TID_W, self.layer), self.Cy, self.Cx,
+        return _store(wl, weight(seed_for(wl.seed_id, TID_W, self.layer), self.Cy, self.Cx,
                                  wl.w_variance(self.Cx)))
 
     def calib_x(self, j: int, B: int) -> np.ndarray:
-        return _store(self.wl, self._x(seed_for(self.wl.config, 4 + 2 * j, self.layer), B))
+        return _store(self.wl, self._x(seed_for(self.wl.seed_id, 4 + 2 * j, self.layer), B))
 
     def calib_g(self, j: int, B: int, step: int = 0) -> np.ndarray:
-        s = seed_for(self.wl.config, 5 + 2 * j, self.layer) + 100_000 * step
+        s = seed_for(self.wl.seed_id, 5 + 2 * j, self.layer) + 100_000 * step
         return _store(self.wl, self._g(s, B, step))
