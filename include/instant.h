@@ -127,10 +127,10 @@ size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, inst
 
 /*
  * Both products of the low-rank backward (关键设计 3: g_w ~ g_hat_y1 x_hat and
- * g_tilde_x = Q^T g_hat_y2 w) in one call: the same results as
+ * g_tilde_x = Q^T g_hat_y2 w) in one call: the same products as
  * instant_grad_w(Sx, xhat, gw, accumulate, ...) followed by
- * instant_grad_x(Sq, w, Q, gx, ws, ...), with the same arguments, layouts and
- * limits.  Where the single-kernel input gradient applies (bf16, short Cy) the
+ * instant_grad_x(Sq, w, Q, gx, ws, ...) (g_w may differ in the order of its
+ * fp32 additions), with the same arguments, layouts and limits.  Where the single-kernel input gradient applies (bf16, short Cy) the
  * weight-gradient tiles run inside the same launch, on the SMs the input
  * gradient leaves free; otherwise the two calls are made in turn.
  */
