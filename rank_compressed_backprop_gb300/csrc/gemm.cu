@@ -81,9 +81,9 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     int issued = 0;
+    int s = 0, par = 0;  // ring slot and round parity of chunk i, kept without divisions
     for (int i = 0; i < nkc; ++i) {
-      const int s = i % NS;
-      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
+      if (i >= NS && !mbar_wait(&empty[s], par ^ 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
@@ -105,6 +105,10 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_2d(sb, &tmap_b, &full[s], k0, n0);
       }
       ++issued;
+      if (++s == NS) {
+        s = 0;
+        par ^= 1;
+      }
     }
     for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
       if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
@@ -112,9 +116,9 @@ __global__ void __launch_bounds__(128, 1)
     // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc = idesc_bf16_f32(128, BN, A_MN, B_MN);
     bool ok = true;
+    int s = 0, par = 0;
     for (int i = 0; i < nkc; ++i) {
-      const int s = i % NS;
-      if (!mbar_wait(&full[s], (i / NS) & 1)) {
+      if (!mbar_wait(&full[s], par)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;
@@ -131,6 +135,10 @@ __global__ void __launch_bounds__(128, 1)
         umma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
       }
       umma_commit(&empty[s]);
+      if (++s == NS) {
+        s = 0;
+        par ^= 1;
+      }
     }
     if (ok && nkc > 0) umma_commit(done);
   }

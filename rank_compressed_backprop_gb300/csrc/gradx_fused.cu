@@ -200,9 +200,9 @@ __device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CU
       fence_proxy_async_global();
     }
     int issued = 0;
+    int s = 0, par = 0;  // ring slot and round parity of chunk i, kept without divisions
     for (int i = 0; i < nk; ++i) {
-      const int s = i % NS;
-      if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
+      if (i >= NS && !mbar_wait(&empty[s], par ^ 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
@@ -213,15 +213,19 @@ __device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CU
       tma_load_2d(sa + A_BYTES / 2, tmap_sx, &full[s], m0 + 64, k0);
       tma_load_2d(sa + A_BYTES, tmap_xh, &full[s], n0, k0);
       ++issued;
+      if (++s == NS) {
+        s = 0;
+        par ^= 1;
+      }
     }
     for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
       if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, 64, /*a_mn=*/1, /*b_mn=*/1);
     bool ok = true;
+    int s = 0, par = 0;
     for (int i = 0; i < nk; ++i) {
-      const int s = i % NS;
-      if (!mbar_wait(&full[s], (i / NS) & 1)) {
+      if (!mbar_wait(&full[s], par)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;
@@ -236,6 +240,10 @@ __device__ __forceinline__ void grad_w_tile(const CUtensorMap* tmap_sx, const CU
         umma_bf16(tmem, ad, bd, idesc, (i | kk) != 0);
       }
       umma_commit(&empty[s]);
+      if (++s == NS) {
+        s = 0;
+        par ^= 1;
+      }
     }
     if (ok && nk > 0) umma_commit(done);
   }
@@ -437,9 +445,9 @@ __global__ void __launch_bounds__(320, 2)
         fence_proxy_async_global();
       }
       int issued = 0;
+      int s = 0, par = 0;  // ring slot and round parity of chunk i, kept without divisions
       for (int i = 0; i < nkc; ++i) {
-        const int s = i % NS;
-        if (i >= NS && !mbar_wait(&empty[s], ((i / NS) - 1) & 1)) {
+        if (i >= NS && !mbar_wait(&empty[s], par ^ 1)) {
           raise_fault(FAULT_WAIT_EMPTY);
           break;
         }
@@ -452,6 +460,10 @@ __global__ void __launch_bounds__(320, 2)
         for (int h = 0; h < BN / 64; ++h)
           tma_load_2d(sb + h * (64 * BK * 2), &tmap_w, &full[s], n0 + 64 * h, k0);
         ++issued;
+        if (++s == NS) {
+          s = 0;
+          par ^= 1;
+        }
       }
       for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i)
         if (!mbar_wait(&full[i % NS], (i / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
@@ -463,9 +475,9 @@ __global__ void __launch_bounds__(320, 2)
     if (lane == 0) {
       constexpr uint32_t idesc1 = idesc_bf16_f32(128, BN, /*a_mn=*/0, /*b_mn=*/1);
       bool ok = true;
+      int s = 0, par = 0;
       for (int i = 0; i < nkc; ++i) {
-        const int s = i % NS;
-        if (!mbar_wait(&full[s], (i / NS) & 1)) {
+        if (!mbar_wait(&full[s], par)) {
           raise_fault(FAULT_WAIT_FULL);
           ok = false;
           break;
@@ -480,6 +492,10 @@ __global__ void __launch_bounds__(320, 2)
           umma_bf16(acc1, ad, bd, idesc1, (i | kk) != 0);
         }
         umma_commit(&empty[s]);
+        if (++s == NS) {
+          s = 0;
+          par ^= 1;
+        }
       }
       if (ok) umma_commit(acc1_full);
     }
@@ -596,9 +612,8 @@ __global__ void __launch_bounds__(320, 2)
       tc_fence_after();
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t b_base = smem_u32(sB);
+      int s = 0, t = 0;  // (sample, token tile) of job j, kept without divisions
       for (int j = 0; ok && j < njobs; ++j) {
-        const int s = j / nlt;
-        const int t = j - s * nlt;
         const int buf = j & 1;
         if (j >= 2 && !mbar_wait(&t_empty[buf], ((j >> 1) - 1) & 1)) {
           raise_fault(FAULT_WAIT_EMPTY);
@@ -613,6 +628,10 @@ __global__ void __launch_bounds__(320, 2)
           umma_bf16(tmem + BN + buf * BN, ad, bd, idesc2, kk != 0);
         }
         umma_commit(&t_full[buf]);
+        if (++t == nlt) {
+          t = 0;
+          ++s;
+        }
       }
     }
   } else if (epi) {
@@ -624,9 +643,8 @@ __global__ void __launch_bounds__(320, 2)
     const int grp = (warp - 2) >> 2;
     const int gt = et & 127;
     int it = 0;
+    int s = grp / nlt, t = grp - (grp / nlt) * nlt;  // (sample, token tile) of job j
     for (int j = grp; j < njobs; j += 2, ++it) {
-      const int s = j / nlt;
-      const int t = j - s * nlt;
       uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
       if (gt == 0 && it >= 2) tma_store_wait_read<1>();
       if (grp == 0) named_barrier<2>(128); else named_barrier<3>(128);
@@ -659,6 +677,11 @@ __global__ void __launch_bounds__(320, 2)
           if (n0 + 64 * h < f.Cx)
             tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, (lt0 + t) * BM, s0 + s);
         tma_store_commit();
+      }
+      t += 2;
+      while (t >= nlt) {
+        t -= nlt;
+        ++s;
       }
     }
     if (gt == 0) tma_store_wait_all();

@@ -87,19 +87,24 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0 && lane == 0) {
     const uint32_t bytes = diag ? TILE_BYTES : STAGE;
     int issued = 0;
+    // (sample, channel chunk) of iteration it, kept without divisions
+    int b = it_begin / a.nkc, kc = it_begin - (it_begin / a.nkc) * a.nkc;
     for (int it = 0; it < niter; ++it) {
       const int s = it % kSyrkStages;
       if (it >= kSyrkStages && !mbar_wait(&empty[s], ((it / kSyrkStages) - 1) & 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
-      const int b = (it_begin + it) / a.nkc;
-      const int c0 = ((it_begin + it) % a.nkc) * BK;
+      const int c0 = kc * BK;
       uint8_t* dst = smem + s * STAGE;
       mbar_arrive_expect_tx(&full[s], bytes);
       tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
       if (!diag) tma_load_3d(dst + TILE_BYTES, &tmap_t, &full[s], c0, j0, b);
       ++issued;
+      if (++kc == a.nkc) {
+        kc = 0;
+        ++b;
+      }
     }
     for (int it = issued - kSyrkStages < 0 ? 0 : issued - kSyrkStages; it < issued; ++it)
       if (!mbar_wait(&full[it % kSyrkStages], (it / kSyrkStages) & 1)) raise_fault(FAULT_WAIT_FULL);
