@@ -11,12 +11,17 @@
 //            whatever the stage holds and are never used);
 //   phase 2  the epilogue warps turn acc1 into bf16 and write, per sample, the
 //            MN-major B operand [Ry (padded to 16) x BN] of the expansion
-//            straight into shared memory;
+//            straight into shared memory.  When the token range is split over
+//            a cluster (dims 1 x 1 x cl), each CTA's phase 1 covers only a
+//            slice of K = Cy; the slices are summed through DSMEM (each CTA
+//            reduces a share of the rows from all peers' fp32 partials, then
+//            writes the bf16 rows into every CTA's operands: two cluster
+//            barriers);
 //   phase 3  for every (sample, token tile): TMEM acc2 = Q^T[tile] B_s (one
 //            K = Ry MMA chain, two accumulators in flight) -> bf16 -> swizzled
 //            staging (reusing the phase-1 ring) -> TMA bulk store.
-// Used when Cy is small enough that every CTA can afford to recompute its
-// g_hat_x tile (the token range is split across CTAs for parallelism).
+// Used when the K-slice of Cy per cluster CTA stays short (at most 16 chunks
+// of 64); the token range is split across the cluster for parallelism.
 //
 // The same launch can also compute the weight gradient g_w = Sx^T x_hat
 // (关键设计 3): extra grid rows of CTAs (clusters of their own, no cluster
