@@ -344,3 +344,52 @@ def test_decode_bf16_bits():
     assert vals[0] == 1.0 and vals[1] == -1.0 and vals[3] == 0.0
     assert vals[2] == 3.140625
     assert vals[4] == 2.0 ** 127 * (255.0 / 128.0)
+
+
+def test_reconstruction_error_hand_worked_values():
+    """Exact values worked out by hand (INSTANT page, 关键设计 2: the fraction of
+    the gradient that the rank-R projector loses).  Each case is chosen so that
+    a plausible slip gives another number: the squared ratio (no square root),
+    a per-sample mean instead of the pooled Frobenius ratio, a normalisation by
+    ||t||^2, or the projector applied the wrong way round."""
+    L, C = 9, 2
+    V = np.eye(L)[:3]                       # keeps tokens 0, 1, 2
+    t = np.zeros((1, L, C))
+    t[0, 0, 0] = 2.0
+    t[0, 1, 1] = 2.0
+    t[0, 2, 0] = 2.0
+    t[0, 2, 1] = 2.0                        # kept energy 16
+    t[0, 5, 1] = 3.0                        # lost energy 9
+    e = O.reconstruction_error(t, V)
+    assert abs(e - 0.6) < 1e-15             # 3 / 5; the square would be 0.36
+    # a second sample that the projector keeps whole: pooled 3/7, not the
+    # per-sample mean (0.6 + 0) / 2 = 0.3
+    t2 = np.zeros((2, L, C))
+    t2[0] = t[0]
+    t2[1, 0, 0], t2[1, 1, 0], t2[1, 2, 1] = 4.0, 2.0, 2.0      # energy 24, all kept
+    assert abs(O.reconstruction_error(t2, V) - 3.0 / 7.0) < 1e-15
+    # one row that is not an axis: v = (0.6, 0.8, 0); t = (1, 0, 0) projects to
+    # 0.6 v = (0.36, 0.48, 0), leaving (0.64, -0.48, 0) of norm 0.8
+    v = np.array([[0.6, 0.8, 0.0]])
+    assert abs(O.reconstruction_error(np.array([[[1.0], [0.0], [0.0]]]), v) - 0.8) < 1e-15
+    # (3, 4, 5): (3, 4) lies on v, 5 is lost: 5 / sqrt(50)
+    got = O.reconstruction_error(np.array([[[3.0], [4.0], [5.0]]]), v)
+    assert abs(got - 5.0 / np.sqrt(50.0)) < 1e-15
+    # a vector orthogonal to v is lost whole, one on v is kept whole
+    assert abs(O.reconstruction_error(np.array([[[4.0], [-3.0], [0.0]]]), v) - 1.0) < 1e-15
+    assert O.reconstruction_error(np.array([[[3.0], [4.0], [0.0]]]), v) < 1e-15
+
+
+def test_reconstruction_error_planted_closed_form():
+    """t = V^T a + n with n orthogonal to the rows of V: the error is
+    ||n|| / sqrt(||a||^2 + ||n||^2) exactly (the two parts are orthogonal)."""
+    rng = _rng(15)
+    B, L, C, R = 3, 40, 7, 5
+    Qf, _ = np.linalg.qr(rng.standard_normal((L, L)))
+    V = Qf[:, :R].T                         # orthonormal rows
+    W = Qf[:, R:]                           # basis of the orthogonal complement
+    a = rng.standard_normal((B, R, C))
+    n = 0.3 * rng.standard_normal((B, L - R, C))
+    t = V.T[None] @ a + W[None] @ n
+    want = np.sqrt(np.sum(n * n)) / np.sqrt(np.sum(a * a) + np.sum(n * n))
+    assert abs(O.reconstruction_error(t, V) - want) < 1e-12
