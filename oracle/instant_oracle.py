@@ -60,6 +60,8 @@ __all__ = [
     "grad_x",
     "low_rank_backward",
     "vanilla_backward",
+    "forward",
+    "forward_compress",
     "accumulate_autocorrelation",
     "eig_desc",
     "frobenius_energy",
@@ -157,6 +159,19 @@ def low_rank_backward(x, g_y, w, P, Q, tally=None) -> dict:
     gxh = grad_x_core(Sq, w, tally)
     gx = expand(Q, gxh, tally)
     return {"x_hat": xh, "Sx": Sx, "Sq": Sq, "g_w": gw, "gx_hat": gxh, "g_x": gx}
+
+
+def forward(x, w, tally=None) -> np.ndarray:
+    """The layer's forward ``y_b = x_b w^T``: ``[B,L,Cx], [Cy,Cx] -> [B,L,Cy]``
+    (整体框架: the forward product itself is left as it is)."""
+    x, w = decode(x), decode(w)
+    return _mm(tally, x, w.T[None])
+
+
+def forward_compress(x, w, P, tally=None) -> dict:
+    """The forward pass as INSTANT runs it: ``y = x w^T`` and the stored
+    activation ``x_hat = P x`` (整体框架: x_hat is kept instead of x)."""
+    return {"y": forward(x, w, tally), "x_hat": compress_act(x, P, tally)}
 
 
 def vanilla_backward(x, g_y, w, tally=None) -> dict:

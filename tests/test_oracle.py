@@ -393,3 +393,42 @@ def test_reconstruction_error_planted_closed_form():
     t = V.T[None] @ a + W[None] @ n
     want = np.sqrt(np.sum(n * n)) / np.sqrt(np.sum(a * a) + np.sum(n * n))
     assert abs(O.reconstruction_error(t, V) - want) < 1e-12
+
+
+def test_forward_by_scalar_loops():
+    """y[b, l, o] = sum_c x[b, l, c] w[o, c], checked element by element."""
+    rng = _rng(16)
+    B, L, Cx, Cy = 2, 5, 7, 3
+    x = rng.standard_normal((B, L, Cx))
+    w = rng.standard_normal((Cy, Cx))
+    y = O.forward(x, w)
+    assert y.shape == (B, L, Cy)
+    for b in range(B):
+        for l in range(L):
+            for o in range(Cy):
+                acc = 0.0
+                for c in range(Cx):
+                    acc += x[b, l, c] * w[o, c]
+                assert abs(y[b, l, o] - acc) < 1e-12
+    # w = I gives x back; a permutation matrix permutes the channels
+    assert np.array_equal(O.forward(x, np.eye(Cx)), x)
+    perm = np.eye(Cx)[[3, 0, 6, 1, 5, 2, 4]]
+    assert np.array_equal(O.forward(x, perm), x[:, :, [3, 0, 6, 1, 5, 2, 4]])
+
+
+def test_forward_compress_returns_both_products():
+    rng = _rng(17)
+    B, L, Cx, Cy, Rx = 2, 16, 8, 6, 3
+    x = rng.standard_normal((B, L, Cx))
+    w = rng.standard_normal((Cy, Cx))
+    P = _orthonormal_rows(rng, Rx, L)
+    out = O.forward_compress(x, w, P)
+    assert np.allclose(out["y"], O.forward(x, w), rtol=0, atol=0)
+    assert np.allclose(out["x_hat"], O.compress_act(x, P), rtol=0, atol=0)
+    # x_hat = P x: with P the first Rx unit rows, x_hat is the first Rx tokens
+    E = np.eye(L)[:Rx]
+    assert np.array_equal(O.forward_compress(x, w, E)["x_hat"], x[:, :Rx, :])
+    # the forward FLOPs of one sample: 2 L Cx Cy (half the vanilla backward's 4 L Cx Cy)
+    t = O.FlopTally()
+    O.forward(x[:1], w, t)
+    assert t.flops == 2 * L * Cx * Cy == O.flops_vanilla(L, Cx, Cy) // 2
