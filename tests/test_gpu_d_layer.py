@@ -8,7 +8,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from gpu_util import rel, stored, to_dev, to_np, torch_or_skip
+from gpu_util import assert_parity, rel, stored, to_dev, to_np, torch_or_skip
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,8 @@ def test_layer_step_schedule_and_oracle(torch):
     P = lay.P.view(torch.int16).cpu().numpy().view(np.uint16)
     Q = lay.Q.view(torch.int16).cpu().numpy().view(np.uint16)
     ref = O.low_rank_backward(x, g, w, P, Q)
-    assert rel(to_np(gw), ref["g_w"]) <= 2e-2
-    assert rel(to_np(gx), ref["g_x"]) <= 2e-2
+    assert_parity(to_np(gw), ref["g_w"], 2e-2, "g_w")
+    assert_parity(to_np(gx), ref["g_x"], 2e-2, "g_x")
 
 
 def test_cuda_graph_replay_matches_eager(torch):

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import orthonormal_rows, rel, rng, stored, to_dev, to_np, torch_or_skip
+from gpu_util import assert_parity, orthonormal_rows, rel, rng, stored, to_dev, to_np, torch_or_skip
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,6 @@ def test_projection_reads_what_its_predecessor_wrote(torch, graph):
     for i in range(links):
         want = O.compress_act(cur, P)                 # fp64 from the stored bits
         got = to_np(bufs[i + 1])
-        assert np.isfinite(got).all()
-        assert rel(got, want) <= 2e-2
+        assert_parity(got, want, 2e-2, f"link {i}")
         cur = stored(got, "bf16")                     # the next link reads the stored values
     assert api.device_status() == 0
