@@ -268,7 +268,13 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
  *              the solved block
  *   ws         device scratch of instant_calib_workspace_bytes(L, r_cap) bytes
  * Method: L <= 128 -> one-CTA cyclic Jacobi on the full matrix; larger L ->
- * block subspace iteration with Rayleigh-Ritz (block <= 128 columns).
+ * block subspace iteration with Rayleigh-Ritz (block <= 128 columns), as a
+ * single launch of an 8-CTA cluster up to L = 2048 with blocks of 16 or 32
+ * columns, as a host loop of launches otherwise.  A Ritz pair counts as
+ * converged when its residual is below 1e-3 of its own Ritz value (so that
+ * the trailing rows of a decaying spectrum are accurate too), or when it is
+ * below prm->tol (default 2e-5) times the largest Ritz value and no longer
+ * shrinking (the fp32 rounding floor).
  * Returns INSTANT_ERR_NOT_CONVERGED when the cap is hit or when k + p does not
  * fit the block, INSTANT_ERR_NONFINITE when E is not finite and positive.
  * Synchronises `stream`.
@@ -290,7 +296,7 @@ size_t instant_calib_workspace_bytes(int L, int r_cap);
  * alone (same kernels, same arithmetic: bit for bit on the one-launch solver;
  * the multi-launch path adds some partial sums with atomics, so any two of its
  * runs agree only up to that rounding order); the problems that the
- * one-launch solver takes (128 < L <= 512, block of 16 or 32 columns) run
+ * one-launch solver takes (128 < L <= 2048, block of 16 or 32 columns) run
  * together, one 8-CTA cluster each, up to 16 per launch, with one
  * synchronisation for all of them.
  *

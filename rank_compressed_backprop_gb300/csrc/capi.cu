@@ -32,9 +32,20 @@ bool instant::pdl_enabled() {
   return on;
 }
 
-namespace {
+int instant::sm_count() {
+  // queried once per device (the grids below are sized in multiples of it)
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
-constexpr int kTargetCtas = 2 * 152;  // two waves' worth of work on 152 SMs
+namespace {
 
 // ---------------------------------------------------------------------------
 // tensor maps (driver entry point fetched through the runtime; no -lcuda)
@@ -58,9 +69,11 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-// bf16 tiled map with the 128-byte swizzle; dims/strides innermost first
+// tiled map with the 128-byte swizzle (bf16 unless stated); dims/strides
+// innermost first
 bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box) {
+              const uint64_t* strides_bytes, const uint32_t* box,
+              CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn f = encoder();
   if (!f) return false;
   cuuint64_t d[5], s[5];
@@ -71,7 +84,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
     e[i] = 1;
     if (i < rank - 1) s[i] = strides_bytes[i];
   }
-  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
+  return f(m, type, rank, const_cast<void*>(base), d, s, b, e,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -145,8 +158,9 @@ GemmPlan plan_gemm(int M, int N, int K) {
   p.nk = cdiv(K, 64);
   const int tm = cdiv(M, 128);
   p.BN = 64;
+  const int nsm = sm_count();
   for (int bn : {256, 128}) {
-    if (tm * cdiv(N, bn) >= 152) {
+    if (tm * cdiv(N, bn) >= nsm) {
       p.BN = bn;
       break;
     }
@@ -154,7 +168,7 @@ GemmPlan plan_gemm(int M, int N, int K) {
   const int tiles = tm * cdiv(N, p.BN);
   p.splits = 1;
   for (int s : {8, 4, 2}) {
-    if (s <= p.nk && tiles * s <= kTargetCtas) {
+    if (s <= p.nk && tiles * s <= 2 * nsm) {  // two waves' worth of work
       p.splits = s;
       break;
     }
@@ -162,6 +176,17 @@ GemmPlan plan_gemm(int M, int N, int K) {
   p.cps = cdiv(p.nk, p.splits);
   p.stages = 4;
   return p;
+}
+
+// weight gradient: the write-streaming kernel when the contraction fits its
+// resident x_hat strip (K <= 256) and the output has several tiles per SM;
+// else the split-K GEMM.  INSTANT_GRADW_PATH=gemm|stream forces one.
+bool use_gradw_stream(int M, int N, int K) {
+  if (K > 64 * kGradWMaxChunks) return false;
+  const char* v = std::getenv("INSTANT_GRADW_PATH");
+  if (v && std::strcmp(v, "gemm") == 0) return false;
+  if (v && std::strcmp(v, "stream") == 0) return true;
+  return static_cast<long long>(cdiv(M, 128)) * cdiv(N, 64) >= 4ll * sm_count();
 }
 
 size_t grad_x_ws(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
@@ -232,7 +257,7 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
   const int kper = cdiv(f.nk, f.cl);
   f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;
   // smaller sample tiles when the grid would not cover the SMs
-  while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < 152) f.spt /= 2;
+  while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < sm_count()) f.spt /= 2;
   f.a_rows = std::min(128, round_up(f.spt * Ry, 8));
   f.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
   f.Q = Q;
@@ -400,6 +425,7 @@ ClusterSolveArgs cluster_args(const SolveJob& j) {
   ca.r_cap = j.r_cap;
   ca.out_bf16 = j.out_bf16;
   ca.res = j.w.res;
+  ca.Vg = j.w.V;
   return ca;
 }
 
@@ -576,12 +602,6 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   }
   if (!aligned16(Sx) || !aligned16(xhat) || !aligned16(gw) || Cx % 8 != 0 || Cy % 8 != 0)
     return INSTANT_ERR_ALIGN;
-  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
-  g.BN = p.BN;
-  g.nk = p.nk;
-  g.splits = p.splits;
-  g.chunks_per_split = p.cps;
-  g.stages = p.stages;
   CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.K)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
@@ -591,6 +611,33 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   const uint32_t bb[2] = {64, 64};
   if (!make_map(&ma, Sx, 2, da, sa, ba) || !make_map(&mb, xhat, 2, db, sb, bb))
     return INSTANT_ERR_CUDA;
+  if (use_gradw_stream(g.M, g.N, g.K)) {
+    // short contraction, large output: the persistent write-streaming kernel
+    GradWStreamArgs a;
+    a.M = g.M;
+    a.N = g.N;
+    a.K = g.K;
+    a.nkc = cdiv(g.K, 64);
+    a.mt = cdiv(g.M, 128);
+    a.nt = cdiv(g.N, 64);
+    a.stages = a.nkc == 1 ? kGradWStages : 3;
+    a.accumulate = g.accumulate;
+    CUtensorMap mo;
+    const uint64_t dout[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
+    const uint64_t sout[1] = {static_cast<uint64_t>(Cx) * 4};
+    const uint32_t bout[2] = {32, 128};
+    if (!make_map(&mo, gw, 2, dout, sout, bout, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return INSTANT_ERR_CUDA;
+    const long long tiles = static_cast<long long>(a.mt) * a.nt;
+    const int ctas = static_cast<int>(std::min<long long>(tiles, sm_count()));
+    return from_cuda(launch_gradw_stream(ma, mb, mo, a, ctas, st));
+  }
+  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
+  g.BN = p.BN;
+  g.nk = p.nk;
+  g.splits = p.splits;
+  g.chunks_per_split = p.cps;
+  g.stages = p.stages;
   return from_cuda(launch_gemm_bf16(ma, mb, g, st));
 }
 
@@ -600,14 +647,29 @@ size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, inst
   return grad_x_ws(B, Cx, Cy, Ry, dt);
 }
 
-instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes, int B,
-                                   int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The two halves of the two-kernel input gradient, each split into a plan
+// (every argument checked, every tensor map encoded) and its launch, so that
+// a caller running both can report any error before either launches.
+struct CorePlan {
+  GemmArgs g;
+  CUtensorMap ma, mb;
+  const void* Sq;
+  const void* w;
+};
+
+instant_status plan_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes, int B,
+                                int Cx, int Cy, int Ry, instant_dtype dt, CorePlan* pl) {
   if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
   if (!Sq || !w) return INSTANT_ERR_ARG;
   if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
   if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  GemmArgs g;
+  GemmArgs& g = pl->g;
+  pl->Sq = Sq;
+  pl->w = w;
   g.M = B * Ry;
   g.N = Cx;
   g.K = Cy;
@@ -622,7 +684,7 @@ instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size
     g.splits = 1;
     g.chunks_per_split = g.nk;
     g.stages = 1;
-    return from_cuda(launch_gemm_f32(g, static_cast<const float*>(Sq), static_cast<const float*>(w), st));
+    return INSTANT_OK;
   }
   if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
     return INSTANT_ERR_ALIGN;
@@ -633,25 +695,37 @@ instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
   g.stages = p.stages;
-  CUtensorMap ma, mb;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.M)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
   const uint32_t ba[2] = {64, 128};
   const uint64_t db[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
   const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
   const uint32_t bb[2] = {64, 64};
-  if (!make_map(&ma, Sq, 2, da, sa, ba) || !make_map(&mb, w, 2, db, sb, bb)) return INSTANT_ERR_CUDA;
-  return from_cuda(launch_gemm_bf16(ma, mb, g, st));
+  if (!make_map(&pl->ma, Sq, 2, da, sa, ba) || !make_map(&pl->mb, w, 2, db, sb, bb))
+    return INSTANT_ERR_CUDA;
+  return INSTANT_OK;
 }
 
-instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws_bytes, int B, int L,
-                              int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+instant_status run_grad_x_core(const CorePlan& pl, cudaStream_t st) {
+  if (!pl.g.out_bf16)
+    return from_cuda(launch_gemm_f32(pl.g, static_cast<const float*>(pl.Sq),
+                                     static_cast<const float*>(pl.w), st));
+  return from_cuda(launch_gemm_bf16(pl.ma, pl.mb, pl.g, st));
+}
+
+struct ExpandPlan {
+  ExpandArgs e;
+  bool f32;
+  CUtensorMap mq, mg, mo;
+};
+
+instant_status plan_expand(const void* Q, void* gx, const void* ws, size_t ws_bytes, int B, int L,
+                           int Cx, int Cy, int Ry, instant_dtype dt, ExpandPlan* pl) {
   if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
   if (!Q || !gx) return INSTANT_ERR_ARG;
   if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
   if (!ws || ws_bytes < grad_x_ws(B, Cx, Cy, Ry, dt)) return INSTANT_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  ExpandArgs e;
+  ExpandArgs& e = pl->e;
   e.B = B;
   e.L = L;
   e.Cx = Cx;
@@ -663,18 +737,18 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
   e.out = gx;
   e.q_tma = 0;
   e.BN = 128;
-  if (dt == INSTANT_F32) return from_cuda(launch_expand_f32(e, st));
+  pl->f32 = dt == INSTANT_F32;
+  if (pl->f32) return INSTANT_OK;
   if (!aligned16(gx) || !aligned16(ws) || Cx % 8 != 0) return INSTANT_ERR_ALIGN;
   // column strip width: keep at least ~1.5 strips per SM
-  e.BN = cdiv(Cx, 128) * B >= 228 ? 128 : 64;
+  e.BN = cdiv(Cx, 128) * B >= 3 * sm_count() / 2 ? 128 : 64;
   e.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
-  CUtensorMap mq, mg, mo;
-  std::memset(&mq, 0, sizeof(mq));
+  std::memset(&pl->mq, 0, sizeof(pl->mq));
   if (e.q_tma) {
     const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
     const uint64_t s2[1] = {static_cast<uint64_t>(L) * 2};
     const uint32_t b2[2] = {64, static_cast<uint32_t>(e.KR)};
-    if (!make_map(&mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
+    if (!make_map(&pl->mq, Q, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
   }
   const uint64_t dg[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Ry), static_cast<uint64_t>(B)};
   const uint64_t sg[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(Ry) * Cx * 2};
@@ -682,9 +756,46 @@ instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws
   const uint64_t dout[3] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};
   const uint64_t sout[2] = {static_cast<uint64_t>(Cx) * 2, static_cast<uint64_t>(L) * Cx * 2};
   const uint32_t bout[3] = {64, 128, 1};
-  if (!make_map(&mg, ws, 3, dg, sg, bg) || !make_map(&mo, gx, 3, dout, sout, bout))
+  if (!make_map(&pl->mg, ws, 3, dg, sg, bg) || !make_map(&pl->mo, gx, 3, dout, sout, bout))
     return INSTANT_ERR_CUDA;
-  return from_cuda(launch_expand_bf16(mq, mg, mo, e, st));
+  return INSTANT_OK;
+}
+
+instant_status run_expand(const ExpandPlan& pl, cudaStream_t st) {
+  if (pl.f32) return from_cuda(launch_expand_f32(pl.e, st));
+  return from_cuda(launch_expand_bf16(pl.mq, pl.mg, pl.mo, pl.e, st));
+}
+
+}  // namespace
+
+instant_status instant::grad_x_two_kernels(const void* Sq, const void* w, const void* Q, void* gx,
+                                           void* ws, size_t ws_bytes, int B, int L, int Cx,
+                                           int Cy, int Ry, instant_dtype dt, cudaStream_t st) {
+  CorePlan cp;
+  ExpandPlan ep;
+  instant_status s = plan_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, &cp);
+  if (s != INSTANT_OK) return s;
+  s = plan_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, &ep);
+  if (s != INSTANT_OK) return s;
+  s = run_grad_x_core(cp, st);
+  if (s != INSTANT_OK) return s;
+  return run_expand(ep, st);
+}
+
+extern "C" {
+
+instant_status instant_grad_x_core(const void* Sq, const void* w, void* ws, size_t ws_bytes, int B,
+                                   int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+  CorePlan cp;
+  const instant_status s = plan_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, &cp);
+  return s != INSTANT_OK ? s : run_grad_x_core(cp, static_cast<cudaStream_t>(stream));
+}
+
+instant_status instant_expand(const void* Q, void* gx, const void* ws, size_t ws_bytes, int B, int L,
+                              int Cx, int Cy, int Ry, instant_dtype dt, void* stream) {
+  ExpandPlan ep;
+  const instant_status s = plan_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, &ep);
+  return s != INSTANT_OK ? s : run_expand(ep, static_cast<cudaStream_t>(stream));
 }
 
 instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
@@ -700,9 +811,8 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
   if (use_fused_grad_x(L, Cy, Ry, dt))
     return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{nullptr, nullptr, nullptr, 0, 0},
                         static_cast<cudaStream_t>(stream));
-  const instant_status s = instant_grad_x_core(Sq, w, ws, ws_bytes, B, Cx, Cy, Ry, dt, stream);
-  if (s != INSTANT_OK) return s;
-  return instant_expand(Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
+  return grad_x_two_kernels(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt,
+                            static_cast<cudaStream_t>(stream));
 }
 
 instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int accumulate,
@@ -833,7 +943,8 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
       s.Cout = it.C;
       const int iters = s.B * s.nkc;
       const double share = static_cast<double>(iters) / static_cast<double>(total);
-      int splits = std::max(1, static_cast<int>(kTargetCtas * share / ntiles));
+      // two CTAs per SM: the grid fills every SM twice
+      int splits = std::max(1, static_cast<int>(2 * sm_count() * share / ntiles));
       splits = std::min(splits, 64);
       splits = std::min(splits, std::max(1, iters / 4));
       s.it_per_split = cdiv(iters, splits);
@@ -1001,6 +1112,8 @@ instant_status instant_device_status(int clear, void* stream) {
   if (read_fault_eig(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   if (read_fault_fused(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_gradw(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   return total ? INSTANT_ERR_DEVICE : INSTANT_OK;
 }

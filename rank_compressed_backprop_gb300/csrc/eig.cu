@@ -7,7 +7,8 @@
 // Only the top R eigenpairs are needed.  L <= 128: one CTA runs a cyclic
 // (round-robin parallel) Jacobi method on the whole matrix in shared memory.
 // Larger L: block subspace iteration with a Rayleigh-Ritz step every
-// iteration.  Each iteration is five launches:
+// iteration, as one cluster launch where the rows fit (k_solve_cluster below),
+// otherwise as a host loop whose iterations are five launches:
 //   orth   (1 CTA)  T = D W_G Lambda_G^(-1/2) from the Gram matrix of Z
 //   apply  (grid)   V = Z T                         (orthonormal basis)
 //   cv     (grid)   Y = C V / n,  H += V^T Y
@@ -322,6 +323,8 @@ __device__ __forceinline__ float hash_uniform(uint32_t i, uint32_t j) {
 // starting block: columns j < n_seed are the seed rows (a previous projector,
 // row j = column j), the rest deterministic pseudo-random
 __global__ void k_sub_init(int L, int m, const void* seed, int n_seed, int seed_bf16, SolverWs w) {
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) w.res->res2_prev[i] = __int_as_float(0x7f800000);
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < L * m; idx += gridDim.x * blockDim.x) {
     const int i = idx / m, j = idx - (idx / m) * m;
     float v = hash_uniform(i, j);
@@ -645,6 +648,22 @@ __device__ int k_rule(const double* theta, int m, double target) {
   return m + 1;
 }
 
+// Convergence of Ritz pair i (used by both subspace-iteration paths).  Its
+// eigenvector error is about residual / gap, so a residual that is small only
+// against the largest Ritz value theta_1 leaves the trailing vectors of a
+// decaying spectrum inaccurate.  A pair is converged when its residual is
+// below kRitzRelTol * theta_i, or -- at the rounding floor of the fp32 C V
+// product, which can lie above that for small theta_i -- when it is below
+// tol * theta_1 and no longer shrinking (at least half the previous check's
+// squared residual).
+constexpr double kRitzRelTol = 1e-3;
+
+__host__ __device__ inline bool ritz_converged(double r2, double r2_prev, double th_i, double th_1,
+                                               double tol) {
+  if (r2 <= kRitzRelTol * kRitzRelTol * th_i * th_i) return true;
+  return r2 <= tol * tol * th_1 * th_1 && r2 >= 0.5 * r2_prev;
+}
+
 __global__ void k_sub_check(int L, int m, double eps, int p, int r_override, double tol,
                             double inv_n2, SolverWs w) {
   if (threadIdx.x != 0) return;
@@ -659,9 +678,9 @@ __global__ void k_sub_check(int L, int m, double eps, int p, int r_override, dou
   r->block_short = fits ? 0 : 1;
   int conv = fits ? 1 : 0;
   const double th1 = r->theta[0];
-  const double lim = tol * tol * th1 * th1;
   for (int i = 0; i < R && i < m && conv; ++i)
-    if (!(static_cast<double>(r->res2[i]) <= lim)) conv = 0;
+    if (!ritz_converged(r->res2[i], r->res2_prev[i], r->theta[i], th1, tol)) conv = 0;
+  for (int i = 0; i < m; ++i) r->res2_prev[i] = r->res2[i];
   r->converged = conv;
 }
 
@@ -725,10 +744,13 @@ __global__ void k_finalize(int L, int m, double eps, int p, int r_override, int 
 }
 
 // ---------------------------------------------------------------------------
-// whole subspace iteration in one launch: a cluster of 8 CTAs (128 < L <= 512,
-// block m <= 32).  CTA q owns rows [q*rp, (q+1)*rp) of every tall matrix and
-// streams the same rows of C for Y = C V / n, gathering the rest of V from its
-// peers' shared memory.  The m x m steps (Rayleigh-Ritz Jacobi, Cholesky-QR,
+// whole subspace iteration in one launch: a cluster of 8 CTAs (128 < L, block
+// m <= 32, while the CTA's rows fit in shared memory: L <= 2048 for m = 32).
+// CTA q owns rows [q*rp, (q+1)*rp) of every tall matrix and streams the same
+// rows of C for Y = C V / n.  Up to L = 512 it gathers the rest of V from its
+// peers' shared memory; beyond that the basis no longer fits next to the
+// CTA's rows, so every CTA publishes its rows of V in the solver workspace and
+// streams V tiles from L2 along with the C tiles.  The m x m steps (Rayleigh-Ritz Jacobi, Cholesky-QR,
 // convergence test) run in every CTA on partial sums that each CTA adds in
 // rank order, so all CTAs hold identical copies; the decision to stop is
 // still taken from rank 0 so that every CTA leaves the loop together.
@@ -914,7 +936,7 @@ __device__ __forceinline__ void add_square(float v, float& hi, float& lo, int& b
   lo += err + sq_err;
 }
 
-constexpr int kCvTileRows = 64;  // rows of C per CTA (L <= 512)
+constexpr int kCvTileRows = 64;  // rows of C per staged tile
 constexpr int kCvTileL = 64;     // columns of C per staged tile
 constexpr int kCvTileLd = 68;    // padded row stride: 16-byte rows, conflict-free column reads
 
@@ -930,6 +952,23 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
     } else {
       for (int e = 0; e < 4; ++e)
         d[e] = (rr < nr && l0 + c4 + e < L) ? Cown[static_cast<size_t>(rr) * L + l0 + c4 + e] : 0.f;
+    }
+  }
+  cp_async_commit();
+}
+
+// stage rows [t * 64, t * 64 + 64) of V [L, m] (fp32, rows 16-byte aligned:
+// m is 16 or 32) into a [64][m] tile; rows past L are zero
+__device__ __forceinline__ void stage_v_tile(float* dst, const float* V, int L, int m, int t) {
+  const int l0 = t * kCvTileL;
+  const int q4 = m / 4;
+  for (int i = threadIdx.x; i < kCvTileL * q4; i += blockDim.x) {
+    const int rr = i / q4, c4 = (i - rr * q4) * 4;
+    float* d = dst + rr * m + c4;
+    if (l0 + rr < L) {
+      cp_async16(d, V + static_cast<size_t>(l0 + rr) * m + c4);
+    } else {
+      d[0] = d[1] = d[2] = d[3] = 0.f;
     }
   }
   cp_async_commit();
@@ -953,7 +992,7 @@ __device__ __forceinline__ float cluster_sum8(const float* p) {
 
 struct ClusterLay {
   uint32_t V, Y, Z, U, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
-      ct, total;
+      vt, ct, total;
 };
 
 __host__ __device__ inline uint32_t lay_take(uint32_t& o, size_t bytes) {
@@ -962,10 +1001,17 @@ __host__ __device__ inline uint32_t lay_take(uint32_t& o, size_t bytes) {
   return r;
 }
 
+// Above this token length the whole basis no longer fits next to the CTA's
+// rows: each CTA keeps only its own rows of V and publishes them through the
+// solver workspace, and C V streams tiles of C and of V from L2.
+constexpr int kClusterGatherMaxL = 512;
+
 __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   ClusterLay c;
   uint32_t o = 0;
-  c.V = lay_take(o, 4u * L * m);       // the whole basis, gathered each iteration
+  const bool big = L > kClusterGatherMaxL;
+  // the whole basis, gathered each iteration (own rows only for long L)
+  c.V = lay_take(o, 4u * (big ? rp : L) * m);
   c.Y = lay_take(o, 4u * rp * m);      // own rows of Y = C V / n
   c.Z = lay_take(o, 4u * rp * m);      // own rows of Z = Y W (or Y)
   c.U = lay_take(o, 4u * rp * m);      // own rows of the Ritz vectors U = V W
@@ -985,7 +1031,8 @@ __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   c.dsc = lay_take(o, 4u * kMaxBlock);
   c.pv = lay_take(o, 4u * kMaxBlock);
   c.jac = lay_take(o, jac_smem_bytes(m));
-  if (m == 16) {
+  c.vt = big ? lay_take(o, 4u * 2 * kCvTileL * m) : o;  // two V tiles for Y = C V (long L)
+  if (m == 16 && !big) {
     // the CTA's rows of C stay in shared memory for the whole solve
     c.ct = lay_take(o, 4u * rp * cres_ld(L));
   } else {
@@ -1027,10 +1074,14 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
   float* pv = reinterpret_cast<float*>(csm + lay.pv);
   JacSmem js = jac_carve(csm + lay.jac, m);
   float* Ct = reinterpret_cast<float*>(csm + lay.ct);
+  float* Vt = reinterpret_cast<float*>(csm + lay.vt);
+  const bool big = L > kClusterGatherMaxL;
   __shared__ double s_E;
   __shared__ int s_bad, s_dec, s_jfail, s_deficient, s_cflag, s_useT, s_k, s_R;
   __shared__ float s_scale;
   __shared__ double wred[kClusterThreads / 32];
+  __shared__ float s_r2prev[M];  // rank 0: squared residuals at the previous check
+  for (int i = threadIdx.x; i < M; i += blockDim.x) s_r2prev[i] = __int_as_float(0x7f800000);
 
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
@@ -1040,7 +1091,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
   constexpr int ld = m + 1;
   const float* Cown = a.C + static_cast<size_t>(r0) * L;
 
-  constexpr bool kResident = (M == 16);
+  const bool kResident = (M == 16) && !big;
   const bool vecC = (L & 3) == 0 && (reinterpret_cast<uintptr_t>(a.C) & 15) == 0;
   if (kResident) {
     // load the own rows of C once (cp.async when rows are 16-byte aligned)
@@ -1157,7 +1208,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
 
   int dec = 0;  // 1 converged, 2 block too short, 3 iteration cap
   constexpr int cpg = m / 4;  // columns per thread group in C V
-  float* Vown = Vall + static_cast<size_t>(r0) * m;
+  float* Vown = big ? Vall : Vall + static_cast<size_t>(r0) * m;
   for (int it = 0;; ++it) {
     // ---- orthonormalise Z (Gram partials in Gp): V = Z D L^-T ----
     cluster_sync();
@@ -1192,15 +1243,25 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         Vown[idx] = v;
       }
     }
-    // ---- gather the other rows of V from the peers ----
-    cluster_sync();
-    for (int q = 0; q < kClusterCtas; ++q) {
-      if (q == rank) continue;
-      const int q0 = q * rp;
-      const int nq = min(rp, L - q0);
-      float* dst = Vall + static_cast<size_t>(q0) * m;
-      for (int i4 = tid; i4 < nq * m / 4; i4 += nthr)
-        reinterpret_cast<float4*>(dst)[i4] = dsmem_ld_f4(dsmem_addr(dst + 4 * i4, q));
+    if (big) {
+      // ---- publish the own rows of V in the workspace (read back by every CTA) ----
+      __syncthreads();
+      float* vg = a.Vg + static_cast<size_t>(r0) * m;
+      for (int i4 = tid; i4 < nr * m / 4; i4 += nthr)
+        reinterpret_cast<float4*>(vg)[i4] = reinterpret_cast<const float4*>(Vown)[i4];
+      __threadfence();
+      cluster_sync();
+    } else {
+      // ---- gather the other rows of V from the peers ----
+      cluster_sync();
+      for (int q = 0; q < kClusterCtas; ++q) {
+        if (q == rank) continue;
+        const int q0 = q * rp;
+        const int nq = min(rp, L - q0);
+        float* dst = Vall + static_cast<size_t>(q0) * m;
+        for (int i4 = tid; i4 < nq * m / 4; i4 += nthr)
+          reinterpret_cast<float4*>(dst)[i4] = dsmem_ld_f4(dsmem_addr(dst + 4 * i4, q));
+      }
     }
     __syncthreads();
     // ---- Y = C[own rows, :] V / n ----
@@ -1226,6 +1287,48 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < cpg; ++c) Y[r * m + cg * cpg + c] = acc[c] * a.inv_n;
+      }
+    } else if (big) {
+      // C and V streamed through double-buffered cp.async tiles, 64 own rows
+      // at a time (V rows from the workspace, where every CTA published its own)
+      const int ntile = (L + kCvTileL - 1) / kCvTileL;
+      for (int g0 = 0; g0 < nr; g0 += kCvTileRows) {
+        const int gr = min(kCvTileRows, nr - g0);
+        const float* Cg = Cown + static_cast<size_t>(g0) * L;
+        const int r = tid >> 2, cg = tid & 3;
+        float acc[cpg];
+#pragma unroll
+        for (int c = 0; c < cpg; ++c) acc[c] = 0.f;
+        stage_c_tile(Ct, Cg, gr, L, 0, vecC);
+        stage_v_tile(Vt, a.Vg, L, m, 0);
+        for (int t = 0; t < ntile; ++t) {
+          if (t + 1 < ntile) {
+            stage_c_tile(Ct + ((t + 1) & 1) * kCvTileRows * kCvTileLd, Cg, gr, L, t + 1, vecC);
+            stage_v_tile(Vt + ((t + 1) & 1) * kCvTileL * m, a.Vg, L, m, t + 1);
+            cp_async_wait<2>();  // tile t's two groups have landed
+          } else {
+            cp_async_wait<0>();
+          }
+          __syncthreads();
+          const float* crow = Ct + (t & 1) * kCvTileRows * kCvTileLd + r * kCvTileLd;
+          const int nl = min(kCvTileL, L - t * kCvTileL);
+          const float* vb = Vt + (t & 1) * kCvTileL * m + cg * cpg;
+          for (int l = 0; l < nl; ++l) {
+            const float cv = crow[l];
+#pragma unroll
+            for (int c4 = 0; c4 < cpg; c4 += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(vb + l * m + c4);
+              acc[c4] = fmaf(cv, v.x, acc[c4]);
+              acc[c4 + 1] = fmaf(cv, v.y, acc[c4 + 1]);
+              acc[c4 + 2] = fmaf(cv, v.z, acc[c4 + 2]);
+              acc[c4 + 3] = fmaf(cv, v.w, acc[c4 + 3]);
+            }
+          }
+          __syncthreads();  // the buffers are refilled two tiles later
+        }
+        if (r < gr)
+#pragma unroll
+          for (int c = 0; c < cpg; ++c) Y[(g0 + r) * m + cg * cpg + c] = acc[c] * a.inv_n;
       }
     } else {
       // C streamed through double-buffered cp.async tiles
@@ -1335,9 +1438,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
       if (R > L) R = L;
       const bool fits = k <= m && R <= m - 1;
       int conv = fits ? 1 : 0;
-      const double lim = a.tol * a.tol * th[0] * th[0];
       for (int i = 0; i < R && i < m && conv; ++i)
-        if (!(static_cast<double>(r2[i]) <= lim)) conv = 0;
+        if (!ritz_converged(r2[i], s_r2prev[i], th[i], th[0], a.tol)) conv = 0;
+      for (int i = 0; i < m; ++i) s_r2prev[i] = r2[i];
       int d = conv ? 1 : 0;
       if (!d && !fits && it >= 15) d = 2;
       if (!d && it >= a.max_iter - 1) d = 3;
@@ -1545,9 +1648,10 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
 }
 
 bool cluster_solve_fits(int L, int m) {
-  if (L <= 128 || L > 512 || (m != 16 && m != 32)) return false;
+  if (L <= 128 || (m != 16 && m != 32)) return false;
   const int rp = (L + kClusterCtas - 1) / kClusterCtas;
-  return cluster_layout(L, m, rp).total <= 200 * 1024;
+  // (the static shared arrays of the kernel take about 2 KB more)
+  return cluster_layout(L, m, rp).total <= (L > kClusterGatherMaxL ? 216 : 200) * 1024;
 }
 
 cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStream_t st) {
@@ -1561,7 +1665,7 @@ cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStre
   }
   const size_t bytes = cluster_layout(L, m, rp).total;
   auto kern = m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 216 * 1024);
   if (e != cudaSuccess) return e;
   return launch_ex(kern, dim3(1, count, kClusterCtas), dim3(kClusterThreads), bytes, st,
                    kClusterCtas, false, b);

@@ -54,6 +54,25 @@ cudaError_t launch_gemm_bf16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
 cudaError_t launch_gemm_f32(const GemmArgs& g, const float* A, const float* Bm, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
+// weight gradient with a short contraction, streamed to HBM:
+// gw[m, n] (+)= sum_k Sx[k, m] xh[k, n], K = B * Rx <= 64 * kGradWMaxChunks
+// ---------------------------------------------------------------------------
+struct GradWStreamArgs {
+  int M, N, K;       // gw [M = Cy, N = Cx] fp32; Sx [K, M], xh [K, N] bf16
+  int nkc;           // ceil(K / 64)
+  int mt, nt;        // ceil(M / 128) row tiles, ceil(N / 64) column strips
+  int stages;        // Sx chunk ring depth, 2..kGradWStages
+  int accumulate;    // 1: gw += result
+};
+
+constexpr int kGradWStages = 4;
+constexpr int kGradWMaxChunks = 4;
+size_t gradw_stream_smem_bytes(const GradWStreamArgs& g);
+cudaError_t launch_gradw_stream(const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
+                                const CUtensorMap& tmap_gw, const GradWStreamArgs& g, int ctas,
+                                cudaStream_t st);
+
+// ---------------------------------------------------------------------------
 // rank-R expansion: out[b, l, c] = sum_r Q[r, l] * (sum_s gxh[s][b*Ry + r, c])
 // ---------------------------------------------------------------------------
 struct ExpandArgs {
@@ -159,6 +178,7 @@ struct SolverResult {      // lives at the start of the solver workspace
   int pad_;
   double theta[128];       // Ritz values (descending)
   float res2[128];         // squared residual norms of the Ritz vectors
+  float res2_prev[128];    // the same at the previous convergence check
 };
 
 struct SolverWs {
@@ -197,7 +217,8 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
                                    double inv_n2, SolverWs w, cudaStream_t st);
 
 // the whole subspace iteration + projector rows in one launch of an 8-CTA
-// cluster (128 < L <= 512, block m <= 32); rp is set by the launcher
+// cluster (128 < L, block m of 16 or 32, while cluster_solve_fits); rp is set
+// by the launcher
 struct ClusterSolveArgs {
   const float* C;
   int L, m, rp;
@@ -213,6 +234,7 @@ struct ClusterSolveArgs {
   void* rows_out;        // [r_cap, L]; written unless the block proved too short
   int r_cap, out_bf16;
   SolverResult* res;
+  float* Vg;             // [L, m] scratch: the basis exchanged through L2 (L > 512)
 };
 bool cluster_solve_fits(int L, int m);
 cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st);
@@ -231,6 +253,21 @@ cudaError_t launch_recon(const void* t, const void* Q, const void* S, int B, int
 
 // host-side count of kernel launches issued by the library
 void count_launches(unsigned int n);
+
+// streaming multiprocessors of the current device (queried once per device)
+int sm_count();
+
+}  // namespace instant
+
+#include "instant.h"
+
+namespace instant {
+
+// g_tilde_x = Q^T (Sq w) as two launches (g_hat_x in `ws`): every argument is
+// checked and both launches are planned before the first one is issued
+instant_status grad_x_two_kernels(const void* Sq, const void* w, const void* Q, void* gx, void* ws,
+                                  size_t ws_bytes, int B, int L, int Cx, int Cy, int Ry,
+                                  instant_dtype dt, cudaStream_t st);
 
 // programmatic dependent launch on/off (INSTANT_NO_PDL=1 turns it off)
 bool pdl_enabled();
@@ -274,5 +311,6 @@ cudaError_t read_fault_expand(unsigned int* out, int clear);
 cudaError_t read_fault_syrk(unsigned int* out, int clear);
 cudaError_t read_fault_eig(unsigned int* out, int clear);
 cudaError_t read_fault_fused(unsigned int* out, int clear);
+cudaError_t read_fault_gradw(unsigned int* out, int clear);
 
 }  // namespace instant

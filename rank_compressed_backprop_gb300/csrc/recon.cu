@@ -126,7 +126,8 @@ cudaError_t launch_recon(const void* t, const void* Q, const void* S, int B, int
   cudaError_t e = cudaMemsetAsync(totals, 0, 2 * sizeof(double), st);
   if (e != cudaSuccess) return e;
   const long long rows = static_cast<long long>(B) * L;
-  const int grid = static_cast<int>(rows < 4 * 152 ? rows : 4 * 152);
+  const long long cap = 4ll * sm_count();
+  const int grid = static_cast<int>(rows < cap ? rows : cap);
   const size_t smem = sizeof(float) * R * L;
   // 16-byte loads when every row of t and S starts on a 16-byte boundary
   const int vec = (C % 8 == 0 && (reinterpret_cast<uintptr_t>(t) & 15) == 0 &&

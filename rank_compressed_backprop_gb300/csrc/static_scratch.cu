@@ -14,14 +14,14 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
-#include <mutex>
+#include <cstdint>
 
 #include "instant.h"
+#include "kernels.h"
 
 namespace {
 
 constexpr size_t kScratchBytes = INSTANT_GRAD_X_STATIC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // g_hat_x of one call: [B*Ry, Cx] in the call's dtype.  The first kernel
 // overwrites every element the second one reads (no accumulation, and rows
@@ -29,27 +29,18 @@ constexpr int kMaxDevices = 64;
 // buffer never needs clearing.
 __device__ __align__(256) unsigned char g_gxh_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.  The lookup may load the module on
-// that device, which is why the first call on a device has to happen outside
-// any stream capture.
+// Device address of the scratch array in the current device's context.  It
+// is looked up on every call rather than cached: a cached address would go
+// stale if the context were destroyed and recreated (cudaDeviceReset), and the
+// lookup is cheap once the module is loaded.  The first lookup on a device
+// may load the module there, which is why the first call on a device has to
+// happen outside any stream capture.
 cudaError_t scratch_address(void** out) {
-  int dev = -1;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_gxh_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_gxh_scratch);
-    if (e != cudaSuccess) return e;
-    if (!p) return cudaErrorInvalidSymbol;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  if (!p) return cudaErrorInvalidSymbol;
+  *out = p;
   return cudaSuccess;
 }
 
@@ -63,9 +54,15 @@ extern "C" instant_status instant_grad_x_static(const void* Sq, const void* w, c
   if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Ry < 1 || Ry > 64) return INSTANT_ERR_SHAPE;
   const size_t need = instant_grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt);
   if (need == 0 || need > kScratchBytes) return INSTANT_ERR_WORKSPACE;
+  // the layout rules of the bf16 path, checked before any CUDA call (the
+  // array itself is 256-byte aligned)
+  const auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (dt == INSTANT_BF16 && (!aligned16(Sq) || !aligned16(w) || !aligned16(gx) || Cx % 8 != 0 ||
+                             Cy % 8 != 0))
+    return INSTANT_ERR_ALIGN;
   void* ws = nullptr;
   if (scratch_address(&ws) != cudaSuccess) return INSTANT_ERR_CUDA;
-  const instant_status s = instant_grad_x_core(Sq, w, ws, kScratchBytes, B, Cx, Cy, Ry, dt, stream);
-  if (s != INSTANT_OK) return s;
-  return instant_expand(Q, gx, ws, kScratchBytes, B, L, Cx, Cy, Ry, dt, stream);
+  // both launches are checked and planned before the first is issued
+  return instant::grad_x_two_kernels(Sq, w, Q, gx, ws, kScratchBytes, B, L, Cx, Cy, Ry, dt,
+                                     static_cast<cudaStream_t>(stream));
 }

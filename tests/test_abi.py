@@ -68,6 +68,22 @@ def test_validation_without_gpu(L):
     assert L.instant_calib_accumulate(fake, fake, 1, 9000, 8, 1, null) == 2
 
 
+def test_static_grad_x_checks_alignment_before_any_launch(L):
+    """instant_grad_x_static: a misaligned bf16 gx (or a row pitch that is not
+    a multiple of 8) is reported before anything is launched, and before the
+    call touches the device at all."""
+    fake = ctypes.c_void_p(0x1000)
+    odd = ctypes.c_void_p(0x1002)
+    null = ctypes.c_void_p(0)
+    n0 = L.instant_launch_count()
+    assert L.instant_grad_x_static(fake, fake, fake, odd, 4, 64, 256, 256, 8, 1, null) == 4
+    assert L.instant_grad_x_static(odd, fake, fake, fake, 4, 64, 256, 256, 8, 1, null) == 4
+    assert L.instant_grad_x_static(fake, odd, fake, fake, 4, 64, 256, 256, 8, 1, null) == 4
+    assert L.instant_grad_x_static(fake, fake, fake, fake, 4, 64, 252, 256, 8, 1, null) == 4
+    assert L.instant_grad_x_static(fake, fake, fake, fake, 4, 64, 256, 252, 8, 1, null) == 4
+    assert L.instant_launch_count() == n0
+
+
 def test_calib_solve_validation_without_gpu(L):
     from rank_compressed_backprop_gb300._lib import CalibParams
 

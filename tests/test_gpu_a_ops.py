@@ -8,7 +8,8 @@ import numpy as np
 import pytest
 
 import oracle as O
-from gpu_util import orthonormal_rows, rel, rng, stored, to_dev, to_np, tol, torch_or_skip
+from gpu_util import (assert_parity, nan_like, orthonormal_rows, rel, rng, stored, to_dev, to_np,
+                      tol, torch_or_skip)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,11 +41,11 @@ def test_compress_act(torch, dtype, B, L, C, Rx):
     g = rng(100 + L + C)
     x = stored(g.standard_normal((B, L, C)), dtype)
     P = stored(orthonormal_rows(g, Rx, L), dtype)
-    xh = torch.empty(B, Rx, C, dtype=_tdt(torch, dtype), device="cuda")
+    xh = nan_like(torch, (B, Rx, C), _tdt(torch, dtype))
     _api().compress_act(to_dev(x), to_dev(P), xh)
     torch.cuda.synchronize()
     ref = O.compress_act(x, P)
-    assert rel(to_np(xh), ref) <= tol(dtype)
+    assert_parity(to_np(xh), ref, tol(dtype), "x_hat")
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -56,13 +57,13 @@ def test_project_grad(torch, dtype, B, L, C, Rx, Ry):
     gy = stored(g.standard_normal((B, L, C)), dtype)
     PQ = stored(orthonormal_rows(g, Rx + Ry, L), dtype)
     dt = _tdt(torch, dtype)
-    Sx = torch.empty(B * Rx, C, dtype=dt, device="cuda")
-    Sq = torch.empty(B * Ry, C, dtype=dt, device="cuda")
+    Sx = nan_like(torch, (B * Rx, C), dt)
+    Sq = nan_like(torch, (B * Ry, C), dt)
     _api().project_grad(to_dev(gy), to_dev(PQ), Sx, Sq, Rx, Ry)
     torch.cuda.synchronize()
     rx, rq = O.project_grad(gy, PQ[:Rx], PQ[Rx:])
-    assert rel(to_np(Sx).reshape(B, Rx, C), rx) <= tol(dtype)
-    assert rel(to_np(Sq).reshape(B, Ry, C), rq) <= tol(dtype)
+    assert_parity(to_np(Sx).reshape(B, Rx, C), rx, tol(dtype), "Sx")
+    assert_parity(to_np(Sq).reshape(B, Ry, C), rq, tol(dtype), "Sq")
 
 
 # --------------------------------------------------------------------------
@@ -77,13 +78,13 @@ def test_grad_w(torch, dtype, B, Rx, Cx, Cy, accumulate):
     Sx = stored(g.standard_normal((B * Rx, Cy)), dtype)
     xh = stored(g.standard_normal((B, Rx, Cx)), dtype)
     gw0 = g.standard_normal((Cy, Cx)).astype(np.float32)
-    gw = to_dev(gw0) if accumulate else torch.empty(Cy, Cx, dtype=torch.float32, device="cuda")
+    gw = to_dev(gw0) if accumulate else nan_like(torch, (Cy, Cx), torch.float32)
     _api().grad_w(to_dev(Sx), to_dev(xh), gw, B, accumulate=accumulate)
     torch.cuda.synchronize()
     ref = O.grad_w(O.decode(Sx).reshape(B, Rx, Cy), O.decode(xh))
     if accumulate:
         ref = ref + gw0.astype(np.float64)
-    assert rel(to_np(gw), ref) <= (1e-5 if dtype == "f32" else 2e-3)
+    assert_parity(to_np(gw), ref, 1e-5 if dtype == "f32" else 2e-3, "g_w")
 
 
 # --------------------------------------------------------------------------
@@ -100,13 +101,13 @@ def test_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
     w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), dtype)
     Q = stored(orthonormal_rows(g, Ry, L), dtype)
     dt = _tdt(torch, dtype)
-    gx = torch.empty(B, L, Cx, dtype=dt, device="cuda")
+    gx = nan_like(torch, (B, L, Cx), dt)
     ws = torch.empty(max(api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, dt), 16), dtype=torch.uint8,
                      device="cuda")
     api.grad_x(to_dev(Sq), to_dev(w), to_dev(Q), gx, ws)
     torch.cuda.synchronize()
     ref = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
-    assert rel(to_np(gx), ref) <= tol(dtype)
+    assert_parity(to_np(gx), ref, tol(dtype), "g_x")
 
 
 # --------------------------------------------------------------------------
@@ -126,7 +127,7 @@ def test_calib_accumulate(torch, dtype, B, L, C):
     torch.cuda.synchronize()
     ref = O.accumulate_autocorrelation(t2, O.accumulate_autocorrelation(t1))
     got = to_np(Cd)
-    assert rel(got, ref) <= (1e-5 if dtype == "f32" else 1e-4)
+    assert_parity(got, ref, 1e-5 if dtype == "f32" else 1e-4, "C")
     assert np.array_equal(got, got.T) or rel(got, got.T) < 1e-6
 
 
@@ -151,7 +152,7 @@ def test_calib_accumulate_batch(torch, dtype, L, dims):
     torch.cuda.synchronize()
     for t, cb, cs in zip(ts, Cb, Cs):
         ref = O.accumulate_autocorrelation(t)
-        assert rel(to_np(cb), ref) <= (1e-5 if dtype == "f32" else 1e-4)
+        assert_parity(to_np(cb), ref, 1e-5 if dtype == "f32" else 1e-4, "C (batched)")
         # the same fp32 sums in another order: up to ~sqrt(B * Cdim) * 2^-24 apart
         assert rel(to_np(cb), to_np(cs)) <= 5e-5
 
@@ -193,5 +194,41 @@ def test_grad_w_x_matches_the_oracle(torch, dtype, B, L, Cx, Cy, Rx, Ry, accumul
     if accumulate:
         ref_w = ref_w + gw0.astype(np.float64)
     ref_x = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
-    assert rel(to_np(gw), ref_w) <= (1e-5 if dtype == "f32" else 2e-3)
-    assert rel(to_np(gx), ref_x) <= tol(dtype)
+    assert_parity(to_np(gw), ref_w, 1e-5 if dtype == "f32" else 2e-3, "g_w")
+    assert_parity(to_np(gx), ref_x, tol(dtype), "g_x")
+
+
+# --------------------------------------------------------------------------
+# grad_w through the write-streaming kernel (short contraction, K = B*Rx <= 256)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("B,Rx,Cx,Cy", [
+    (3, 8, 200, 328),       # K = 24: one partial chunk; ragged strip and row tile
+    (8, 16, 520, 1000),     # K = 128: two chunks
+    (16, 16, 264, 2056),    # K = 256: the largest contraction the kernel takes
+    (5, 8, 4104, 1544),     # 845 tiles: CTA ranges cross column strips
+    (2, 8, 38400, 128),     # one row tile per strip: x_hat reloaded for every tile
+])
+def test_grad_w_stream(torch, monkeypatch, B, Rx, Cx, Cy, accumulate):
+    monkeypatch.setenv("INSTANT_GRADW_PATH", "stream")
+    g = rng(3300 + B + Cx + Cy)
+    Sx = stored(g.standard_normal((B * Rx, Cy)), "bf16")
+    xh = stored(g.standard_normal((B, Rx, Cx)), "bf16")
+    gw0 = g.standard_normal((Cy, Cx)).astype(np.float32)
+    gw = to_dev(gw0) if accumulate else nan_like(torch, (Cy, Cx), torch.float32)
+    api = _api()
+    n0 = api.launch_count()
+    api.grad_w(to_dev(Sx), to_dev(xh), gw, B, accumulate=accumulate)
+    torch.cuda.synchronize()
+    assert api.launch_count() - n0 == 1
+    ref = O.grad_w(O.decode(Sx).reshape(B, Rx, Cy), O.decode(xh))
+    if accumulate:
+        ref = ref + gw0.astype(np.float64)
+    assert_parity(to_np(gw), ref, 2e-3, "g_w")
+    # the split-K GEMM gives the same products (fp32 sums in another order)
+    monkeypatch.setenv("INSTANT_GRADW_PATH", "gemm")
+    gw2 = to_dev(gw0) if accumulate else nan_like(torch, (Cy, Cx), torch.float32)
+    api.grad_w(to_dev(Sx), to_dev(xh), gw2, B, accumulate=accumulate)
+    torch.cuda.synchronize()
+    assert_parity(to_np(gw), to_np(gw2), 1e-5, "g_w stream vs gemm")
+    assert api.device_status() == 0

@@ -174,3 +174,38 @@ def test_mid_size_solve_converges_in_one_launch(torch, r_override):
     n0 = api.launch_count()
     api.calib_solve(C, 64, rows, eps=0.95, p=2, r_override=r_override, warm_start=True)
     assert api.launch_count() - n0 == 1
+
+
+@pytest.mark.parametrize("path", ["one_launch", "multi_launch"])
+@pytest.mark.parametrize("L", [1024, 1500, 2048])
+def test_long_solvers_match_the_oracle(torch, monkeypatch, path, L):
+    """512 < L <= 2048: the one-launch cluster solve with the basis exchanged
+    through the workspace (each CTA keeps only its own rows), and the
+    multi-launch loop, against the oracle; 1500 tokens leave the last CTA a
+    shorter share of rows."""
+    if path == "multi_launch":
+        monkeypatch.setenv("INSTANT_SOLVER_MULTI", "1")
+    lam = 5e6 * np.arange(1, L + 1, dtype=np.float64) ** -2.0 + 41.0
+    C = _planted_C(90 + L, L, lam, n=64)
+    _check(torch, C, 64, eps=0.95, p=4, r_override=16, scale_on=True, r_cap=16,
+           out_dtype=torch.bfloat16)
+    _check(torch, C, 64, eps=0.95, p=2, r_override=8, scale_on=False, r_cap=8,
+           out_dtype=torch.float32)
+
+
+@pytest.mark.parametrize("r_override", [8, 16])
+def test_long_solve_converges_in_one_launch(torch, r_override):
+    from rank_compressed_backprop_gb300 import api
+
+    L = 2048
+    lam = 5e6 * np.arange(1, L + 1, dtype=np.float64) ** -2.0 + 41.0
+    C = to_dev(_planted_C(95, L, lam, n=64))
+    rows = torch.empty(r_override, L, dtype=torch.bfloat16, device="cuda")
+    n0 = api.launch_count()
+    res = api.calib_solve(C, 64, rows, eps=0.95, p=4, r_override=r_override)
+    assert api.launch_count() - n0 == 1
+    assert res.R == r_override
+    n0 = api.launch_count()
+    api.calib_solve(C, 64, rows, eps=0.95, p=4, r_override=r_override, warm_start=True)
+    assert api.launch_count() - n0 == 1
+    assert api.device_status() == 0

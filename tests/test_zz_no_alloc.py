@@ -10,7 +10,9 @@ import ctypes
 import numpy as np
 import pytest
 
-from gpu_util import orthonormal_rows, rel, rng, stored, to_dev, to_np, tol, torch_or_skip
+import oracle as O
+from gpu_util import (assert_parity, nan_like, orthonormal_rows, rng, stored, to_dev, to_np, tol,
+                      torch_or_skip)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,21 +33,21 @@ CASES = [
 
 def _inputs(torch, dtype, B, L, Cx, Cy, Ry, seed):
     g = rng(seed)
-    Sq = to_dev(stored(g.standard_normal((B * Ry, Cy)), dtype))
-    w = to_dev(stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), dtype))
-    Q = to_dev(stored(orthonormal_rows(g, Ry, L), dtype))
-    return Sq, w, Q
+    host = (stored(g.standard_normal((B * Ry, Cy)), dtype),
+            stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), dtype),
+            stored(orthonormal_rows(g, Ry, L), dtype))
+    return tuple(to_dev(a) for a in host), host
 
 
 @pytest.mark.parametrize("dtype,B,L,Cx,Cy,Ry", CASES)
 def test_static_scratch_matches_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
     from rank_compressed_backprop_gb300 import api
 
-    Sq, w, Q = _inputs(torch, dtype, B, L, Cx, Cy, Ry, 9100 + B + Ry)
+    (Sq, w, Q), (Sq_h, w_h, Q_h) = _inputs(torch, dtype, B, L, Cx, Cy, Ry, 9100 + B + Ry)
     tdt = Sq.dtype
     ws = torch.empty(max(api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, tdt), 16), dtype=torch.uint8,
                      device="cuda")
-    ref = torch.empty(B, L, Cx, dtype=tdt, device="cuda")
+    ref = nan_like(torch, (B, L, Cx), tdt)
     api.grad_x(Sq, w, Q, ref, ws)
     first = torch.full((B, L, Cx), float("nan"), dtype=tdt, device="cuda")
     second = torch.full((B, L, Cx), float("nan"), dtype=tdt, device="cuda")
@@ -59,12 +61,32 @@ def test_static_scratch_matches_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
 
     assert _lib.lib().instant_device_status(1, None) == 0
     r = to_np(ref)
+    oracle = O.grad_x(O.decode(Sq_h).reshape(B, Ry, Cy), w_h, Q_h)
+    assert_parity(r, oracle, tol(dtype), "grad_x vs oracle")
     for out in (first, second):
         o = to_np(out)
-        assert np.isfinite(o).all()
-        assert rel(o, r) <= tol(dtype)
+        assert_parity(o, r, tol(dtype), "grad_x_static vs grad_x")
+        assert_parity(o, oracle, tol(dtype), "grad_x_static vs oracle")
     # the two calls in a row run the same kernels on the same inputs
     assert torch.equal(first, second)
+
+
+def test_static_scratch_rejects_a_misaligned_output_before_launching(torch):
+    from rank_compressed_backprop_gb300._lib import lib
+
+    B, L, Cx, Cy, Ry = 2, 64, 256, 256, 8
+    (Sq, w, Q), _ = _inputs(torch, "bf16", B, L, Cx, Cy, Ry, 9200)
+    buf = torch.full((B * L * Cx + 8,), 3.0, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    n0 = lib().instant_launch_count()
+    st = lib().instant_grad_x_static(ctypes.c_void_p(Sq.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                     ctypes.c_void_p(Q.data_ptr()),
+                                     ctypes.c_void_p(buf.data_ptr() + 2),   # 2 bytes off
+                                     B, L, Cx, Cy, Ry, 1, None)
+    assert st == 4                                                     # INSTANT_ERR_ALIGN
+    assert lib().instant_launch_count() == n0
+    torch.cuda.synchronize()
+    assert bool((buf == 3.0).all())
 
 
 def test_static_scratch_rejects_sizes_beyond_the_array(torch):
