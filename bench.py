@@ -1,15 +1,21 @@
 """Benchmark of the INSTANT low-rank linear backward on one GB300 (or N replicas).
 
-A step is one training step of a BERT-base-block-shaped linear layer
-(B=32, L=512, Cx=Cy=768, Rx=Ry=8, bf16 with fp32 accumulation) through every
-row of the hot path: activation compression (x_hat = P x), the one-read
-gradient projection, g_w, g_hat_x and the rank-R expansion, captured as one
-CUDA graph per rotating buffer set; every N_t steps (default 100, counted from
-the first timed step) the calibration phase runs eagerly: the autocorrelation
-statistics of the step's batch plus one resident calibration batch (64 samples)
-and the two eigen-solves that rewrite [P; Q].
+Headline workload: the long-sequence wide linear (4096 -> 11008, B=4, L=2048,
+Rx=Ry=16, bf16 with fp32 accumulation, planted spectrum sigma_i ~ 1/i).  A step
+is one training step of the layer through every row of the hot path:
+activation compression (x_hat = P x), the one-read gradient projection, g_w,
+g_hat_x and the rank-R expansion, captured as CUDA graphs over rotating buffer
+sets.  Every N_t steps (default 100) the calibration phase runs eagerly: the
+autocorrelation statistics of 64 samples (the step's batch plus resident
+calibration samples) and the two eigen-solves that rewrite [P; Q].  It is
+charged at 1/N_t of its measured time per step; the oracle arm charges its own
+calibration the same way.
 
-Output: one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+The BERT-base block, the BERT FFN pair and the ViT-MLP pair are measured the
+same way (without the end-to-end and CPU legs) and reported under
+``detail.workloads``.
+
+Output: one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
 """
 
@@ -18,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -31,29 +38,33 @@ if ROOT not in sys.path:
 
 METRIC = "low-rank linear-backward layers/s and achieved HBM GB/s (% of roofline) on 1 GB300"
 UNIT = "layers/s"
-WORKLOAD = "bert_base_block"
-NSETS = 8
+HEADLINE = "long_seq_4096_11008"
+DETAIL_WORKLOADS = "bert_base_block,bert_ffn_pair,vit_mlp_pair_49"
+L2_BYTES = 129 << 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--detail-workloads", default=DETAIL_WORKLOADS,
+                    help="comma-separated workloads measured for detail.workloads ('' for none)")
     ap.add_argument("--nt", type=int, default=100, help="recalibration period N_t")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-iters", type=int, default=400)
-    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--cpu-baseline-only", action="store_true",
                     help="print the oracle's cpu_baseline object and exit (no GPU)")
     ap.add_argument("--mode", choices=["bench", "kernels", "drift"], default="bench",
                     help="kernels: after a first (cold) calibration, run one recalibration "
-                         "period of the timed loop eagerly -- a warm-started calibration and "
-                         "N_t steps -- and exit (the case ncu captures); prints the number of "
-                         "library launches before the period as 'skip=N'; drift: the "
-                         "oversampling study on the drifting ViT-MLP workload (reconstruction "
-                         "error per step for p in 0,2,4 and N_t in 5,10,100)")
+                         "period eagerly -- a warm-started calibration and N_t steps -- and "
+                         "exit (the case ncu captures); prints the number of library launches "
+                         "before the period as 'skip=N'; drift: the oversampling study on the "
+                         "drifting ViT-MLP workload (reconstruction error per step for p in "
+                         "0,2,4 and N_t in 5,10,100)")
     return ap.parse_args()
 
 
@@ -100,10 +111,11 @@ def aggregate(elapsed_s: float, units_per_rank: float, world: int, device=None):
 
 
 # ---------------------------------------------------------------------------
-# helpers
+# algorithmic bytes and flops per launch (compulsory reads + writes, bf16
+# tensors and fp32 g_w; the intermediates Sx, Sq, g_hat_x count where a
+# launch reads or writes them through HBM)
 # ---------------------------------------------------------------------------
 def layer_bytes(B, L, Cx, Cy, Rx, Ry):
-    """Compulsory HBM bytes of one step (bf16 tensors, fp32 g_w)."""
     return {
         "compress_act": B * L * Cx * 2 + Rx * L * 2 + B * Rx * Cx * 2,
         "project_grad": B * L * Cy * 2 + (Rx + Ry) * L * 2 + B * (Rx + Ry) * Cy * 2,
@@ -113,8 +125,6 @@ def layer_bytes(B, L, Cx, Cy, Rx, Ry):
         "grad_x": B * Ry * Cy * 2 + Cy * Cx * 2 + Ry * L * 2 + B * L * Cx * 2,
         "grad_w_x": (B * Rx * (Cy + Cx) * 2 + Cy * Cx * 4
                      + B * Ry * Cy * 2 + Cy * Cx * 2 + Ry * L * 2 + B * L * Cx * 2),
-        # the whole backward (one call): inputs g_y, [P; Q], x_hat, w; outputs
-        # Sx, Sq, g_w, g_x
         "backward": (B * L * Cy * 2 + (Rx + Ry) * L * 2 + B * (Rx + Ry) * Cy * 2
                      + B * Rx * Cx * 2 + Cy * Cx * 2 + Cy * Cx * 4 + B * L * Cx * 2),
     }
@@ -139,14 +149,16 @@ def measured_peaks():
     if os.path.exists(p):
         d = json.load(open(p))
         return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
 
 
 KERNEL_SOURCES = {
     "compress_act": ("project.cu", "project_tile.cuh"),
     "project_grad": ("project.cu", "project_tile.cuh"),
-    "grad_w": ("gemm.cu",), "grad_x_core": ("gemm.cu",), "expand": ("expand.cu",),
+    "grad_w": ("gemm.cu", "gradw_stream.cu"), "grad_x_core": ("gemm.cu",), "expand": ("expand.cu",),
     "grad_x": ("gradx_fused.cu", "project_tile.cuh"),
     "grad_w_x": ("gradx_fused.cu", "project_tile.cuh"),
     "backward": ("gradx_fused.cu", "project_tile.cuh"),
@@ -161,18 +173,18 @@ def source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel's
-    sources are unchanged since; else None."""
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded from an ncu capture of this kernel on
+    this workload, if the kernel's sources are unchanged since; else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
     for line in open(p):
         parts = line.split()
-        if len(parts) >= 3 and parts[0] == kernel:
-            if parts[2] != source_hash(kernel):
+        if len(parts) >= 4 and parts[0] == kernel and parts[1] == workload:
+            if parts[3] != source_hash(kernel):
                 return None
-            return float(parts[1])
+            return float(parts[2])
     return None
 
 
@@ -232,16 +244,32 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# workload
+# workloads
 # ---------------------------------------------------------------------------
-def make_workload():
+def workload_config(name: str, nt: int, world: int) -> dict:
+    """The `config` object, identical in both arms."""
     import workloads as W
 
-    wl = W.workload(WORKLOAD)
-    li = W.LayerInputs(wl)
-    B = wl.B
-    return wl, li, {"x": li.x(), "g": li.g_y(), "w": li.w(),
-                    "xc": li.calib_x(1, B), "gc": li.calib_g(1, B)}
+    wl = W.workload(name)
+    layers = [list(c) for c in wl.layers]
+    li = W.LayerInputs(wl, 0)
+    step_bytes = sum(layer_bytes(wl.B, wl.L, cx, cy, wl.Rx, wl.Ry)["compress_act"]
+                     + layer_bytes(wl.B, wl.L, cx, cy, wl.Rx, wl.Ry)["backward"]
+                     for cx, cy in wl.layers)
+    return {
+        "workload": f"{wl.name}: B={wl.B} L={wl.L} layers {layers} (Cx, Cy) Rx=Ry={wl.Rx}, bf16 "
+                    f"with fp32 accumulation, planted spectrum",
+        "name": name,
+        "B": wl.B, "L": wl.L, "Cx": li.Cx, "Cy": li.Cy, "Rx": wl.Rx, "Ry": wl.Ry,
+        "layers": layers,
+        "step": "per layer: compress_act + backward (the projection of g_y, then g_w and g_x)",
+        "calibration_every": nt,
+        "calibration_samples": wl.calib_samples, "calibration_p": wl.p, "eps": wl.eps,
+        "calibration_charge": "1/N_t of the calibration phase's measured time per step",
+        "l2": f"inputs larger than L2: one step reads and writes {step_bytes / 1e6:.0f} MB "
+              f"of compulsory traffic (L2 {L2_BYTES >> 20} MB); rotating buffer sets",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+    }
 
 
 def to_dev(a, dev):
@@ -251,11 +279,319 @@ def to_dev(a, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
 
 
+def resident_calibration(li, wl):
+    """Host chunks of the calibration samples beyond the step's own batch:
+    calib_samples - B samples in chunks of B (seeds j = 1, 2, ...)."""
+    rest = max(0, wl.calib_samples - wl.B)
+    xs, gs = [], []
+    j = 1
+    while rest > 0:
+        n = min(wl.B, rest)
+        xs.append(li.calib_x(j, n))
+        gs.append(li.calib_g(j, n))
+        rest -= n
+        j += 1
+    return xs, gs
+
+
+class LayerBench:
+    """One layer of a workload on the GPU: its InstantLinear, rotating buffer
+    sets and resident calibration samples."""
+
+    def __init__(self, wl, layer, dev, nsets_hint=None):
+        import numpy as np
+        import torch
+        import workloads as W
+        from rank_compressed_backprop_gb300 import InstantLinear
+
+        li = W.LayerInputs(wl, layer)
+        self.wl, self.li = wl, li
+        self.B, self.L, self.Rx, self.Ry = wl.B, wl.L, wl.Rx, wl.Ry
+        self.Cx, self.Cy = li.Cx, li.Cy
+        bf = torch.bfloat16
+        self.host = {"x": li.x(), "g": li.g_y(), "w": li.w()}
+        self.w = to_dev(self.host["w"], dev)
+        self.lay = InstantLinear(self.w, B=self.B, L=self.L, Rx=self.Rx, Ry=self.Ry, n_t=100,
+                                 eps=wl.eps, p=wl.p)
+        xs, gs = resident_calibration(li, wl)
+        self.xc = torch.cat([to_dev(a, dev) for a in xs]) if xs else None
+        self.gc = torch.cat([to_dev(a, dev) for a in gs]) if gs else None
+        x0, g0 = to_dev(self.host["x"], dev), to_dev(self.host["g"], dev)
+        B, L, Cx, Cy, Rx = self.B, self.L, self.Cx, self.Cy, self.Rx
+        per_set = (B * L * (Cx + Cy) * 2 + B * Rx * Cx * 2 + Cy * Cx * 4 + B * L * Cx * 2)
+        n = nsets_hint or int(min(8, max(3, math.ceil(600e6 / per_set))))
+        self.sets = []
+        for _ in range(n):
+            self.sets.append({
+                "x": x0.clone(), "g": g0.clone(),
+                "xhat": torch.empty(B, Rx, Cx, dtype=bf, device=dev),
+                "gw": torch.empty(Cy, Cx, dtype=torch.float32, device=dev),
+                "gx": torch.empty(B, L, Cx, dtype=bf, device=dev),
+            })
+        del x0, g0
+        self.set_bytes = per_set
+
+    def calibrate(self, s):
+        self.lay.accumulate(s["x"], s["g"])
+        if self.xc is not None:
+            self.lay.accumulate(self.xc, self.gc)
+        return self.lay.recalibrate()
+
+    def step(self, s):
+        self.lay.compress(s["x"], out=s["xhat"])
+        self.lay.backward(s["g"], xhat=s["xhat"], gw=s["gw"], gx=s["gx"])
+
+    def kernels(self):
+        """The library calls of the step, each alone (for per-kernel timing)."""
+        from rank_compressed_backprop_gb300 import api
+
+        lay, w, B, Rx, Ry, Cy = self.lay, self.w, self.B, self.Rx, self.Ry, self.Cy
+        ws = lay.ws_gx
+        return {
+            "compress_act": lambda s: api.compress_act(s["x"], lay.P, s["xhat"]),
+            "project_grad": lambda s: api.project_grad(s["g"], lay.PQ, lay.Sx, lay.Sq, Rx, Ry),
+            "grad_w": lambda s: api.grad_w(lay.Sx, s["xhat"], s["gw"], B),
+            "grad_x": lambda s: api.grad_x(lay.Sq, w, lay.Q, s["gx"], ws),
+            "grad_w_x": lambda s: api.grad_w_x(lay.Sx, s["xhat"], s["gw"], lay.Sq, w, lay.Q, s["gx"],
+                                               ws, B),
+            "backward": lambda s: api.backward(s["g"], lay.PQ, s["xhat"], w, lay.Sx, lay.Sq, s["gw"],
+                                               s["gx"], lay.ws_bw, Rx),
+            "grad_x_core": lambda s: api.grad_x_core(lay.Sq, w, ws, B),
+            "expand": lambda s: api.expand(lay.Q, s["gx"], ws, Cy),
+        }
+
+
+def graph_time_us(fn, sets, iters, stream):
+    """Device time per call of `fn` from a CUDA graph of back-to-back calls over
+    the rotating sets (no host launch overhead)."""
+    import torch
+
+    n = len(sets)
+    per_graph = 5 * n
+    for i in range(n):
+        fn(sets[i])
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    kg = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs):
+        with torch.cuda.graph(kg, stream=cs):
+            for i in range(per_graph):
+                fn(sets[i % n])
+    torch.cuda.current_stream().wait_stream(cs)
+    kg.replay()
+    torch.cuda.synchronize()
+    reps = max(1, iters // per_graph)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        kg.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / (reps * per_graph)
+
+
+def kernel_figures(lb, kus, peaks):
+    """Per-kernel achieved GB/s, TFLOP/s and roofline fractions: HBM fraction
+    for every kernel, and for the two dense products the fraction of
+    min(P_tc, AI * BW)."""
+    nb = layer_bytes(lb.B, lb.L, lb.Cx, lb.Cy, lb.Rx, lb.Ry)
+    nf = layer_flops(lb.B, lb.L, lb.Cx, lb.Cy, lb.Rx, lb.Ry)
+    out = {}
+    for k, us in kus.items():
+        gbs = nb[k] / (us * 1e-6) / 1e9
+        tf = nf[k] / (us * 1e-6) / 1e12
+        d = {"us": round(us, 3), "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+             "tflops": round(tf, 2)}
+        if k in ("grad_w", "grad_x_core"):
+            ai = nf[k] / nb[k]
+            bound = min(peaks["bf16_tflops"], ai * peaks["hbm_gbs"] / 1e3)
+            d["ai_flop_per_byte"] = round(ai, 1)
+            d["bound_tflops"] = round(bound, 1)
+            d["bound_frac"] = round(tf / bound, 4)
+        out[k] = d
+    return out
+
+
+def step_kernels_of(lb):
+    """The launches one step of this layer makes (compress, projection, and the
+    single fused g_w+g_x launch or its three-launch form)."""
+    from rank_compressed_backprop_gb300 import api
+
+    s = lb.sets[0]
+    c0 = api.launch_count()
+    lb.kernels()["grad_w_x"](s)
+    n = api.launch_count() - c0
+    return ["compress_act", "project_grad"] + (["grad_w_x"] if n == 1 else
+                                               ["grad_w", "grad_x_core", "expand"])
+
+
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+def measure_workload(name, args, dev, world, stream, full: bool):
+    """Builds the workload's layers and measures: the timed loop (K steps,
+    calibration every N_t charged at 1/N_t), per-kernel graph timings and the
+    calibration's parts.  Returns a dict of results (plus the layer benches)."""
+    import torch
+    import workloads as W
+    from rank_compressed_backprop_gb300 import api
+
+    wl = W.workload(name)
+    lbs = [LayerBench(wl, i, dev) for i in range(len(wl.layers))]
+    nsets = min(len(lb.sets) for lb in lbs)
+
+    def calibrate(i):
+        return [lb.calibrate(lb.sets[i % nsets]) for lb in lbs]
+
+    def step(i):
+        for lb in lbs:
+            lb.step(lb.sets[i % nsets])
+
+    cal0 = calibrate(0)
+    for i in range(nsets):
+        step(i)
+    torch.cuda.synchronize()
+    if args.mode == "kernels":
+        print(f"skip={api.launch_count()}", flush=True)
+        calibrate(0)
+        for i in range(args.nt):
+            step(i)
+        torch.cuda.synchronize()
+        if api.device_status() != 0:
+            raise RuntimeError("device status set")
+        print(f"period_launches={api.launch_count()}", flush=True)
+        return None
+    c0 = api.launch_count()
+    step(0)
+    launches_per_step = api.launch_count() - c0
+
+    # one graph runs the step on each buffer set in turn; single-step graphs
+    # cover a remainder
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    graphs = []
+    with torch.cuda.stream(cs):
+        gall = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gall, stream=cs):
+            for i in range(nsets):
+                step(i)
+        for i in range(nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                step(i)
+            graphs.append(g)
+    torch.cuda.current_stream().wait_stream(cs)
+    torch.cuda.synchronize()
+
+    def run_steps(first, count, cal_events=None):
+        """Steps first..first+count-1; with cal_events, the calibration phase
+        runs before the group holding a multiple of N_t, between two events."""
+        i, end = first, first + count
+        while i < end:
+            n = nsets if (i % nsets == 0 and end - i >= nsets) else 1
+            if cal_events is not None and any((j % args.nt) == 0 for j in range(i, i + n)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                calibrate(i)
+                e1.record(stream)
+                cal_events.append((e0, e1))
+            if n == nsets:
+                gall.replay()
+            else:
+                graphs[i % nsets].replay()
+            i += n
+
+    run_steps(0, max(args.warmup, 3))
+    calibrate(0)  # warm path of the calibration (warm-started solve)
+    torch.cuda.synchronize()
+
+    # ---- timed region ----
+    res = {"wl": wl, "lbs": lbs, "cal0": cal0, "nsets": nsets, "launches_per_step": launches_per_step}
+    cal_events = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(torch.cuda.current_device()) if full else None
+    if clk:
+        clk.__enter__()
+    barrier()
+    torch.cuda.synchronize()
+    lc0 = api.launch_count()
+    start.record(stream)
+    run_steps(0, args.steps, cal_events)
+    end.record(stream)
+    torch.cuda.synchronize()
+    lc1 = api.launch_count()
+    barrier()
+    if clk:
+        clk.__exit__(None, None, None)
+        res["clocks"] = clk.summary()
+    elapsed = start.elapsed_time(end) / 1e3
+    cal_s = sum(a.elapsed_time(b) for a, b in cal_events) / 1e3
+    n_cal = len(cal_events)
+    step_s = elapsed - cal_s
+    cal_avg = cal_s / n_cal
+    charged = step_s + cal_avg * args.steps / args.nt
+    res.update(elapsed_s=elapsed, cal_s=cal_s, n_cal=n_cal, step_s=step_s, cal_avg_s=cal_avg,
+               charged_s=charged,
+               gpu_launches=(lc1 - lc0) + launches_per_step * args.steps)
+    res["value"], res["slowest_s"] = aggregate(charged, float(args.steps), world, dev)
+
+    # ---- per-kernel device times (graphs of back-to-back launches) ----
+    peaks = measured_peaks()
+    per_layer = []
+    for li, lb in enumerate(lbs):
+        kus = {k: graph_time_us(fn, lb.sets[:nsets], args.kernel_iters, stream)
+               for k, fn in lb.kernels().items()}
+        per_layer.append({"layer": [lb.Cx, lb.Cy], "step_kernels": step_kernels_of(lb),
+                          "kernels": kernel_figures(lb, kus, peaks)})
+    res["per_layer"] = per_layer
+
+    # ---- the step graph alone ----
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nstep = max(nsets, int(200e3 / max(1.0, step_s * 1e6 / args.steps)) // nsets * nsets)
+    a.record(stream)
+    run_steps(0, nstep)
+    b.record(stream)
+    torch.cuda.synchronize()
+    res["step_graph_us"] = a.elapsed_time(b) * 1e3 / nstep
+
+    # ---- calibration parts: accumulation of every statistic (the tensor-bound
+    # step) and the solves ----
+    s0 = [lb.sets[0] for lb in lbs]
+    for lb, s in zip(lbs, s0):
+        lb.lay.accumulate(s["x"], s["g"])
+        if lb.xc is not None:
+            lb.lay.accumulate(lb.xc, lb.gc)
+    reps = 5
+    a.record(stream)
+    for _ in range(reps):
+        for lb, s in zip(lbs, s0):
+            lb.lay.accumulate(s["x"], s["g"])
+            if lb.xc is not None:
+                lb.lay.accumulate(lb.xc, lb.gc)
+    b.record(stream)
+    torch.cuda.synchronize()
+    acc_us = a.elapsed_time(b) * 1e3 / reps
+    acc_flops = sum(wl.calib_samples * wl.L * (wl.L + 1) * (lb.Cx + lb.Cy) for lb in lbs)
+    t0 = time.perf_counter()
+    for lb in lbs:
+        lb.lay.recalibrate()
+    solve_ms = (time.perf_counter() - t0) * 1e3
+    res["calibration_parts"] = {
+        "accumulate_all_statistics_us": round(acc_us, 2),
+        # upper triangle incl. the diagonal: L(L+1) flops per channel and sample
+        "accumulate_tflops": round(acc_flops / (acc_us * 1e-6) / 1e12, 1),
+        "accumulate_tensor_frac": round(acc_flops / (acc_us * 1e-6) / 1e12 / peaks["bf16_tflops"], 4),
+        "accumulate_tensor_frac_of_sustained": round(
+            acc_flops / (acc_us * 1e-6) / 1e12 / peaks["bf16_tflops_sustained"], 4),
+        "solve_all_wall_ms": round(solve_ms, 3),
+        "calibration_phase_ms": round(cal_avg * 1e3, 3),
+    }
+    if api.device_status() != 0:
+        raise RuntimeError("device status set")
+    return res
+
+
 def run_ours(args):
-    import numpy as np
     import torch
 
     rank, world, local = dist_env()
@@ -266,266 +602,104 @@ def run_ours(args):
     from rank_compressed_backprop_gb300.build import build
 
     build()
-    from rank_compressed_backprop_gb300 import InstantLinear, api
+    import workloads as W
 
-    wl, li, data = make_workload()
-    B, L, Rx, Ry = wl.B, wl.L, wl.Rx, wl.Ry
-    Cx, Cy = li.Cx, li.Cy
-    bf = torch.bfloat16
-    w = to_dev(data["w"], dev)
-    lay = InstantLinear(w, B=B, L=L, Rx=Rx, Ry=Ry, n_t=args.nt, eps=wl.eps, p=wl.p)
-    x0, g0 = to_dev(data["x"], dev), to_dev(data["g"], dev)
-    xc, gc = to_dev(data["xc"], dev), to_dev(data["gc"], dev)
-    sets = []
-    for _ in range(NSETS):
-        sets.append({
-            "x": x0.clone(), "g": g0.clone(),
-            "xhat": torch.empty(B, Rx, Cx, dtype=bf, device=dev),
-            "gw": torch.empty(Cy, Cx, dtype=torch.float32, device=dev),
-            "gx": torch.empty(B, L, Cx, dtype=bf, device=dev),
-        })
-    set_bytes = sum(t.numel() * t.element_size() for t in sets[0].values())
-
-    def calibrate(s):
-        lay.accumulate(s["x"], s["g"])
-        lay.accumulate(xc, gc)
-        return lay.recalibrate()
-
-    def step_eager(s):
-        lay.compress(s["x"], out=s["xhat"])
-        lay.backward(s["g"], xhat=s["xhat"], gw=s["gw"], gx=s["gx"])
-
-    # first calibration, then one eager step per set (sets kernel attributes)
-    cal0 = calibrate(sets[0])
-    for s in sets:
-        step_eager(s)
-    torch.cuda.synchronize()
-    if args.mode == "kernels":
-        torch.cuda.synchronize()
-        print(f"skip={api.launch_count()}", flush=True)
-        calibrate(sets[0])
-        for i in range(args.nt):
-            step_eager(sets[i % NSETS])
-        torch.cuda.synchronize()
-        if api.device_status() != 0:
-            raise RuntimeError("device status set")
-        print(f"period_launches={api.launch_count()}", flush=True)
-        return
-    launches_per_step = None
-    c0 = api.launch_count()
-    step_eager(sets[0])
-    launches_per_step = api.launch_count() - c0
-
-    # one CUDA graph runs the step on each of the NSETS buffer sets in turn (as
-    # a model's graph runs the step of each of its layers); single-step graphs
-    # cover a remainder of steps
-    graphs = []
-    cs = torch.cuda.Stream()
-    cs.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cs):
-        g8 = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g8, stream=cs):
-            for s in sets:
-                step_eager(s)
-        for s in sets:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=cs):
-                step_eager(s)
-            graphs.append(g)
-    torch.cuda.current_stream().wait_stream(cs)
-    torch.cuda.synchronize()
-
-    def run_steps(first: int, count: int, with_calibration: bool):
-        """Steps first..first+count-1; calibration before the group that
-        contains a multiple of N_t.  Returns the number of calibrations."""
-        ncal = 0
-        i = first
-        end_i = first + count
-        while i < end_i:
-            n = NSETS if (i % NSETS == 0 and end_i - i >= NSETS) else 1
-            if with_calibration and any((j % args.nt) == 0 for j in range(i, i + n)):
-                calibrate(sets[i % NSETS])
-                ncal += 1
-            if n == NSETS:
-                g8.replay()
-            else:
-                graphs[i % NSETS].replay()
-            i += n
-        return ncal
-
-    # ---- warm-up ----
-    run_steps(0, max(args.warmup, NSETS), with_calibration=False)
-    torch.cuda.synchronize()
-
-    # ---- timed region ----
     stream = torch.cuda.current_stream()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        lc0 = api.launch_count()
-        start.record(stream)
-        n_cal = run_steps(0, args.steps, with_calibration=True)
-        end.record(stream)
-        torch.cuda.synchronize()
-        lc1 = api.launch_count()
-        barrier()
-    elapsed = start.elapsed_time(end) / 1e3
-    graph_launches = launches_per_step * args.steps
-    gpu_launches = (lc1 - lc0) + graph_launches  # eager calibration launches + graph kernels
-    value, slowest = aggregate(elapsed, float(args.steps), world, dev)
-    ms_per_step = slowest * 1e3 / args.steps
-
-    # ---- per-kernel durations (eager launches on the current stream) ----
-    ws = lay.ws_gx
-    kern = {
-        "compress_act": lambda s: api.compress_act(s["x"], lay.P, s["xhat"]),
-        "project_grad": lambda s: api.project_grad(s["g"], lay.PQ, lay.Sx, lay.Sq, Rx, Ry),
-        "grad_w": lambda s: api.grad_w(lay.Sx, s["xhat"], s["gw"], B),
-        "grad_x": lambda s: api.grad_x(lay.Sq, w, lay.Q, s["gx"], ws),
-        "grad_w_x": lambda s: api.grad_w_x(lay.Sx, s["xhat"], s["gw"], lay.Sq, w, lay.Q, s["gx"], ws,
-                                           B),
-        "backward": lambda s: api.backward(s["g"], lay.PQ, s["xhat"], w, lay.Sx, lay.Sq, s["gw"],
-                                           s["gx"], lay.ws_bw, Rx),
-        "grad_x_core": lambda s: api.grad_x_core(lay.Sq, w, ws, B),
-        "expand": lambda s: api.expand(lay.Q, s["gx"], ws, Cy),
-    }
-    kus = {}
-    per_graph = 5 * NSETS
-    for name, fn in kern.items():
-        # a graph of back-to-back launches of this one kernel over the rotating
-        # sets: device time per launch without host launch overhead
-        for i in range(NSETS):
-            fn(sets[i])
-        kg = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cs):
-            with torch.cuda.graph(kg, stream=cs):
-                for i in range(per_graph):
-                    fn(sets[i % NSETS])
-        torch.cuda.current_stream().wait_stream(cs)
-        kg.replay()
-        torch.cuda.synchronize()
-        reps = max(1, args.kernel_iters // per_graph)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            kg.replay()
-        b.record(stream)
-        torch.cuda.synchronize()
-        kus[name] = a.elapsed_time(b) * 1e3 / (reps * per_graph)
-    # the step graph alone (no calibration) for context
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    run_steps(0, 2000, with_calibration=False)
-    b.record(stream)
-    torch.cuda.synchronize()
-    step_only_us = a.elapsed_time(b) * 1e3 / 2000
-    # calibration phase alone
-    t0 = time.perf_counter()
-    for i in range(5):
-        calibrate(sets[i % NSETS])
-    torch.cuda.synchronize()
-    cal_ms = (time.perf_counter() - t0) * 1e3 / 5
-    # its parts: the batched accumulation of both statistics (one launch, the
-    # tensor-bound step), and the solve of both (one launch + a synchronisation)
-    s0 = sets[0]
-    for _ in range(3):
-        lay.accumulate(s0["x"], s0["g"])
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(20):
-        lay.accumulate(s0["x"], s0["g"])
-    b.record(stream)
-    torch.cuda.synchronize()
-    acc_us = a.elapsed_time(b) * 1e3 / 20
-    t0 = time.perf_counter()
-    lay.recalibrate()
-    solve_ms = (time.perf_counter() - t0) * 1e3
-
+    r = measure_workload(args.workload, args, dev, world, stream, full=True)
+    if r is None:
+        return
+    wl, lbs = r["wl"], r["lbs"]
     peaks = measured_peaks()
-    nbytes = layer_bytes(B, L, Cx, Cy, Rx, Ry)
-    nflops = layer_flops(B, L, Cx, Cy, Rx, Ry)
-    step_kernels = ["compress_act", "project_grad", "grad_w_x"]
-    dom = max(step_kernels, key=lambda k: kus[k])
-    achieved = nbytes[dom] / (kus[dom] * 1e-6) / 1e9
+    # roofline: the longest launch of the step (all of them HBM-bound here)
+    cands = []
+    for pl, lb in zip(r["per_layer"], lbs):
+        for k in pl["step_kernels"]:
+            cands.append((pl["kernels"][k]["us"], k, lb))
+    _, dom, dlb = max(cands, key=lambda c: c[0])
+    nbytes = layer_bytes(dlb.B, dlb.L, dlb.Cx, dlb.Cy, dlb.Rx, dlb.Ry)[dom]
+    dus = [pl for pl in r["per_layer"] if pl["layer"] == [dlb.Cx, dlb.Cy]][0]["kernels"][dom]["us"]
+    achieved = nbytes / (dus * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": peaks["source"] + " (burst copy)",
-                "bytes_per_launch": nbytes[dom], "traffic": ncu_traffic(dom)}
+                "bytes_per_launch": nbytes, "us_per_launch": dus,
+                "traffic": ncu_traffic(dom, args.workload)}
 
-    # ---- end to end through the public API with host buffers ----
-    e2e = run_e2e(args, lay, data, dev, xc, gc)
+    e2e = run_e2e(args, lbs[0], dev) if len(lbs) == 1 else None
 
-    # ---- CPU baseline (the oracle as it stands) ----
     cpu = cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, data, args.nt)
-        cpu1 = cpu_baseline_1thread(args.nt)
+        cpu = cpu_baseline(args.workload, args.nt)
+        cpu1 = cpu_baseline_1thread(args.workload, args.nt)
 
-    clocks = clk.summary()
-    step_bytes = sum(nbytes[k] for k in step_kernels)
+    details = {}
+    for name in [n for n in args.detail_workloads.split(",") if n and n != args.workload]:
+        d = measure_workload(name, args, dev, world, stream, full=False)
+        details[name] = {
+            "layers_per_s": round(d["value"] * len(d["lbs"]), 2),
+            "steps_per_s": round(d["value"], 2),
+            "ms_per_step": round(d["charged_s"] * 1e3 / args.steps, 5),
+            "step_graph_us": round(d["step_graph_us"], 3),
+            "calibration_phase_ms": round(d["cal_avg_s"] * 1e3, 3),
+            "calibration_parts": d["calibration_parts"],
+            "per_layer": d["per_layer"],
+            "calibration_k": [[c.k for c in cl] for cl in d["cal0"]],
+        }
+        del d
+        torch.cuda.empty_cache()
+
+    lb = lbs[0]
+    B, L, Cx, Cy, Rx, Ry = lb.B, lb.L, lb.Cx, lb.Cy, lb.Rx, lb.Ry
+    nl = len(lbs)
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "metric": METRIC, "value": round(r["value"] * nl, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(r["slowest_s"] * 1e3 / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded planted-spectrum activations and gradients)",
-        "config": {
-            "workload": "BERT-base-block linear, B=32 L=512 Cx=Cy=768 Rx=Ry=8, sigma_i ~ i^-1.5",
-            "B": B, "L": L, "Cx": Cx, "Cy": Cy, "Rx": Rx, "Ry": Ry,
-            "step": "compress_act + backward (project_grad, then g_w and g_x in one launch); CUDA graphs of 8 steps "
-                    "(one per rotating buffer set); calibration (2x accumulate over 64 samples "
-                    "+ 2 solves) every N_t steps",
-            "calibration_every": args.nt, "calibrations_timed": n_cal,
-            "l2": f"{NSETS} rotating buffer sets of {set_bytes / 1e6:.0f} MB "
-                  f"({NSETS * set_bytes / 1e6:.0f} MB > 129 MB L2)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-        },
+        "config": workload_config(args.workload, args.nt, world),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": int(gpu_launches),
-        "clocks": clocks,
+        "gpu_launches": int(r["gpu_launches"]),
+        "clocks": r.get("clocks"),
         "detail": {
-            "kernel_us": {k: round(v, 3) for k, v in kus.items()},
-            "kernel_gbs": {k: round(nbytes[k] / (kus[k] * 1e-6) / 1e9, 1) for k in kus},
-            "step_kernels": step_kernels,
-            "kernel_tflops": {k: round(nflops[k] / (kus[k] * 1e-6) / 1e12, 2) for k in kus},
-            "step_graph_us": round(step_only_us, 3),
-            "step_graph_layers_per_s": round(1e6 / step_only_us, 1),
-            "step_algorithmic_bytes": step_bytes,
-            "step_graph_hbm_gbs": round(step_bytes / (step_only_us * 1e-6) / 1e9, 1),
-            "calibration_ms": round(cal_ms, 3),
+            "per_layer": r["per_layer"],
+            "step_graph_us": round(r["step_graph_us"], 3),
+            "step_graph_layers_per_s": round(1e6 * nl / r["step_graph_us"], 1),
+            "timed_region": {"elapsed_s": round(r["elapsed_s"], 5), "steps_s": round(r["step_s"], 5),
+                             "calibrations": r["n_cal"], "calibration_s": round(r["cal_s"], 5),
+                             "charged_s": round(r["charged_s"], 5)},
+            "buffer_sets": r["nsets"], "set_bytes": lb.set_bytes,
+            "calibration_parts": r["calibration_parts"],
             "cpu_baseline_1thread": cpu1,
-            "calibration_parts": {
-                "accumulate_x_and_g_us": round(acc_us, 2),
-                # upper triangle incl. the diagonal: L(L+1) flops per channel and sample
-                "accumulate_tflops": round(B * L * (L + 1) * (Cx + Cy) / (acc_us * 1e-6) / 1e12, 1),
-                "accumulate_tensor_frac": round(B * L * (L + 1) * (Cx + Cy) / (acc_us * 1e-6) / 1e12
-                                                / peaks["bf16_tflops"], 4),
-                "solve_both_wall_ms": round(solve_ms, 3)},
-            "launches_per_step": launches_per_step,
-            "calibration_k": [cal0[0].k, cal0[1].k],
+            "launches_per_step": r["launches_per_step"],
+            "calibration_k": [c.k for c in r["cal0"][0]],
             "flops_vanilla_per_layer": 4 * B * L * Cx * Cy,
             "flops_low_rank_per_layer": 2 * B * (Rx + Ry) * (Cx * Cy + L * Cx + L * Cy),
             "activation_memory_ratio": L / Rx,
+            "peaks": peaks,
+            "workloads": details,
         },
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
-def run_e2e(args, lay, data, dev, xc, gc):
+def run_e2e(args, lb, dev):
     """Same metric through the public API, inputs from pinned host memory and
     results read back every step.  Three streams form a pipeline over two
     device buffer sets: while step i computes (InstantLinear.compress and
     .backward), the inputs of step i+1 go up and the results of step i-1 come
     down; events keep every buffer from being overwritten before it is
-    consumed.  The calibration steps run as in the timed loop (every N_t)."""
+    consumed.  The calibration phase runs every N_t steps as in the timed
+    loop and is charged the same way (1/N_t of its time per step)."""
     import numpy as np
     import torch
 
-    x_h = torch.from_numpy(np.ascontiguousarray(data["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
-    g_h = torch.from_numpy(np.ascontiguousarray(data["g"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    lay = lb.lay
+    x_h = torch.from_numpy(np.ascontiguousarray(lb.host["x"]).view(np.int16)).view(torch.bfloat16).pin_memory()
+    g_h = torch.from_numpy(np.ascontiguousarray(lb.host["g"]).view(np.int16)).view(torch.bfloat16).pin_memory()
     nbuf = 2
     xs = [torch.empty_like(x_h, device=dev) for _ in range(nbuf)]
     gs = [torch.empty_like(g_h, device=dev) for _ in range(nbuf)]
@@ -540,6 +714,7 @@ def run_e2e(args, lay, data, dev, xc, gc):
     ev_c = [torch.cuda.Event() for _ in range(nbuf)]
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]
     steps = args.e2e_steps
+    cal_events = []
 
     def upload(i):
         k = i % nbuf
@@ -550,15 +725,22 @@ def run_e2e(args, lay, data, dev, xc, gc):
             gs[k].copy_(g_h, non_blocking=True)
             ev_in[k].record(s_in)
 
-    def compute(i):
+    def compute(i, timed):
         k = i % nbuf
         s_c.wait_event(ev_in[k])
         if i >= nbuf:
             s_c.wait_event(ev_out[k])  # step i-2's results have been read back
         if i % args.nt == 0:
+            # the step's batch plus the resident calibration samples, then the solve
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_c)
             lay.accumulate(xs[k], gs[k])
-            lay.accumulate(xc, gc)
+            if lb.xc is not None:
+                lay.accumulate(lb.xc, lb.gc)
             lay.recalibrate()
+            e1.record(s_c)
+            if timed:
+                cal_events.append((e0, e1))
         lay.compress(xs[k], out=xh[k])
         lay.backward(gs[k], xhat=xh[k], gw=gws[k], gx=gxs[k])
         ev_c[k].record(s_c)
@@ -568,15 +750,15 @@ def run_e2e(args, lay, data, dev, xc, gc):
             gx_h[k].copy_(gxs[k], non_blocking=True)
             ev_out[k].record(s_out)
 
-    def run(n, first):
+    def run(n, first, timed):
         upload(first)
         for i in range(first, first + n):
             if i + 1 < first + n:
                 upload(i + 1)
-            compute(i)
+            compute(i, timed)
         s_c.wait_event(ev_out[(first + n - 1) % nbuf])
 
-    run(4, 1)
+    run(4, 1, False)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -584,23 +766,26 @@ def run_e2e(args, lay, data, dev, xc, gc):
     a.record(s_c)
     s_in.wait_stream(s_c)
     s_out.wait_stream(s_c)
-    run(steps, 0)
+    run(steps, 0, True)
     b.record(s_c)
     torch.cuda.synchronize()
     el = a.elapsed_time(b) / 1e3
+    cal = sum(e0.elapsed_time(e1) for e0, e1 in cal_events) / 1e3
+    charged = el - cal + (cal / max(1, len(cal_events))) * steps / args.nt
     _, world, _ = dist_env()
-    val, _ = aggregate(el, float(steps), world, dev)
+    val, _ = aggregate(charged, float(steps), world, dev)
     return {"value": round(val, 2), "unit": UNIT,
             "h2d_bytes_per_step": x_h.numel() * 2 + g_h.numel() * 2,
             "d2h_bytes_per_step": gw_h[0].numel() * 4 + gx_h[0].numel() * 2,
-            "steps": steps,
+            "steps": steps, "elapsed_s": round(el, 5), "calibration_s": round(cal, 5),
             "api": "InstantLinear.compress/backward (eager); per step the inputs are copied from "
                    "pinned host memory and g_w, g_x read back into pinned host memory, pipelined "
-                   "over two buffer sets on separate copy streams"}
+                   "over two buffer sets on separate copy streams; calibration every N_t charged "
+                   "at 1/N_t"}
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle timing
+# the oracle on the host (cpu_baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def _cores():
     try:
@@ -609,58 +794,88 @@ def _cores():
         return os.cpu_count()
 
 
-def oracle_sample_step(O, data, Pb, Qb, bs):
-    O.low_rank_backward(data["x"][:bs], data["g"][:bs], data["w"], Pb, Qb)
+class OracleSample:
+    """The oracle's share of a workload: one sample of each layer's batch for
+    the step, and one sample of x and g_y for the accumulation."""
+
+    def __init__(self, name):
+        import workloads as W
+
+        self.wl = W.workload(name)
+        self.layers = []
+        for i in range(len(self.wl.layers)):
+            li = W.LayerInputs(self.wl, i, B=1)
+            self.layers.append({"x": li.x(), "g": li.g_y(), "w": li.w()})
+        self.bs = 1
+
+    def calibration(self, O, W):
+        """Accumulation time per sample (both statistics of every layer) and
+        the solve time; returns (acc_s_per_sample, solve_s, projectors)."""
+        wl = self.wl
+        t0 = time.perf_counter()
+        Cs = [(O.accumulate_autocorrelation(d["x"]), O.accumulate_autocorrelation(d["g"]))
+              for d in self.layers]
+        t_acc = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        proj = []
+        for CX, CG in Cs:
+            cx = O.calibrate(CX, self.bs, eps=wl.eps, p=wl.p, r_override=wl.Rx)
+            cg = O.calibrate(CG, self.bs, eps=wl.eps, p=wl.p, r_override=wl.Ry)
+            proj.append((W.f32_to_bf16_bits(cx["rows"]), W.f32_to_bf16_bits(cg["rows"])))
+        t_solve = time.perf_counter() - t0
+        return t_acc / self.bs, t_solve, proj
+
+    def step(self, O, proj):
+        for d, (Pb, Qb) in zip(self.layers, proj):
+            O.low_rank_backward(d["x"], d["g"], d["w"], Pb, Qb)
+
+    @property
+    def frac(self):
+        return self.bs / self.wl.B
 
 
-def oracle_calibration(O, data, wl, frac_samples):
-    import numpy as np
-
-    CX = O.accumulate_autocorrelation(data["x"][:frac_samples])
-    CX = O.accumulate_autocorrelation(data["xc"][:frac_samples], CX)
-    CG = O.accumulate_autocorrelation(data["g"][:frac_samples])
-    CG = O.accumulate_autocorrelation(data["gc"][:frac_samples], CG)
-    n = 2 * frac_samples
-    cx = O.calibrate(CX, n, eps=wl.eps, p=wl.p, r_override=wl.Rx)
-    cg = O.calibrate(CG, n, eps=wl.eps, p=wl.p, r_override=wl.Ry)
-    return cx, cg, np
-
-
-def cpu_baseline(wl, data, nt, budget_s: float = 15.0):
-    """Oracle step time on a bounded sample: bs of B samples per step and the
-    calibration on the same fraction of its 64 samples, amortised over N_t."""
+def oracle_rates(name, nt, budget_s):
+    """Oracle time of one whole step (scaled from the sample) and of one whole
+    calibration phase (the accumulation scaled to calib_samples, plus the
+    solve), on the host cores."""
     import oracle as O
     import workloads as W
 
-    bs = max(1, wl.B // 8)
-    t0 = time.perf_counter()
-    cx, cg, _ = oracle_calibration(O, data, wl, bs)
-    t_cal = time.perf_counter() - t0
-    Pb = W.f32_to_bf16_bits(cx["rows"])
-    Qb = W.f32_to_bf16_bits(cg["rows"])
+    smp = OracleSample(name)
+    acc_ps, t_solve, proj = smp.calibration(O, W)
+    t_cal = acc_ps * smp.wl.calib_samples + t_solve
+    smp.step(O, proj)  # warm
     n, t1 = 0, time.perf_counter()
     while True:
-        oracle_sample_step(O, data, Pb, Qb, bs)
+        smp.step(O, proj)
         n += 1
         if time.perf_counter() - t1 > budget_s or n >= 200:
             break
-    t_step = (time.perf_counter() - t1) / n
-    frac = bs / wl.B
-    per_layer = (t_step + t_cal / nt) / frac
-    return {"value": round(1.0 / per_layer, 4), "unit": UNIT, "cores": _cores(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle: {n} steps on {bs} of {wl.B} samples "
-                      f"({t_step:.3f} s each) + one calibration on {2 * bs} of 64 samples "
-                      f"({t_cal:.2f} s) amortised over N_t={nt}; scaled to whole layers"}
+    t_step = (time.perf_counter() - t1) / n / smp.frac
+    return smp, t_step, t_cal, acc_ps, t_solve, n
 
 
-def cpu_baseline_1thread(nt: int):
+def cpu_baseline(name, nt, budget_s: float = 10.0):
+    smp, t_step, t_cal, acc_ps, t_solve, n = oracle_rates(name, nt, budget_s)
+    per_step = t_step + t_cal / nt
+    nl = len(smp.wl.layers)
+    return {"value": round(nl / per_step, 4), "unit": UNIT, "cores": _cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle: {n} steps on {smp.bs} of {smp.wl.B} samples per layer "
+                      f"({t_step * smp.frac:.3f} s each, scaled to the batch); calibration: "
+                      f"accumulation of one sample ({acc_ps:.2f} s) scaled to "
+                      f"{smp.wl.calib_samples} + the solves ({t_solve:.2f} s), charged at 1/N_t "
+                      f"(N_t={nt})"}
+
+
+def cpu_baseline_1thread(name, nt: int):
     """The same oracle sample on one host thread (BLAS and OpenMP pinned to
     one thread in a child process, so that the parent's pools are untouched)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                NUMEXPR_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--nt", str(nt)]
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-only", "--nt", str(nt),
+           "--workload", name]
     try:
-        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
         line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
         d = json.loads(line)
         d["cores"] = 1
@@ -670,47 +885,37 @@ def cpu_baseline_1thread(nt: int):
 
 
 def run_reference(args):
-    """The oracle arm: same metric, config and unit, on the host cores."""
+    """The oracle arm: same metric, config, unit and warm-up, on the host
+    cores; K oracle steps on a one-sample share of each batch, plus the
+    calibration phase (accumulation of a sample scaled to the calibration
+    samples, and the solves) charged at 1/N_t per step as in the GPU arm."""
     rank, world, _ = dist_env()
     if rank != 0:
         return
     import oracle as O
     import workloads as W
 
-    wl, _, data = make_workload()
-    bs = max(1, wl.B // 8)
-    cx, cg, _ = oracle_calibration(O, data, wl, bs)
-    Pb, Qb = W.f32_to_bf16_bits(cx["rows"]), W.f32_to_bf16_bits(cg["rows"])
-    steps = min(args.steps, 60)
-    for _ in range(min(args.warmup, 3)):
-        oracle_sample_step(O, data, Pb, Qb, bs)
-    # the schedule of the timed loop: a calibration every N_t steps.  With
-    # fewer than N_t steps the one calibration is charged at 1/N_t per step,
-    # as in the GPU arm's period.
-    t_steps = t_cal = 0.0
-    n_cal = 0
-    for i in range(steps):
-        if i % args.nt == 0:
-            t0 = time.perf_counter()
-            cx, cg, _ = oracle_calibration(O, data, wl, bs)
-            Pb, Qb = W.f32_to_bf16_bits(cx["rows"]), W.f32_to_bf16_bits(cg["rows"])
-            t_cal += time.perf_counter() - t0
-            n_cal += 1
-        t0 = time.perf_counter()
-        oracle_sample_step(O, data, Pb, Qb, bs)
-        t_steps += time.perf_counter() - t0
-    el = t_steps + (t_cal / n_cal) * steps / args.nt
-    frac = bs / wl.B
-    value = steps * frac / el
-    sample = (f"{steps} oracle steps on {bs} of {wl.B} samples each ({t_steps / steps:.3f} s per "
-              f"step) + calibration on {2 * bs} of 64 samples ({t_cal / n_cal:.2f} s) charged at "
-              f"1/N_t per step; layers counted as fractions")
+    smp = OracleSample(args.workload)
+    acc_ps, t_solve, proj = smp.calibration(O, W)
+    t_cal = acc_ps * smp.wl.calib_samples + t_solve
+    for _ in range(args.warmup):
+        smp.step(O, proj)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        smp.step(O, proj)
+    t_steps = (time.perf_counter() - t0) / smp.frac
+    charged = t_steps + t_cal * args.steps / args.nt
+    nl = len(smp.wl.layers)
+    value = nl * args.steps / charged
+    sample = (f"{args.steps} oracle steps on {smp.bs} of {smp.wl.B} samples per layer "
+              f"({t_steps * smp.frac / args.steps:.3f} s each, scaled to the batch); calibration: "
+              f"accumulation of one sample ({acc_ps:.2f} s) scaled to {smp.wl.calib_samples} + the "
+              f"solves ({t_solve:.2f} s), charged at 1/N_t (N_t={args.nt})")
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
-           "n_gpus": world, "steps": steps, "warmup": min(args.warmup, 3),
-           "ms_per_step": round(el * 1e3 / steps, 3), "higher_is_better": True,
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(charged * 1e3 / args.steps, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": "BERT-base-block linear, B=32 L=512 Cx=Cy=768 Rx=Ry=8",
-                      "calibration_every": args.nt},
+           "config": workload_config(args.workload, args.nt, world),
            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": _cores(),
                             "kind": "oracle", "sample": sample},
            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -783,8 +988,7 @@ def run_drift(args):
 def main():
     args = parse()
     if args.cpu_baseline_only:
-        wl, _, data = make_workload()
-        print(json.dumps(cpu_baseline(wl, data, args.nt, budget_s=8.0)))
+        print(json.dumps(cpu_baseline(args.workload, args.nt, budget_s=8.0)))
         return
     if args.mode == "drift":
         run_drift(args)
