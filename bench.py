@@ -58,11 +58,15 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--cpu-baseline-only", action="store_true",
                     help="print the oracle's cpu_baseline object and exit (no GPU)")
-    ap.add_argument("--mode", choices=["bench", "kernels", "drift"], default="bench",
+    ap.add_argument("--mode", choices=["bench", "kernels", "profile", "drift"], default="bench",
                     help="kernels: after a first (cold) calibration, run one recalibration "
                          "period eagerly -- a warm-started calibration and N_t steps -- and "
                          "exit (the case ncu captures); prints the number of library launches "
-                         "before the period as 'skip=N'; drift: the oversampling study on the "
+                         "before the period as 'skip=N'; profile: each step kernel of the "
+                         "workload's first layer and one accumulation of both statistics of "
+                         "its batch, launched twice (a warm-up group, then the group a profiler "
+                         "captures), with no calibration samples resident; drift: the "
+                         "oversampling study on the "
                          "drifting ViT-MLP workload (reconstruction error per step for p in "
                          "0,2,4 and N_t in 5,10,100)")
     return ap.parse_args()
@@ -412,6 +416,44 @@ def kernel_figures(lb, kus, peaks):
     return out
 
 
+def forward_figures(lb, args, stream, peaks):
+    """The layer's forward y = x w^T with x_hat = P x from the same x tiles
+    (one launch), against the same GEMM without the side output followed by
+    compress_act (two launches); cuBLAS (torch.matmul) for context."""
+    import torch
+    from rank_compressed_backprop_gb300 import api
+
+    B, L, Cx, Cy, Rx = lb.B, lb.L, lb.Cx, lb.Cy, lb.Rx
+    lay = lb.lay
+    y = torch.empty(B, L, Cy, dtype=torch.bfloat16, device=lay.w.device)
+    ws = api.forward_workspace(B, L, Cx, Rx, torch.bfloat16, lay.w.device)
+    sets = lb.sets
+    fused = lambda s: api.forward(s["x"], lay.w, y, lay.P, s["xhat"], ws)  # noqa: E731
+    alone = lambda s: api.forward(s["x"], lay.w, y)  # noqa: E731
+
+    def separate(s):
+        api.forward(s["x"], lay.w, y)
+        api.compress_act(s["x"], lay.P, s["xhat"])
+
+    def cublas(s):
+        torch.matmul(s["x"].view(B * L, Cx), lay.w.t(), out=y.view(B * L, Cy))
+
+    n0 = api.launch_count()
+    fused(sets[0])
+    fused_launches = api.launch_count() - n0
+    iters = max(20, args.kernel_iters // 10)
+    us = {k: graph_time_us(f, sets, iters, stream)
+          for k, f in (("fused", fused), ("gemm_alone", alone), ("gemm_then_compress", separate),
+                       ("cublas_matmul", cublas))}
+    flops = 2.0 * B * L * Cx * Cy
+    out = {"launches_fused": fused_launches}
+    for k, v in us.items():
+        tf = flops / (v * 1e-6) / 1e12
+        out[k] = {"us": round(v, 2), "tflops": round(tf, 1),
+                  "tensor_frac": round(tf / peaks["bf16_tflops"], 4)}
+    return out
+
+
 def step_kernels_of(lb):
     """The launches one step of this layer makes (compress, projection, and the
     single fused g_w+g_x launch or its three-launch form)."""
@@ -626,6 +668,7 @@ def run_ours(args):
                 "traffic": ncu_traffic(dom, args.workload)}
 
     e2e = run_e2e(args, lbs[0], dev) if len(lbs) == 1 else None
+    fwd = forward_figures(lbs[0], args, stream, peaks)
 
     cpu = cpu1 = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -679,6 +722,7 @@ def run_ours(args):
             "flops_low_rank_per_layer": 2 * B * (Rx + Ry) * (Cx * Cy + L * Cx + L * Cy),
             "activation_memory_ratio": L / Rx,
             "peaks": peaks,
+            "forward": fwd,
             "workloads": details,
         },
     }
@@ -923,6 +967,54 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile(args):
+    """Two groups of the step's launches on the first layer of the workload
+    (compress_act, project_grad, grad_w, grad_x_core, expand, one accumulation
+    of both statistics of the step's batch, and the forward with x_hat), the
+    second for a profiler to capture; the projector is the one calibrated from
+    the step's own batch."""
+    import torch
+    import workloads as W
+    from rank_compressed_backprop_gb300.build import build
+
+    build()
+    from rank_compressed_backprop_gb300 import InstantLinear, api
+
+    wl = W.workload(args.workload)
+    li = W.LayerInputs(wl, 0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x, g, w = to_dev(li.x(), dev), to_dev(li.g_y(), dev), to_dev(li.w(), dev)
+    B, L, Cx, Cy, Rx, Ry = wl.B, wl.L, li.Cx, li.Cy, wl.Rx, wl.Ry
+    lay = InstantLinear(w, B=B, L=L, Rx=Rx, Ry=Ry, eps=wl.eps, p=wl.p)
+    lay.accumulate(x, g)
+    lay.recalibrate()
+    y = torch.empty(B, L, Cy, dtype=torch.bfloat16, device=dev)
+    wsf = api.forward_workspace(B, L, Cx, Rx, torch.bfloat16, dev)
+    order = ["compress_act", "project_grad", "grad_w", "grad_x_core", "expand", "accumulate",
+             "forward"]
+
+    def group():
+        api.compress_act(x, lay.P, lay.xhat)
+        api.project_grad(g, lay.PQ, lay.Sx, lay.Sq, Rx, Ry)
+        api.grad_w(lay.Sx, lay.xhat, lay.gw, B)
+        api.grad_x_core(lay.Sq, w, lay.ws_gx, B)
+        api.expand(lay.Q, lay.gx, lay.ws_gx, Cy)
+        api.calib_accumulate_batch([(x, lay.C_X), (g, lay.C_G)])
+        api.forward(x, w, y, lay.P, lay.xhat, wsf)
+
+    torch.cuda.synchronize()
+    c0 = api.launch_count()
+    group()
+    torch.cuda.synchronize()
+    per_group = api.launch_count() - c0
+    group()
+    torch.cuda.synchronize()
+    if api.device_status() != 0:
+        raise RuntimeError("device status set")
+    print(json.dumps({"mode": "profile", "workload": args.workload, "order": order,
+                      "launches_per_group": per_group}), flush=True)
+
+
 def run_drift(args):
     """Oversampling under subspace drift: per-step ||g - Q^T Q g|| / ||g|| on the
     first layer of the drifting ViT-MLP workload, for p in {0, 2, 4} and
@@ -992,6 +1084,8 @@ def main():
         return
     if args.mode == "drift":
         run_drift(args)
+    elif args.mode == "profile":
+        run_profile(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -84,6 +84,32 @@ instant_status instant_compress_act(const void* x, const void* P, void* xhat,
                                     instant_dtype dt, void* stream);
 
 /*
+ * The layer's forward with the stored activation computed on the way
+ * (整体框架: the forward product y = x w^T is unchanged, and the layer keeps
+ * x_hat = P x for its backward instead of x):
+ *   y_b = x_b w^T,   x_hat_b = P x_b   (P may be NULL with Rx = 0: y only)
+ *   x     [B, L, Cx]  dtype dt (read)      w  [Cy, Cx] dtype dt (read)
+ *   P     [Rx, L]     dtype dt (read)      y  [B, L, Cy] dtype dt (written)
+ *   xhat  [B, Rx, Cx] dtype dt (written)
+ *   ws    device scratch of instant_forward_workspace_bytes(B, L, Cx, Rx, dt)
+ *         bytes, ZEROED by the caller before its first use; every call leaves
+ *         it zero again (fp32 partial sums of x_hat and per-sample counters),
+ *         so one workspace serves every later call.  Calls that share a
+ *         workspace must not overlap in time.
+ * bf16: a persistent tcgen05 GEMM (128 x 192 tiles, fp32 accumulation, bf16
+ * y); where L % 128 == 0, Cx % 128 == 0 and Rx <= 32, the tiles of the first column strip
+ * also contract the x tiles they have staged with P, so x is read from HBM
+ * once for both products; otherwise x_hat comes from instant_compress_act's
+ * kernel after the GEMM (two launches).  x_hat is formed in fp32 and rounded
+ * once to bf16, as by instant_compress_act.  f32: plain FFMA kernels.
+ * Limits: 0 <= Rx <= 64; bf16 rows 16-byte aligned (Cx, Cy multiples of 8).
+ */
+instant_status instant_forward(const void* x, const void* w, const void* P, void* y, void* xhat,
+                               void* ws, size_t ws_bytes, int B, int L, int Cx, int Cy, int Rx,
+                               instant_dtype dt, void* stream);
+size_t instant_forward_workspace_bytes(int B, int L, int Cx, int Rx, instant_dtype dt);
+
+/*
  * Gradient projection with one read of g_y (关键设计 3):
  *   Sx_b = P g_y,b  (so g_hat_y1,b = Sx_b^T)    Sq_b = Q g_y,b  (g_hat_y2,b)
  *   gy  [B, L, Cy]      dtype dt (read)

@@ -86,6 +86,8 @@ _PROTOS = {
     "instant_grad_w": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x": (_i, [_vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
     "instant_grad_x_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "instant_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i, _vp]),
+    "instant_forward_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "instant_grad_w_x": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _i, _i, _i, _i, _i, _i,
                               _i, _vp]),
     "instant_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _i, _i, _i, _i,

@@ -17,6 +17,8 @@ from ._lib import (GRAD_X_STATIC_SCRATCH_BYTES, INSTANT_BF16, INSTANT_F32, Accum
 
 __all__ = [
     "compress_act",
+    "forward",
+    "forward_workspace",
     "project_grad",
     "grad_w",
     "grad_x",
@@ -85,6 +87,37 @@ def compress_act(x: torch.Tensor, P: torch.Tensor, xhat: torch.Tensor, stream=No
     check(lib().instant_compress_act(_dev(x, "x"), _dev(P, "P"), _dev(xhat, "xhat"), B, L, Cx, Rx,
                                      dtype_code(x.dtype), _stream(stream)), "instant_compress_act")
     return xhat
+
+
+def forward_workspace(B: int, L: int, Cx: int, Rx: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """A zeroed workspace for :func:`forward` (it must start at zero; every call
+    leaves it zero)."""
+    n = int(lib().instant_forward_workspace_bytes(B, L, Cx, Rx, dtype_code(dtype)))
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def forward(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, P: torch.Tensor | None = None,
+            xhat: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """``y[b] = x[b] w^T`` and, with ``P``, ``xhat[b] = P x[b]`` in the same pass:
+    x ``[B, L, Cx]``, w ``[Cy, Cx]``, y ``[B, L, Cy]``, P ``[Rx, L]``,
+    xhat ``[B, Rx, Cx]``; ws from :func:`forward_workspace`."""
+    B, L, Cx = x.shape
+    Cy = w.shape[0]
+    if w.shape != (Cy, Cx) or y.shape != (B, L, Cy):
+        raise ValueError("forward: inconsistent shapes")
+    Rx = 0
+    if P is not None:
+        Rx = P.shape[0]
+        if P.shape != (Rx, L) or xhat is None or xhat.shape != (B, Rx, Cx) or ws is None:
+            raise ValueError("forward: P needs xhat [B, Rx, Cx] and a workspace")
+        _same_dtype(x.dtype, ("P", P), ("xhat", xhat))
+    _same_dtype(x.dtype, ("w", w), ("y", y))
+    check(lib().instant_forward(_dev(x, "x"), _dev(w, "w"), _dev(P, "P") if P is not None else None,
+                                _dev(y, "y"), _dev(xhat, "xhat") if P is not None else None,
+                                _dev(ws, "ws") if ws is not None else None,
+                                ws.numel() * ws.element_size() if ws is not None else 0, B, L, Cx,
+                                Cy, Rx, dtype_code(x.dtype), _stream(stream)), "instant_forward")
+    return y, xhat
 
 
 def project_grad(g_y: torch.Tensor, PQ: torch.Tensor, Sx: torch.Tensor, Sq: torch.Tensor,

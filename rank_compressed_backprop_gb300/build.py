@@ -20,7 +20,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libinstant.so")
 
 SOURCES = ["capi.cu", "project.cu", "gemm.cu", "expand.cu", "gradx_fused.cu", "syrk.cu", "eig.cu",
-           "static_scratch.cu", "recon.cu", "gradw_stream.cu"]
+           "static_scratch.cu", "recon.cu", "gradw_stream.cu",
+           "forward.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

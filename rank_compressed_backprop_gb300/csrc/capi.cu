@@ -118,10 +118,34 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   a.pq = pq;
   a.out0 = out0;
   a.out1 = out1;
+  // token split: when the (sample, 128-column) tiles leave SMs idle or
+  // unevenly loaded, up to four CTAs of a cluster share each tile's token axis
+  // (every share at least 8 chunks of 64 tokens) and reduce their fp32 partial
+  // sums through distributed shared memory.  INSTANT_PROJ_SPLIT=S forces S.
+  {
+    const long long tiles = static_cast<long long>(B) * cdiv(C, 128);
+    a.split = 1;
+    while (a.split < 4 && tiles * a.split < 2ll * sm_count() && a.nk / (a.split + 1) >= 8) ++a.split;
+    if (const char* v = std::getenv("INSTANT_PROJ_SPLIT")) {
+      const int f = std::atoi(v);
+      if (f >= 1 && f <= 4) a.split = std::min(f, std::max(1, a.nk));
+    }
+    // short token axes: several samples per CTA (about 4 chunks of work per
+    // CTA) while the grid still fills two CTAs per SM.  INSTANT_PROJ_SPB=n forces n.
+    a.spb = 1;
+    if (a.split == 1) {
+      const long long room = tiles / (2ll * sm_count());
+      a.spb = static_cast<int>(std::max(1ll, std::min<long long>(cdiv(4, a.nk), room)));
+      if (const char* v = std::getenv("INSTANT_PROJ_SPB")) {
+        const int f = std::atoi(v);
+        if (f >= 1) a.spb = std::min(f, B);
+      }
+    }
+  }
   // L2 prefetch: the whole tile while the grid's prefetches stay within a
   // quarter of L2 (all of a BERT-base batch), else the ring's worth
   {
-    const long long ctas = static_cast<long long>(B) * cdiv(C, 128);
+    const long long ctas = static_cast<long long>(B) * cdiv(C, 128) * a.split;
     const long long budget = (32ll << 20) / std::max(1ll, ctas) / (128 * 64 * 2);
     a.pf_chunks = static_cast<int>(std::min<long long>(a.nk, std::max<long long>(kProjectStages, budget)));
   }
@@ -320,6 +344,8 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
     a.out1 = const_cast<void*>(Sq);
     a.pq_tma = (L % 8 == 0 && aligned16(pp->PQ)) ? 1 : 0;
     a.pf_chunks = 0;  // its tiles start after the wait
+    a.split = 1;
+    a.spb = 1;
     if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) {
       if (no_room) *no_room = true;
       return INSTANT_ERR_SHAPE;
@@ -641,6 +667,84 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   return from_cuda(launch_gemm_bf16(ma, mb, g, st));
 }
 
+size_t instant_forward_workspace_bytes(int B, int L, int Cx, int Rx, instant_dtype dt) {
+  (void)L;
+  if (B < 1 || Cx < 1 || Rx < 0 || !dtype_ok(dt)) return 0;
+  if (dt == INSTANT_F32 || Rx == 0) return 16;
+  // fp32 x_hat accumulation [B, Rx, Cx], then one counter per sample
+  return ((static_cast<size_t>(B) * Rx * Cx * 4 + 255) & ~static_cast<size_t>(255)) +
+         ((static_cast<size_t>(B) * 4 + 255) & ~static_cast<size_t>(255));
+}
+
+instant_status instant_forward(const void* x, const void* w, const void* P, void* y, void* xhat,
+                               void* ws, size_t ws_bytes, int B, int L, int Cx, int Cy, int Rx,
+                               instant_dtype dt, void* stream) {
+  if (!dtype_ok(dt)) return INSTANT_ERR_DTYPE;
+  if (!x || !w || !y || (Rx > 0 && (!P || !xhat))) return INSTANT_ERR_ARG;
+  if (B < 1 || L < 1 || Cx < 1 || Cy < 1 || Rx < 0 || Rx > 64) return INSTANT_ERR_SHAPE;
+  if (Rx > 0 && (!ws || ws_bytes < instant_forward_workspace_bytes(B, L, Cx, Rx, dt)))
+    return INSTANT_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long M = static_cast<long long>(B) * L;
+  if (M > 0x7fffffffll) return INSTANT_ERR_SHAPE;
+  if (dt == INSTANT_F32) {
+    if (launch_forward_f32(static_cast<const float*>(x), static_cast<const float*>(w),
+                           static_cast<float*>(y), static_cast<int>(M), Cy, Cx, st) != cudaSuccess)
+      return INSTANT_ERR_CUDA;
+    return Rx > 0 ? project(x, P, xhat, nullptr, B, L, Cx, Rx, 0, dt, st) : INSTANT_OK;
+  }
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || Cx % 8 != 0 || Cy % 8 != 0 ||
+      (Rx > 0 && (!aligned16(xhat) || !aligned16(ws))))
+    return INSTANT_ERR_ALIGN;
+  // x_hat from the GEMM's own x tiles when a 128-token tile never straddles
+  // two samples, the channels come in pairs of 64-channel chunks and the rows
+  // fit the small accumulator; otherwise the forward GEMM and then the
+  // projection kernel
+  const bool side = Rx > 0 && L % 128 == 0 && Cx % 128 == 0 && Rx <= 32 && aligned16(P) &&
+                    !std::getenv("INSTANT_NO_FUSED_FORWARD");
+  ForwardArgs a;
+  a.M = static_cast<int>(M);
+  a.N = Cy;
+  a.K = Cx;
+  a.mt = cdiv(a.M, 128);
+  a.nt = cdiv(Cy, kForwardBN);
+  a.nkc = cdiv(Cx, 64);
+  a.group = 16;
+  a.Rx = side ? Rx : 0;
+  a.L = L;
+  a.xh32 = side ? static_cast<float*>(ws) : nullptr;
+  a.xh = side ? xhat : nullptr;
+  a.cnt = side ? reinterpret_cast<unsigned int*>(
+                     static_cast<uint8_t*>(ws) +
+                     ((static_cast<size_t>(B) * Rx * Cx * 4 + 255) & ~static_cast<size_t>(255)))
+               : nullptr;
+  CUtensorMap mx, mw, my, mp;
+  std::memset(&mp, 0, sizeof(mp));
+  const uint64_t dx[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(M)};
+  const uint64_t sx[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bx[2] = {64, 128};
+  const uint64_t dw[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
+  const uint64_t sw[1] = {static_cast<uint64_t>(Cx) * 2};
+  const uint32_t bw[2] = {64, static_cast<uint32_t>(kForwardBN)};
+  const uint64_t dy[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(M)};
+  const uint64_t sy[1] = {static_cast<uint64_t>(Cy) * 2};
+  const uint32_t by[2] = {64, 128};
+  if (!make_map(&mx, x, 2, dx, sx, bx) || !make_map(&mw, w, 2, dw, sw, bw) ||
+      !make_map(&my, y, 2, dy, sy, by))
+    return INSTANT_ERR_CUDA;
+  if (side) {
+    const uint64_t dp[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Rx)};
+    const uint64_t sp[1] = {static_cast<uint64_t>(L) * 2};
+    const uint32_t bp[2] = {64, static_cast<uint32_t>(Rx)};
+    if (!make_map(&mp, P, 2, dp, sp, bp)) return INSTANT_ERR_CUDA;
+  }
+  const long long tiles = static_cast<long long>(a.mt) * a.nt;
+  const int ctas = static_cast<int>(std::min<long long>(tiles, sm_count()));
+  if (launch_forward_bf16(mx, mw, my, mp, a, ctas, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+  if (Rx > 0 && !side) return project(x, P, xhat, nullptr, B, L, Cx, Rx, 0, dt, st);
+  return INSTANT_OK;
+}
+
 size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt) {
   (void)L;
   if (B < 1 || Cx < 1 || Cy < 1 || Ry < 1 || !dtype_ok(dt)) return 0;
@@ -737,11 +841,22 @@ instant_status plan_expand(const void* Q, void* gx, const void* ws, size_t ws_by
   e.out = gx;
   e.q_tma = 0;
   e.BN = 128;
+  e.spb = 1;
   pl->f32 = dt == INSTANT_F32;
   if (pl->f32) return INSTANT_OK;
   if (!aligned16(gx) || !aligned16(ws) || Cx % 8 != 0) return INSTANT_ERR_ALIGN;
   // column strip width: keep at least ~1.5 strips per SM
   e.BN = cdiv(Cx, 128) * B >= 3 * sm_count() / 2 ? 128 : 64;
+  // short token axes: several samples per CTA (about 4 token tiles of work per
+  // CTA) while the grid still fills two CTAs per SM.  INSTANT_EXPAND_SPB=n forces n.
+  {
+    const long long room = static_cast<long long>(cdiv(Cx, e.BN)) * B / (2ll * sm_count());
+    e.spb = static_cast<int>(std::max(1ll, std::min<long long>(cdiv(4, e.nlt), room)));
+    if (const char* v = std::getenv("INSTANT_EXPAND_SPB")) {
+      const int f = std::atoi(v);
+      if (f >= 1) e.spb = std::min(f, B);
+    }
+  }
   e.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
   std::memset(&pl->mq, 0, sizeof(pl->mq));
   if (e.q_tma) {
@@ -1114,6 +1229,8 @@ instant_status instant_device_status(int clear, void* stream) {
   if (read_fault_fused(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   if (read_fault_gradw(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
+  total |= v;
+  if (read_fault_forward(&v, clear) != cudaSuccess) return INSTANT_ERR_CUDA;
   total |= v;
   return total ? INSTANT_ERR_DEVICE : INSTANT_OK;
 }

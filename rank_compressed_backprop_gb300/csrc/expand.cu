@@ -7,11 +7,12 @@
 // element the FFMA pipes cannot keep up with the write stream at Ry >= 8, so
 // the contraction runs on the tensor cores.
 //
-// One CTA owns one (sample, BN-column) strip of the output and walks its
-// 128-token tiles:
-//   warp 0  TMA producer: the strip's g_hat_x block once (MN-major B operand),
-//           then Q^T tiles (MN-major A operand, read straight from Q [Ry, L])
-//           through a 4-stage ring;
+// One CTA owns one BN-column strip of the output for one sample (or a few
+// consecutive samples when the token axis is short) and walks its 128-token
+// tiles:
+//   warp 0  TMA producer: the strip's g_hat_x block once per sample (MN-major
+//           B operand, two buffers), then Q^T tiles (MN-major A operand, read
+//           straight from Q [Ry, L]) through a ring;
 //   warp 1  MMA issuer: one K = Ry (padded to 16) tcgen05 MMA chain per tile
 //           into one of two TMEM accumulators (double buffered);
 //   warps 2-9  epilogue (two warps per TMEM lane quarter, split by columns):
@@ -39,7 +40,7 @@ __host__ __device__ inline Lay expand_layout(int BN, int KR) {
   l.stg = 0;
   l.b = 4 * (BN / 64) * BOX;
   l.b_bytes = (BN / 64) * KR * 128;
-  l.a = l.b + l.b_bytes;
+  l.a = l.b + 2 * l.b_bytes;  // two g_hat_x strips: the next sample's loads early
   l.a_stage = 2 * KR * 128;
   l.bar = l.a + kExpandStages * l.a_stage;
   l.total = l.bar + 256;
@@ -62,15 +63,20 @@ __global__ void __launch_bounds__(320, 2)
   uint8_t* sA = smem + lay.a;
   uint64_t* a_full = reinterpret_cast<uint64_t*>(smem + lay.bar);
   uint64_t* a_empty = a_full + kExpandStages;
-  uint64_t* b_full = a_empty + kExpandStages;
-  uint64_t* t_full = b_full + 1;
+  uint64_t* b_full = a_empty + kExpandStages;   // [2]
+  uint64_t* b_empty = b_full + 2;               // [2]
+  uint64_t* t_full = b_empty + 2;
   uint64_t* t_empty = t_full + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(t_empty + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BN;
-  const int b = blockIdx.y;
+  // samples b0 .. b1-1 of this CTA, each walked over its token tiles: job j is
+  // (sample b0 + j / nlt, token tile j % nlt)
+  const int b0 = blockIdx.y * e.spb;
+  const int b1 = min(e.B, b0 + e.spb);
+  const int njobs = (b1 - b0) * e.nlt;
   const int KR = e.KR;
 
   if (threadIdx.x == 0) {
@@ -78,8 +84,9 @@ __global__ void __launch_bounds__(320, 2)
       mbar_init(&a_full[s], 1);
       mbar_init(&a_empty[s], 1);
     }
-    mbar_init(b_full, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
       mbar_init(&t_full[i], 1);
       mbar_init(&t_empty[i], 4);  // one arrival per warp of the epilogue group
     }
@@ -98,21 +105,58 @@ __global__ void __launch_bounds__(320, 2)
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
   pdl_wait();
+  // Q^T tiles filled by threads (no TMA: L % 8 != 0) stay resident when they
+  // all fit the ring: every sample of the CTA reuses them
+  const bool res = !e.q_tma && e.nlt <= kExpandStages;
+  if (res) {
+    const uint16_t* Q = static_cast<const uint16_t*>(e.Q);
+    for (int idx = threadIdx.x; idx < e.nlt * KR * BM; idx += blockDim.x) {
+      const int t = idx / (KR * BM);
+      const int rem = idx - t * (KR * BM);
+      const int r = rem / BM;
+      const int ll = rem - r * BM;
+      const int l = t * BM + ll;
+      const uint16_t v = (r < e.Ry && l < e.L) ? Q[static_cast<size_t>(r) * e.L + l] : 0;
+      *reinterpret_cast<uint16_t*>(sA + t * lay.a_stage + (ll >> 6) * KR * 128 + sw128_offset(r, ll & 63)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+  }
 
   if (warp == 0) {
     // ---------------- producer ----------------
-    if (lane == 0) {
-      mbar_arrive_expect_tx(b_full, lay.b_bytes);
-      for (int h = 0; h < BN / 64; ++h)
-        tma_load_3d(sB + h * KR * 128, &tmap_g, b_full, n0 + 64 * h, 0, b);
-    }
     const uint16_t* Q = static_cast<const uint16_t*>(e.Q);
-    int issued = 0;
-    for (int lt = 0; lt < e.nlt; ++lt) {
-      const int s = lt % kExpandStages;
-      bool ok = true;
-      if (lane == 0 && lt >= kExpandStages &&
-          !mbar_wait(&a_empty[s], ((lt / kExpandStages) - 1) & 1)) {
+    int issued = 0, nb = 0;
+    int s = 0, par = 0;     // ring slot and round parity of job j
+    int lt = 0, sj = 0;     // token tile and sample index (within the CTA) of job j
+    bool ok = true;
+    for (int j = 0; ok && j < njobs; ++j) {
+      if (lt == 0) {
+        // the g_hat_x strip of sample b0 + sj into buffer sj & 1
+        if (lane == 0) {
+          const int bi = sj & 1;
+          if (sj >= 2 && !mbar_wait(&b_empty[bi], ((sj >> 1) - 1) & 1)) {
+            raise_fault(FAULT_WAIT_EMPTY);
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(&b_full[bi], lay.b_bytes);
+            for (int h = 0; h < BN / 64; ++h)
+              tma_load_3d(sB + bi * lay.b_bytes + h * KR * 128, &tmap_g, &b_full[bi], n0 + 64 * h, 0,
+                          b0 + sj);
+            ++nb;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+      if (res) {
+        if (++lt == e.nlt) {
+          lt = 0;
+          ++sj;
+        }
+        continue;
+      }
+      if (lane == 0 && j >= kExpandStages && !mbar_wait(&a_empty[s], par ^ 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         ok = false;
       }
@@ -140,53 +184,79 @@ __global__ void __launch_bounds__(320, 2)
         if (lane == 0) mbar_arrive(&a_full[s]);
       }
       ++issued;
+      if (++s == kExpandStages) {
+        s = 0;
+        par ^= 1;
+      }
+      if (++lt == e.nlt) {
+        lt = 0;
+        ++sj;
+      }
     }
     if (lane == 0) {
-      for (int lt = issued - kExpandStages < 0 ? 0 : issued - kExpandStages; lt < issued; ++lt)
-        if (!mbar_wait(&a_full[lt % kExpandStages], (lt / kExpandStages) & 1))
-          raise_fault(FAULT_WAIT_FULL);
-      if (!mbar_wait(b_full, 0)) raise_fault(FAULT_WAIT_FULL);
+      for (int k = 0; k < kExpandStages && k < issued; ++k) {
+        if (--s < 0) {
+          s = kExpandStages - 1;
+          par ^= 1;
+        }
+        if (!mbar_wait(&a_full[s], par)) raise_fault(FAULT_WAIT_FULL);
+      }
+      if (nb > 0 && !mbar_wait(&b_full[(nb - 1) & 1], ((nb - 1) >> 1) & 1)) raise_fault(FAULT_WAIT_FULL);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN, /*a_mn=*/1, /*b_mn=*/1);
-      bool ok = mbar_wait(b_full, 0);
-      if (!ok) raise_fault(FAULT_WAIT_FULL);
-      const uint32_t b_base = smem_u32(sB);
-      for (int lt = 0; ok && lt < e.nlt; ++lt) {
-        const int s = lt % kExpandStages;
-        const int buf = lt & 1;
-        if (lt >= 2 && !mbar_wait(&t_empty[buf], ((lt >> 1) - 1) & 1)) {
+      int s = 0, par = 0, lt = 0, sj = 0;
+      for (int j = 0; j < njobs; ++j) {
+        const int bi = sj & 1;
+        if (lt == 0 && !mbar_wait(&b_full[bi], (sj >> 1) & 1)) {
+          raise_fault(FAULT_WAIT_FULL);
+          break;
+        }
+        const int buf = j & 1;
+        if (j >= 2 && !mbar_wait(&t_empty[buf], ((j >> 1) - 1) & 1)) {
           raise_fault(FAULT_WAIT_EMPTY);
           break;
         }
-        if (!mbar_wait(&a_full[s], (lt / kExpandStages) & 1)) {
+        if (!res && !mbar_wait(&a_full[s], par)) {
           raise_fault(FAULT_WAIT_FULL);
           break;
         }
         tc_fence_after();
-        const uint32_t a_base = smem_u32(sA + s * lay.a_stage);
+        const uint32_t a_base = smem_u32(sA + (res ? lt : s) * lay.a_stage);
+        const uint32_t b_base = smem_u32(sB + bi * lay.b_bytes);
         for (int kk = 0; kk < KR / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(a_base + kk * 2048, KR * 128, 1024);
           const uint64_t bd = sdesc_sw128(b_base + kk * 2048, KR * 128, 1024);
           umma_bf16(tmem + buf * BN, ad, bd, idesc, kk != 0);
         }
-        umma_commit(&a_empty[s]);
+        if (!res) umma_commit(&a_empty[s]);
         umma_commit(&t_full[buf]);
+        if (++s == kExpandStages) {
+          s = 0;
+          par ^= 1;
+        }
+        if (++lt == e.nlt) {
+          lt = 0;
+          ++sj;
+          if (j + 1 < njobs) umma_commit(&b_empty[bi]);  // this strip may be replaced
+        }
       }
     }
   } else {
     // ---------------- epilogue (warps 2..9) ----------------
     // two groups of four warps (one per TMEM lane quarter); group g handles
-    // tiles g, g+2, ... from accumulator g, so two tiles are converted at once.
+    // jobs g, g+2, ... from accumulator g, so two tiles are converted at once.
     // Each group double-buffers its staging and tracks its own store groups.
     const int grp = (warp - 2) >> 2;       // 0 or 1
     const int gt = (threadIdx.x - 64) & 127;  // thread index within the group
     const int quarter = warp & 3;          // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;   // token row within the tile
     int it = 0;
-    for (int lt = grp; lt < e.nlt; lt += 2, ++it) {
+    for (int j = grp; j < njobs; j += 2, ++it) {
+      const int sj = j / e.nlt;
+      const int lt = j - sj * e.nlt;
       uint8_t* st = stg + (2 * grp + (it & 1)) * (BN / 64) * BOX;
       if (gt == 0 && it >= 2) tma_store_wait_read<1>();
       if (grp == 0) named_barrier<1>(128); else named_barrier<2>(128);
@@ -216,7 +286,7 @@ __global__ void __launch_bounds__(320, 2)
       if (grp == 0) named_barrier<1>(128); else named_barrier<2>(128);
       if (gt == 0) {
         for (int h = 0; h < BN / 64; ++h)
-          if (n0 + 64 * h < e.Cx) tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, lt * BM, b);
+          if (n0 + 64 * h < e.Cx) tma_store_3d(&tmap_out, st + h * BOX, n0 + 64 * h, lt * BM, b0 + sj);
         tma_store_commit();
       }
     }
@@ -255,8 +325,9 @@ cudaError_t launch_bn(const CUtensorMap& tq, const CUtensorMap& tg, const CUtens
     if (err != cudaSuccess) return err;
     configured_ = bytes;
   }
-  return launch_ex(k_expand_bf16<BN>, dim3((e.Cx + BN - 1) / BN, e.B), dim3(320), bytes, st, 1,
-                   pdl_enabled(), tq, tg, to, e);
+  if (e.spb < 1) return cudaErrorInvalidValue;
+  return launch_ex(k_expand_bf16<BN>, dim3((e.Cx + BN - 1) / BN, (e.B + e.spb - 1) / e.spb), dim3(320),
+                   bytes, st, 1, pdl_enabled(), tq, tg, to, e);
 }
 
 }  // namespace

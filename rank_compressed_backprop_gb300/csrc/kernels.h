@@ -18,6 +18,9 @@ struct ProjectArgs {
   int nk;            // ceil(L / 64)
   int pq_tma;        // 1: PQ tiles arrive by TMA; 0: threads fill all of PQ up front
   int pf_chunks;     // leading 64-token chunks of its tile a CTA prefetches into L2
+  int split;         // CTAs sharing a tile's token axis (1..4, a cluster along grid z);
+                     // their fp32 partial sums are reduced through DSMEM
+  int spb;           // samples per CTA (1 with a split): short token axes share a CTA
   const void* pq;    // [Rx+Ry, L]
   void* out0;        // [B*Rx, C]
   void* out1;        // [B*Ry, C] or null
@@ -73,6 +76,29 @@ cudaError_t launch_gradw_stream(const CUtensorMap& tmap_sx, const CUtensorMap& t
                                 cudaStream_t st);
 
 // ---------------------------------------------------------------------------
+// forward y = x w^T (bf16, fp32 accumulation) with the optional side output
+// x_hat = P x computed from the staged x tiles
+// ---------------------------------------------------------------------------
+constexpr int kForwardBN = 192;    // output tile: 128 tokens x 192 columns of y
+constexpr int kForwardStages = 4;  // 40 KB each
+struct ForwardArgs {
+  int M, N, K;       // y [M = B*L, N = Cy], x [M, K = Cx], w [N, K]
+  int mt, nt, nkc;   // ceil(M / 128), ceil(N / 192), ceil(K / 64)
+  int group;         // m tiles per rasterization group
+  int Rx;            // rows of P (0: no side output; else <= 32, L % 128 == 0)
+  int L;             // tokens per sample
+  float* xh32;       // [B, Rx, K] fp32 accumulation, zero before and after a launch
+  void* xh;          // [B, Rx, K] bf16 x_hat
+  unsigned int* cnt; // [B] finished tiles per sample, zero before and after a launch
+};
+size_t forward_bf16_smem_bytes();
+cudaError_t launch_forward_bf16(const CUtensorMap& tmap_x, const CUtensorMap& tmap_w,
+                                const CUtensorMap& tmap_y, const CUtensorMap& tmap_p,
+                                const ForwardArgs& a, int ctas, cudaStream_t st);
+cudaError_t launch_forward_f32(const float* x, const float* w, float* y, int M, int N, int K,
+                               cudaStream_t st);
+
+// ---------------------------------------------------------------------------
 // rank-R expansion: out[b, l, c] = sum_r Q[r, l] * (sum_s gxh[s][b*Ry + r, c])
 // ---------------------------------------------------------------------------
 struct ExpandArgs {
@@ -81,6 +107,7 @@ struct ExpandArgs {
   int BN;            // column tile (64, 128 or 256)
   int nlt;           // ceil(L / 128) token tiles, looped over inside one CTA
   int q_tma;         // 1: Q tiles arrive by TMA (L % 8 == 0); 0: threads fill them
+  int spb;           // consecutive samples per CTA (short token axes)
   const void* gxh;   // [B*Ry][Cx], same dtype as out (fp32 path: fp32)
   const void* Q;     // [Ry, L]
   void* out;         // [B, L, Cx]
@@ -312,5 +339,6 @@ cudaError_t read_fault_syrk(unsigned int* out, int clear);
 cudaError_t read_fault_eig(unsigned int* out, int clear);
 cudaError_t read_fault_fused(unsigned int* out, int clear);
 cudaError_t read_fault_gradw(unsigned int* out, int clear);
+cudaError_t read_fault_forward(unsigned int* out, int clear);
 
 }  // namespace instant

@@ -16,10 +16,13 @@
 // project_tile.cuh).  One CTA per (128-column tile, sample) over the whole
 // token axis; a 4-stage ring (73 KB of shared memory) lets three CTAs share
 // an SM.  Before waiting for its predecessor, each CTA prefetches its tile
-// into L2, so the ring mostly refills from L2.  (A token split over a 2-CTA
-// cluster with a DSMEM reduction measured slower at every batch from 2 to 64
-// samples of a BERT-base block: its two cluster barriers cost more than the
-// balance it bought.)
+// into L2, so the ring mostly refills from L2.  When those tiles would leave
+// SMs idle (few samples, e.g. four 2048-token samples of 4096 channels: 128
+// tiles for 152 SMs), two to four CTAs of a cluster share each tile's token
+// axis and sum their fp32 partials through distributed shared memory; with
+// short token axes (a BERT-base batch: 8 chunks per tile) the two cluster
+// barriers cost more than the balance buys, so the split is kept for shares
+// of at least 8 chunks.
 #include "kernels.h"
 #include "project_tile.cuh"
 #include "tc.cuh"
@@ -45,6 +48,11 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem_cols = NT <= 32 ? 32 : (NT <= 64 ? 64 : 128);
 
   ProjPipe pipe = proj_pipe(smem, bars, NT, a.nk, a.pq_tma, 0);
+  // token share of this CTA: the split CTAs of a tile form one cluster along z
+  const int S = a.split;
+  const int rank = blockIdx.z;
+  const int k0 = static_cast<int>(static_cast<long long>(a.nk) * rank / S);
+  const int nkl = static_cast<int>(static_cast<long long>(a.nk) * (rank + 1) / S) - k0;
   if (threadIdx.x == 0) {
     proj_init_barriers(pipe);
     fence_barrier_init();
@@ -53,7 +61,7 @@ __global__ void __launch_bounds__(128, 1)
     // the input tile streams into L2 while the predecessor finishes (issued
     // before the TMEM allocation, which may wait for TMEM the predecessor's
     // CTAs on this SM still hold)
-    proj_prefetch(&tmap_t, a, blockIdx.y, blockIdx.x * kProjBM);
+    proj_prefetch(&tmap_t, a, blockIdx.y * a.spb, blockIdx.x * kProjBM, k0, nkl);
   }
   if (threadIdx.x < 32) {
     tmem_alloc(tmem_slot, tmem_cols);
@@ -69,10 +77,72 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
   }
   pipe.tmem = *tmem_slot;
-  proj_tile<1>(&tmap_t, &tmap_pq, a, NT, blockIdx.y, blockIdx.x * kProjBM, pipe);
+  if (S == 1) {
+    // a.spb consecutive samples of the same column tile (short token axes:
+    // one launch's fixed costs and the projector in shared memory are shared)
+    const int b0 = blockIdx.y * a.spb;
+    const int b1 = min(a.B, b0 + a.spb);
+    for (int b = b0; b < b1; ++b) {
+      if (threadIdx.x == 0 && b + 1 < b1) proj_prefetch(&tmap_t, a, b + 1, blockIdx.x * kProjBM);
+      proj_tile<1>(&tmap_t, &tmap_pq, a, NT, b, blockIdx.x * kProjBM, pipe);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tmem_dealloc(pipe.tmem, tmem_cols);
+    return;
+  }
+  // ---- token split: partial sums in the idle ring, reduced across the cluster ----
+  float* part = reinterpret_cast<float*>(pipe.sA);  // [NT][128] fp32
+  proj_tile<1>(&tmap_t, &tmap_pq, a, NT, blockIdx.y, blockIdx.x * kProjBM, pipe, k0, nkl, part);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(pipe.tmem, tmem_cols);
+  cluster_sync();
+  {
+    // rank z writes columns [z * 128 / S, (z + 1) * 128 / S) of every row, in
+    // pieces of 8 columns (16 bytes of bf16), summing the S partials in rank order
+    const int b = blockIdx.y;  // spb == 1 with a split
+    const int c_tile = blockIdx.x * kProjBM;
+    const int Rt = a.Rx + a.Ry;
+    const int p0 = kProjBM / 8 * rank / S, p1 = kProjBM / 8 * (rank + 1) / S;
+    const int np = p1 - p0;
+    uint16_t* out0 = static_cast<uint16_t*>(a.out0);
+    uint16_t* out1 = static_cast<uint16_t*>(a.out1);
+    for (int idx = threadIdx.x; idx < Rt * np; idx += blockDim.x) {
+      const int r = idx / np;
+      const int piece = p0 + (idx - r * np);
+      const float* src = part + r * kProjBM + piece * 8;
+      float4 lo[4], hi[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < S) {
+          lo[q] = dsmem_ld_f4(dsmem_addr(src, q));
+          hi[q] = dsmem_ld_f4(dsmem_addr(src + 4, q));
+        }
+      float4 l = lo[0], h = hi[0];
+#pragma unroll
+      for (int q = 1; q < 4; ++q)
+        if (q < S) {
+          l.x += lo[q].x; l.y += lo[q].y; l.z += lo[q].z; l.w += lo[q].w;
+          h.x += hi[q].x; h.y += hi[q].y; h.z += hi[q].z; h.w += hi[q].w;
+        }
+      const int c = c_tile + piece * 8;
+      uint16_t* dst = r < a.Rx ? out0 + (static_cast<size_t>(b) * a.Rx + r) * a.C + c
+                               : out1 + (static_cast<size_t>(b) * a.Ry + (r - a.Rx)) * a.C + c;
+      const uint4 v = make_uint4(pack_bf16x2(l.x, l.y), pack_bf16x2(l.z, l.w), pack_bf16x2(h.x, h.y),
+                                 pack_bf16x2(h.z, h.w));
+      if (c + 8 <= a.C) {
+        *reinterpret_cast<uint4*>(dst) = v;
+      } else {
+        const uint16_t e[8] = {static_cast<uint16_t>(v.x & 0xffffu), static_cast<uint16_t>(v.x >> 16),
+                               static_cast<uint16_t>(v.y & 0xffffu), static_cast<uint16_t>(v.y >> 16),
+                               static_cast<uint16_t>(v.z & 0xffffu), static_cast<uint16_t>(v.z >> 16),
+                               static_cast<uint16_t>(v.w & 0xffffu), static_cast<uint16_t>(v.w >> 16)};
+        for (int j = 0; c + j < a.C; ++j) dst[j] = e[j];
+      }
+    }
+  }
+  cluster_sync();  // peers may still read this CTA's partial sums
 }
 
 // fp32 path (no tensor cores, no TF32): one thread per output element.
@@ -108,8 +178,10 @@ cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tm
     if (e != cudaSuccess) return e;
     configured_ = bytes;
   }
-  return launch_ex(k_project_bf16, dim3((a.C + kProjBM - 1) / kProjBM, a.B, 1), dim3(128), bytes,
-                   st, 1, pdl_enabled(), tmap_t, tmap_pq, a);
+  if (a.split < 1 || a.split > 4) return cudaErrorInvalidValue;
+  if (a.spb < 1 || (a.split > 1 && a.spb != 1)) return cudaErrorInvalidValue;
+  return launch_ex(k_project_bf16, dim3((a.C + kProjBM - 1) / kProjBM, (a.B + a.spb - 1) / a.spb, a.split),
+                   dim3(128), bytes, st, a.split, pdl_enabled(), tmap_t, tmap_pq, a);
 }
 
 cudaError_t launch_project_f32(const ProjectArgs& a, const float* t, cudaStream_t st) {

@@ -108,10 +108,11 @@ __device__ __forceinline__ void proj_fill_pq(const ProjectArgs& a, const ProjPip
 // resident early under programmatic dependent launch, and its first loads
 // then hit L2).
 __device__ __forceinline__ void proj_prefetch(const CUtensorMap* tmap_t, const ProjectArgs& a, int b,
-                                              int c0) {
-  for (int i = 0; i < a.pf_chunks && i < a.nk; ++i) {
-    tma_prefetch_l2_3d(tmap_t, c0, i * kProjBK, b);
-    if (c0 + 64 < a.C) tma_prefetch_l2_3d(tmap_t, c0 + 64, i * kProjBK, b);
+                                              int c0, int k0 = 0, int nkl = -1) {
+  const int nk = nkl < 0 ? a.nk : nkl;
+  for (int i = 0; i < a.pf_chunks && i < nk; ++i) {
+    tma_prefetch_l2_3d(tmap_t, c0, (k0 + i) * kProjBK, b);
+    if (c0 + 64 < a.C) tma_prefetch_l2_3d(tmap_t, c0 + 64, (k0 + i) * kProjBK, b);
   }
 }
 
@@ -119,13 +120,18 @@ __device__ __forceinline__ void proj_prefetch(const CUtensorMap* tmap_t, const P
 // threads of the CTA must not touch the ring meanwhile).  On return every
 // store of the tile has been issued by its thread and the accumulator is free
 // for the next tile (named barrier BAR over the 128 threads).
+// With part != nullptr the tile covers only the 64-token chunks k0 .. k0+nkl-1
+// (one share of a token split) and, instead of writing the planes, leaves
+// its fp32 partial sums in part[r * 128 + column], r < NT (shared memory of
+// this CTA, e.g. the idle ring), for the caller to reduce.
 template <int BAR>
 __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUtensorMap* tmap_pq,
                                           const ProjectArgs& a, int NT, int b, int c0,
-                                          ProjPipe& p) {
+                                          ProjPipe& p, int k0 = 0, int nkl = -1,
+                                          float* part = nullptr) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nk = a.nk;
+  const int nk = nkl < 0 ? a.nk : nkl;
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
     const uint32_t bytes = kProjABytes + (a.pq_tma ? p.b_stage_bytes : 0);
@@ -139,9 +145,10 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
       }
       mbar_arrive_expect_tx(&p.full[s], bytes);
       uint8_t* dst = p.sA + s * kProjABytes;
-      tma_load_3d(dst, tmap_t, &p.full[s], c0, i * kProjBK, b);
-      tma_load_3d(dst + kProjHalfA, tmap_t, &p.full[s], c0 + 64, i * kProjBK, b);
-      if (a.pq_tma) tma_load_2d(p.sB + s * p.b_stage_bytes, tmap_pq, &p.full[s], i * kProjBK, 0);
+      const int l0 = (k0 + i) * kProjBK;
+      tma_load_3d(dst, tmap_t, &p.full[s], c0, l0, b);
+      tma_load_3d(dst + kProjHalfA, tmap_t, &p.full[s], c0 + 64, l0, b);
+      if (a.pq_tma) tma_load_2d(p.sB + s * p.b_stage_bytes, tmap_pq, &p.full[s], l0, 0);
       ++issued;
     }
     // every copy this thread issued has landed before it moves on (the ring is
@@ -165,7 +172,7 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
       }
       tc_fence_after();
       const uint32_t a_base = smem_u32(p.sA + s * kProjABytes);
-      const uint32_t b_base = smem_u32(p.sB + (a.pq_tma ? s : i) * p.b_stage_bytes);
+      const uint32_t b_base = smem_u32(p.sB + (a.pq_tma ? s : k0 + i) * p.b_stage_bytes);
 #pragma unroll
       for (int kk = 0; kk < kProjBK / 16; ++kk) {
         // A (MN-major): 16 tokens = 2 groups of 8 rows of 128 B; the second
@@ -188,6 +195,26 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
   uint16_t* out0 = static_cast<uint16_t*>(a.out0);
   uint16_t* out1 = static_cast<uint16_t*>(a.out1);
   const int Rt = a.Rx + a.Ry;
+  if (part != nullptr) {
+    // one share of a token split: the fp32 partial sums, for the caller
+    for (int j0 = 0; j0 < NT; j0 += 16) {
+      float v[16];
+      if (nk > 0) {
+        tmem_ld16(taddr + j0, v);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) v[jj] = 0.f;
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) part[(j0 + jj) * kProjBM + row] = v[jj];
+    }
+    tc_fence_before();
+    named_barrier<BAR>(128);  // accumulator read by all four warps
+    tc_fence_after();
+    p.chunk += nk;
+    p.tiles += 1;
+    return;
+  }
   // the bf16 tile [Rt rows][128 columns] staged in the ring (idle: every MMA
   // has completed, so every copy into it has landed), then written back in
   // 16-byte pieces of the output rows

@@ -46,6 +46,7 @@ class InstantLinear:
                                   device=dev)
         self.last_calibration = None
         self._cal = None   # the solve's argument block, built on first use
+        self.ws_fwd = None  # forward workspace (zeroed), built on first use
 
     # views of the stacked projector
     @property
@@ -57,6 +58,20 @@ class InstantLinear:
         return self.PQ[self.Rx:]
 
     # ---- the per-step path -------------------------------------------------
+    def forward(self, x: torch.Tensor, y: torch.Tensor | None = None,
+                xhat: torch.Tensor | None = None) -> torch.Tensor:
+        """The layer's forward ``y = x w^T``; the compressed activation
+        ``x_hat = P x`` is formed from the same pass over ``x`` and kept for the
+        backward (returns ``y``)."""
+        B, L, _ = x.shape
+        if y is None:
+            y = torch.empty(B, L, self.Cy, dtype=self.dtype, device=x.device)
+        if self.ws_fwd is None:
+            self.ws_fwd = api.forward_workspace(self.B, self.L, self.Cx, self.Rx, self.dtype,
+                                                x.device)
+        api.forward(x, self.w, y, self.P, self.xhat if xhat is None else xhat, self.ws_fwd)
+        return y
+
     def compress(self, x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
         """Forward-side activation compression ``x_hat = P x``."""
         return api.compress_act(x, self.P, self.xhat if out is None else out)

@@ -232,3 +232,78 @@ def test_grad_w_stream(torch, monkeypatch, B, Rx, Cx, Cy, accumulate):
     torch.cuda.synchronize()
     assert_parity(to_np(gw), to_np(gw2), 1e-5, "g_w stream vs gemm")
     assert api.device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# projection with the token axis split across a cluster
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("split", [2, 3, 4])
+@pytest.mark.parametrize("B,L,C,Rx,Ry", [(2, 2048, 392, 16, 16),   # 32 chunks, ragged columns
+                                         (3, 1000, 256, 8, 0),     # ragged token tail, compress
+                                         (1, 130, 136, 5, 7)])     # 3 chunks: short shares
+def test_projection_token_split(torch, monkeypatch, split, B, L, C, Rx, Ry):
+    monkeypatch.setenv("INSTANT_PROJ_SPLIT", str(split))
+    g = rng(3700 + L + C + split)
+    t = stored(g.standard_normal((B, L, C)), "bf16")
+    PQ = stored(orthonormal_rows(g, Rx + Ry, L), "bf16")
+    api = _api()
+    out0 = nan_like(torch, (B * Rx, C), torch.bfloat16)
+    if Ry:
+        out1 = nan_like(torch, (B * Ry, C), torch.bfloat16)
+        api.project_grad(to_dev(t), to_dev(PQ), out0, out1, Rx, Ry)
+    else:
+        api.compress_act(to_dev(t), to_dev(PQ), out0.view(B, Rx, C))
+    torch.cuda.synchronize()
+    r0, r1 = O.project_grad(t, PQ[:Rx], PQ[Rx:]) if Ry else (O.compress_act(t, PQ), None)
+    assert_parity(to_np(out0).reshape(B, Rx, C), r0, 2e-2, "first plane")
+    if Ry:
+        assert_parity(to_np(out1).reshape(B, Ry, C), r1, 2e-2, "second plane")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("spb", [2, 3, 8])
+@pytest.mark.parametrize("B,L,C,Rx,Ry", [(7, 49, 448, 8, 8),     # ViT tokens, a ragged last group
+                                         (5, 100, 264, 8, 0)])   # compress, two chunks, ragged columns
+def test_projection_samples_per_cta(torch, monkeypatch, spb, B, L, C, Rx, Ry):
+    """Several samples per CTA (short token axes): the same planes as one
+    sample per CTA."""
+    monkeypatch.setenv("INSTANT_PROJ_SPB", str(spb))
+    g = rng(3800 + L + C + spb)
+    t = stored(g.standard_normal((B, L, C)), "bf16")
+    PQ = stored(orthonormal_rows(g, Rx + Ry, L), "bf16")
+    api = _api()
+    out0 = nan_like(torch, (B * Rx, C), torch.bfloat16)
+    if Ry:
+        out1 = nan_like(torch, (B * Ry, C), torch.bfloat16)
+        api.project_grad(to_dev(t), to_dev(PQ), out0, out1, Rx, Ry)
+    else:
+        api.compress_act(to_dev(t), to_dev(PQ), out0.view(B, Rx, C))
+    torch.cuda.synchronize()
+    r0, r1 = O.project_grad(t, PQ[:Rx], PQ[Rx:]) if Ry else (O.compress_act(t, PQ), None)
+    assert_parity(to_np(out0).reshape(B, Rx, C), r0, 2e-2, "first plane")
+    if Ry:
+        assert_parity(to_np(out1).reshape(B, Ry, C), r1, 2e-2, "second plane")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("spb", [2, 3, 8])
+@pytest.mark.parametrize("B,L,Cx,Cy,Ry", [(7, 49, 448, 1792, 8),    # ViT tokens, ragged last group
+                                          (5, 300, 264, 136, 16)])  # three token tiles per sample
+def test_expand_samples_per_cta(torch, monkeypatch, spb, B, L, Cx, Cy, Ry):
+    """The expansion with several samples per CTA (two g_hat_x strips in
+    flight) against the oracle."""
+    monkeypatch.setenv("INSTANT_EXPAND_SPB", str(spb))
+    api = _api()
+    g = rng(3900 + L + Cx + spb)
+    Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
+    Q = stored(orthonormal_rows(g, Ry, L), "bf16")
+    gx = nan_like(torch, (B, L, Cx), torch.bfloat16)
+    ws = torch.full((api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, torch.bfloat16),), 255,
+                    dtype=torch.uint8, device="cuda")
+    api.grad_x_core(to_dev(Sq), to_dev(w), ws, B)
+    api.expand(to_dev(Q), gx, ws, Cy)
+    torch.cuda.synchronize()
+    ref = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
+    assert_parity(to_np(gx), ref, 2e-2, "g_x")
+    assert api.device_status() == 0
