@@ -213,6 +213,50 @@ bool use_gradw_stream(int M, int N, int K) {
   return static_cast<long long>(cdiv(M, 128)) * cdiv(N, 64) >= 4ll * sm_count();
 }
 
+// Split of the autocorrelation work (statistic p: B[p] samples of nkc[p]
+// 64-channel chunks on each of `ntiles` tiles): cs[p] channel ranges per tile,
+// each CTA walking all its samples in order (so the CTAs running at one time
+// read the same sample and its tiles meet in L2), and bs[p] sample ranges only
+// when the channel ranges alone cannot fill the GPU.  Among grids of w whole
+// waves of two CTAs per SM (w = 1..8) it takes the one whose slowest CTA
+// finishes first, counting a CTA's set-up and atomic flush as 12 iterations;
+// a CTA keeps at least 4 iterations and a tile at most 64 CTAs (more
+// concurrent atomic adds into one tile cost more than they save: 256 samples
+// of 197 tokens on GB300).
+void plan_syrk(int n, const int* B, const int* nkc, int ntiles, int* cs, int* bs) {
+  const long long slots = 2ll * sm_count();
+  double total = 0.0;
+  for (int p = 0; p < n; ++p) total += static_cast<double>(B[p]) * nkc[p] * ntiles;
+  double best = 1e300;
+  for (int w = 1; w <= 8; ++w) {
+    int c[kMaxSyrkBatch], s[kMaxSyrkBatch];
+    long long ctas = 0;
+    long long maxw = 0;
+    for (int p = 0; p < n; ++p) {
+      const double work = static_cast<double>(B[p]) * nkc[p] * ntiles;
+      int per_tile = static_cast<int>(std::lround(w * slots * work / total / ntiles));
+      per_tile = std::max(1, std::min(per_tile, 64));
+      c[p] = std::min(per_tile, nkc[p]);
+      s[p] = std::max(1, std::min(B[p], per_tile / c[p]));
+      // at least 4 iterations per CTA
+      while (c[p] * s[p] > 1 && static_cast<long long>(cdiv(nkc[p], c[p])) * cdiv(B[p], s[p]) < 4) {
+        if (s[p] > 1) --s[p]; else --c[p];
+      }
+      ctas += static_cast<long long>(ntiles) * c[p] * s[p];
+      maxw = std::max<long long>(maxw, static_cast<long long>(cdiv(nkc[p], c[p])) * cdiv(B[p], s[p]));
+    }
+    const long long waves = (ctas + slots - 1) / slots;
+    const double cost = static_cast<double>(waves) * (maxw + 12);
+    if (cost < best) {
+      best = cost;
+      for (int p = 0; p < n; ++p) {
+        cs[p] = c[p];
+        bs[p] = s[p];
+      }
+    }
+  }
+}
+
 size_t grad_x_ws(int B, int Cx, int Cy, int Ry, instant_dtype dt) {
   (void)Cy;
   return static_cast<size_t>(B) * Ry * Cx * (dt == INSTANT_F32 ? sizeof(float) : 2);
@@ -1024,28 +1068,25 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
       s.ntiles = ntiles;
       s.nkc = cdiv(s.C, 64);
       s.Cout = items[i].C;
-      s.splits = 1;
-      s.it_per_split = s.B * s.nkc;
+      s.splits = s.cs = s.bs = 1;
       if (launch_syrk_f32(s, static_cast<const float*>(items[i].t), st) != cudaSuccess)
         return INSTANT_ERR_CUDA;
     }
     return INSTANT_OK;
   }
-  // groups of up to kMaxSyrkBatch statistics per launch; within a launch the
-  // (sample, channel chunk) iterations of every statistic are split evenly so
-  // that the whole grid fills two CTAs per SM, each CTA with at least 4 chunks
-  // and at most 64 CTAs adding into one tile (measured on GB300: BERT-base
-  // batch 19.5 -> 16.8 us against whole-sample splits; more splits than 64 per
-  // tile lose to the atomic adds, e.g. 256 ViT samples of 197 tokens)
+  // groups of up to kMaxSyrkBatch statistics per launch
   for (int g0 = 0; g0 < count; g0 += kMaxSyrkBatch) {
     const int n = std::min(kMaxSyrkBatch, count - g0);
-    long long total = 0;
-    for (int i = 0; i < n; ++i)
-      total += static_cast<long long>(items[g0 + i].B) * cdiv(items[g0 + i].Cdim, 64);
     SyrkBatch b;
     CUtensorMap maps[kMaxSyrkBatch];
     b.count = n;
     b.split0[0] = 0;
+    int Bs[kMaxSyrkBatch], nkcs[kMaxSyrkBatch], cs[kMaxSyrkBatch], bs[kMaxSyrkBatch];
+    for (int i = 0; i < n; ++i) {
+      Bs[i] = items[g0 + i].B;
+      nkcs[i] = cdiv(items[g0 + i].Cdim, 64);
+    }
+    plan_syrk(n, Bs, nkcs, ntiles, cs, bs);
     for (int i = 0; i < n; ++i) {
       const instant_accumulate_item& it = items[g0 + i];
       SyrkArgs& s = b.s[i];
@@ -1054,16 +1095,11 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
       s.C = it.Cdim;
       s.nblk = nblk;
       s.ntiles = ntiles;
-      s.nkc = cdiv(it.Cdim, 64);
+      s.nkc = nkcs[i];
       s.Cout = it.C;
-      const int iters = s.B * s.nkc;
-      const double share = static_cast<double>(iters) / static_cast<double>(total);
-      // two CTAs per SM: the grid fills every SM twice
-      int splits = std::max(1, static_cast<int>(2 * sm_count() * share / ntiles));
-      splits = std::min(splits, 64);
-      splits = std::min(splits, std::max(1, iters / 4));
-      s.it_per_split = cdiv(iters, splits);
-      s.splits = cdiv(iters, s.it_per_split);
+      s.cs = cs[i];
+      s.bs = bs[i];
+      s.splits = s.cs * s.bs;
       b.split0[i + 1] = b.split0[i] + s.splits;
       const uint64_t d3[3] = {static_cast<uint64_t>(it.Cdim), static_cast<uint64_t>(L),
                               static_cast<uint64_t>(it.B)};

@@ -171,8 +171,9 @@ struct SyrkArgs {
   int B, L, C;
   int nblk;          // ceil(L / 128)
   int ntiles;        // nblk * (nblk + 1) / 2 upper-triangle tiles
-  int splits;        // splits of the (sample, channel chunk) iterations (grid y)
-  int it_per_split;  // consecutive iterations per split (a split may cross samples)
+  int splits;        // CTAs per tile (grid y) = cs * bs
+  int cs;            // channel ranges per tile (each CTA walks all of its samples)
+  int bs;            // sample ranges per tile (small statistics only)
   int nkc;           // ceil(C / 64)
   float* Cout;       // [L, L]
 };

@@ -5,11 +5,13 @@
 // storing the batch.  This is the one truly tensor-bound step (2L flops per
 // byte of t), so it is a tcgen05 GEMM over the upper-triangle 128x128 tiles of
 // C: both operands are K-major row blocks of the same sample (K = channels),
-// streamed by TMA; the sum over samples continues the K loop.  The (sample,
-// 64-channel chunk) iterations are split into equal ranges across grid y (a
-// range may cross samples), sized so that two CTAs per SM cover the GPU, and
-// every CTA adds its tile (and, off the diagonal, the mirrored tile) into C
-// with fp32 atomics.
+// streamed by TMA; the sum over samples continues the K loop.  Grid y splits
+// each tile's work into channel ranges (every CTA walks all of its samples in
+// order, so the CTAs running at one time read the same sample and its tiles
+// meet in L2) and, for small statistics only, sample ranges; the host sizes
+// the splits so that the CTAs carry equal work and fill whole waves of two
+// CTAs per SM.  Every CTA adds its tile (and, off the diagonal, the mirrored
+// tile) into C with fp32 atomics.
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -43,7 +45,11 @@ __global__ void __launch_bounds__(128, 1)
   while (p + 1 < batch.count && static_cast<int>(blockIdx.y) >= batch.split0[p + 1]) ++p;
   const SyrkArgs& a = batch.s[p];
   const CUtensorMap& tmap_t = p == 0 ? tmap0 : (p == 1 ? tmap1 : (p == 2 ? tmap2 : tmap3));
+  // split index -> (channel range, sample range): every CTA walks its samples
+  // in order, each over its own channel chunks
   const int split = static_cast<int>(blockIdx.y) - batch.split0[p];
+  const int ks = split % a.cs;
+  const int bsx = split / a.cs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -59,10 +65,11 @@ __global__ void __launch_bounds__(128, 1)
   const bool diag = bi == bj;
   const int i0 = bi * BT;
   const int j0 = bj * BT;
-  const int it_begin = split * a.it_per_split;
-  int it_end = it_begin + a.it_per_split;
-  if (it_end > a.B * a.nkc) it_end = a.B * a.nkc;
-  const int niter = it_end > it_begin ? it_end - it_begin : 0;
+  const int kc_lo = static_cast<int>(static_cast<long long>(a.nkc) * ks / a.cs);
+  const int kc_hi = static_cast<int>(static_cast<long long>(a.nkc) * (ks + 1) / a.cs);
+  const int b_lo = static_cast<int>(static_cast<long long>(a.B) * bsx / a.bs);
+  const int b_hi = static_cast<int>(static_cast<long long>(a.B) * (bsx + 1) / a.bs);
+  const int niter = (kc_hi - kc_lo) * (b_hi - b_lo);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSyrkStages; ++s) {
@@ -88,7 +95,7 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t bytes = diag ? TILE_BYTES : STAGE;
     int issued = 0;
     // (sample, channel chunk) of iteration it, kept without divisions
-    int b = it_begin / a.nkc, kc = it_begin - (it_begin / a.nkc) * a.nkc;
+    int b = b_lo, kc = kc_lo;
     for (int it = 0; it < niter; ++it) {
       const int s = it % kSyrkStages;
       if (it >= kSyrkStages && !mbar_wait(&empty[s], ((it / kSyrkStages) - 1) & 1)) {
@@ -101,8 +108,8 @@ __global__ void __launch_bounds__(128, 1)
       tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
       if (!diag) tma_load_3d(dst + TILE_BYTES, &tmap_t, &full[s], c0, j0, b);
       ++issued;
-      if (++kc == a.nkc) {
-        kc = 0;
+      if (++kc == kc_hi) {
+        kc = kc_lo;
         ++b;
       }
     }
@@ -193,7 +200,8 @@ size_t syrk_bf16_smem_bytes() { return kSyrkStages * STAGE + 256 + 1024; }
 cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b, cudaStream_t st) {
   if (b.count < 1 || b.count > kMaxSyrkBatch || b.split0[0] != 0) return cudaErrorInvalidValue;
   for (int p = 0; p < b.count; ++p)
-    if (b.s[p].L != b.s[0].L || b.split0[p + 1] != b.split0[p] + b.s[p].splits || b.s[p].splits < 1)
+    if (b.s[p].L != b.s[0].L || b.split0[p + 1] != b.split0[p] + b.s[p].splits || b.s[p].splits < 1 ||
+        b.s[p].cs < 1 || b.s[p].bs < 1 || b.s[p].cs * b.s[p].bs != b.s[p].splits)
       return cudaErrorInvalidValue;
   const size_t bytes = syrk_bf16_smem_bytes();
   static size_t configured_ = 0;

@@ -134,6 +134,8 @@ def test_calib_accumulate(torch, dtype, B, L, C):
 @pytest.mark.parametrize("dtype,L,dims", [
     ("bf16", 512, [(32, 768), (32, 3072)]),                    # a layer's C_X and C_G, one launch
     ("bf16", 300, [(3, 200), (5, 264), (2, 64), (4, 136), (1, 8)]),   # five: two launches
+    ("bf16", 2048, [(3, 520), (2, 1096)]),                    # channel ranges per tile
+    ("bf16", 49, [(40, 448), (40, 1792)]),                    # sample ranges per tile too
     ("f32", 72, [(2, 40), (3, 48)]),
 ])
 def test_calib_accumulate_batch(torch, dtype, L, dims):
