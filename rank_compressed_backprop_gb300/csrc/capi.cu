@@ -989,9 +989,12 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
   if (use_fused_grad_x(L, Cy, Ry, dt))
     return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{Sx, xhat, gw, accumulate, Rx},
                         static_cast<cudaStream_t>(stream));
-  const instant_status s = instant_grad_w(Sx, xhat, gw, accumulate, B, Rx, Cx, Cy, dt, stream);
+  // g_tilde_x first, g_w last: g_w depends on neither of g_tilde_x's two
+  // launches, and in this order a step of a 4096 -> 11008 layer (with the two
+  // projections before it) measured 124.5 us against 129.3 us with g_w first
+  const instant_status s = instant_grad_x(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
   if (s != INSTANT_OK) return s;
-  return instant_grad_x(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt, stream);
+  return instant_grad_w(Sx, xhat, gw, accumulate, B, Rx, Cx, Cy, dt, stream);
 }
 
 size_t instant_backward_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt) {
