@@ -957,21 +957,111 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
   cp_async_commit();
 }
 
-// stage rows [t * 64, t * 64 + 64) of V [L, m] (fp32, rows 16-byte aligned:
-// m is 16 or 32) into a [64][m] tile; rows past L are zero
-__device__ __forceinline__ void stage_v_tile(float* dst, const float* V, int L, int m, int t) {
-  const int l0 = t * kCvTileL;
-  const int q4 = m / 4;
-  for (int i = threadIdx.x; i < kCvTileL * q4; i += blockDim.x) {
-    const int rr = i / q4, c4 = (i - rr * q4) * 4;
-    float* d = dst + rr * m + c4;
-    if (l0 + rr < L) {
-      cp_async16(d, V + static_cast<size_t>(l0 + rr) * m + c4);
-    } else {
-      d[0] = d[1] = d[2] = d[3] = 0.f;
+constexpr int kClusterCtas = 8;
+constexpr int kClusterThreads = 256;
+
+// Long token axes: Y = C V over all of the CTA's rows at once.  Each thread
+// accumulates RB rows x 8 columns of Y, so that one 16-byte load of C (four
+// tokens of one row) and two of V (eight columns of one token) feed up to 32
+// FMAs; C and V arrive in 16-token chunks through a 4-deep cp.async ring.
+constexpr int kCvBigK = 16;       // tokens per chunk
+constexpr int kCvBigLd = 20;      // padded row stride of a C chunk: 16-byte rows, conflict-free
+constexpr int kCvBigStages = 4;
+constexpr int kCvBigRows = 256;   // rows of a C chunk: the CTA's rows (L <= 8 * 256)
+
+// stage tokens [t * 16, t * 16 + 16) of the CTA's nr rows of C and of V [L, m]
+// into one ring slot; tokens past L are zero in both (an empty group past the end)
+__device__ __forceinline__ void stage_cv_chunk(float* cdst, float* vdst, const float* Cown, int nr,
+                                               const float* V, int L, int m, int t, bool vec) {
+  const int l0 = t * kCvBigK;
+  if (l0 < L) {
+    constexpr int q = kCvBigK / 4;
+    for (int i = threadIdx.x; i < nr * q; i += blockDim.x) {
+      const int rr = i / q, c4 = (i - rr * q) * 4;
+      float* d = cdst + rr * kCvBigLd + c4;
+      const float* s = Cown + static_cast<size_t>(rr) * L + l0 + c4;
+      if (vec && l0 + c4 + 4 <= L) {
+        cp_async16(d, s);
+      } else {
+        for (int e = 0; e < 4; ++e) d[e] = l0 + c4 + e < L ? s[e] : 0.f;
+      }
+    }
+    const int q4 = m / 4;
+    for (int i = threadIdx.x; i < kCvBigK * q4; i += blockDim.x) {
+      const int rr = i / q4, c4 = (i - rr * q4) * 4;
+      float* d = vdst + rr * m + c4;
+      if (l0 + rr < L) {
+        cp_async16(d, V + static_cast<size_t>(l0 + rr) * m + c4);
+      } else {
+        d[0] = d[1] = d[2] = d[3] = 0.f;
+      }
     }
   }
   cp_async_commit();
+}
+
+// Y[r, :] = C[own row r, :] V / n for the CTA's nr rows; thread (slot, cg)
+// owns rows slot + i * slots (i < RB) and columns [8 cg, 8 cg + 8).  V is read
+// from the workspace where every CTA of the cluster published its rows.
+template <int M, int RB>
+__device__ __forceinline__ void cv_big(const float* Cown, int nr, const float* Vg, int L, bool vec,
+                                       float* Cs, float* Vs, float* Y, float inv_n) {
+  constexpr int ncg = M / 8;
+  constexpr int slots = kClusterThreads / ncg;
+  constexpr int cstage = kCvBigRows * kCvBigLd, vstage = kCvBigK * M;
+  const int cg = threadIdx.x % ncg, slot = threadIdx.x / ncg;
+  float acc[RB][8];
+#pragma unroll
+  for (int i = 0; i < RB; ++i)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
+  const int nch = (L + kCvBigK - 1) / kCvBigK;
+  for (int s = 0; s < kCvBigStages - 1; ++s)
+    stage_cv_chunk(Cs + s * cstage, Vs + s * vstage, Cown, nr, Vg, L, M, s, vec);
+  for (int t = 0; t < nch; ++t) {
+    cp_async_wait<kCvBigStages - 2>();  // chunk t's group (this thread's copies) has landed
+    __syncthreads();                    // ... everyone's; the slot of chunk t - 1 is free
+    {
+      const int s = t + kCvBigStages - 1;
+      const int b = s % kCvBigStages;
+      stage_cv_chunk(Cs + b * cstage, Vs + b * vstage, Cown, nr, Vg, L, M, s, vec);
+    }
+    const int b = t % kCvBigStages;
+    const float* cb = Cs + b * cstage + slot * kCvBigLd;
+    const float* vb = Vs + b * vstage + cg * 8;
+#pragma unroll
+    for (int k4 = 0; k4 < kCvBigK; k4 += 4) {
+      float4 c[RB];
+#pragma unroll
+      for (int i = 0; i < RB; ++i) c[i] = *reinterpret_cast<const float4*>(cb + i * slots * kCvBigLd + k4);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 v0 = *reinterpret_cast<const float4*>(vb + (k4 + kk) * M);
+        const float4 v1 = *reinterpret_cast<const float4*>(vb + (k4 + kk) * M + 4);
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+          const float cv = kk == 0 ? c[i].x : (kk == 1 ? c[i].y : (kk == 2 ? c[i].z : c[i].w));
+          acc[i][0] = fmaf(cv, v0.x, acc[i][0]);
+          acc[i][1] = fmaf(cv, v0.y, acc[i][1]);
+          acc[i][2] = fmaf(cv, v0.z, acc[i][2]);
+          acc[i][3] = fmaf(cv, v0.w, acc[i][3]);
+          acc[i][4] = fmaf(cv, v1.x, acc[i][4]);
+          acc[i][5] = fmaf(cv, v1.y, acc[i][5]);
+          acc[i][6] = fmaf(cv, v1.z, acc[i][6]);
+          acc[i][7] = fmaf(cv, v1.w, acc[i][7]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();  // the empty groups past the end
+  __syncthreads();     // the ring is free for the next iteration's prologue
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    const int r = slot + i * slots;
+    if (r < nr)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) Y[r * M + cg * 8 + c] = acc[i][c] * inv_n;
+  }
 }
 
 // row stride of the resident C rows: 4 mod 32 words, so that the eight rows a
@@ -991,7 +1081,7 @@ __device__ __forceinline__ float cluster_sum8(const float* p) {
 }
 
 struct ClusterLay {
-  uint32_t V, Y, Z, U, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
+  uint32_t V, Y, Hp, Gp, resp, r2, W, T, Lf, th, dpart, ipart, aval, aidx, flag, dsc, pv, jac,
       vt, ct, total;
 };
 
@@ -1012,9 +1102,9 @@ __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   const bool big = L > kClusterGatherMaxL;
   // the whole basis, gathered each iteration (own rows only for long L)
   c.V = lay_take(o, 4u * (big ? rp : L) * m);
-  c.Y = lay_take(o, 4u * rp * m);      // own rows of Y = C V / n
-  c.Z = lay_take(o, 4u * rp * m);      // own rows of Z = Y W (or Y)
-  c.U = lay_take(o, 4u * rp * m);      // own rows of the Ritz vectors U = V W
+  // own rows of Y = C V / n, overwritten in place by Z = Y W (the next block);
+  // the Ritz vectors U = V W overwrite the own rows of V in the same way
+  c.Y = lay_take(o, 4u * rp * m);
   c.Hp = lay_take(o, 4u * m * m);      // partial V^T Y (read by the peers)
   c.Gp = lay_take(o, 4u * m * m);      // partial Z^T Z (read by the peers)
   c.resp = lay_take(o, 4u * m);        // partial residual norms (read by the peers)
@@ -1031,19 +1121,20 @@ __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   c.dsc = lay_take(o, 4u * kMaxBlock);
   c.pv = lay_take(o, 4u * kMaxBlock);
   c.jac = lay_take(o, jac_smem_bytes(m));
-  c.vt = big ? lay_take(o, 4u * 2 * kCvTileL * m) : o;  // two V tiles for Y = C V (long L)
-  if (m == 16 && !big) {
+  if (big) {
+    // the ring of C and V chunks for Y = C V
+    c.ct = lay_take(o, 4u * kCvBigStages * kCvBigRows * kCvBigLd);
+    c.vt = lay_take(o, 4u * kCvBigStages * kCvBigK * m);
+  } else if (m == 16) {
     // the CTA's rows of C stay in shared memory for the whole solve
     c.ct = lay_take(o, 4u * rp * cres_ld(L));
   } else {
     c.ct = lay_take(o, 4u * 2 * kCvTileRows * kCvTileLd);  // two C tiles for Y = C V
   }
+  if (!big) c.vt = o;
   c.total = o;
   return c;
 }
-
-constexpr int kClusterCtas = 8;
-constexpr int kClusterThreads = 256;
 
 template <int M>
 __global__ void __launch_bounds__(kClusterThreads, 1)
@@ -1055,8 +1146,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
   const ClusterLay lay = cluster_layout(L, m, rp);
   float* Vall = reinterpret_cast<float*>(csm + lay.V);
   float* Y = reinterpret_cast<float*>(csm + lay.Y);
-  float* Z = reinterpret_cast<float*>(csm + lay.Z);
-  float* U = reinterpret_cast<float*>(csm + lay.U);
+  float* Z = Y;  // Z = Y W replaces Y in place
   float* Hp = reinterpret_cast<float*>(csm + lay.Hp);
   float* Gp = reinterpret_cast<float*>(csm + lay.Gp);
   float* resp = reinterpret_cast<float*>(csm + lay.resp);
@@ -1209,6 +1299,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
   int dec = 0;  // 1 converged, 2 block too short, 3 iteration cap
   constexpr int cpg = m / 4;  // columns per thread group in C V
   float* Vown = big ? Vall : Vall + static_cast<size_t>(r0) * m;
+  float* U = Vown;  // U = V W replaces the own rows of V in place
   for (int it = 0;; ++it) {
     // ---- orthonormalise Z (Gram partials in Gp): V = Z D L^-T ----
     cluster_sync();
@@ -1289,46 +1380,12 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         for (int c = 0; c < cpg; ++c) Y[r * m + cg * cpg + c] = acc[c] * a.inv_n;
       }
     } else if (big) {
-      // C and V streamed through double-buffered cp.async tiles, 64 own rows
-      // at a time (V rows from the workspace, where every CTA published its own)
-      const int ntile = (L + kCvTileL - 1) / kCvTileL;
-      for (int g0 = 0; g0 < nr; g0 += kCvTileRows) {
-        const int gr = min(kCvTileRows, nr - g0);
-        const float* Cg = Cown + static_cast<size_t>(g0) * L;
-        const int r = tid >> 2, cg = tid & 3;
-        float acc[cpg];
-#pragma unroll
-        for (int c = 0; c < cpg; ++c) acc[c] = 0.f;
-        stage_c_tile(Ct, Cg, gr, L, 0, vecC);
-        stage_v_tile(Vt, a.Vg, L, m, 0);
-        for (int t = 0; t < ntile; ++t) {
-          if (t + 1 < ntile) {
-            stage_c_tile(Ct + ((t + 1) & 1) * kCvTileRows * kCvTileLd, Cg, gr, L, t + 1, vecC);
-            stage_v_tile(Vt + ((t + 1) & 1) * kCvTileL * m, a.Vg, L, m, t + 1);
-            cp_async_wait<2>();  // tile t's two groups have landed
-          } else {
-            cp_async_wait<0>();
-          }
-          __syncthreads();
-          const float* crow = Ct + (t & 1) * kCvTileRows * kCvTileLd + r * kCvTileLd;
-          const int nl = min(kCvTileL, L - t * kCvTileL);
-          const float* vb = Vt + (t & 1) * kCvTileL * m + cg * cpg;
-          for (int l = 0; l < nl; ++l) {
-            const float cv = crow[l];
-#pragma unroll
-            for (int c4 = 0; c4 < cpg; c4 += 4) {
-              const float4 v = *reinterpret_cast<const float4*>(vb + l * m + c4);
-              acc[c4] = fmaf(cv, v.x, acc[c4]);
-              acc[c4 + 1] = fmaf(cv, v.y, acc[c4 + 1]);
-              acc[c4 + 2] = fmaf(cv, v.z, acc[c4 + 2]);
-              acc[c4 + 3] = fmaf(cv, v.w, acc[c4 + 3]);
-            }
-          }
-          __syncthreads();  // the buffers are refilled two tiles later
-        }
-        if (r < gr)
-#pragma unroll
-          for (int c = 0; c < cpg; ++c) Y[(g0 + r) * m + cg * cpg + c] = acc[c] * a.inv_n;
+      constexpr int slots = kClusterThreads / (M / 8);
+      switch ((nr + slots - 1) / slots) {
+        case 1: cv_big<M, 1>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 2: cv_big<M, 2>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 3: cv_big<M, 3>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        default: cv_big<M, 4>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
       }
     } else {
       // C streamed through double-buffered cp.async tiles
@@ -1395,18 +1452,29 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
       W[row * ld + js.rank[col]] = js.V[row * ld + col];
     }
     __syncthreads();
-    // ---- U = V W, Z = Y W (own rows); residual and Gram partials ----
-    for (int idx = tid; idx < nr * m; idx += nthr) {
-      const int r = idx / m, j = idx % m;
-      float u = 0.f, z = 0.f;
+    // ---- U = V W and Z = Y W in place (own rows); residual and Gram partials ----
+    {
+      // the M lanes of a row hold its entries; lane j forms column j from the
+      // row read through shuffles, so the row is read before it is overwritten
+      constexpr int rows_per_warp = 32 / M;
+      const int lane = tid & 31, sub = lane / M, j = lane % M;
+      for (int rb = (tid >> 5) * rows_per_warp; rb < nr; rb += (nthr >> 5) * rows_per_warp) {
+        const int r = rb + sub;
+        const bool ok = r < nr;
+        const float v = ok ? Vown[r * m + j] : 0.f;
+        const float y = ok ? Y[r * m + j] : 0.f;
+        float u = 0.f, z = 0.f;
 #pragma unroll
-      for (int k = 0; k < m; ++k) {
-        const float wk = W[k * ld + j];
-        u = fmaf(Vown[r * m + k], wk, u);
-        z = fmaf(Y[r * m + k], wk, z);
+        for (int k = 0; k < M; ++k) {
+          const float wk = W[k * ld + j];
+          u = fmaf(__shfl_sync(0xffffffffu, v, sub * M + k), wk, u);
+          z = fmaf(__shfl_sync(0xffffffffu, y, sub * M + k), wk, z);
+        }
+        if (ok) {
+          U[r * m + j] = u;
+          Z[r * m + j] = z;
+        }
       }
-      U[idx] = u;
-      Z[idx] = z;
     }
     __syncthreads();
     for (int j = tid; j < m; j += nthr) {
@@ -1648,7 +1716,7 @@ cudaError_t launch_solver_finalize(int L, int m, double eps, int p, int r_overri
 }
 
 bool cluster_solve_fits(int L, int m) {
-  if (L <= 128 || (m != 16 && m != 32)) return false;
+  if (L <= 128 || L > kClusterCtas * kCvBigRows || (m != 16 && m != 32)) return false;
   const int rp = (L + kClusterCtas - 1) / kClusterCtas;
   // (the static shared arrays of the kernel take about 2 KB more)
   return cluster_layout(L, m, rp).total <= (L > kClusterGatherMaxL ? 216 : 200) * 1024;
