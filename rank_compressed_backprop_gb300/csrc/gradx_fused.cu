@@ -364,8 +364,8 @@ __global__ void __launch_bounds__(320, 2)
   const int s0 = item_y * f.spt;                 // first sample of the tile
   const int m0 = s0 * f.Ry;                      // first g_hat_x row of the tile
   const int lt0 = crank * f.lt_per;              // first token tile
-  const int kper = (f.nk + f.cl - 1) / f.cl;     // phase-1 chunks per cluster rank
-  const int kc0 = crank * kper;
+  const int kper = f.kfull ? f.nk : (f.nk + f.cl - 1) / f.cl;  // phase-1 chunks per rank
+  const int kc0 = f.kfull ? 0 : crank * kper;
   int nkc = f.nk - kc0;
   if (nkc > kper) nkc = kper;
   if (nkc < 0) nkc = 0;
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(320, 2)
     tc_fence_after();
     fence_proxy_async_smem();
   }
-  if (f.cl > 1) {
+  if (f.cl > 1 && !f.kfull) {
     // every CTA of the cluster holds a K-slice of the tile.  Reduce-scatter:
     // CTA r sums rows [r*rows_per, ...) over all slices; all-gather: it writes
     // the bf16 result into the expansion operands of every CTA of the cluster.

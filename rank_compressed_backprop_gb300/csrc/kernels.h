@@ -133,6 +133,8 @@ struct FusedArgs {
   int lt_per;        // token tiles per CTA
   int cl;            // cluster size along the token axis (1, 2, 4, 8): phase 1's K
                      // range is split across the cluster and reduced through DSMEM
+  int kfull;         // 1: every CTA of the cluster runs phase 1 over the whole K
+                     // (no exchange; the cluster only splits the token range)
   int q_tma;         // 1: Q^T tiles by TMA (L % 8 == 0); 0: threads fill them
   int a_rows;        // Sq rows per phase-1 TMA box (spt * Ry rounded up to 8, <= 128):
                      // the MMA still reads 128 rows, the ones past the box are unused

@@ -200,6 +200,38 @@ def test_grad_w_x_matches_the_oracle(torch, dtype, B, L, Cx, Cy, Rx, Ry, accumul
     assert_parity(to_np(gx), ref_x, tol(dtype), "g_x")
 
 
+@pytest.mark.parametrize("kfull", ["0", "1"])
+@pytest.mark.parametrize("B,L,Cx,Cy,Rx,Ry", [
+    (32, 512, 768, 768, 8, 8),      # BERT-base block: 12 chunks over a cluster of 4
+    (6, 384, 200, 520, 4, 16),      # 9 chunks over a cluster of 2, ragged strip
+])
+def test_fused_phase_one_whole_or_split(torch, monkeypatch, B, L, Cx, Cy, Rx, Ry, kfull):
+    """The single-kernel input gradient with every cluster CTA running the
+    whole K of g_hat_x = Sq w (no exchange), or each a slice reduced through
+    distributed shared memory: both against the oracle, and the same g_w."""
+    api = _api()
+    monkeypatch.setenv("INSTANT_FUSED_KFULL", kfull)
+    g = rng(1400 + B + L + Cy)
+    Sx = stored(g.standard_normal((B * Rx, Cy)), "bf16")
+    xh = stored(g.standard_normal((B, Rx, Cx)), "bf16")
+    Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
+    Q = stored(orthonormal_rows(g, Ry, L), "bf16")
+    gw = torch.full((Cy, Cx), float("nan"), dtype=torch.float32, device="cuda")
+    gx = torch.full((B, L, Cx), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.full((api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, torch.bfloat16),), 255,
+                    dtype=torch.uint8, device="cuda")
+    n0 = api.launch_count()
+    api.grad_w_x(to_dev(Sx), to_dev(xh), gw, to_dev(Sq), to_dev(w), to_dev(Q), gx, ws, B)
+    torch.cuda.synchronize()
+    assert api.launch_count() - n0 == 1
+    ref_w = O.grad_w(O.decode(Sx).reshape(B, Rx, Cy), O.decode(xh))
+    ref_x = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
+    assert_parity(to_np(gw), ref_w, 2e-3, "g_w")
+    assert_parity(to_np(gx), ref_x, 2e-2, "g_x")
+    assert api.device_status() == 0
+
+
 # --------------------------------------------------------------------------
 # grad_w through the write-streaming kernel (short contraction, K = B*Rx <= 256)
 # --------------------------------------------------------------------------
