@@ -230,8 +230,8 @@ bool use_gradw_stream(int M, int N, int K) {
 // a CTA keeps at least 4 iterations and a tile at most 64 CTAs (more
 // concurrent atomic adds into one tile cost more than they save: 256 samples
 // of 197 tokens on GB300).
-void plan_syrk(int n, const int* B, const int* nkc, int ntiles, int* cs, int* bs) {
-  const long long slots = 2ll * sm_count();
+void plan_syrk(int n, const int* B, const int* nkc, int ntiles, int per_sm, int* cs, int* bs) {
+  const long long slots = static_cast<long long>(per_sm) * sm_count();
   double total = 0.0;
   for (int p = 0; p < n; ++p) total += static_cast<double>(B[p]) * nkc[p] * ntiles;
   double best = 1e300;
@@ -1098,12 +1098,19 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
     CUtensorMap maps[kMaxSyrkBatch];
     b.count = n;
     b.split0[0] = 0;
+    // 128 x 256 tiles, one CTA per SM (INSTANT_SYRK_NARROW: 128 x 128, two per SM)
+    b.wide = std::getenv("INSTANT_SYRK_NARROW") ? 0 : 1;
+    int ntiles_b = ntiles;
+    if (b.wide) {
+      ntiles_b = 0;
+      for (int i = 0; i < nblk; ++i) ntiles_b += (nblk - i + 1) / 2;
+    }
     int Bs[kMaxSyrkBatch], nkcs[kMaxSyrkBatch], cs[kMaxSyrkBatch], bs[kMaxSyrkBatch];
     for (int i = 0; i < n; ++i) {
       Bs[i] = items[g0 + i].B;
       nkcs[i] = cdiv(items[g0 + i].Cdim, 64);
     }
-    plan_syrk(n, Bs, nkcs, ntiles, cs, bs);
+    plan_syrk(n, Bs, nkcs, ntiles_b, b.wide ? 1 : 2, cs, bs);
     for (int i = 0; i < n; ++i) {
       const instant_accumulate_item& it = items[g0 + i];
       SyrkArgs& s = b.s[i];
@@ -1111,7 +1118,7 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
       s.L = L;
       s.C = it.Cdim;
       s.nblk = nblk;
-      s.ntiles = ntiles;
+      s.ntiles = ntiles_b;
       s.nkc = nkcs[i];
       s.Cout = it.C;
       s.cs = cs[i];

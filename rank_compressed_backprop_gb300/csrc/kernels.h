@@ -172,7 +172,8 @@ cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tm
 struct SyrkArgs {
   int B, L, C;
   int nblk;          // ceil(L / 128)
-  int ntiles;        // nblk * (nblk + 1) / 2 upper-triangle tiles
+  int ntiles;        // upper-triangle tiles: nblk * (nblk + 1) / 2 of 128 x 128, or
+                     // sum_i ceil((nblk - i) / 2) of 128 x 256
   int splits;        // CTAs per tile (grid y) = cs * bs
   int cs;            // channel ranges per tile (each CTA walks all of its samples)
   int bs;            // sample ranges per tile (small statistics only)
@@ -180,8 +181,9 @@ struct SyrkArgs {
   float* Cout;       // [L, L]
 };
 
-constexpr int kSyrkStages = 3;  // 96 KB of stages: two CTAs per SM
-size_t syrk_bf16_smem_bytes();
+constexpr int kSyrkStages = 3;      // narrow tiles: 96 KB of stages, two CTAs per SM
+constexpr int kSyrkWideStages = 4;  // wide tiles: 192 KB of stages, one CTA per SM
+size_t syrk_bf16_smem_bytes(bool wide);
 cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st);
 // up to kMaxSyrkBatch statistics of one token length in one launch: problem p
 // owns grid rows [split0[p], split0[p + 1])
@@ -190,6 +192,7 @@ struct SyrkBatch {
   SyrkArgs s[kMaxSyrkBatch];
   int split0[kMaxSyrkBatch + 1];
   int count;
+  int wide;  // 1: 128 x 256 tiles (ntiles counts them), 0: 128 x 128
 };
 cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b, cudaStream_t st);
 cudaError_t launch_syrk_f32(const SyrkArgs& s, const float* t, cudaStream_t st);

@@ -3,9 +3,17 @@
 //   C[i, j] += sum_b sum_c t[b, i, c] * t[b, j, c]      (t = x or g_y)
 // i.e. the token-by-token autocorrelation accumulated over a batch without
 // storing the batch.  This is the one truly tensor-bound step (2L flops per
-// byte of t), so it is a tcgen05 GEMM over the upper-triangle 128x128 tiles of
-// C: both operands are K-major row blocks of the same sample (K = channels),
-// streamed by TMA; the sum over samples continues the K loop.  Grid y splits
+// byte of t), so it is a tcgen05 GEMM over the upper triangle of C: both
+// operands are K-major row blocks of the same sample (K = channels), streamed
+// by TMA; the sum over samples continues the K loop.  Two tile shapes:
+//   * wide (the default): 128 x 256 tiles -- row block bi against the column
+//     blocks bj, bj + 1 (bj = bi + 2p) -- one CTA per SM with a 4-stage ring of
+//     48 KB.  Per 64-channel chunk it reads 48 KB for 4.2 MFLOP (a 128 x 128
+//     tile reads 32 KB for 2.1 MFLOP): with 128 x 128 tiles every SM needs
+//     ~96 B/clk of operands at the tensor peak, more than L2 delivers to all
+//     SMs at once.  A pair on the diagonal (bj = bi) loads its 256 rows once
+//     and takes the first 128 as the A operand;
+//   * narrow: 128 x 128 tiles, two CTAs per SM with a 3-stage ring of 32 KB.  Grid y splits
 // each tile's work into channel ranges (every CTA walks all of its samples in
 // order, so the CTAs running at one time read the same sample and its tiles
 // meet in L2) and, for small statistics only, sample ranges; the host sizes
@@ -19,10 +27,16 @@ namespace instant {
 
 namespace {
 
-constexpr int BT = 128;                  // tile edge
+constexpr int BT = 128;                  // tile edge (rows; columns of a narrow tile)
 constexpr int BK = 64;                   // channels per stage
 constexpr int TILE_BYTES = BT * BK * 2;  // 16 KB
-constexpr int STAGE = 2 * TILE_BYTES;
+
+template <bool WIDE>
+struct SyrkShape {
+  static constexpr int BN = WIDE ? 2 * BT : BT;                  // tile columns
+  static constexpr int STAGE = TILE_BYTES + BN * BK * 2;         // A rows + B rows
+  static constexpr int STAGES = WIDE ? kSyrkWideStages : kSyrkStages;
+};
 
 __device__ __forceinline__ void tile_coords(int t, int nblk, int& bi, int& bj) {
   // t enumerates (bi, bj), bi <= bj, row by row
@@ -36,6 +50,20 @@ __device__ __forceinline__ void tile_coords(int t, int nblk, int& bi, int& bj) {
   bj = i + rem;
 }
 
+// wide tiles: t enumerates (bi, bj = bi + 2p), row by row; bj + 1 may be past
+// the last block (its rows load as zeros and are not stored)
+__device__ __forceinline__ void pair_coords(int t, int nblk, int& bi, int& bj) {
+  int i = 0;
+  int rem = t;
+  while (rem >= (nblk - i + 1) / 2) {
+    rem -= (nblk - i + 1) / 2;
+    ++i;
+  }
+  bi = i;
+  bj = i + 2 * rem;
+}
+
+template <bool WIDE>
 __global__ void __launch_bounds__(128, 1)
     k_syrk_bf16(const __grid_constant__ CUtensorMap tmap0, const __grid_constant__ CUtensorMap tmap1,
                 const __grid_constant__ CUtensorMap tmap2, const __grid_constant__ CUtensorMap tmap3,
@@ -53,15 +81,21 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kSyrkStages * STAGE);
-  uint64_t* empty = full + kSyrkStages;
-  uint64_t* done = empty + kSyrkStages;
+  using SH = SyrkShape<WIDE>;
+  constexpr int STAGE = SH::STAGE;
+  constexpr int NS = SH::STAGES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NS * STAGE);
+  uint64_t* empty = full + NS;
+  uint64_t* done = empty + NS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bi, bj;
-  tile_coords(blockIdx.x, a.nblk, bi, bj);
+  if (WIDE)
+    pair_coords(blockIdx.x, a.nblk, bi, bj);
+  else
+    tile_coords(blockIdx.x, a.nblk, bi, bj);
   const bool diag = bi == bj;
   const int i0 = bi * BT;
   const int j0 = bj * BT;
@@ -72,7 +106,7 @@ __global__ void __launch_bounds__(128, 1)
   const int niter = (kc_hi - kc_lo) * (b_hi - b_lo);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kSyrkStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -81,7 +115,7 @@ __global__ void __launch_bounds__(128, 1)
     prefetch_tmap(&tmap_t);
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, BT);
+    tmem_alloc(tmem_slot, SH::BN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -92,42 +126,53 @@ __global__ void __launch_bounds__(128, 1)
   pdl_wait();
 
   if (warp == 0 && lane == 0) {
-    const uint32_t bytes = diag ? TILE_BYTES : STAGE;
+    // narrow: A rows at the stage start, B rows after them (none on the
+    // diagonal); wide: B's 256 rows after the A slot, A's own rows only off
+    // the diagonal (on it, A is B's first half)
+    const uint32_t bytes = diag ? (WIDE ? 2 * TILE_BYTES : TILE_BYTES) : STAGE;
     int issued = 0;
     // (sample, channel chunk) of iteration it, kept without divisions
     int b = b_lo, kc = kc_lo;
+    int s = 0;
     for (int it = 0; it < niter; ++it) {
-      const int s = it % kSyrkStages;
-      if (it >= kSyrkStages && !mbar_wait(&empty[s], ((it / kSyrkStages) - 1) & 1)) {
+      if (it >= NS && !mbar_wait(&empty[s], ((it / NS) - 1) & 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
       const int c0 = kc * BK;
       uint8_t* dst = smem + s * STAGE;
       mbar_arrive_expect_tx(&full[s], bytes);
-      tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
-      if (!diag) tma_load_3d(dst + TILE_BYTES, &tmap_t, &full[s], c0, j0, b);
+      if (WIDE) {
+        if (!diag) tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
+        tma_load_3d(dst + TILE_BYTES, &tmap_t, &full[s], c0, j0, b);
+        tma_load_3d(dst + 2 * TILE_BYTES, &tmap_t, &full[s], c0, j0 + BT, b);
+      } else {
+        tma_load_3d(dst, &tmap_t, &full[s], c0, i0, b);
+        if (!diag) tma_load_3d(dst + TILE_BYTES, &tmap_t, &full[s], c0, j0, b);
+      }
       ++issued;
       if (++kc == kc_hi) {
         kc = kc_lo;
         ++b;
       }
+      if (++s == NS) s = 0;
     }
-    for (int it = issued - kSyrkStages < 0 ? 0 : issued - kSyrkStages; it < issued; ++it)
-      if (!mbar_wait(&full[it % kSyrkStages], (it / kSyrkStages) & 1)) raise_fault(FAULT_WAIT_FULL);
+    for (int it = issued - NS < 0 ? 0 : issued - NS; it < issued; ++it)
+      if (!mbar_wait(&full[it % NS], (it / NS) & 1)) raise_fault(FAULT_WAIT_FULL);
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t idesc = idesc_bf16_f32(128, SH::BN, 0, 0);
     bool ok = true;
+    int s = 0, par = 0;
     for (int it = 0; it < niter; ++it) {
-      const int s = it % kSyrkStages;
-      if (!mbar_wait(&full[s], (it / kSyrkStages) & 1)) {
+      if (!mbar_wait(&full[s], par)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t a_base = smem_u32(smem + s * STAGE);
-      const uint32_t b_base = diag ? a_base : a_base + TILE_BYTES;
+      const uint32_t stage = smem_u32(smem + s * STAGE);
+      const uint32_t b_base = (WIDE || !diag) ? stage + TILE_BYTES : stage;
+      const uint32_t a_base = (WIDE && diag) ? b_base : stage;
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
@@ -135,6 +180,10 @@ __global__ void __launch_bounds__(128, 1)
         umma_bf16(tmem, ad, bd, idesc, (it | kk) != 0);
       }
       umma_commit(&empty[s]);
+      if (++s == NS) {
+        s = 0;
+        par ^= 1;
+      }
     }
     if (ok && niter > 0) umma_commit(done);
   }
@@ -147,10 +196,12 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const bool vec_ok = (a.L & 3) == 0;
 #pragma unroll 1
-    for (int jc = 0; jc < BT; jc += 16) {
+    for (int jc = 0; jc < SH::BN; jc += 16) {
       float v[16];
       tmem_ld16(taddr + jc, v);
       const int j = j0 + jc;
+      // a column block other than the row block also lands mirrored
+      const bool mirror = !diag || jc >= BT;
       if (i < a.L) {
         float* row = a.Cout + static_cast<size_t>(i) * a.L;
 #pragma unroll
@@ -165,7 +216,7 @@ __global__ void __launch_bounds__(128, 1)
               if (jj + e2 < a.L) atomicAdd(row + jj + e2, v[4 * q + e2]);
           }
         }
-        if (!diag) {
+        if (mirror) {
           // mirrored tile: C[j, i] += D[i, j]; lanes write consecutive i
 #pragma unroll
           for (int q = 0; q < 16; ++q)
@@ -176,7 +227,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, BT);
+  if (warp == 0) tmem_dealloc(tmem, SH::BN);
 }
 
 // fp32 path: one thread per (i, j), full matrix.
@@ -193,9 +244,25 @@ __global__ void k_syrk_f32(const float* __restrict__ t, SyrkArgs a) {
   a.Cout[static_cast<size_t>(i) * a.L + j] += acc;
 }
 
+template <bool WIDE>
+size_t syrk_smem_bytes() {
+  return SyrkShape<WIDE>::STAGES * SyrkShape<WIDE>::STAGE + 256 + 1024;
+}
+
+template <bool WIDE>
+cudaError_t configure_syrk() {
+  static size_t configured_ = 0;
+  const size_t bytes = syrk_smem_bytes<WIDE>();
+  if (bytes <= configured_) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k_syrk_bf16<WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+  if (e == cudaSuccess) configured_ = bytes;
+  return e;
+}
+
 }  // namespace
 
-size_t syrk_bf16_smem_bytes() { return kSyrkStages * STAGE + 256 + 1024; }
+size_t syrk_bf16_smem_bytes(bool wide) { return wide ? syrk_smem_bytes<true>() : syrk_smem_bytes<false>(); }
 
 cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b, cudaStream_t st) {
   if (b.count < 1 || b.count > kMaxSyrkBatch || b.split0[0] != 0) return cudaErrorInvalidValue;
@@ -203,20 +270,18 @@ cudaError_t launch_syrk_bf16_batch(const CUtensorMap* tmaps, const SyrkBatch& b,
     if (b.s[p].L != b.s[0].L || b.split0[p + 1] != b.split0[p] + b.s[p].splits || b.s[p].splits < 1 ||
         b.s[p].cs < 1 || b.s[p].bs < 1 || b.s[p].cs * b.s[p].bs != b.s[p].splits)
       return cudaErrorInvalidValue;
-  const size_t bytes = syrk_bf16_smem_bytes();
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_syrk_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
+  const cudaError_t e = b.wide ? configure_syrk<true>() : configure_syrk<false>();
+  if (e != cudaSuccess) return e;
   const CUtensorMap& m0 = tmaps[0];
   const CUtensorMap& m1 = tmaps[b.count > 1 ? 1 : 0];
   const CUtensorMap& m2 = tmaps[b.count > 2 ? 2 : 0];
   const CUtensorMap& m3 = tmaps[b.count > 3 ? 3 : 0];
-  return launch_ex(k_syrk_bf16, dim3(b.s[0].ntiles, b.split0[b.count]), dim3(128), bytes, st, 1,
-                   pdl_enabled(), m0, m1, m2, m3, b);
+  const dim3 grid(b.s[0].ntiles, b.split0[b.count]);
+  if (b.wide)
+    return launch_ex(k_syrk_bf16<true>, grid, dim3(128), syrk_smem_bytes<true>(), st, 1, pdl_enabled(),
+                     m0, m1, m2, m3, b);
+  return launch_ex(k_syrk_bf16<false>, grid, dim3(128), syrk_smem_bytes<false>(), st, 1, pdl_enabled(),
+                   m0, m1, m2, m3, b);
 }
 
 cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaStream_t st) {
@@ -225,6 +290,7 @@ cudaError_t launch_syrk_bf16(const CUtensorMap& tmap_t, const SyrkArgs& s, cudaS
   b.split0[0] = 0;
   b.split0[1] = s.splits;
   b.count = 1;
+  b.wide = 0;
   return launch_syrk_bf16_batch(&tmap_t, b, st);
 }
 

@@ -113,10 +113,22 @@ def test_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
 # --------------------------------------------------------------------------
 # calib_accumulate
 # --------------------------------------------------------------------------
+def _syrk_tiles(monkeypatch, tiles):
+    """128 x 256 tiles (the default) or 128 x 128 (INSTANT_SYRK_NARROW)."""
+    if tiles == "narrow":
+        monkeypatch.setenv("INSTANT_SYRK_NARROW", "1")
+    else:
+        monkeypatch.delenv("INSTANT_SYRK_NARROW", raising=False)
+
+
+@pytest.mark.parametrize("tiles", ["wide", "narrow"])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("B,L,C", [(2, 64, 64), (3, 300, 200), (4, 49, 448), (2, 256, 1032),
-                                   (1, 520, 72)])
-def test_calib_accumulate(torch, dtype, B, L, C):
+                                   (1, 520, 72), (2, 1000, 136)])
+def test_calib_accumulate(torch, monkeypatch, dtype, B, L, C, tiles):
+    if dtype == "f32" and tiles == "narrow":
+        pytest.skip("one fp32 path")
+    _syrk_tiles(monkeypatch, tiles)
     g = rng(500 + L + C)
     t1 = stored(g.standard_normal((B, L, C)), dtype)
     t2 = stored(g.standard_normal((B + 1, L, C)), dtype)
@@ -138,7 +150,11 @@ def test_calib_accumulate(torch, dtype, B, L, C):
     ("bf16", 49, [(40, 448), (40, 1792)]),                    # sample ranges per tile too
     ("f32", 72, [(2, 40), (3, 48)]),
 ])
-def test_calib_accumulate_batch(torch, dtype, L, dims):
+@pytest.mark.parametrize("tiles", ["wide", "narrow"])
+def test_calib_accumulate_batch(torch, monkeypatch, dtype, L, dims, tiles):
+    if dtype == "f32" and tiles == "narrow":
+        pytest.skip("one fp32 path")
+    _syrk_tiles(monkeypatch, tiles)
     g = rng(700 + L + len(dims))
     ts = [stored(g.standard_normal((B, L, C)), dtype) for B, C in dims]
     api = _api()
