@@ -1098,8 +1098,9 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
     CUtensorMap maps[kMaxSyrkBatch];
     b.count = n;
     b.split0[0] = 0;
-    // 128 x 256 tiles, one CTA per SM (INSTANT_SYRK_NARROW: 128 x 128, two per SM)
-    b.wide = std::getenv("INSTANT_SYRK_NARROW") ? 0 : 1;
+    // 128 x 256 tiles, one CTA per SM (INSTANT_SYRK_NARROW: 128 x 128, two per
+    // SM); a single row block (L <= 128) would spend half of a wide tile on zeros
+    b.wide = (nblk >= 2 && !std::getenv("INSTANT_SYRK_NARROW")) ? 1 : 0;
     int ntiles_b = ntiles;
     if (b.wide) {
       ntiles_b = 0;

@@ -66,6 +66,28 @@ __global__ void __launch_bounds__(128, 1)
     fence_barrier_init();
     prefetch_tmap(&tmap_a);
     prefetch_tmap(&tmap_b);
+    // the ring's first chunks into L2 while the predecessor finishes (w for
+    // g_hat_x comes from HBM; L2 is the point of coherence, so a line fetched
+    // early is still updated by the predecessor's writes); at most 32 MB over
+    // the grid
+    const long long ctas = static_cast<long long>(gridDim.x) * gridDim.y * gridDim.z;
+    const long long cap = (32ll << 20) / (ctas * STAGE);
+    const int npf = static_cast<int>(cap < nkc ? (cap < NS ? cap : NS) : (nkc < NS ? nkc : NS));
+    for (int i = 0; i < npf; ++i) {
+      const int k0 = (kc_begin + i) * BK;
+      if (A_MN) {
+        tma_prefetch_l2_2d(&tmap_a, m0, k0);
+        tma_prefetch_l2_2d(&tmap_a, m0 + 64, k0);
+      } else {
+        tma_prefetch_l2_2d(&tmap_a, k0, m0);
+      }
+      if (B_MN) {
+#pragma unroll
+        for (int h = 0; h < BN / 64; ++h) tma_prefetch_l2_2d(&tmap_b, n0 + 64 * h, k0);
+      } else {
+        tma_prefetch_l2_2d(&tmap_b, k0, n0);
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, BN);
