@@ -540,6 +540,55 @@ bool cluster_finish(SolveJob& j, const SolverResult& res, SolveOut* o, double* e
   return true;
 }
 
+// L <= 128 without host round trips: the energies, one full-Jacobi launch
+// for all the statistics (one CTA each; a statistic whose energy is not
+// finite and positive is skipped) and the projector rows, all queued on the
+// stream; small_finish reads each result block afterwards
+instant_status solve_small_async(std::vector<SolveJob*>& js, cudaStream_t st) {
+  for (size_t i0 = 0; i0 < js.size(); i0 += kMaxJacobiBatch) {
+    const size_t n = std::min<size_t>(kMaxJacobiBatch, js.size() - i0);
+    JacobiBatch b;
+    b.L = js[i0]->L;
+    b.max_sweeps = js[i0]->max_sweeps;
+    b.count = static_cast<int>(n);
+    for (size_t u = 0; u < n; ++u) {
+      SolveJob& j = *js[i0 + u];
+      if (launch_solver_energy(j.C, j.L, j.w, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+      b.C[u] = j.C;
+      b.inv_n[u] = static_cast<float>(j.inv_n);
+      b.w[u] = j.w;
+      b.max_sweeps = std::max(b.max_sweeps, j.max_sweeps);
+    }
+    if (launch_jacobi_full_batch(b, st) != cudaSuccess) return INSTANT_ERR_CUDA;
+    for (size_t u = 0; u < n; ++u) {
+      SolveJob& j = *js[i0 + u];
+      if (launch_solver_finalize(j.L, j.L, j.prm.eps, j.prm.p, j.prm.r_override,
+                                 j.prm.scale_on ? 1 : 0, j.rows_out, j.r_cap, j.out_bf16, j.inv_n2,
+                                 j.w, st) != cudaSuccess)
+        return INSTANT_ERR_CUDA;
+    }
+  }
+  return INSTANT_OK;
+}
+
+void small_finish(const SolveJob& j, const SolverResult& res, SolveOut* o, double* eig_out,
+                  instant_status* status) {
+  const double E = res.energy_sum * j.inv_n2;
+  if (res.nonfinite || !std::isfinite(E) || !(E > 0.0)) {
+    *status = INSTANT_ERR_NONFINITE;
+    return;
+  }
+  instant_status st1 = res.jacobi_failed ? INSTANT_ERR_NOT_CONVERGED : INSTANT_OK;
+  if (res.R > j.r_cap && st1 == INSTANT_OK) st1 = INSTANT_ERR_SHAPE;
+  o->k = res.k;
+  o->R = res.R < j.r_cap ? res.R : j.r_cap;
+  o->scale = res.scale;
+  o->energy = E;
+  if (eig_out)
+    for (int i = 0; i < j.r_cap; ++i) eig_out[i] = i < j.L ? res.theta[i] : 0.0;
+  *status = st1;
+}
+
 // energy, then full Jacobi (L <= 128) or the multi-launch subspace iteration
 // with host-side convergence checks, then the projector rows
 instant_status solve_multi(SolveJob& j, SolveOut* o, double* eig_out, cudaStream_t st) {
@@ -1098,9 +1147,14 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
     CUtensorMap maps[kMaxSyrkBatch];
     b.count = n;
     b.split0[0] = 0;
-    // 128 x 256 tiles, one CTA per SM (INSTANT_SYRK_NARROW: 128 x 128, two per
-    // SM); a single row block (L <= 128) would spend half of a wide tile on zeros
-    b.wide = (nblk >= 2 && !std::getenv("INSTANT_SYRK_NARROW")) ? 1 : 0;
+    // 128 x 256 tiles, one CTA per SM, from 8 row blocks (L > 896) on
+    // (INSTANT_SYRK_NARROW: 128 x 128, two per SM).  With fewer blocks the
+    // pairs that run past the last block waste more (1/6 of the work at 4
+    // blocks): the FFN's L = 512 statistics measured 174 us wide against 150
+    // us narrow, the long-sequence L = 2048 ones 2.59 ms against 3.05 ms.
+    // INSTANT_SYRK_WIDE forces wide tiles for any L above 128.
+    b.wide = (nblk >= 8 && !std::getenv("INSTANT_SYRK_NARROW")) ? 1 : 0;
+    if (nblk >= 2 && std::getenv("INSTANT_SYRK_WIDE")) b.wide = 1;
     int ntiles_b = ntiles;
     if (b.wide) {
       ntiles_b = 0;
@@ -1227,8 +1281,18 @@ instant_status instant_calib_solve_batch(instant_calib_problem* problems, int co
       }
     }
   }
+  // the small statistics (L <= 128): queued too, results in the same block
+  std::vector<char> small(count, 0);
+  std::vector<SolveJob*> sj;
+  for (int i = 0; i < count; ++i) {
+    if (launched[i] || jobs[i].L > 128 || std::getenv("INSTANT_SOLVER_MULTI")) continue;
+    jobs[i].w.res = res_dev + i;
+    sj.push_back(&jobs[i]);
+    small[i] = 1;
+  }
+  if (!sj.empty() && solve_small_async(sj, st) != INSTANT_OK) return INSTANT_ERR_CUDA;
   bool any = false;
-  for (int i = 0; i < count; ++i) any = any || launched[i];
+  for (int i = 0; i < count; ++i) any = any || launched[i] || small[i];
   if (any && cudaMemcpyAsync(res.data(), res_dev, sizeof(SolverResult) * count,
                              cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return INSTANT_ERR_CUDA;
@@ -1238,7 +1302,13 @@ instant_status instant_calib_solve_batch(instant_calib_problem* problems, int co
     instant_calib_problem& q = problems[i];
     SolveOut o;
     instant_status s1 = INSTANT_OK;
-    const bool done = launched[i] && cluster_finish(jobs[i], res[i], &o, q.eig_out, &s1);
+    bool done = false;
+    if (small[i]) {
+      small_finish(jobs[i], res[i], &o, q.eig_out, &s1);
+      done = true;
+    } else if (launched[i]) {
+      done = cluster_finish(jobs[i], res[i], &o, q.eig_out, &s1);
+    }
     if (!done) s1 = solve_multi(jobs[i], &o, q.eig_out, st);
     q.k = o.k;
     q.R = o.R;

@@ -280,12 +280,32 @@ __host__ __device__ inline size_t jac_smem_bytes(int n) {
 // ---------------------------------------------------------------------------
 // full Jacobi (L <= 128): theta (desc) -> res->theta, vectors -> U[:, rank]
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void jacobi_full(const float* __restrict__ C, int L, float inv_n,
+                                            int max_sweeps, SolverWs w);
+
 __global__ void __launch_bounds__(kJacThreads) k_jacobi_full(const float* __restrict__ C, int L,
                                                              float inv_n, int max_sweeps,
                                                              SolverWs w) {
+  jacobi_full(C, L, inv_n, max_sweeps, w);
+}
+
+// one statistic per CTA
+__global__ void __launch_bounds__(kJacThreads) k_jacobi_full_batch(const __grid_constant__ JacobiBatch b) {
+  const int i = blockIdx.x;
+  jacobi_full(b.C[i], b.L, b.inv_n[i], b.max_sweeps, b.w[i]);
+}
+
+__device__ __forceinline__ void jacobi_full(const float* __restrict__ C, int L, float inv_n,
+                                            int max_sweeps, SolverWs w) {
   extern __shared__ uint8_t smem[];
   JacSmem s = jac_carve(smem, L);
   const int ld = L + 1;
+  // a statistic whose energy is not finite and positive is not solved (the
+  // caller reports it from the result block)
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = w.res->nonfinite || !(w.res->energy_sum > 0.0);
+  __syncthreads();
+  if (s_skip) return;
   for (int idx = threadIdx.x; idx < L * L; idx += blockDim.x) {
     const int i = idx / L, j = idx - (idx / L) * L;
     s.A[i * ld + j] = 0.5f * (C[i * L + j] + C[j * L + i]) * inv_n;
@@ -689,6 +709,8 @@ __global__ void k_finalize(int L, int m, double eps, int p, int r_override, int 
   __shared__ int sR;
   __shared__ float ss;
   SolverResult* r = w.res;
+  // no projector from a statistic whose energy is not finite and positive
+  if (r->nonfinite || !(r->energy_sum > 0.0)) return;
   if (threadIdx.x == 0) {
     const double E = r->energy_sum * inv_n2;
     int k = k_rule(r->theta, m, eps * E);
@@ -1629,6 +1651,8 @@ cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t
   const size_t count = static_cast<size_t>(L) * L;
   int blocks = static_cast<int>((count + 255) / 256);
   if (blocks > 1024) blocks = 1024;
+  // up to L = 128 one block: the same sum, in the same order, on every call
+  if (L <= 128) blocks = 1;
   k_solver_energy<<<blocks, 256, 0, st>>>(C, count, w.res);
   count_launches(2);
   return cudaGetLastError();
@@ -1638,6 +1662,16 @@ static cudaError_t set_smem(const void* f, size_t bytes) {
   // 200 KB up front for every solver kernel: one attribute call per kernel
   (void)bytes;
   return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+}
+
+cudaError_t launch_jacobi_full_batch(const JacobiBatch& b, cudaStream_t st) {
+  if (b.count < 1 || b.count > kMaxJacobiBatch || b.L < 1 || b.L > 128) return cudaErrorInvalidValue;
+  const size_t bytes = jac_smem_bytes(b.L);
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(k_jacobi_full_batch), bytes);
+  if (e != cudaSuccess) return e;
+  k_jacobi_full_batch<<<b.count, jac_threads(b.L), bytes, st>>>(b);
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_sweeps, SolverWs w,

@@ -230,7 +230,16 @@ size_t solver_workspace_bytes(int L);
 SolverWs solver_carve(void* ws, int L);
 
 cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t st);
+constexpr int kMaxJacobiBatch = 16;
 // full Jacobi of C/n (L <= 128): eigenvalues -> res->theta, vectors -> U columns
+// several statistics of one L <= 128 in one launch, one CTA each
+struct JacobiBatch {
+  const float* C[kMaxJacobiBatch];
+  float inv_n[kMaxJacobiBatch];
+  SolverWs w[kMaxJacobiBatch];
+  int L, max_sweeps, count;
+};
+cudaError_t launch_jacobi_full_batch(const JacobiBatch& b, cudaStream_t st);
 cudaError_t launch_jacobi_full(const float* C, int L, double inv_n, int max_sweeps, SolverWs w,
                                cudaStream_t st);
 // subspace iteration building blocks

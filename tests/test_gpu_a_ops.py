@@ -114,10 +114,12 @@ def test_grad_x(torch, dtype, B, L, Cx, Cy, Ry):
 # calib_accumulate
 # --------------------------------------------------------------------------
 def _syrk_tiles(monkeypatch, tiles):
-    """128 x 256 tiles (the default) or 128 x 128 (INSTANT_SYRK_NARROW)."""
+    """128 x 256 tiles (forced for any L > 128) or 128 x 128 (forced)."""
     if tiles == "narrow":
         monkeypatch.setenv("INSTANT_SYRK_NARROW", "1")
+        monkeypatch.delenv("INSTANT_SYRK_WIDE", raising=False)
     else:
+        monkeypatch.setenv("INSTANT_SYRK_WIDE", "1")
         monkeypatch.delenv("INSTANT_SYRK_NARROW", raising=False)
 
 

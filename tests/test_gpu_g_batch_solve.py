@@ -140,3 +140,30 @@ def test_bad_problem_stops_the_whole_call(torch):
     assert st == [0, 8]
     assert res[0].R == 8 and not bool((good == 3.0).all())
     assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("L", [49, 100, 128])
+def test_small_statistics_in_one_synchronisation(torch, L):
+    """L <= 128 (full Jacobi): the batch queues every problem's launches and
+    reads all results with one synchronisation; each result is bit for bit
+    the single call's, and a statistic without energy fails alone, its rows
+    untouched."""
+    from rank_compressed_backprop_gb300 import api
+
+    specs = [(_planted(360 + L + i, L, _spectrum(L, 1e4, 1.5 + 0.5 * i, 1.0), 32), 32, 8,
+              dict(eps=0.95, p=2, r_override=0)) for i in range(3)]
+    res_b, res_s, rows_b, rows_s = _solve_both(torch, specs, torch.bfloat16)
+    _same(res_b, res_s, rows_b, rows_s, torch)
+    for r in res_b:
+        assert r.R >= 1
+    C = to_dev(specs[0][0])
+    good = torch.full((8, L), 3.0, device="cuda")
+    bad = torch.full((8, L), 3.0, device="cuda")
+    Z = torch.zeros(L, L, device="cuda")
+    res, st = api.calib_solve_batch([dict(C=C, n_samples=32, rows_out=good, r_override=8),
+                                     dict(C=Z, n_samples=32, rows_out=bad, r_override=8)],
+                                    raise_on_error=False)
+    assert st == [0, 8]
+    assert res[0].R == 8 and not bool((good == 3.0).all())
+    assert bool((bad == 3.0).all())
+    assert api.device_status() == 0
