@@ -337,7 +337,7 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
   f.kfull = (f.cl > 1 && f.nk <= 12) ? 1 : 0;
   if (const char* v = std::getenv("INSTANT_FUSED_KFULL")) f.kfull = (f.cl > 1 && std::atoi(v) != 0) ? 1 : 0;
   const int kper = f.kfull ? f.nk : cdiv(f.nk, f.cl);
-  f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;
+  f.stages = kper < 3 ? (kper < 1 ? 1 : kper) : 3;  // deepened below for compact stages
   // smaller sample tiles when the grid would not cover the SMs
   while (f.spt > 2 && cdiv(Cx, f.BN) * cdiv(B, f.spt) * f.cl < sm_count()) f.spt /= 2;
   f.a_rows = std::min(128, round_up(f.spt * Ry, 8));
@@ -418,6 +418,13 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
       const uint32_t b2[2] = {64, static_cast<uint32_t>(a.NT)};
       if (!make_map(&mpq, pp->PQ, 2, d2, s2, b2)) return INSTANT_ERR_CUDA;
     }
+  }
+  // at most 64 rows of Sq: 16 KB phase-1 stages, so up to 5 of them while two
+  // CTAs still share an SM (a BERT-base block's phase 1 streams 12 chunks per
+  // CTA against L2 latency: the deeper ring keeps more of them in flight)
+  if (f.a_rows <= 64 && f.BN == 64 && kper > 3) {
+    f.stages = std::min(kper, 5);
+    while (f.stages > 3 && gradx_fused_smem_bytes(f) > 113 * 1024) --f.stages;
   }
   return from_cuda(launch_gradx_fused(ms, mw, mq, mo, msx, mxh, mgy, mpq, f, st));
 }

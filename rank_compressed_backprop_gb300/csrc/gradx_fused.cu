@@ -60,10 +60,18 @@ struct FLay {
 
 // gw: the launch also runs weight-gradient tiles, whose 3-stage ring needs 72 KB;
 // proj_bytes: the projection phase's ring (0: none), also at the start
+// A slot of a phase-1 stage: with at most 64 rows of Sq (and 64-column strips)
+// only 8 KB are loaded; the M = 128 MMA then reads rows 64..127 from the B
+// slot after it, results that are never used.  The smaller stage lets the
+// ring run deeper.
+__host__ __device__ inline uint32_t fused_a_bytes(int a_rows, int BN) {
+  return (a_rows <= 64 && BN == 64) ? A_BYTES / 2 : A_BYTES;
+}
+
 __host__ __device__ inline FLay fused_layout(int BN, int KR, int stages, int lt_per, int spt,
-                                             bool gw, uint32_t proj_bytes) {
+                                             bool gw, uint32_t proj_bytes, uint32_t a_bytes) {
   FLay l;
-  l.stage = A_BYTES + BN * BK * 2;
+  l.stage = a_bytes + BN * BK * 2;
   l.ring = 0;
   const uint32_t ring_bytes = stages * l.stage;
   const uint32_t stg_bytes = 4 * (BN / 64) * BOX;  // staging reuses the ring after phase 1
@@ -303,7 +311,8 @@ __global__ void __launch_bounds__(320, 2)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int KR = f.KR;
   const int NS = f.stages;
-  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f));
+  const uint32_t a_bytes = fused_a_bytes(f.a_rows, BN);
+  const FLay lay = fused_layout(BN, KR, NS, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f), a_bytes);
   uint8_t* ring = smem + lay.ring;
   uint8_t* stg = smem + lay.stg;
   uint8_t* sQ = smem + lay.qt;
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(320, 2)
           break;
         }
         uint8_t* sa = ring + s * lay.stage;
-        uint8_t* sb = sa + A_BYTES;
+        uint8_t* sb = sa + a_bytes;
         const int k0 = (kc0 + i) * BK;
         mbar_arrive_expect_tx(&full[s], f.a_rows * BK * 2 + BN * BK * 2);
         tma_load_2d(sa, &tmap_sq, &full[s], k0, m0);
@@ -489,7 +498,7 @@ __global__ void __launch_bounds__(320, 2)
         }
         tc_fence_after();
         const uint32_t a_base = smem_u32(ring + s * lay.stage);
-        const uint32_t b_base = a_base + A_BYTES;
+        const uint32_t b_base = a_base + a_bytes;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
@@ -707,7 +716,8 @@ dim3 fused_grid(const FusedArgs& f) {
 }
 
 size_t fused_smem_bytes(const FusedArgs& f) {
-  size_t b = fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f))
+  size_t b = fused_layout(f.BN, f.KR, f.stages, f.lt_per, f.spt, f.gw_mt > 0, fused_proj_bytes(f),
+                          fused_a_bytes(f.a_rows, f.BN))
                  .total +
              1024;
   // with the projection phase at most two CTAs share an SM, so that two
@@ -752,7 +762,7 @@ cudaError_t launch_gradx_fused(const CUtensorMap& tmap_sq, const CUtensorMap& tm
                                const CUtensorMap& tmap_sx, const CUtensorMap& tmap_xh,
                                const CUtensorMap& tmap_gy, const CUtensorMap& tmap_pq,
                                const FusedArgs& f, cudaStream_t st) {
-  if (f.stages < 1 || f.stages > 4 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
+  if (f.stages < 1 || f.stages > 6 || f.spt < 1 || f.spt * f.Ry > 128) return cudaErrorInvalidValue;
   if (f.a_rows < f.spt * f.Ry || f.a_rows > BM || f.a_rows % 8 != 0) return cudaErrorInvalidValue;
   if (f.cl != 1 && f.cl != 2 && f.cl != 4 && f.cl != 8) return cudaErrorInvalidValue;
   if (f.lt_per * f.cl < f.nlt) return cudaErrorInvalidValue;

@@ -128,7 +128,7 @@ struct FusedArgs {
   int spt;           // samples per g_hat_x tile (spt * Ry <= 128)
   int BN;            // column strip (64 or 128)
   int nk;            // ceil(Cy / 64)
-  int stages;        // phase-1 TMA ring depth (1..4)
+  int stages;        // phase-1 TMA ring depth (1..6)
   int nlt;           // ceil(L / 128)
   int lt_per;        // token tiles per CTA
   int cl;            // cluster size along the token axis (1, 2, 4, 8): phase 1's K
