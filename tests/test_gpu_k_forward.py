@@ -49,6 +49,7 @@ def _run(torch, dtype, B, L, Cx, Cy, Rx, seed):
     ("bf16", 2, 256, 512, 768, 8, True),       # two token tiles per sample, four column tiles
     ("bf16", 3, 384, 256, 200, 16, True),      # column tail (200 % 192)
     ("bf16", 1, 128, 4096, 392, 32, True),     # the largest fused rank, 64 channel chunks
+    ("bf16", 32, 512, 768, 768, 8, True),      # the BERT-base block's layer (B = 32, L = 512)
     ("bf16", 2, 256, 264, 200, 16, False),     # 264 channels: no chunk pairs -> two launches
     ("bf16", 2, 130, 256, 384, 8, False),      # 130 tokens: tiles straddle samples -> two launches
     ("bf16", 2, 256, 512, 384, 40, False),     # rank beyond the flush warp -> two launches
