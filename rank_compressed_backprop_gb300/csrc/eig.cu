@@ -232,8 +232,12 @@ __device__ bool block_jacobi(float* A, float* A2, float* V, int n, int ld, float
 
 // threads for a one-CTA Jacobi of order n: barriers are nearly free for a
 // single warp, so small problems run on one warp
+// threads of a full-Jacobi CTA: a round updates (N/2)^2 2x2 blocks and N^2/2
+// entries of V, about 15 dependent shared-memory items a thread at 128 threads
+// for N = 50; with 512 the round is shorter (the ViT-MLP statistics, L = 49:
+// see the calibration notes)
 __host__ __device__ inline int jac_threads(int n) {
-  return n <= 24 ? 32 : (n <= 40 ? 64 : (n <= 72 ? 128 : 256));
+  return n <= 24 ? 128 : 512;
 }
 
 // rank of diagonal entry i in descending order (ties: lower index first)
