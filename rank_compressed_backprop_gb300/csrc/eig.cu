@@ -986,10 +986,8 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
 constexpr int kClusterCtas = 8;
 constexpr int kClusterThreads = 256;
 
-// Long token axes: Y = C V over all of the CTA's rows at once.  Each thread
-// accumulates RB rows x 8 columns of Y, so that one 16-byte load of C (four
-// tokens of one row) and two of V (eight columns of one token) feed up to 32
-// FMAs; C and V arrive in 16-token chunks through a 4-deep cp.async ring.
+// Long token axes: Y = C V over all of the CTA's rows at once (see cv_big);
+// C and V arrive in 16-token chunks through a 4-deep cp.async ring.
 constexpr int kCvBigK = 16;       // tokens per chunk
 constexpr int kCvBigLd = 20;      // padded row stride of a C chunk: 16-byte rows, conflict-free
 constexpr int kCvBigStages = 4;
@@ -1026,16 +1024,22 @@ __device__ __forceinline__ void stage_cv_chunk(float* cdst, float* vdst, const f
   cp_async_commit();
 }
 
-// Y[r, :] = C[own row r, :] V / n for the CTA's nr rows; thread (slot, cg)
-// owns rows slot + i * slots (i < RB) and columns [8 cg, 8 cg + 8).  V is read
-// from the workspace where every CTA of the cluster published its rows.
+// Y[r, :] = C[own row r, :] V / n for the CTA's nr rows.  The CTA's threads
+// form two halves, each taking 8 of a chunk's 16 tokens; thread (slot, cg) of
+// a half owns rows slot + i * slots (i < RB) and columns [8 cg, 8 cg + 8), so
+// per 4 tokens RB 16-byte loads of C and 8 of V feed 32 RB FMAs.  The halves'
+// sums meet in the idle ring at the end.  V is read from the workspace where
+// every CTA of the cluster published its rows.
 template <int M, int RB>
 __device__ __forceinline__ void cv_big(const float* Cown, int nr, const float* Vg, int L, bool vec,
                                        float* Cs, float* Vs, float* Y, float inv_n) {
+  constexpr int NH = kClusterThreads / 2;  // threads of a half
   constexpr int ncg = M / 8;
-  constexpr int slots = kClusterThreads / ncg;
+  constexpr int slots = NH / ncg;
   constexpr int cstage = kCvBigRows * kCvBigLd, vstage = kCvBigK * M;
-  const int cg = threadIdx.x % ncg, slot = threadIdx.x / ncg;
+  const int half = threadIdx.x / NH;
+  const int t = threadIdx.x - half * NH;
+  const int cg = t % ncg, slot = t / ncg;
   float acc[RB][8];
 #pragma unroll
   for (int i = 0; i < RB; ++i)
@@ -1044,19 +1048,19 @@ __device__ __forceinline__ void cv_big(const float* Cown, int nr, const float* V
   const int nch = (L + kCvBigK - 1) / kCvBigK;
   for (int s = 0; s < kCvBigStages - 1; ++s)
     stage_cv_chunk(Cs + s * cstage, Vs + s * vstage, Cown, nr, Vg, L, M, s, vec);
-  for (int t = 0; t < nch; ++t) {
-    cp_async_wait<kCvBigStages - 2>();  // chunk t's group (this thread's copies) has landed
-    __syncthreads();                    // ... everyone's; the slot of chunk t - 1 is free
+  for (int t2 = 0; t2 < nch; ++t2) {
+    cp_async_wait<kCvBigStages - 2>();  // chunk t2's group (this thread's copies) has landed
+    __syncthreads();                    // ... everyone's; the slot of chunk t2 - 1 is free
     {
-      const int s = t + kCvBigStages - 1;
+      const int s = t2 + kCvBigStages - 1;
       const int b = s % kCvBigStages;
       stage_cv_chunk(Cs + b * cstage, Vs + b * vstage, Cown, nr, Vg, L, M, s, vec);
     }
-    const int b = t % kCvBigStages;
-    const float* cb = Cs + b * cstage + slot * kCvBigLd;
-    const float* vb = Vs + b * vstage + cg * 8;
+    const int b = t2 % kCvBigStages;
+    const float* cb = Cs + b * cstage + slot * kCvBigLd + half * (kCvBigK / 2);
+    const float* vb = Vs + b * vstage + half * (kCvBigK / 2) * M + cg * 8;
 #pragma unroll
-    for (int k4 = 0; k4 < kCvBigK; k4 += 4) {
+    for (int k4 = 0; k4 < kCvBigK / 2; k4 += 4) {
       float4 c[RB];
 #pragma unroll
       for (int i = 0; i < RB; ++i) c[i] = *reinterpret_cast<const float4*>(cb + i * slots * kCvBigLd + k4);
@@ -1080,14 +1084,25 @@ __device__ __forceinline__ void cv_big(const float* Cown, int nr, const float* V
     }
   }
   cp_async_wait<0>();  // the empty groups past the end
-  __syncthreads();     // the ring is free for the next iteration's prologue
+  __syncthreads();     // the ring is idle: the second half parks its sums there
+  float* red = Cs;     // [RB * 8][NH]
+  if (half == 1) {
 #pragma unroll
-  for (int i = 0; i < RB; ++i) {
-    const int r = slot + i * slots;
-    if (r < nr)
+    for (int i = 0; i < RB; ++i)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) Y[r * M + cg * 8 + c] = acc[i][c] * inv_n;
+      for (int c = 0; c < 8; ++c) red[(i * 8 + c) * NH + t] = acc[i][c];
   }
+  __syncthreads();
+  if (half == 0) {
+#pragma unroll
+    for (int i = 0; i < RB; ++i) {
+      const int r = slot + i * slots;
+      if (r < nr)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) Y[r * M + cg * 8 + c] = (acc[i][c] + red[(i * 8 + c) * NH + t]) * inv_n;
+    }
+  }
+  __syncthreads();  // the ring is free for the next iteration's prologue
 }
 
 // row stride of the resident C rows: 4 mod 32 words, so that the eight rows a
@@ -1406,12 +1421,16 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
         for (int c = 0; c < cpg; ++c) Y[r * m + cg * cpg + c] = acc[c] * a.inv_n;
       }
     } else if (big) {
-      constexpr int slots = kClusterThreads / (M / 8);
+      constexpr int slots = (kClusterThreads / 2) / (M / 8);
       switch ((nr + slots - 1) / slots) {
         case 1: cv_big<M, 1>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
         case 2: cv_big<M, 2>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
         case 3: cv_big<M, 3>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
-        default: cv_big<M, 4>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 4: cv_big<M, 4>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 5: cv_big<M, 5>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 6: cv_big<M, 6>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        case 7: cv_big<M, 7>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
+        default: cv_big<M, 8>(Cown, nr, a.Vg, L, vecC, Ct, Vt, Y, a.inv_n); break;
       }
     } else {
       // C streamed through double-buffered cp.async tiles
