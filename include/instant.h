@@ -156,9 +156,11 @@ size_t instant_grad_x_workspace_bytes(int B, int L, int Cx, int Cy, int Ry, inst
  * g_tilde_x = Q^T g_hat_y2 w) in one call: the same products as
  * instant_grad_w(Sx, xhat, gw, accumulate, ...) followed by
  * instant_grad_x(Sq, w, Q, gx, ws, ...) (g_w may differ in the order of its
- * fp32 additions), with the same arguments, layouts and limits.  Where the single-kernel input gradient applies (bf16, short Cy) the
- * weight-gradient tiles run inside the same launch, on the SMs the input
- * gradient leaves free; otherwise the two calls are made in turn.
+ * fp32 additions), with the same arguments, layouts and limits.  Where the
+ * single-kernel input gradient applies (bf16, short Cy, and at most 64 MiB of
+ * g_tilde_x when L >= 128) the weight-gradient tiles run inside the same
+ * launch, on the SMs the input gradient leaves free; otherwise the two calls
+ * are made in turn.
  */
 instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int accumulate,
                                 const void* Sq, const void* w, const void* Q, void* gx,
@@ -172,8 +174,8 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
  * by instant_grad_w_x(Sx, xhat, gw, accumulate, Sq, w, Q = rows Rx.. of PQ,
  * gx, ...), which is what it runs.  With the environment variable
  * INSTANT_ONE_LAUNCH_BACKWARD set, and where the single-kernel input gradient
- * applies (bf16, short Cy), it is ONE launch instead: clusters take tickets
- * as they start; the first tickets project (sample, 128-column) tiles of g_y
+ * applies (bf16, short Cy, and at most 64 MiB of g_tilde_x when L >= 128), it
+ * is ONE launch instead: clusters take tickets as they start; the first tickets project (sample, 128-column) tiles of g_y
  * and signal each finished tile through counters in `ws`, the input-gradient
  * items of a sample group wait for their group's tiles and the
  * weight-gradient tiles for all of them (a consumer only waits for smaller

@@ -286,9 +286,15 @@ int fused_cluster(int L) {
   return cl;
 }
 
-bool use_fused_grad_x(int L, int Cy, int Ry, instant_dtype dt) {
+bool use_fused_grad_x(int B, int L, int Cx, int Cy, int Ry, instant_dtype dt) {
   if (dt != INSTANT_BF16 || Ry > 64) return false;
   if (std::getenv("INSTANT_NO_FUSED_GRAD_X")) return false;
+  // a large g_tilde_x on 128-token tiles streams out faster from the
+  // standalone expansion (one wave of equal job runs): on a 3072 -> 768 FFN
+  // layer (B = 32, L = 512, 100 MB) g_hat_x, the expansion and g_w took
+  // 36.6 us in three launches against 41.2 us fused, while the BERT-base
+  // block (25 MB) stays fused (11.5 against 19.2 us), as do 49-token tiles
+  if (L >= 128 && static_cast<long long>(B) * L * Cx * 2 > (64ll << 20)) return false;
   // each CTA recomputes a K-slice of its g_hat_x tile: keep that slice short
   return cdiv(cdiv(Cy, 64), fused_cluster(L)) <= 16;
 }
@@ -955,23 +961,46 @@ instant_status plan_expand(const void* Q, void* gx, const void* ws, size_t ws_by
   e.out = gx;
   e.q_tma = 0;
   e.BN = 128;
-  e.spb = 1;
+  e.qres = 0;
+  e.nb = 1;
+  e.total = 0;
+  e.ctas = 0;
   pl->f32 = dt == INSTANT_F32;
   if (pl->f32) return INSTANT_OK;
   if (!aligned16(gx) || !aligned16(ws) || Cx % 8 != 0) return INSTANT_ERR_ALIGN;
-  // column strip width: keep at least ~1.5 strips per SM
-  e.BN = cdiv(Cx, 128) * B >= 3 * sm_count() / 2 ? 128 : 64;
-  // short token axes: several samples per CTA (about 4 token tiles of work per
-  // CTA) while the grid still fills two CTAs per SM.  INSTANT_EXPAND_SPB=n forces n.
-  {
-    const long long room = static_cast<long long>(cdiv(Cx, e.BN)) * B / (2ll * sm_count());
-    e.spb = static_cast<int>(std::max(1ll, std::min<long long>(cdiv(4, e.nlt), room)));
-    if (const char* v = std::getenv("INSTANT_EXPAND_SPB")) {
-      const int f = std::atoi(v);
-      if (f >= 1) e.spb = std::min(f, B);
-    }
+  // 64-column strips: two CTAs share an SM (128 columns hold one)
+  e.BN = 64;
+  if (const char* v = std::getenv("INSTANT_EXPAND_BN")) {
+    const int f = std::atoi(v);
+    if (f == 64 || f == 128) e.BN = f;
   }
   e.q_tma = (L % 8 == 0 && aligned16(Q)) ? 1 : 0;
+  // Q^T resident for short token axes, a ring of four g_hat_x blocks: each
+  // only while the shared memory still fits
+  constexpr size_t kSmemMax = 227 * 1024;
+  e.qres = e.nlt <= kExpandMaxQRes ? 1 : 0;
+  e.nb = kExpandMaxBRing;
+  if (expand_bf16_smem_bytes(e) > kSmemMax) e.nb = 2;
+  if (expand_bf16_smem_bytes(e) > kSmemMax) e.qres = 0;
+  if (expand_bf16_smem_bytes(e) > kSmemMax) return INSTANT_ERR_SHAPE;
+  const long long total = static_cast<long long>(cdiv(Cx, e.BN)) * B * e.nlt;
+  if (total > (1ll << 30)) return INSTANT_ERR_SHAPE;
+  e.total = static_cast<int>(total);
+  // one wave.  When the (strip, sample) groups fill at least half of the
+  // resident slots, one CTA per group walks the group's token tiles: the CTAs
+  // then write the same token rows of every strip together (on the
+  // long-sequence layer 12.8 us against 13.3 us with equal runs).  Otherwise as
+  // many CTAs as fit take equal runs of jobs (groups are split where runs
+  // meet).  INSTANT_EXPAND_CTAS=n forces the grid size.
+  const int per_sm = expand_bf16_ctas_per_sm(e);
+  if (per_sm < 1) return INSTANT_ERR_CUDA;
+  const long long slots = static_cast<long long>(per_sm) * sm_count();
+  const long long groups = total / e.nlt;
+  e.ctas = static_cast<int>((groups <= slots && 2 * groups >= slots) ? groups : std::min(total, slots));
+  if (const char* v = std::getenv("INSTANT_EXPAND_CTAS")) {
+    const int f = std::atoi(v);
+    if (f >= 1) e.ctas = static_cast<int>(std::min<long long>(f, total));
+  }
   std::memset(&pl->mq, 0, sizeof(pl->mq));
   if (e.q_tma) {
     const uint64_t d2[2] = {static_cast<uint64_t>(L), static_cast<uint64_t>(Ry)};
@@ -1037,7 +1066,7 @@ instant_status instant_grad_x(const void* Sq, const void* w, const void* Q, void
   if (dt == INSTANT_BF16 && (!aligned16(Sq) || !aligned16(w) || !aligned16(gx) || !aligned16(ws) ||
                              Cx % 8 != 0 || Cy % 8 != 0))
     return INSTANT_ERR_ALIGN;
-  if (use_fused_grad_x(L, Cy, Ry, dt))
+  if (use_fused_grad_x(B, L, Cx, Cy, Ry, dt))
     return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{nullptr, nullptr, nullptr, 0, 0},
                         static_cast<cudaStream_t>(stream));
   return grad_x_two_kernels(Sq, w, Q, gx, ws, ws_bytes, B, L, Cx, Cy, Ry, dt,
@@ -1056,7 +1085,7 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
       (!aligned16(Sx) || !aligned16(xhat) || !aligned16(gw) || !aligned16(Sq) || !aligned16(w) ||
        !aligned16(gx) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0))
     return INSTANT_ERR_ALIGN;
-  if (use_fused_grad_x(L, Cy, Ry, dt))
+  if (use_fused_grad_x(B, L, Cx, Cy, Ry, dt))
     return grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry, GradWPart{Sx, xhat, gw, accumulate, Rx},
                         static_cast<cudaStream_t>(stream));
   // g_tilde_x first, g_w last: g_w depends on neither of g_tilde_x's two
@@ -1096,7 +1125,7 @@ instant_status instant_backward(const void* gy, const void* PQ, const void* xhat
   // one launch on request: correct, but measured slower than the two launches
   // below on a BERT-base block (23.9 against 18.9 us: the projection tiles
   // finish late and the input-gradient items still take ~9 us after their signal)
-  if (use_fused_grad_x(L, Cy, Ry, dt) && std::getenv("INSTANT_ONE_LAUNCH_BACKWARD")) {
+  if (use_fused_grad_x(B, L, Cx, Cy, Ry, dt) && std::getenv("INSTANT_ONE_LAUNCH_BACKWARD")) {
     const ProjPart pp{gy, PQ, Sx, Rx, static_cast<unsigned int*>(ws)};
     bool no_room = false;
     const instant_status s = grad_x_fused(Sq, w, Q, gx, B, L, Cx, Cy, Ry,

@@ -104,17 +104,23 @@ cudaError_t launch_forward_f32(const float* x, const float* w, float* y, int M, 
 struct ExpandArgs {
   int B, L, Cx, Ry;
   int KR;            // Ry rounded up to a multiple of 16
-  int BN;            // column tile (64, 128 or 256)
-  int nlt;           // ceil(L / 128) token tiles, looped over inside one CTA
+  int BN;            // column tile (64 or 128)
+  int nlt;           // ceil(L / 128) token tiles
   int q_tma;         // 1: Q tiles arrive by TMA (L % 8 == 0); 0: threads fill them
-  int spb;           // consecutive samples per CTA (short token axes)
+  int qres;          // 1: all nlt (<= kExpandMaxQRes) Q^T tiles stay resident
+  int nb;            // g_hat_x blocks in flight (1..kExpandMaxBRing)
+  int total;         // jobs: ceil(Cx / BN) * B * nlt
+  int ctas;          // grid size (1..total); each CTA takes an equal run of jobs
   const void* gxh;   // [B*Ry][Cx], same dtype as out (fp32 path: fp32)
   const void* Q;     // [Ry, L]
   void* out;         // [B, L, Cx]
 };
 
-constexpr int kExpandStages = 2;
+constexpr int kExpandStages = 2;    // Q^T ring (more than kExpandMaxQRes token tiles)
+constexpr int kExpandMaxBRing = 4;
+constexpr int kExpandMaxQRes = 4;
 size_t expand_bf16_smem_bytes(const ExpandArgs& e);
+int expand_bf16_ctas_per_sm(const ExpandArgs& e);  // 0 if the configuration cannot launch
 cudaError_t launch_expand_bf16(const CUtensorMap& tmap_q, const CUtensorMap& tmap_g,
                                const CUtensorMap& tmap_out, const ExpandArgs& e, cudaStream_t st);
 cudaError_t launch_expand_f32(const ExpandArgs& e, cudaStream_t st);

@@ -339,15 +339,45 @@ def test_projection_samples_per_cta(torch, monkeypatch, spb, B, L, C, Rx, Ry):
     assert api.device_status() == 0
 
 
-@pytest.mark.parametrize("spb", [2, 3, 8])
-@pytest.mark.parametrize("B,L,Cx,Cy,Ry", [(7, 49, 448, 1792, 8),    # ViT tokens, ragged last group
-                                          (5, 300, 264, 136, 16)])  # three token tiles per sample
-def test_expand_samples_per_cta(torch, monkeypatch, spb, B, L, Cx, Cy, Ry):
-    """The expansion with several samples per CTA (two g_hat_x strips in
-    flight) against the oracle."""
-    monkeypatch.setenv("INSTANT_EXPAND_SPB", str(spb))
+def test_expand_configurations_in_turn(torch, monkeypatch):
+    """Expansions whose shared-memory sizes differ, in the order large, small,
+    large again (the second large one plans from cached figures): each still
+    launches and matches the oracle."""
+    monkeypatch.setenv("INSTANT_EXPAND_BN", "64")
     api = _api()
-    g = rng(3900 + L + Cx + spb)
+    for i, (B, L, Cx, Cy, Ry) in enumerate([(4, 512, 256, 64, 16), (6, 49, 192, 64, 16),
+                                            (4, 512, 256, 64, 16)]):
+        g = rng(3950 + i)
+        Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
+        w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
+        Q = stored(orthonormal_rows(g, Ry, L), "bf16")
+        gx = nan_like(torch, (B, L, Cx), torch.bfloat16)
+        ws = torch.empty((api.grad_x_workspace_bytes(B, L, Cx, Cy, Ry, torch.bfloat16),),
+                         dtype=torch.uint8, device="cuda")
+        api.grad_x_core(to_dev(Sq), to_dev(w), ws, B)
+        api.expand(to_dev(Q), gx, ws, Cy)
+        torch.cuda.synchronize()
+        ref = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
+        assert_parity(to_np(gx), ref, 2e-2, f"g_x, configuration {i}")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 7])  # 0: the planned grid
+@pytest.mark.parametrize("bn", [64, 128])
+@pytest.mark.parametrize("B,L,Cx,Cy,Ry", [(7, 49, 448, 1792, 8),    # ViT tokens, ragged strips
+                                          (5, 300, 264, 136, 16),   # three token tiles per sample
+                                          (3, 600, 200, 72, 8),     # five tiles: the Q^T ring (TMA)
+                                          (2, 530, 136, 64, 16),    # five tiles, L % 8 != 0: filled ring
+                                          (3, 300, 264, 136, 64)])  # Ry = 64: two g_hat_x slots at BN 128
+def test_expand_job_runs(torch, monkeypatch, ctas, bn, B, L, Cx, Cy, Ry):
+    """The expansion with the (strip, sample, token tile) jobs cut into equal
+    runs over a forced grid (one CTA takes every job; runs starting inside a
+    sample or a strip) and both strip widths, against the oracle."""
+    if ctas:
+        monkeypatch.setenv("INSTANT_EXPAND_CTAS", str(ctas))
+    monkeypatch.setenv("INSTANT_EXPAND_BN", str(bn))
+    api = _api()
+    g = rng(3900 + L + Cx + Ry + ctas + bn)
     Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
     w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
     Q = stored(orthonormal_rows(g, Ry, L), "bf16")
