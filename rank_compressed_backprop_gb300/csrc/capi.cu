@@ -46,6 +46,30 @@ int instant::sm_count() {
   return n;
 }
 
+int instant::resident_ctas_per_sm(const void* kernel, int threads, size_t smem, int tmem_cols) {
+  cudaFuncAttributes fa;
+  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess)
+    return 0;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+  const size_t per_cta = smem + fa.sharedSizeBytes + static_cast<size_t>(reserved);
+  int n = 0;
+  for (;;) {
+    const int m = n + 1;
+    const bool fits = static_cast<size_t>(m) * per_cta <= static_cast<size_t>(smem_sm) &&
+                      m * threads <= threads_sm && (m * warps + 3) / 4 * regs_warp <= regs_sm / 4 &&
+                      m * tmem_cols <= 512 && m <= 32;
+    if (!fits) break;
+    n = m;
+  }
+  return n;
+}
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -137,17 +161,7 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
       const int f = std::atoi(v);
       if (f >= 1 && f <= 4) a.split = std::min(f, std::max(1, a.nk));
     }
-    // short token axes: several samples per CTA (about 4 chunks of work per
-    // CTA) while the grid still fills two CTAs per SM.  INSTANT_PROJ_SPB=n forces n.
     a.spb = 1;
-    if (a.split == 1) {
-      const long long room = tiles / (2ll * sm_count());
-      a.spb = static_cast<int>(std::max(1ll, std::min<long long>(cdiv(4, a.nk), room)));
-      if (const char* v = std::getenv("INSTANT_PROJ_SPB")) {
-        const int f = std::atoi(v);
-        if (f >= 1) a.spb = std::min(f, B);
-      }
-    }
   }
   // L2 prefetch: the whole tile while the grid's prefetches stay within a
   // quarter of L2 (all of a BERT-base batch), else the ring's worth
@@ -162,6 +176,27 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   }
   a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
+  // short token axes (at most 4 chunks): each CTA takes several consecutive
+  // samples of its column tile, the fewest that still make the grid one wave
+  // of resident CTAs (49-token ViT-MLP batches of 256: 7.0 / 17.6 us for
+  // 1,024 / 3,584 tiles against 11.4 / 35.7 us at one sample per CTA and
+  // 21.2 us for the latter at four, which took two waves).
+  // INSTANT_PROJ_SPB=n forces n.
+  if (a.split == 1) {
+    if (a.nk <= 4) {
+      const int per_sm = project_bf16_ctas_per_sm(a);
+      if (per_sm < 1) return INSTANT_ERR_CUDA;
+      const long long slots = static_cast<long long>(per_sm) * sm_count();
+      const long long ct = cdiv(C, 128);
+      long long s = std::max(1ll, (ct * B + slots - 1) / slots);
+      while (s < B && ct * ((B + s - 1) / s) > slots) ++s;
+      a.spb = static_cast<int>(std::min<long long>(s, B));
+    }
+    if (const char* v = std::getenv("INSTANT_PROJ_SPB")) {
+      const int f = std::atoi(v);
+      if (f >= 1) a.spb = std::min(f, B);
+    }
+  }
   CUtensorMap mt, mpq;
   std::memset(&mpq, 0, sizeof(mpq));
   const uint64_t dt3[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(L), static_cast<uint64_t>(B)};

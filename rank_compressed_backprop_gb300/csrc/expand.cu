@@ -393,31 +393,11 @@ cudaError_t launch_bn(const CUtensorMap& tq, const CUtensorMap& tg, const CUtens
                    to, e);
 }
 
-// CTAs of the kernel that fit on one SM with this configuration's shared
-// memory, registers (each of the four SM sub-partitions holds a quarter of the
-// register file and of the warps) and TMEM columns
 template <int BN>
 int resident_bn(const ExpandArgs& e) {
   const size_t bytes = expand_bf16_smem_bytes(e);
   if (ensure_smem<BN>(bytes) != cudaSuccess) return 0;
-  cudaFuncAttributes fa;
-  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
-  if (cudaFuncGetAttributes(&fa, k_expand_bf16<BN>) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess)
-    return 0;
-  constexpr int kWarps = 320 / 32;
-  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
-  int n = 0;
-  while (n < 4) {
-    const int m = n + 1;
-    const bool fits = static_cast<size_t>(m) * (bytes + fa.sharedSizeBytes + reserved) <= static_cast<size_t>(smem_sm) &&
-                      (m * kWarps + 3) / 4 * regs_warp <= regs_sm / 4 && m * 2 * BN <= 512;
-    if (!fits) break;
-    n = m;
-  }
-  return n;
+  return resident_ctas_per_sm(reinterpret_cast<const void*>(k_expand_bf16<BN>), 320, bytes, 2 * BN);
 }
 
 }  // namespace

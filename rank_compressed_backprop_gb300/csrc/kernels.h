@@ -28,6 +28,7 @@ struct ProjectArgs {
 
 constexpr int kProjectStages = 4;  // 2 and 3 stages measured slower on GB300
 size_t project_bf16_smem_bytes(const ProjectArgs& a);
+int project_bf16_ctas_per_sm(const ProjectArgs& a);  // 0 if a query fails
 cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq,
                                 const ProjectArgs& a, cudaStream_t st);
 cudaError_t launch_project_f32(const ProjectArgs& a, const float* t, cudaStream_t st);
@@ -304,6 +305,13 @@ void count_launches(unsigned int n);
 
 // streaming multiprocessors of the current device (queried once per device)
 int sm_count();
+
+// CTAs of `kernel` (launched with `threads` threads and `smem` bytes of dynamic
+// shared memory, allocating `tmem_cols` TMEM columns) that one SM holds at
+// once: shared memory, threads, TMEM, and registers per SM sub-partition (each
+// of the four holds a quarter of the register file and of the CTA's warps;
+// the occupancy query does not model this split).  0 if a query fails.
+int resident_ctas_per_sm(const void* kernel, int threads, size_t smem, int tmem_cols);
 
 }  // namespace instant
 

@@ -167,17 +167,47 @@ size_t project_bf16_smem_bytes(const ProjectArgs& a) {
   return project_smem_bytes(a.NT, a.nk, a.pq_tma) + 1024;
 }
 
+namespace {
+
+// the dynamic shared memory limit only ever grows (smaller configurations fit
+// under it)
+cudaError_t ensure_project_smem(size_t bytes) {
+  static size_t configured_ = 0;
+  if (bytes <= configured_) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k_project_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+  if (e == cudaSuccess) configured_ = bytes;
+  return e;
+}
+
+}  // namespace
+
+int project_bf16_ctas_per_sm(const ProjectArgs& a) {
+  // one query per shared-memory size and TMEM width
+  static int count_[16] = {};
+  static size_t key_[16] = {};
+  const size_t bytes = project_bf16_smem_bytes(a);
+  const int cols = a.NT <= 32 ? 32 : (a.NT <= 64 ? 64 : 128);
+  const size_t key = bytes * 4 + static_cast<size_t>(cols / 32);
+  for (int i = 0; i < 16; ++i)
+    if (key_[i] == key) return count_[i];
+  if (ensure_project_smem(bytes) != cudaSuccess) return 0;
+  const int n = resident_ctas_per_sm(reinterpret_cast<const void*>(k_project_bf16), 128, bytes, cols);
+  for (int i = 0; i < 16; ++i)
+    if (key_[i] == 0) {
+      key_[i] = key;
+      count_[i] = n;
+      break;
+    }
+  return n;
+}
+
 cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq,
                                 const ProjectArgs& a, cudaStream_t st) {
   if (a.NT < 16 || a.NT > 128 || a.NT % 16 != 0) return cudaErrorInvalidValue;
   const size_t bytes = project_bf16_smem_bytes(a);
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_project_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
+  const cudaError_t err = ensure_project_smem(bytes);
+  if (err != cudaSuccess) return err;
   if (a.split < 1 || a.split > 4) return cudaErrorInvalidValue;
   if (a.spb < 1 || (a.split > 1 && a.spb != 1)) return cudaErrorInvalidValue;
   return launch_ex(k_project_bf16, dim3((a.C + kProjBM - 1) / kProjBM, (a.B + a.spb - 1) / a.spb, a.split),
