@@ -231,6 +231,10 @@ GemmPlan plan_gemm(int M, int N, int K) {
       break;
     }
   }
+  if (const char* v = std::getenv("INSTANT_GEMM_BN")) {
+    const int f = std::atoi(v);
+    if (f == 64 || f == 128 || f == 256) p.BN = f;
+  }
   const int tiles = tm * cdiv(N, p.BN);
   p.splits = 1;
   for (int s : {8, 4, 2}) {
@@ -238,6 +242,10 @@ GemmPlan plan_gemm(int M, int N, int K) {
       p.splits = s;
       break;
     }
+  }
+  if (const char* v = std::getenv("INSTANT_GEMM_SPLITS")) {
+    const int f = std::atoi(v);
+    if ((f == 1 || f == 2 || f == 4 || f == 8) && f <= p.nk) p.splits = f;
   }
   p.cps = cdiv(p.nk, p.splits);
   p.stages = 4;
