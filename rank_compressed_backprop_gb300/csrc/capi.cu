@@ -149,6 +149,7 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   a.pq = pq;
   a.out0 = out0;
   a.out1 = out1;
+  a.stages = kProjectStages;
   // token split: when the (sample, 128-column) tiles leave SMs idle or
   // unevenly loaded, up to four CTAs of a cluster share each tile's token axis
   // (every share at least 8 chunks of 64 tokens) and reduce their fp32 partial
@@ -176,6 +177,14 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   }
   a.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
+  // tiles of at most two chunks need no deeper ring: with two stages twice as
+  // many CTAs share an SM and hide each other's per-sample latency.
+  // INSTANT_PROJ_STAGES=2|4 forces the depth (2 only without a split).
+  if (a.split == 1 && a.nk <= 2) a.stages = 2;
+  if (const char* v = std::getenv("INSTANT_PROJ_STAGES")) {
+    const int f = std::atoi(v);
+    if (f == kProjectStages || (f == 2 && a.split == 1)) a.stages = f;
+  }
   // short token axes (at most 4 chunks): each CTA takes several consecutive
   // samples of its column tile, the fewest that still make the grid one wave
   // of resident CTAs (49-token ViT-MLP batches of 256: 7.0 / 17.6 us for
@@ -453,6 +462,7 @@ instant_status grad_x_fused(const void* Sq, const void* w, const void* Q, void* 
     a.pf_chunks = 0;  // its tiles start after the wait
     a.split = 1;
     a.spb = 1;
+    a.stages = kProjectStages;
     if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) {
       if (no_room) *no_room = true;
       return INSTANT_ERR_SHAPE;

@@ -21,6 +21,7 @@ struct ProjectArgs {
   int split;         // CTAs sharing a tile's token axis (1..4, a cluster along grid z);
                      // their fp32 partial sums are reduced through DSMEM
   int spb;           // samples per CTA (1 with a split): short token axes share a CTA
+  int stages;        // A ring depth: kProjectStages, or 2 (at most two chunks, no split)
   const void* pq;    // [Rx+Ry, L]
   void* out0;        // [B*Rx, C]
   void* out1;        // [B*Ry, C] or null

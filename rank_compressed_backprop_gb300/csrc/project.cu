@@ -31,10 +31,13 @@ namespace instant {
 
 namespace {
 
-__host__ __device__ inline uint32_t project_smem_bytes(int NT, int nk, int pq_tma) {
-  return proj_layout(NT, nk, pq_tma).bytes + 128;  // + barriers and the TMEM slot
+__host__ __device__ inline uint32_t project_smem_bytes(int NT, int nk, int pq_tma, int ns) {
+  return proj_layout(NT, nk, pq_tma, ns).bytes + 128;  // + barriers and the TMEM slot
 }
 
+// NS: ring depth (kProjectStages; 2 for tiles of at most two chunks, so that
+// twice the CTAs share an SM and hide each other's per-sample latency)
+template <int NS>
 __global__ void __launch_bounds__(128, 1)
     k_project_bf16(const __grid_constant__ CUtensorMap tmap_t,
                    const __grid_constant__ CUtensorMap tmap_pq, ProjectArgs a) {
@@ -42,19 +45,19 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int NT = a.NT;
-  const ProjLayout lay = proj_layout(NT, a.nk, a.pq_tma);
+  const ProjLayout lay = proj_layout(NT, a.nk, a.pq_tma, NS);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kProjBarriers);
   const uint32_t tmem_cols = NT <= 32 ? 32 : (NT <= 64 ? 64 : 128);
 
-  ProjPipe pipe = proj_pipe(smem, bars, NT, a.nk, a.pq_tma, 0);
+  ProjPipe pipe = proj_pipe(smem, bars, NT, a.nk, a.pq_tma, 0, NS);
   // token share of this CTA: the split CTAs of a tile form one cluster along z
   const int S = a.split;
   const int rank = blockIdx.z;
   const int k0 = static_cast<int>(static_cast<long long>(a.nk) * rank / S);
   const int nkl = static_cast<int>(static_cast<long long>(a.nk) * (rank + 1) / S) - k0;
   if (threadIdx.x == 0) {
-    proj_init_barriers(pipe);
+    proj_init_barriers(pipe, NS);
     fence_barrier_init();
     prefetch_tmap(&tmap_t);
     if (a.pq_tma) prefetch_tmap(&tmap_pq);
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(128, 1)
     const int b1 = min(a.B, b0 + a.spb);
     for (int b = b0; b < b1; ++b) {
       if (threadIdx.x == 0 && b + 1 < b1) proj_prefetch(&tmap_t, a, b + 1, blockIdx.x * kProjBM);
-      proj_tile<1>(&tmap_t, &tmap_pq, a, NT, b, blockIdx.x * kProjBM, pipe);
+      proj_tile<1, NS>(&tmap_t, &tmap_pq, a, NT, b, blockIdx.x * kProjBM, pipe);
     }
     tc_fence_before();
     __syncthreads();
@@ -93,7 +96,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   // ---- token split: partial sums in the idle ring, reduced across the cluster ----
   float* part = reinterpret_cast<float*>(pipe.sA);  // [NT][128] fp32
-  proj_tile<1>(&tmap_t, &tmap_pq, a, NT, blockIdx.y, blockIdx.x * kProjBM, pipe, k0, nkl, part);
+  proj_tile<1, NS>(&tmap_t, &tmap_pq, a, NT, blockIdx.y, blockIdx.x * kProjBM, pipe, k0, nkl, part);
   tc_fence_before();
   __syncthreads();
   if (threadIdx.x < 32) tmem_dealloc(pipe.tmem, tmem_cols);
@@ -164,35 +167,51 @@ __global__ void k_project_f32(const float* __restrict__ t, ProjectArgs a) {
 }  // namespace
 
 size_t project_bf16_smem_bytes(const ProjectArgs& a) {
-  return project_smem_bytes(a.NT, a.nk, a.pq_tma) + 1024;
+  return project_smem_bytes(a.NT, a.nk, a.pq_tma, a.stages) + 1024;
 }
 
 namespace {
 
 // the dynamic shared memory limit only ever grows (smaller configurations fit
 // under it)
+template <int NS>
 cudaError_t ensure_project_smem(size_t bytes) {
   static size_t configured_ = 0;
   if (bytes <= configured_) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(k_project_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const cudaError_t e = cudaFuncSetAttribute(k_project_bf16<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(bytes));
   if (e == cudaSuccess) configured_ = bytes;
   return e;
 }
 
+template <int NS>
+int resident_project(size_t bytes, int cols) {
+  if (ensure_project_smem<NS>(bytes) != cudaSuccess) return 0;
+  return resident_ctas_per_sm(reinterpret_cast<const void*>(k_project_bf16<NS>), 128, bytes, cols);
+}
+
+template <int NS>
+cudaError_t launch_ns(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq, const ProjectArgs& a,
+                      cudaStream_t st) {
+  const size_t bytes = project_bf16_smem_bytes(a);
+  const cudaError_t err = ensure_project_smem<NS>(bytes);
+  if (err != cudaSuccess) return err;
+  return launch_ex(k_project_bf16<NS>, dim3((a.C + kProjBM - 1) / kProjBM, (a.B + a.spb - 1) / a.spb, a.split),
+                   dim3(128), bytes, st, a.split, pdl_enabled(), tmap_t, tmap_pq, a);
+}
+
 }  // namespace
 
 int project_bf16_ctas_per_sm(const ProjectArgs& a) {
-  // one query per shared-memory size and TMEM width
+  // one query per shared-memory size, TMEM width and ring depth
   static int count_[16] = {};
   static size_t key_[16] = {};
   const size_t bytes = project_bf16_smem_bytes(a);
   const int cols = a.NT <= 32 ? 32 : (a.NT <= 64 ? 64 : 128);
-  const size_t key = bytes * 4 + static_cast<size_t>(cols / 32);
+  const size_t key = (bytes * 4 + static_cast<size_t>(cols / 32)) * 8 + static_cast<size_t>(a.stages);
   for (int i = 0; i < 16; ++i)
     if (key_[i] == key) return count_[i];
-  if (ensure_project_smem(bytes) != cudaSuccess) return 0;
-  const int n = resident_ctas_per_sm(reinterpret_cast<const void*>(k_project_bf16), 128, bytes, cols);
+  const int n = a.stages == 2 ? resident_project<2>(bytes, cols) : resident_project<kProjectStages>(bytes, cols);
   for (int i = 0; i < 16; ++i)
     if (key_[i] == 0) {
       key_[i] = key;
@@ -205,13 +224,12 @@ int project_bf16_ctas_per_sm(const ProjectArgs& a) {
 cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq,
                                 const ProjectArgs& a, cudaStream_t st) {
   if (a.NT < 16 || a.NT > 128 || a.NT % 16 != 0) return cudaErrorInvalidValue;
-  const size_t bytes = project_bf16_smem_bytes(a);
-  const cudaError_t err = ensure_project_smem(bytes);
-  if (err != cudaSuccess) return err;
   if (a.split < 1 || a.split > 4) return cudaErrorInvalidValue;
   if (a.spb < 1 || (a.split > 1 && a.spb != 1)) return cudaErrorInvalidValue;
-  return launch_ex(k_project_bf16, dim3((a.C + kProjBM - 1) / kProjBM, (a.B + a.spb - 1) / a.spb, a.split),
-                   dim3(128), bytes, st, a.split, pdl_enabled(), tmap_t, tmap_pq, a);
+  // the split's fp32 partials need the whole 4-stage ring
+  if (a.stages == 2 && a.split == 1) return launch_ns<2>(tmap_t, tmap_pq, a, st);
+  if (a.stages != kProjectStages) return cudaErrorInvalidValue;
+  return launch_ns<kProjectStages>(tmap_t, tmap_pq, a, st);
 }
 
 cudaError_t launch_project_f32(const ProjectArgs& a, const float* t, cudaStream_t st) {

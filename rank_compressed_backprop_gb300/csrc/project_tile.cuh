@@ -29,25 +29,26 @@ constexpr int kProjBK = 64;                     // tokens per chunk
 constexpr int kProjABytes = kProjBM * kProjBK * 2;  // 16 KB: two 64-column boxes
 constexpr int kProjHalfA = kProjABytes / 2;
 
-// ring of kProjectStages A stages, then the PQ stages (or all of PQ)
+// ring of ns (kProjectStages, or 2 for tiles of at most two chunks) A stages,
+// then the PQ stages (or all of PQ)
 struct ProjLayout {
   uint32_t a_off, b_off, b_stage_bytes, bytes;
 };
 
-__host__ __device__ inline ProjLayout proj_layout(int NT, int nk, int pq_tma) {
+__host__ __device__ inline ProjLayout proj_layout(int NT, int nk, int pq_tma, int ns = kProjectStages) {
   ProjLayout l;
   l.a_off = 0;
-  l.b_off = kProjectStages * kProjABytes;
+  l.b_off = ns * kProjABytes;
   l.b_stage_bytes = NT * 128;
-  const uint32_t b_total = pq_tma ? kProjectStages * l.b_stage_bytes : nk * l.b_stage_bytes;
+  const uint32_t b_total = pq_tma ? ns * l.b_stage_bytes : nk * l.b_stage_bytes;
   l.bytes = l.b_off + ((b_total + 1023u) & ~1023u);
   return l;
 }
 
 // per-CTA pipeline state; every role thread advances its own copy identically
 struct ProjPipe {
-  uint64_t* full;    // [kProjectStages]
-  uint64_t* empty;   // [kProjectStages]
+  uint64_t* full;    // [ns]
+  uint64_t* empty;   // [ns]
   uint64_t* done;    // accumulator complete
   uint8_t* sA;
   uint8_t* sB;
@@ -58,12 +59,12 @@ struct ProjPipe {
 };
 
 __device__ __forceinline__ ProjPipe proj_pipe(uint8_t* region, uint64_t* bars, int NT, int nk,
-                                              int pq_tma, uint32_t tmem) {
-  const ProjLayout l = proj_layout(NT, nk, pq_tma);
+                                              int pq_tma, uint32_t tmem, int ns = kProjectStages) {
+  const ProjLayout l = proj_layout(NT, nk, pq_tma, ns);
   ProjPipe p;
   p.full = bars;
-  p.empty = bars + kProjectStages;
-  p.done = bars + 2 * kProjectStages;
+  p.empty = bars + ns;
+  p.done = bars + 2 * ns;
   p.sA = region + l.a_off;
   p.sB = region + l.b_off;
   p.b_stage_bytes = l.b_stage_bytes;
@@ -73,11 +74,11 @@ __device__ __forceinline__ ProjPipe proj_pipe(uint8_t* region, uint64_t* bars, i
   return p;
 }
 
-constexpr int kProjBarriers = 2 * kProjectStages + 1;
+constexpr int kProjBarriers = 2 * kProjectStages + 1;  // room for the deepest ring
 
 // one thread, before the CTA-wide barrier that publishes the initialisation
-__device__ __forceinline__ void proj_init_barriers(const ProjPipe& p) {
-  for (int s = 0; s < kProjectStages; ++s) {
+__device__ __forceinline__ void proj_init_barriers(const ProjPipe& p, int ns = kProjectStages) {
+  for (int s = 0; s < ns; ++s) {
     mbar_init(&p.full[s], 1);
     mbar_init(&p.empty[s], 1);
   }
@@ -124,7 +125,7 @@ __device__ __forceinline__ void proj_prefetch(const CUtensorMap* tmap_t, const P
 // (one share of a token split) and, instead of writing the planes, leaves
 // its fp32 partial sums in part[r * 128 + column], r < NT (shared memory of
 // this CTA, e.g. the idle ring), for the caller to reduce.
-template <int BAR>
+template <int BAR, int NS = kProjectStages>
 __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUtensorMap* tmap_pq,
                                           const ProjectArgs& a, int NT, int b, int c0,
                                           ProjPipe& p, int k0 = 0, int nkl = -1,
@@ -138,8 +139,8 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
     int issued = 0;
     for (int i = 0; i < nk; ++i) {
       const int g = p.chunk + i;
-      const int s = g % kProjectStages;
-      if (g >= kProjectStages && !mbar_wait(&p.empty[s], ((g / kProjectStages) - 1) & 1)) {
+      const int s = g % NS;
+      if (g >= NS && !mbar_wait(&p.empty[s], ((g / NS) - 1) & 1)) {
         raise_fault(FAULT_WAIT_EMPTY);
         break;
       }
@@ -153,9 +154,9 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
     }
     // every copy this thread issued has landed before it moves on (the ring is
     // reused by whatever follows, also when the MMA side gave up)
-    for (int i = issued - kProjectStages < 0 ? 0 : issued - kProjectStages; i < issued; ++i) {
+    for (int i = issued - NS < 0 ? 0 : issued - NS; i < issued; ++i) {
       const int g = p.chunk + i;
-      if (!mbar_wait(&p.full[g % kProjectStages], (g / kProjectStages) & 1))
+      if (!mbar_wait(&p.full[g % NS], (g / NS) & 1))
         raise_fault(FAULT_WAIT_FULL);
     }
   } else if (warp == 1 && lane == 0) {
@@ -164,8 +165,8 @@ __device__ __forceinline__ void proj_tile(const CUtensorMap* tmap_t, const CUten
     bool ok = true;
     for (int i = 0; i < nk; ++i) {
       const int g = p.chunk + i;
-      const int s = g % kProjectStages;
-      if (!mbar_wait(&p.full[s], (g / kProjectStages) & 1)) {
+      const int s = g % NS;
+      if (!mbar_wait(&p.full[s], (g / NS) & 1)) {
         raise_fault(FAULT_WAIT_FULL);
         ok = false;
         break;

@@ -314,13 +314,16 @@ def test_projection_token_split(torch, monkeypatch, split, B, L, C, Rx, Ry):
     assert api.device_status() == 0
 
 
+@pytest.mark.parametrize("stages", [2, 4])
 @pytest.mark.parametrize("spb", [2, 3, 8])
 @pytest.mark.parametrize("B,L,C,Rx,Ry", [(7, 49, 448, 8, 8),     # ViT tokens, a ragged last group
-                                         (5, 100, 264, 8, 0)])   # compress, two chunks, ragged columns
-def test_projection_samples_per_cta(torch, monkeypatch, spb, B, L, C, Rx, Ry):
-    """Several samples per CTA (short token axes): the same planes as one
-    sample per CTA."""
+                                         (5, 100, 264, 8, 0),    # compress, two chunks, ragged columns
+                                         (3, 128, 136, 64, 64)])  # 128 projector rows, two chunks
+def test_projection_samples_per_cta(torch, monkeypatch, stages, spb, B, L, C, Rx, Ry):
+    """Several samples per CTA (short token axes), with the two-stage and the
+    four-stage ring: against the oracle."""
     monkeypatch.setenv("INSTANT_PROJ_SPB", str(spb))
+    monkeypatch.setenv("INSTANT_PROJ_STAGES", str(stages))
     g = rng(3800 + L + C + spb)
     t = stored(g.standard_normal((B, L, C)), "bf16")
     PQ = stored(orthonormal_rows(g, Rx + Ry, L), "bf16")
