@@ -12,6 +12,9 @@
 #include <cstdio>
 #include <cstring>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <mutex>
 
 #include "instant.h"
@@ -44,6 +47,25 @@ int instant::sm_count() {
     return 1;
   cache[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+
+cudaError_t instant::raise_smem_limit(const void* kernel, size_t bytes, bool max_shared) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> configured;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = configured[std::make_pair(kernel, dev)];
+  if (bytes <= have) return cudaSuccess;
+  if (max_shared) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) have = bytes;
+  return e;
 }
 
 int instant::resident_ctas_per_sm(const void* kernel, int threads, size_t smem, int tmem_cols) {

@@ -1682,9 +1682,9 @@ cudaError_t launch_solver_energy(const float* C, int L, SolverWs w, cudaStream_t
 }
 
 static cudaError_t set_smem(const void* f, size_t bytes) {
-  // 200 KB up front for every solver kernel: one attribute call per kernel
+  // 200 KB up front for every solver kernel: one attribute call per kernel and device
   (void)bytes;
-  return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  return raise_smem_limit(f, 200 * 1024);
 }
 
 cudaError_t launch_jacobi_full_batch(const JacobiBatch& b, cudaStream_t st) {
@@ -1790,7 +1790,7 @@ cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStre
   }
   const size_t bytes = cluster_layout(L, m, rp).total;
   auto kern = m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 216 * 1024);
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), 216 * 1024);
   if (e != cudaSuccess) return e;
   return launch_ex(kern, dim3(1, count, kClusterCtas), dim3(kClusterThreads), bytes, st,
                    kClusterCtas, false, b);

@@ -24,6 +24,10 @@
 // Full 128-byte lines leave the SM through the TMA engine; rows past L are
 // clipped by the tensor map (and lane quarters wholly past L skip their TMEM
 // reads).
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -364,20 +368,10 @@ __global__ void k_expand_f32(ExpandArgs e) {
   static_cast<float*>(e.out)[(static_cast<size_t>(b) * e.L + l) * e.Cx + c] = acc;
 }
 
-// the kernel's dynamic shared memory limit only ever grows (launches and
-// occupancy queries of smaller configurations then fit under it), with the
-// whole unified L1 given to shared memory so that two CTAs fit where they can
 template <int BN>
 cudaError_t ensure_smem(size_t bytes) {
-  static size_t configured_ = 0;
-  if (bytes <= configured_) return cudaSuccess;
-  cudaError_t err = cudaFuncSetAttribute(k_expand_bf16<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(k_expand_bf16<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
-  if (err == cudaSuccess) configured_ = bytes;
-  return err;
+  // two CTAs per SM need the whole unified L1 as shared memory
+  return raise_smem_limit(reinterpret_cast<const void*>(k_expand_bf16<BN>), bytes, true);
 }
 
 template <int BN>
@@ -407,20 +401,21 @@ size_t expand_bf16_smem_bytes(const ExpandArgs& e) {
 }
 
 int expand_bf16_ctas_per_sm(const ExpandArgs& e) {
-  // one occupancy query per (BN, shared-memory size)
-  static int count_[2][8] = {};
-  static size_t bytes_[2][8] = {};
+  // one residency count per (device, BN, shared-memory size)
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, size_t>, int> counts;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const size_t bytes = expand_bf16_smem_bytes(e);
-  const int bi = e.BN == 128 ? 1 : 0;
-  for (int i = 0; i < 8; ++i)
-    if (bytes_[bi][i] == bytes) return count_[bi][i];
+  const auto key = std::make_tuple(dev, e.BN, bytes);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = counts.find(key);
+    if (it != counts.end()) return it->second;
+  }
   const int n = e.BN == 128 ? resident_bn<128>(e) : resident_bn<64>(e);
-  for (int i = 0; i < 8; ++i)
-    if (bytes_[bi][i] == 0) {
-      bytes_[bi][i] = bytes;
-      count_[bi][i] = n;
-      break;
-    }
+  std::lock_guard<std::mutex> lock(mu);
+  if (n > 0) counts[key] = n;
   return n;
 }
 

@@ -413,13 +413,8 @@ cudaError_t launch_forward_bf16(const CUtensorMap& tmap_x, const CUtensorMap& tm
   if (a.Rx < 0 || a.Rx > 32 || (a.Rx > 0 && (a.L % BM != 0 || a.K % 128 != 0)))
     return cudaErrorInvalidValue;
   const size_t bytes = forward_bf16_smem_bytes();
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_forward_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k_forward_bf16), bytes);
+  if (e != cudaSuccess) return e;
   return launch_ex(k_forward_bf16, dim3(ctas), dim3(320), bytes, st, 1, pdl_enabled(), tmap_x,
                    tmap_w, tmap_y, tmap_p, a);
 }

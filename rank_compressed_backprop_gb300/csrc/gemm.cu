@@ -259,14 +259,8 @@ template <int BN, int A_MN, int B_MN>
 cudaError_t launch_cfg(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                        cudaStream_t st) {
   const size_t bytes = gemm_bf16_smem_bytes(g);
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16<BN, A_MN, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k_gemm_bf16<BN, A_MN, B_MN>), bytes);
+  if (e != cudaSuccess) return e;
   return launch_ex(k_gemm_bf16<BN, A_MN, B_MN>, dim3((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.splits),
                    dim3(128), bytes, st, g.splits, pdl_enabled(), ta, tb, g);
 }

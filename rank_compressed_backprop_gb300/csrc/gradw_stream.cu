@@ -301,13 +301,8 @@ cudaError_t launch_gradw_stream(const CUtensorMap& tmap_sx, const CUtensorMap& t
   if (g.nkc < 1 || g.nkc > kGradWMaxChunks || g.stages < 2 || g.stages > kGradWStages || ctas < 1)
     return cudaErrorInvalidValue;
   const size_t bytes = gradw_stream_smem_bytes(g);
-  static size_t configured_ = 0;
-  if (bytes > configured_) {
-    cudaError_t e = cudaFuncSetAttribute(k_gradw_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e != cudaSuccess) return e;
-    configured_ = bytes;
-  }
+  const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k_gradw_stream), bytes);
+  if (e != cudaSuccess) return e;
   return launch_ex(k_gradw_stream, dim3(ctas), dim3(320), bytes, st, 1, pdl_enabled(), tmap_sx,
                    tmap_xh, tmap_gw, g);
 }

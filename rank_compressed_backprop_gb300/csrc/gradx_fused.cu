@@ -729,14 +729,7 @@ size_t fused_smem_bytes(const FusedArgs& f) {
 
 template <int BN>
 cudaError_t configure_smem(size_t bytes) {
-  static std::mutex mu;
-  static size_t configured = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  if (bytes <= configured) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(
-      k_gradx_fused<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
-  if (e == cudaSuccess) configured = bytes;
-  return e;
+  return raise_smem_limit(reinterpret_cast<const void*>(k_gradx_fused<BN>), bytes);
 }
 
 template <int BN>

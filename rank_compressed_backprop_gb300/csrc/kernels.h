@@ -307,6 +307,13 @@ void count_launches(unsigned int n);
 // streaming multiprocessors of the current device (queried once per device)
 int sm_count();
 
+// Raises `kernel`'s dynamic shared memory limit on the current device to at
+// least `bytes`.  It never lowers it, so configurations launched later with
+// less still fit; with max_shared the unified L1 goes to shared memory first
+// (so that as many CTAs as the shared memory allows share an SM).  Thread-safe;
+// one attribute call per new maximum per (kernel, device).
+cudaError_t raise_smem_limit(const void* kernel, size_t bytes, bool max_shared = false);
+
 // CTAs of `kernel` (launched with `threads` threads and `smem` bytes of dynamic
 // shared memory, allocating `tmem_cols` TMEM columns) that one SM holds at
 // once: shared memory, threads, TMEM, and registers per SM sub-partition (each

@@ -23,6 +23,10 @@
 // short token axes (a BERT-base batch: 8 chunks per tile) the two cluster
 // barriers cost more than the balance buys, so the split is kept for shares
 // of at least 8 chunks.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "project_tile.cuh"
 #include "tc.cuh"
@@ -172,16 +176,9 @@ size_t project_bf16_smem_bytes(const ProjectArgs& a) {
 
 namespace {
 
-// the dynamic shared memory limit only ever grows (smaller configurations fit
-// under it)
 template <int NS>
 cudaError_t ensure_project_smem(size_t bytes) {
-  static size_t configured_ = 0;
-  if (bytes <= configured_) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(k_project_bf16<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(bytes));
-  if (e == cudaSuccess) configured_ = bytes;
-  return e;
+  return raise_smem_limit(reinterpret_cast<const void*>(k_project_bf16<NS>), bytes);
 }
 
 template <int NS>
@@ -203,21 +200,22 @@ cudaError_t launch_ns(const CUtensorMap& tmap_t, const CUtensorMap& tmap_pq, con
 }  // namespace
 
 int project_bf16_ctas_per_sm(const ProjectArgs& a) {
-  // one query per shared-memory size, TMEM width and ring depth
-  static int count_[16] = {};
-  static size_t key_[16] = {};
+  // one residency count per (device, shared-memory size, TMEM width, ring depth)
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t, int, int>, int> counts;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const size_t bytes = project_bf16_smem_bytes(a);
   const int cols = a.NT <= 32 ? 32 : (a.NT <= 64 ? 64 : 128);
-  const size_t key = (bytes * 4 + static_cast<size_t>(cols / 32)) * 8 + static_cast<size_t>(a.stages);
-  for (int i = 0; i < 16; ++i)
-    if (key_[i] == key) return count_[i];
+  const auto key = std::make_tuple(dev, bytes, cols, a.stages);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = counts.find(key);
+    if (it != counts.end()) return it->second;
+  }
   const int n = a.stages == 2 ? resident_project<2>(bytes, cols) : resident_project<kProjectStages>(bytes, cols);
-  for (int i = 0; i < 16; ++i)
-    if (key_[i] == 0) {
-      key_[i] = key;
-      count_[i] = n;
-      break;
-    }
+  std::lock_guard<std::mutex> lock(mu);
+  if (n > 0) counts[key] = n;
   return n;
 }
 

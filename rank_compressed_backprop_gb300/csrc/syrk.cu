@@ -251,13 +251,7 @@ size_t syrk_smem_bytes() {
 
 template <bool WIDE>
 cudaError_t configure_syrk() {
-  static size_t configured_ = 0;
-  const size_t bytes = syrk_smem_bytes<WIDE>();
-  if (bytes <= configured_) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(k_syrk_bf16<WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(bytes));
-  if (e == cudaSuccess) configured_ = bytes;
-  return e;
+  return raise_smem_limit(reinterpret_cast<const void*>(k_syrk_bf16<WIDE>), syrk_smem_bytes<WIDE>());
 }
 
 }  // namespace
