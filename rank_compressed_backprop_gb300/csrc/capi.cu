@@ -201,11 +201,34 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
   if (!a.pq_tma && static_cast<size_t>(a.nk) * a.NT * 128 > 96 * 1024) return INSTANT_ERR_SHAPE;
   // tiles of at most two chunks need no deeper ring: with two stages twice as
   // many CTAs share an SM and hide each other's per-sample latency.
-  // INSTANT_PROJ_STAGES=2|4 forces the depth (2 only without a split).
   if (a.split == 1 && a.nk <= 2) a.stages = 2;
+  // A streaming SM reads HBM at a fixed rate, so the launch lasts as long as
+  // the SM with the most bytes streams.  Where halving the token axis (a
+  // 2-CTA cluster, shares of at least 8 chunks) lowers the most tiles an SM
+  // holds, and the halves all fit at once with the two-stage ring, split:
+  // the long-sequence layer's 344 tiles put three on 40 SMs, 688 halves at
+  // most five (2.5 tiles): project_grad 37.2 -> 30.9 us.  (Shorter token axes
+  // lost more to the cluster's barriers: BERT-base 6.2 -> 7.9 us.)
+  if (a.split == 1 && a.spb == 1 && a.nk >= 16 && a.NT <= 64 && !std::getenv("INSTANT_PROJ_SPLIT")) {
+    const long long nsm = sm_count();
+    const long long T = static_cast<long long>(B) * cdiv(C, 128);
+    ProjectArgs h = a;
+    h.split = 2;
+    h.stages = 2;
+    h.pq_tma = (L % 8 == 0 && aligned16(pq)) ? 1 : 0;
+    const int per_sm = project_bf16_ctas_per_sm(h);
+    if (per_sm < 1) return INSTANT_ERR_CUDA;
+    const long long most_whole = 2 * ((T + nsm - 1) / nsm);  // in half tiles
+    const long long most_half = (2 * T + nsm - 1) / nsm;
+    if (2 * T <= per_sm * nsm && most_half < most_whole) {
+      a.split = 2;
+      a.stages = 2;
+    }
+  }
+  // INSTANT_PROJ_STAGES=2|4 forces the depth (2 with a split only up to NT = 64)
   if (const char* v = std::getenv("INSTANT_PROJ_STAGES")) {
     const int f = std::atoi(v);
-    if (f == kProjectStages || (f == 2 && a.split == 1)) a.stages = f;
+    if (f == kProjectStages || (f == 2 && (a.split == 1 || a.NT <= 64))) a.stages = f;
   }
   // short token axes (at most 4 chunks): each CTA takes several consecutive
   // samples of its column tile, the fewest that still make the grid one wave

@@ -224,8 +224,9 @@ cudaError_t launch_project_bf16(const CUtensorMap& tmap_t, const CUtensorMap& tm
   if (a.NT < 16 || a.NT > 128 || a.NT % 16 != 0) return cudaErrorInvalidValue;
   if (a.split < 1 || a.split > 4) return cudaErrorInvalidValue;
   if (a.spb < 1 || (a.split > 1 && a.spb != 1)) return cudaErrorInvalidValue;
-  // the split's fp32 partials need the whole 4-stage ring
-  if (a.stages == 2 && a.split == 1) return launch_ns<2>(tmap_t, tmap_pq, a, st);
+  // a split parks NT x 128 fp32 partials in the idle ring: the two-stage ring
+  // (32 KB) holds them up to NT = 64
+  if (a.stages == 2 && (a.split == 1 || a.NT <= 64)) return launch_ns<2>(tmap_t, tmap_pq, a, st);
   if (a.stages != kProjectStages) return cudaErrorInvalidValue;
   return launch_ns<kProjectStages>(tmap_t, tmap_pq, a, st);
 }

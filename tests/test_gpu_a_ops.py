@@ -290,12 +290,17 @@ def test_grad_w_stream(torch, monkeypatch, B, Rx, Cx, Cy, accumulate):
 # --------------------------------------------------------------------------
 # projection with the token axis split across a cluster
 # --------------------------------------------------------------------------
+@pytest.mark.parametrize("stages", [2, 4])
 @pytest.mark.parametrize("split", [2, 3, 4])
 @pytest.mark.parametrize("B,L,C,Rx,Ry", [(2, 2048, 392, 16, 16),   # 32 chunks, ragged columns
                                          (3, 1000, 256, 8, 0),     # ragged token tail, compress
-                                         (1, 130, 136, 5, 7)])     # 3 chunks: short shares
-def test_projection_token_split(torch, monkeypatch, split, B, L, C, Rx, Ry):
+                                         (1, 130, 136, 5, 7),      # 3 chunks: short shares
+                                         (2, 1024, 264, 32, 32)])  # NT = 64: the largest partials
+def test_projection_token_split(torch, monkeypatch, stages, split, B, L, C, Rx, Ry):
+    """The token axis split over a 2-4 CTA cluster, with the four-stage and
+    the two-stage ring (whose idle ring holds partials up to NT = 64)."""
     monkeypatch.setenv("INSTANT_PROJ_SPLIT", str(split))
+    monkeypatch.setenv("INSTANT_PROJ_STAGES", str(stages))
     g = rng(3700 + L + C + split)
     t = stored(g.standard_normal((B, L, C)), "bf16")
     PQ = stored(orthonormal_rows(g, Rx + Ry, L), "bf16")
@@ -311,6 +316,28 @@ def test_projection_token_split(torch, monkeypatch, split, B, L, C, Rx, Ry):
     assert_parity(to_np(out0).reshape(B, Rx, C), r0, 2e-2, "first plane")
     if Ry:
         assert_parity(to_np(out1).reshape(B, Ry, C), r1, 2e-2, "second plane")
+    assert api.device_status() == 0
+
+
+def test_projection_split_planned_for_the_long_sequence_layer(torch):
+    """The plan's own choice on the long-sequence layer's projection (344
+    tiles: a 2-CTA token split with the two-stage ring) against the oracle on
+    sampled columns of every sample."""
+    B, L, C, R = 4, 2048, 11008, 16
+    g = rng(3750)
+    t = stored(g.standard_normal((B, L, C)) * 0.5, "bf16")
+    PQ = stored(orthonormal_rows(g, 2 * R, L), "bf16")
+    api = _api()
+    Sx = nan_like(torch, (B * R, C), torch.bfloat16)
+    Sq = nan_like(torch, (B * R, C), torch.bfloat16)
+    api.project_grad(to_dev(t), to_dev(PQ), Sx, Sq, R, R)
+    torch.cuda.synchronize()
+    cols = np.unique(np.concatenate([np.arange(0, C, 173), [C - 1, 127, 128, 10943]]))
+    ts = t[:, :, cols]
+    r0, r1 = O.project_grad(ts, PQ[:R], PQ[R:])
+    assert_parity(to_np(Sx).reshape(B, R, C)[:, :, cols], r0, 2e-2, "Sx (sampled columns)")
+    assert_parity(to_np(Sq).reshape(B, R, C)[:, :, cols], r1, 2e-2, "Sq (sampled columns)")
+    assert bool(torch.isfinite(Sx.float()).all()) and bool(torch.isfinite(Sq.float()).all())
     assert api.device_status() == 0
 
 
