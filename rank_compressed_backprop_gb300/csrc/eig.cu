@@ -983,8 +983,15 @@ __device__ __forceinline__ void stage_c_tile(float* dst, const float* Cown, int 
   cp_async_commit();
 }
 
-constexpr int kClusterCtas = 8;
+constexpr int kClusterCtas = 8;  // CTAs of a solver cluster (16 above 1024 tokens)
 constexpr int kClusterThreads = 256;
+
+// cluster size of the one-launch solver: 16 CTAs (a non-portable cluster) for
+// long token axes, where the row-parallel steps dominate (a warm two-iteration
+// solve at L = 2048 took 0.51 ms against 0.63 ms with 8); 8 below, where the
+// replicated m x m steps and the cluster barriers dominate (L = 300: 0.28 ms
+// with 8 against 0.34 ms with 16)
+__host__ __device__ inline int cluster_ctas(int L) { return L > 1024 ? 16 : kClusterCtas; }
 
 // Long token axes: Y = C V over all of the CTA's rows at once (see cv_big);
 // C and V arrive in 16-token chunks through a 4-deep cp.async ring.
@@ -1109,15 +1116,16 @@ __device__ __forceinline__ void cv_big(const float* Cown, int nr, const float* V
 // warp reads at one column fall in distinct banks; rows stay 16-byte aligned
 __host__ __device__ inline int cres_ld(int L) { return (L + 31) / 32 * 32 + 4; }
 
-// sum over the 8 CTAs of the cluster of the float at `p` (the same shared
+// sum over the CTAS CTAs of the cluster of the float at `p` (the same shared
 // address in every CTA), in rank order; every load is issued before the adds
-__device__ __forceinline__ float cluster_sum8(const float* p) {
-  float v[8];
+template <int CTAS>
+__device__ __forceinline__ float cluster_sum(const float* p) {
+  float v[CTAS];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) v[q] = dsmem_ld_f32(dsmem_addr(p, q));
+  for (int q = 0; q < CTAS; ++q) v[q] = dsmem_ld_f32(dsmem_addr(p, q));
   float t = v[0];
 #pragma unroll
-  for (int q = 1; q < 8; ++q) t += v[q];
+  for (int q = 1; q < CTAS; ++q) t += v[q];
   return t;
 }
 
@@ -1177,7 +1185,7 @@ __host__ __device__ inline ClusterLay cluster_layout(int L, int m, int rp) {
   return c;
 }
 
-template <int M>
+template <int M, int CTAS>
 __global__ void __launch_bounds__(kClusterThreads, 1)
     k_solve_cluster(const __grid_constant__ ClusterSolveBatch batch) {
   extern __shared__ __align__(16) uint8_t csm[];
@@ -1299,7 +1307,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
   if (tid == 0) {
     double t = 0.0;
     int bad = 0;
-    for (int q = 0; q < kClusterCtas; ++q) {
+    for (int q = 0; q < CTAS; ++q) {
       t += dsmem_ld_f64(dsmem_addr(dpart, q));
       bad |= dsmem_ld_s32(dsmem_addr(ipart, q));
     }
@@ -1346,7 +1354,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     cluster_sync();
     for (int idx = tid; idx < m * m; idx += nthr) {
       float g = 0.f;
-      g = cluster_sum8(Gp + idx);
+      g = cluster_sum<CTAS>(Gp + idx);
       T[(idx / m) * ld + idx % m] = g;
     }
     __syncthreads();
@@ -1386,7 +1394,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     } else {
       // ---- gather the other rows of V from the peers ----
       cluster_sync();
-      for (int q = 0; q < kClusterCtas; ++q) {
+      for (int q = 0; q < CTAS; ++q) {
         if (q == rank) continue;
         const int q0 = q * rp;
         const int nq = min(rp, L - q0);
@@ -1481,8 +1489,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     cluster_sync();
     for (int idx = tid; idx < m * m; idx += nthr) {
       const int i = idx / m, j = idx % m;
-      const float hij = cluster_sum8(Hp + i * m + j);
-      const float hji = cluster_sum8(Hp + j * m + i);
+      const float hij = cluster_sum<CTAS>(Hp + i * m + j);
+      const float hji = cluster_sum<CTAS>(Hp + j * m + i);
       js.A[i * ld + j] = 0.5f * (hij + hji);
     }
     __syncthreads();
@@ -1540,7 +1548,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     cluster_sync();
     for (int j = tid; j < m; j += nthr) {
       float t = 0.f;
-      t = cluster_sum8(resp + j);
+      t = cluster_sum<CTAS>(resp + j);
       r2[j] = t;
     }
     __syncthreads();
@@ -1601,7 +1609,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1)
     for (int j = tid; j < m; j += nthr) {
       float best = -1.f, val = 0.f;
       int bi = 0x7fffffff;
-      for (int q = 0; q < kClusterCtas; ++q) {
+      for (int q = 0; q < CTAS; ++q) {
         const float v = dsmem_ld_f32(dsmem_addr(aval + j, q));
         const int ix = dsmem_ld_s32(dsmem_addr(aidx + j, q));
         if (fabsf(v) > best || (fabsf(v) == best && ix < bi)) {
@@ -1783,17 +1791,23 @@ cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStre
   if (count < 1 || count > kMaxSolveBatch) return cudaErrorInvalidValue;
   const int L = b.s[0].L, m = b.s[0].m;
   if (!cluster_solve_fits(L, m)) return cudaErrorInvalidValue;
-  const int rp = (L + kClusterCtas - 1) / kClusterCtas;
+  const int ctas = cluster_ctas(L);
+  const int rp = (L + ctas - 1) / ctas;
   for (int i = 0; i < count; ++i) {
     if (b.s[i].L != L || b.s[i].m != m) return cudaErrorInvalidValue;
     b.s[i].rp = rp;
   }
   const size_t bytes = cluster_layout(L, m, rp).total;
-  auto kern = m == 16 ? k_solve_cluster<16> : k_solve_cluster<32>;
+  auto kern = ctas == 16 ? (m == 16 ? k_solve_cluster<16, 16> : k_solve_cluster<32, 16>)
+                         : (m == 16 ? k_solve_cluster<16, kClusterCtas> : k_solve_cluster<32, kClusterCtas>);
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), 216 * 1024);
   if (e != cudaSuccess) return e;
-  return launch_ex(kern, dim3(1, count, kClusterCtas), dim3(kClusterThreads), bytes, st,
-                   kClusterCtas, false, b);
+  if (ctas > 8) {
+    // clusters above 8 CTAs are opt-in
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_ex(kern, dim3(1, count, ctas), dim3(kClusterThreads), bytes, st, ctas, false, b);
 }
 
 cudaError_t launch_cluster_solve(ClusterSolveArgs a, cudaStream_t st) {
