@@ -175,8 +175,9 @@ instant_status instant_grad_w_x(const void* Sx, const void* xhat, float* gw, int
  * gx, ...), which is what it runs.  With the environment variable
  * INSTANT_ONE_LAUNCH_BACKWARD set, and where the single-kernel input gradient
  * applies (bf16, short Cy, and at most 64 MiB of g_tilde_x when L >= 128), it
- * is ONE launch instead: clusters take tickets as they start; the first tickets project (sample, 128-column) tiles of g_y
- * and signal each finished tile through counters in `ws`, the input-gradient
+ * is ONE launch instead: clusters take tickets as they start; the first
+ * tickets project (sample, 128-column) tiles of g_y and signal each finished
+ * tile through counters in `ws`, the input-gradient
  * items of a sample group wait for their group's tiles and the
  * weight-gradient tiles for all of them (a consumer only waits for smaller
  * tickets, so the waits end whatever the scheduling).  That launch measured
@@ -297,8 +298,8 @@ instant_status instant_calib_accumulate_batch(const instant_accumulate_item* ite
  *   ws         device scratch of instant_calib_workspace_bytes(L, r_cap) bytes
  * Method: L <= 128 -> one-CTA cyclic Jacobi on the full matrix; larger L ->
  * block subspace iteration with Rayleigh-Ritz (block <= 128 columns), as a
- * single launch of an 8-CTA cluster up to L = 2048 with blocks of 16 or 32
- * columns, as a host loop of launches otherwise.  A Ritz pair counts as
+ * single launch of one cluster (8 CTAs; 16 above 1024 tokens) up to L = 2048
+ * with blocks of 16 or 32 columns, as a host loop of launches otherwise.  A Ritz pair counts as
  * converged when its residual is below 1e-3 of its own Ritz value (so that
  * the trailing rows of a decaying spectrum are accurate too), or when it is
  * below prm->tol (default 2e-5) times the largest Ritz value and no longer
@@ -325,8 +326,8 @@ size_t instant_calib_workspace_bytes(int L, int r_cap);
  * the multi-launch path adds some partial sums with atomics, so any two of its
  * runs agree only up to that rounding order); the problems that the
  * one-launch solver takes (128 < L <= 2048, block of 16 or 32 columns) run
- * together, one 8-CTA cluster each, up to 16 per launch, with one
- * synchronisation for all of them.
+ * together, one cluster each (8 CTAs; 16 above 1024 tokens), up to 16 per
+ * launch, with one synchronisation for all of them.
  *
  * instant_calib_problem: one statistic.
  *   C, n_samples, prm, rows_out, r_cap, eig_out   as for instant_calib_solve
