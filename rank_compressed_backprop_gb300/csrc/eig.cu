@@ -1791,7 +1791,31 @@ cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStre
   if (count < 1 || count > kMaxSolveBatch) return cudaErrorInvalidValue;
   const int L = b.s[0].L, m = b.s[0].m;
   if (!cluster_solve_fits(L, m)) return cudaErrorInvalidValue;
-  const int ctas = cluster_ctas(L);
+  int ctas = cluster_ctas(L);
+  if (ctas > kClusterCtas) {
+    // clusters above 8 CTAs are opt-in, and need 16 SMs of one GPC: where no
+    // GPC of the device can hold one (the cluster occupancy query) the
+    // cluster stays at 8
+    auto k16 = m == 16 ? k_solve_cluster<16, 16> : k_solve_cluster<32, 16>;
+    const size_t bytes16 = cluster_layout(L, m, (L + 15) / 16).total;
+    int fit = 0;
+    if (raise_smem_limit(reinterpret_cast<const void*>(k16), 216 * 1024) == cudaSuccess &&
+        cudaFuncSetAttribute(k16, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(1, 1, 16);
+      cfg.blockDim = dim3(kClusterThreads);
+      cfg.dynamicSmemBytes = bytes16;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 1;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 16;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&fit, k16, &cfg) != cudaSuccess) fit = 0;
+    }
+    if (fit < 1) ctas = kClusterCtas;
+  }
   const int rp = (L + ctas - 1) / ctas;
   for (int i = 0; i < count; ++i) {
     if (b.s[i].L != L || b.s[i].m != m) return cudaErrorInvalidValue;
@@ -1802,11 +1826,6 @@ cudaError_t launch_cluster_solve_batch(ClusterSolveBatch& b, int count, cudaStre
                          : (m == 16 ? k_solve_cluster<16, kClusterCtas> : k_solve_cluster<32, kClusterCtas>);
   cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(kern), 216 * 1024);
   if (e != cudaSuccess) return e;
-  if (ctas > 8) {
-    // clusters above 8 CTAs are opt-in
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   return launch_ex(kern, dim3(1, count, ctas), dim3(kClusterThreads), bytes, st, ctas, false, b);
 }
 
