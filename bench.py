@@ -335,10 +335,15 @@ class LayerBench:
         del x0, g0
         self.set_bytes = per_set
 
-    def calibrate(self, s):
+    def accumulate(self, s):
+        """The statistics of the step's batch and of the resident calibration
+        samples."""
         self.lay.accumulate(s["x"], s["g"])
         if self.xc is not None:
             self.lay.accumulate(self.xc, self.gc)
+
+    def calibrate(self, s):
+        self.accumulate(s)
         return self.lay.recalibrate()
 
     def step(self, s):
@@ -482,8 +487,15 @@ def measure_workload(name, args, dev, world, stream, full: bool):
     lbs = [LayerBench(wl, i, dev) for i in range(len(wl.layers))]
     nsets = min(len(lb.sets) for lb in lbs)
 
+    # the layers of a model recalibrate at the same step: their statistics are
+    # solved together (one batched call for all layers)
+    from rank_compressed_backprop_gb300 import LayerCalibration
+    layer_cal = LayerCalibration([lb.lay for lb in lbs])
+
     def calibrate(i):
-        return [lb.calibrate(lb.sets[i % nsets]) for lb in lbs]
+        for lb in lbs:
+            lb.accumulate(lb.sets[i % nsets])
+        return layer_cal.recalibrate()
 
     def step(i):
         for lb in lbs:
@@ -615,8 +627,7 @@ def measure_workload(name, args, dev, world, stream, full: bool):
     acc_us = a.elapsed_time(b) * 1e3 / reps
     acc_flops = sum(wl.calib_samples * wl.L * (wl.L + 1) * (lb.Cx + lb.Cy) for lb in lbs)
     t0 = time.perf_counter()
-    for lb in lbs:
-        lb.lay.recalibrate()
+    layer_cal.recalibrate()
     solve_ms = (time.perf_counter() - t0) * 1e3
     res["calibration_parts"] = {
         "accumulate_all_statistics_us": round(acc_us, 2),

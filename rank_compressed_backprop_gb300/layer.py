@@ -137,3 +137,56 @@ class InstantLinear:
         out = self.backward(g_y)
         self.t += 1
         return out
+
+
+class LayerCalibration:
+    """The recalibration of several layers at the same step (整体框架: every
+    layer recalibrates every N_t steps, so a model's layers do it together):
+    the statistics of all of them -- each layer's ``C_X`` into ``P`` and
+    ``C_G`` into ``Q`` -- go to ``instant_calib_solve_batch`` in one call
+    (one launch where the one-launch solver takes the token length, up to 16
+    statistics), instead of one call per layer.  Each layer gets the results
+    its own :meth:`InstantLinear.recalibrate` would give it (bit for bit where
+    the one-launch cluster solver takes L, 128 < L <= 2048).  The layers must
+    share the token length L and the dtype; the argument block and the
+    workspace are built once."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        if not self.layers:
+            raise ValueError("LayerCalibration: no layers")
+        L, dt = self.layers[0].L, self.layers[0].dtype
+        if any(l.L != L or l.dtype != dt for l in self.layers):
+            raise ValueError("LayerCalibration: layers differ in L or dtype")
+        self.batches = []
+        # at most 8 layers (16 statistics) per call
+        for i in range(0, len(self.layers), 8):
+            group = self.layers[i:i + 8]
+            ws = torch.empty(api.calib_batch_workspace_bytes(L, 2 * len(group)), dtype=torch.uint8,
+                             device=group[0].w.device)
+            probs = []
+            for l in group:
+                common = dict(eps=l.eps, p=l.p, scale_on=l.scale_on)
+                probs += [dict(C=l.C_X, rows_out=l.P, **common), dict(C=l.C_G, rows_out=l.Q, **common)]
+            self.batches.append((group, api.CalibBatch(probs, ws), ws))
+
+    def recalibrate(self, r_override: bool = True):
+        """Solves every layer's statistics and clears them; returns the list of
+        ``(result_x, result_g)`` per layer."""
+        out = []
+        for group, batch, _ in self.batches:
+            if any(l.n_x == 0 or l.n_g == 0 for l in group):
+                raise RuntimeError("recalibrate: no statistics accumulated")
+            warm = all(l.last_calibration is not None for l in group)
+            counts, over = [], []
+            for l in group:
+                counts += [l.n_x, l.n_g]
+                over += [l.Rx if r_override else 0, l.Ry if r_override else 0]
+            res = batch.solve(counts, warm_start=warm, r_override=over)
+            for i, l in enumerate(group):
+                l.C_X.zero_()
+                l.C_G.zero_()
+                l.n_x = l.n_g = 0
+                l.last_calibration = (res[2 * i], res[2 * i + 1])
+                out.append(l.last_calibration)
+        return out

@@ -53,6 +53,38 @@ def test_layer_step_schedule_and_oracle(torch):
     assert_parity(to_np(gx), ref["g_x"], 2e-2, "g_x")
 
 
+@pytest.mark.parametrize("L", [49, 136])
+def test_layers_recalibrated_together(torch, L):
+    """LayerCalibration solves several layers' statistics in one call: given
+    the same statistics (copied: the accumulation adds with atomics, so two
+    accumulations may differ in their last bits), each layer's projector, k and
+    R bit for bit as its own recalibrate gives them, cold and warm-started,
+    and the statistics are cleared."""
+    from rank_compressed_backprop_gb300 import LayerCalibration
+
+    x, g, w = _layer_inputs(L=L)
+    x2, g2, w2 = _layer_inputs(L=L, Cx=200, Cy=264)
+    B = x.shape[0]
+    pairs = [(x, g, w), (x2, g2, w2)]
+    alone = [_make_layer(torch, ww, B, L) for _, _, ww in pairs]
+    together = [_make_layer(torch, ww, B, L) for _, _, ww in pairs]
+    cal = LayerCalibration(together)
+    for rnd in range(2):  # cold, then warm-started
+        want = []
+        for a, b, (xx, gg, _) in zip(alone, together, pairs):
+            a.accumulate(to_dev(xx), to_dev(gg))
+            b.C_X.copy_(a.C_X)
+            b.C_G.copy_(a.C_G)
+            b.n_x, b.n_g = a.n_x, a.n_g
+            want.append(a.recalibrate())
+        got = cal.recalibrate()
+        torch.cuda.synchronize()
+        for a, b, (ra, rb) in zip(alone, together, zip(want, got)):
+            assert torch.equal(a.PQ, b.PQ), rnd
+            assert (ra[0].k, ra[0].R, ra[1].k, ra[1].R) == (rb[0].k, rb[0].R, rb[1].k, rb[1].R)
+            assert b.n_x == 0 and int(b.C_X.count_nonzero()) == 0 and int(b.C_G.count_nonzero()) == 0
+
+
 def test_cuda_graph_replay_matches_eager(torch):
     x, g, w = _layer_inputs()
     B, L = x.shape[0], x.shape[1]
