@@ -272,12 +272,20 @@ instant_status project(const void* t, const void* pq, void* out0, void* out1, in
 // GEMM plan: N tile and split-K cluster size for an M x N x K product
 // ---------------------------------------------------------------------------
 struct GemmPlan {
-  int BN, splits, cps, nk, stages;
+  int BN, splits, cps, nk, stages, short_a;
 };
 
-GemmPlan plan_gemm(int M, int N, int K) {
+// short_ok: A is K-major, so M <= 64 may take the 64-row A box (three CTAs
+// share an SM instead of two).  With it K takes the most cluster shares (up to
+// 8) whose CTAs and clusters all fit on the device at once: the long-sequence
+// g_hat_x (64 x 4096, K = 11008, 64 column tiles) at 2 / 4 / 5 / 6 shares
+// took 34 / 23 / 20 / 20 us, and at 7 shares (448 CTAs, not all placeable as
+// 7-CTA clusters) 29 us.  Otherwise the largest split that keeps two waves'
+// worth of work.
+GemmPlan plan_gemm(int M, int N, int K, bool short_ok) {
   GemmPlan p;
   p.nk = cdiv(K, 64);
+  p.short_a = short_ok && M <= 64 && !std::getenv("INSTANT_GEMM_LONG_A");
   const int tm = cdiv(M, 128);
   p.BN = 64;
   const int nsm = sm_count();
@@ -292,19 +300,36 @@ GemmPlan plan_gemm(int M, int N, int K) {
     if (f == 64 || f == 128 || f == 256) p.BN = f;
   }
   const int tiles = tm * cdiv(N, p.BN);
+  p.stages = 4;
   p.splits = 1;
-  for (int s : {8, 4, 2}) {
-    if (s <= p.nk && tiles * s <= 2 * nsm) {  // two waves' worth of work
-      p.splits = s;
-      break;
+  if (p.short_a) {
+    GemmArgs g{};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.b_mn_major = 1;
+    g.BN = p.BN;
+    g.stages = p.stages;
+    g.short_a = 1;
+    const long long slots = static_cast<long long>(gemm_bf16_ctas_per_sm(g)) * nsm;
+    for (int s = 2; s <= 8 && s <= p.nk; ++s) {
+      g.splits = s;
+      if (static_cast<long long>(tiles) * s > slots) break;
+      if (gemm_bf16_max_clusters(g) >= tiles) p.splits = s;
+    }
+  } else {
+    for (int s : {8, 4, 2}) {
+      if (s <= p.nk && tiles * s <= 2 * nsm) {  // two waves' worth of work
+        p.splits = s;
+        break;
+      }
     }
   }
   if (const char* v = std::getenv("INSTANT_GEMM_SPLITS")) {
     const int f = std::atoi(v);
-    if ((f == 1 || f == 2 || f == 4 || f == 8) && f <= p.nk) p.splits = f;
+    if (f >= 1 && f <= 8 && f <= p.nk) p.splits = f;
   }
   p.cps = cdiv(p.nk, p.splits);
-  p.stages = 4;
   return p;
 }
 
@@ -828,7 +853,7 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
   if (!Sx || !xhat || !gw) return INSTANT_ERR_ARG;
   if (B < 1 || Rx < 1 || Cx < 1 || Cy < 1) return INSTANT_ERR_SHAPE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  GemmArgs g;
+  GemmArgs g{};
   g.M = Cy;
   g.N = Cx;
   g.K = B * Rx;
@@ -878,12 +903,13 @@ instant_status instant_grad_w(const void* Sx, const void* xhat, float* gw, int a
     const int ctas = static_cast<int>(std::min<long long>(tiles, sm_count()));
     return from_cuda(launch_gradw_stream(ma, mb, mo, a, ctas, st));
   }
-  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
+  const GemmPlan p = plan_gemm(g.M, g.N, g.K, false);
   g.BN = p.BN;
   g.nk = p.nk;
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
   g.stages = p.stages;
+  g.short_a = 0;
   return from_cuda(launch_gemm_bf16(ma, mb, g, st));
 }
 
@@ -979,7 +1005,7 @@ namespace {
 // (every argument checked, every tensor map encoded) and its launch, so that
 // a caller running both can report any error before either launches.
 struct CorePlan {
-  GemmArgs g;
+  GemmArgs g{};
   CUtensorMap ma, mb;
   const void* Sq;
   const void* w;
@@ -1012,16 +1038,17 @@ instant_status plan_grad_x_core(const void* Sq, const void* w, void* ws, size_t 
   }
   if (!aligned16(Sq) || !aligned16(w) || !aligned16(ws) || Cx % 8 != 0 || Cy % 8 != 0)
     return INSTANT_ERR_ALIGN;
-  const GemmPlan p = plan_gemm(g.M, g.N, g.K);
+  const GemmPlan p = plan_gemm(g.M, g.N, g.K, true);
   g.out_bf16 = 1;
   g.BN = p.BN;
   g.nk = p.nk;
   g.splits = p.splits;
   g.chunks_per_split = p.cps;
   g.stages = p.stages;
+  g.short_a = p.short_a;
   const uint64_t da[2] = {static_cast<uint64_t>(Cy), static_cast<uint64_t>(g.M)};
   const uint64_t sa[1] = {static_cast<uint64_t>(Cy) * 2};
-  const uint32_t ba[2] = {64, 128};
+  const uint32_t ba[2] = {64, static_cast<uint32_t>(p.short_a ? 64 : 128)};
   const uint64_t db[2] = {static_cast<uint64_t>(Cx), static_cast<uint64_t>(Cy)};
   const uint64_t sb[1] = {static_cast<uint64_t>(Cx) * 2};
   const uint32_t bb[2] = {64, 64};

@@ -11,9 +11,16 @@
 // One elected thread issues the MMAs.  These products are small (a few MB), so
 // the grid is widened by splitting K across the CTAs of a thread-block
 // cluster: every CTA parks its fp32 partial tile in its own shared memory, and
-// after a cluster barrier each CTA sums a 128/S-row slice of the tile over
-// all S partials through distributed shared memory and writes it with
-// coalesced stores (fp32, fp32 accumulate, or bf16).  No global scratch.
+// after a cluster barrier each CTA sums a slice of the tile's rows over all S
+// partials through distributed shared memory and writes it with coalesced
+// stores (fp32, fp32 accumulate, or bf16).  No global scratch.
+// A short K-major A (M <= 64, g_hat_x for a few samples) takes a 64-row box:
+// the stage is 8 KB smaller, so more CTAs share an SM, and the M = 128 MMA
+// reads rows 64..127 from the B slot after it (results never used).
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "tc.cuh"
 
@@ -25,7 +32,11 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 
-__host__ __device__ inline uint32_t stage_bytes(int BN) { return A_BYTES + BN * BK * 2; }
+__host__ __device__ inline uint32_t a_bytes(int short_a) { return short_a ? A_BYTES / 2 : A_BYTES; }
+__host__ __device__ inline uint32_t stage_bytes(int BN, int short_a) {
+  return a_bytes(short_a) + BN * BK * 2;
+}
+__host__ __device__ inline int tile_rows(int short_a) { return short_a ? BM / 2 : BM; }
 
 template <int BN, int A_MN, int B_MN>
 __global__ void __launch_bounds__(128, 1)
@@ -34,11 +45,13 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr uint32_t STAGE = A_BYTES + BN * BK * 2;
+  const uint32_t ABYTES = a_bytes(g.short_a);
+  const uint32_t STAGE = stage_bytes(BN, g.short_a);
+  const int ROWS = tile_rows(g.short_a);  // rows of the tile that can hold results
   constexpr int RED_LD = BN + 4;  // fp32 reduction tile row pitch (bank spread)
   const int NS = g.stages;  // ring depth: min(4, chunks per CTA)
   const uint32_t RING = NS * STAGE;
-  constexpr uint32_t REDB = BM * RED_LD * 4;
+  const uint32_t REDB = ROWS * RED_LD * 4;
   const uint32_t BAR_OFF = RING > REDB ? RING : REDB;
   uint8_t* sbase = smem;
   float* red = reinterpret_cast<float*>(smem);  // reuses the stages after the K loop
@@ -111,12 +124,12 @@ __global__ void __launch_bounds__(128, 1)
       }
       const int k0 = (kc_begin + i) * BK;
       uint8_t* sa = sbase + s * STAGE;
-      uint8_t* sb = sa + A_BYTES;
+      uint8_t* sb = sa + ABYTES;
       mbar_arrive_expect_tx(&full[s], STAGE);
       if (A_MN) {  // A stored [K, M]: two 64-wide M boxes of 64 K-rows
         tma_load_2d(sa, &tmap_a, &full[s], m0, k0);
         tma_load_2d(sa + A_BYTES / 2, &tmap_a, &full[s], m0 + 64, k0);
-      } else {     // A stored [M, K]: one box of 64 K x 128 rows
+      } else {     // A stored [M, K]: one box of 64 K x 128 (short: 64) rows
         tma_load_2d(sa, &tmap_a, &full[s], k0, m0);
       }
       if (B_MN) {  // B stored [K, N]: BN/64 boxes of 64 N x 64 K-rows
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(128, 1)
       }
       tc_fence_after();
       const uint32_t a_base = smem_u32(sbase + s * STAGE);
-      const uint32_t b_base = a_base + A_BYTES;
+      const uint32_t b_base = a_base + ABYTES;
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint64_t ad = A_MN ? sdesc_sw128(a_base + kk * 2048, A_BYTES / 2, 1024)
@@ -172,7 +185,7 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   fence_proxy_async_smem();
   __syncthreads();  // every stage is consumed: the ring becomes the reduction tile
-  {
+  if (warp * 32 < ROWS) {
     const int row = warp * 32 + lane;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float* dst = red + row * RED_LD;
@@ -196,8 +209,9 @@ __global__ void __launch_bounds__(128, 1)
 
   // ---------------- epilogue 2: reduce a row slice over the cluster, store ----------------
   {
-    const int rows = BM / g.splits;
-    const int r0 = split * rows;
+    const int per = (ROWS + g.splits - 1) / g.splits;
+    const int r0 = split * per;
+    const int rows = r0 >= ROWS ? 0 : (ROWS - r0 < per ? ROWS - r0 : per);
     constexpr int C4 = BN / 4;
     for (int idx = threadIdx.x; idx < rows * C4; idx += blockDim.x) {
       const int rr = r0 + idx / C4;
@@ -276,18 +290,103 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const GemmAr
   }
 }
 
+template <int A_MN, int B_MN>
+const void* kernel_bn(int BN) {
+  switch (BN) {
+    case 64: return reinterpret_cast<const void*>(k_gemm_bf16<64, A_MN, B_MN>);
+    case 128: return reinterpret_cast<const void*>(k_gemm_bf16<128, A_MN, B_MN>);
+    case 256: return reinterpret_cast<const void*>(k_gemm_bf16<256, A_MN, B_MN>);
+    default: return nullptr;
+  }
+}
+
+const void* kernel_for(const GemmArgs& g) {
+  if (g.a_mn_major && g.b_mn_major) return kernel_bn<1, 1>(g.BN);
+  if (!g.a_mn_major && g.b_mn_major) return kernel_bn<0, 1>(g.BN);
+  if (g.a_mn_major && !g.b_mn_major) return kernel_bn<1, 0>(g.BN);
+  return kernel_bn<0, 0>(g.BN);
+}
+
 }  // namespace
 
 size_t gemm_bf16_smem_bytes(const GemmArgs& g) {
-  const size_t ring = static_cast<size_t>(g.stages) * stage_bytes(g.BN);
-  const size_t red = static_cast<size_t>(BM) * (g.BN + 4) * sizeof(float);
+  const size_t ring = static_cast<size_t>(g.stages) * stage_bytes(g.BN, g.short_a);
+  const size_t red = static_cast<size_t>(tile_rows(g.short_a)) * (g.BN + 4) * sizeof(float);
   return (ring > red ? ring : red) + 256 + 1024;
+}
+
+int gemm_bf16_ctas_per_sm(const GemmArgs& g) {
+  // one residency count per (device, shared-memory size, kernel)
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t, int, int, int>, int> counts;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const size_t bytes = gemm_bf16_smem_bytes(g);
+  const auto key = std::make_tuple(dev, bytes, g.BN, g.a_mn_major, g.b_mn_major);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = counts.find(key);
+    if (it != counts.end()) return it->second;
+  }
+  const void* k = kernel_for(g);
+  const int n = k ? resident_ctas_per_sm(k, 128, bytes, g.BN) : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (n > 0) counts[key] = n;
+  return n;
+}
+
+// Stand-in for the cluster occupancy query: asked about the GEMM kernel itself
+// (66 KB form, GB300) the driver answers 76 clusters of two CTAs and 46 of
+// three, as if one CTA filled an SM, against 228 and 148 for an empty kernel
+// with the same block size and shared memory; so the query runs on that
+// empty kernel, and registers and TMEM are counted separately by the caller.
+__global__ void __launch_bounds__(128, 1) k_cluster_fit(int* p) {
+  extern __shared__ int fit_smem[];
+  if (p) p[threadIdx.x] = fit_smem[threadIdx.x];
+}
+
+int gemm_bf16_max_clusters(const GemmArgs& g) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t, int, int, int, int, int, int>, int> counts;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const size_t bytes = gemm_bf16_smem_bytes(g);
+  const dim3 grid((g.N + g.BN - 1) / g.BN, (g.M + BM - 1) / BM, g.splits);
+  const auto key = std::make_tuple(dev, bytes, g.BN, g.a_mn_major, g.b_mn_major, g.splits,
+                                   static_cast<int>(grid.x), static_cast<int>(grid.y));
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = counts.find(key);
+    if (it != counts.end()) return it->second;
+  }
+  const void* k = reinterpret_cast<const void*>(k_cluster_fit);
+  if (raise_smem_limit(k, bytes) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = bytes;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = g.splits;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (n > 0) counts[key] = n;
+  return n;
 }
 
 cudaError_t launch_gemm_bf16(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& g,
                              cudaStream_t st) {
-  if (g.splits != 1 && g.splits != 2 && g.splits != 4 && g.splits != 8) return cudaErrorInvalidValue;
+  if (g.splits < 1 || g.splits > 8) return cudaErrorInvalidValue;
   if (g.stages < 1 || g.stages > kGemmStages) return cudaErrorInvalidValue;
+  if (g.short_a && (g.a_mn_major || g.M > BM / 2)) return cudaErrorInvalidValue;
   if (g.a_mn_major && g.b_mn_major) return launch_bn<1, 1>(ta, tb, g, st);
   if (!g.a_mn_major && g.b_mn_major) return launch_bn<0, 1>(ta, tb, g, st);
   if (g.a_mn_major && !g.b_mn_major) return launch_bn<1, 0>(ta, tb, g, st);

@@ -43,17 +43,20 @@ struct GemmArgs {
   int b_mn_major;    // 1: B stored [K, N]; 0: B stored [N, K]
   int BN;            // N tile (64, 128 or 256)
   int nk;            // ceil(K / 64)
-  int splits;        // split-K factor = cluster size along grid z (1, 2, 4 or 8);
+  int splits;        // split-K factor = cluster size along grid z (1..8);
                      // partial tiles are reduced through distributed shared memory
   int chunks_per_split;
   int stages;        // TMA ring depth, 1..kGemmStages
   int accumulate;    // fp32 output only: out += D
   int out_bf16;      // 1: bf16 output (round to nearest even); 0: fp32
+  int short_a;       // 1: A stored [M, K] with M <= 64, loaded as a 64-row box
   void* out;         // [M][N]
 };
 
 constexpr int kGemmStages = 4;
 size_t gemm_bf16_smem_bytes(const GemmArgs& g);
+int gemm_bf16_ctas_per_sm(const GemmArgs& g);  // resident CTAs on one SM
+int gemm_bf16_max_clusters(const GemmArgs& g);  // co-resident clusters of g.splits CTAs
 cudaError_t launch_gemm_bf16(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmArgs& g, cudaStream_t st);
 cudaError_t launch_gemm_f32(const GemmArgs& g, const float* A, const float* Bm, cudaStream_t st);

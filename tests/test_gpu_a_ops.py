@@ -420,3 +420,31 @@ def test_expand_job_runs(torch, monkeypatch, ctas, bn, B, L, Cx, Cy, Ry):
     ref = O.grad_x(O.decode(Sq).reshape(B, Ry, Cy), w, Q)
     assert_parity(to_np(gx), ref, 2e-2, "g_x")
     assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3, 5, 7, 8])  # 0: the planned split
+@pytest.mark.parametrize("long_a", [False, True])
+@pytest.mark.parametrize("B,Ry,Cx,Cy", [(4, 16, 1096, 1000),  # M = 64: the 64-row A box, ragged K
+                                        (3, 8, 264, 520),     # M = 24
+                                        (5, 16, 200, 456)])   # M = 80: the 128-row box
+def test_grad_x_core_splits(torch, monkeypatch, splits, long_a, B, Ry, Cx, Cy):
+    """g_hat_x = Sq w from the split-K GEMM with K cut into 1..8 cluster shares
+    (including uneven ones) and either A box, read from the workspace (filled
+    with NaN first) and compared element by element with the oracle."""
+    if splits:
+        monkeypatch.setenv("INSTANT_GEMM_SPLITS", str(splits))
+    if long_a:
+        monkeypatch.setenv("INSTANT_GEMM_LONG_A", "1")
+    api = _api()
+    g = rng(4100 + B + Ry + Cx + Cy + splits)
+    Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
+    n = api.grad_x_workspace_bytes(B, 130, Cx, Cy, Ry, torch.bfloat16)
+    assert n == B * Ry * Cx * 2
+    ws = torch.full((n,), 255, dtype=torch.uint8, device="cuda")
+    api.grad_x_core(to_dev(Sq), to_dev(w), ws, B)
+    torch.cuda.synchronize()
+    got = to_np(ws.view(torch.bfloat16).reshape(B, Ry, Cx))
+    ref = O.grad_x_core(O.decode(Sq).reshape(B, Ry, Cy), w)
+    assert_parity(got, ref, 2e-2, "g_hat_x")
+    assert api.device_status() == 0
