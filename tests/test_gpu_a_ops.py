@@ -448,3 +448,24 @@ def test_grad_x_core_splits(torch, monkeypatch, splits, long_a, B, Ry, Cx, Cy):
     ref = O.grad_x_core(O.decode(Sq).reshape(B, Ry, Cy), w)
     assert_parity(got, ref, 2e-2, "g_hat_x")
     assert api.device_status() == 0
+
+
+def test_grad_x_core_planned_for_the_long_sequence_layer(torch):
+    """The plan's own choice for the long-sequence layer's g_hat_x = Sq w
+    (64 rows, K = 11008: the 64-row A box, K split over a cluster) against
+    the oracle on sampled columns; every element written and finite."""
+    B, Ry, Cx, Cy = 4, 16, 4096, 11008
+    g = rng(4200)
+    Sq = stored(g.standard_normal((B * Ry, Cy)), "bf16")
+    w = stored(g.standard_normal((Cy, Cx)) / np.sqrt(Cy), "bf16")
+    api = _api()
+    ws = torch.full((api.grad_x_workspace_bytes(B, 2048, Cx, Cy, Ry, torch.bfloat16),), 255,
+                    dtype=torch.uint8, device="cuda")
+    api.grad_x_core(to_dev(Sq), to_dev(w), ws, B)
+    torch.cuda.synchronize()
+    got = ws.view(torch.bfloat16).reshape(B, Ry, Cx)
+    assert bool(torch.isfinite(got.float()).all())
+    cols = np.unique(np.concatenate([np.arange(0, Cx, 37), [63, 64, 4032, Cx - 1]]))
+    ref = O.grad_x_core(O.decode(Sq).reshape(B, Ry, Cy), O.decode(w)[:, cols])
+    assert_parity(to_np(got)[:, :, cols], ref, 2e-2, "g_hat_x (sampled columns)")
+    assert api.device_status() == 0
